@@ -1,0 +1,532 @@
+#!/usr/bin/env python
+"""Benchmark of the k-quant batch-1 decode GEMV path on GB300.
+
+A step is one pass of the whole hot path over one synthetic decode token:
+the q8 producer(s) followed by the GEMV(s) of the workload, with the weights
+resident in HBM.  The default workload is the Qwen2.5-7B-shaped ffn_down:
+SwiGLU(g, u) -> q8 -> q6_K 3584 x 18944 GEMV (74 super-blocks per row, so
+split-K).  L2 is defeated by rotating through enough device copies of the
+weights that one rotation exceeds 4x the L2 size.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl mq|reference]
+                    [--workload NAME]
+
+Prints ONE JSON line (rank 0).  value = weight content bytes per step /
+device time per step (GB/s).  --impl reference times the oracle (plain C,
+one host core) on a bounded row sample of the same workload.
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(independent problems, weak scaling, no collective on the data path); the
+step time is the max over ranks and value sums the ranks' bytes.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import shutil
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "content GB/s per k-quant GEMV (bytes/kernel time) and % of GB300 HBM peak"
+DESCR = {
+    "q6k_512x2048": "q6_K 512x2048 GEMV, x -> standalone q8 quantize, batch 1",
+    "ffn_down_7b": "Qwen2.5-7B ffn_down: q6_K 3584x18944 (74 super-blocks/row, split-K), "
+                   "SwiGLU(g,u)->q8 producer, batch 1",
+    "layer_14b": "Qwen2.5-14B attn_v q6_K 1024x5120 + ffn_down q6_K 5120x13824, each fed by "
+                 "rms_norm->q8, batch 1",
+    "lm_head_14b": "Qwen2.5-14B output head q6_K 152064x5120, rms_norm->q8, batch 1",
+    "sweep_14b": "Qwen2.5-14B decode weight sweep: 48 layers x {q,k,o,gate,up q4_K; v,down q6_K} "
+                 "+ q6_K head, fused rms/swiglu/quantize producers, batch 1",
+}
+
+
+# ---------------------------------------------------------------- distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws: int, backend: str):
+    import torch.distributed as dist
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if ws > 1 else None
+
+
+def reduce_max(value: float, dist) -> float:
+    """Max of a float over ranks (identity without a process group)."""
+    if dist is None:
+        return value
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(bytes_per_rank_step: float, steps: int, max_ms: float, world: int) -> float:
+    """Whole-job GB/s: the bytes every rank processed over the slowest rank's time."""
+    return world * bytes_per_rank_step * steps / (max_ms * 1e-3) / 1e9
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the GPU runs the workload."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.idx = gpu_index
+        self.lines = []
+        exe = shutil.which("nvidia-smi")
+        if exe:
+            self.proc = subprocess.Popen([exe, f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(gpu_index), "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict | None:
+        rows = []
+        for t, line in self.lines:
+            if t0 <= t <= t1:
+                f = [s.strip() for s in line.split(",")]
+                if len(f) >= 9:
+                    rows.append(f)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- measured peaks / profiles
+def measured_peak_gbs():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def gemv_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("gemv.cu", "layout.h"):
+        with open(os.path.join(ROOT, "quant_quantized_gemv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per GEMV launch from the committed ncu summary of this
+    workload, if it was taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", f"gemv_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
+    if not m or not h or h.group(1) != gemv_source_hash():
+        return None
+    return float(m.group(1))
+
+
+# ---------------------------------------------------------------- workload on the device
+class DeviceWorkload:
+    """Ops of one decode step: producers writing q8 planes, GEMVs reading them."""
+
+    def __init__(self, name: str, device, l2_bytes: int, min_graphs: int = 16):
+        import torch
+        import quant_quantized_gemv_gb300 as mq
+        self.mq = mq
+        self.name = name
+        self.wl = synth.WORKLOADS[name]
+        self.dev = device
+        self.weight_bytes = self.wl.weight_bytes()
+        self.n_copies = max(1, math.ceil(4 * l2_bytes / self.weight_bytes))
+        g = synth.rng("bench", name)
+        # one host matrix per distinct (fmt, rows, cols): the sweep's 48 layers
+        # share content but get distinct device buffers, so nothing is cached
+        base = {}
+        for _, fmt, rows, cols, _ in self.wl.gemvs:
+            if (fmt, rows, cols) not in base:
+                W = synth.blocks(fmt, g, rows, cols)
+                rep = mq.mq_repack_q6k if fmt == "q6k" else mq.mq_repack_q4k
+                base[(fmt, rows, cols)] = (W, torch.from_numpy(rep(W, rows, cols)).to(device))
+        self.host_w = {k: v[0] for k, v in base.items()}
+        self.ops = []
+        self.inputs = []          # (device tensor, host pinned) pairs copied in by e2e
+        prev_kind, prev_cols, plane, prev_outputs = None, None, None, []
+        for gname, fmt, rows, cols, producer in self.wl.gemvs:
+            if not (producer == "rms" and prev_kind == "rms" and prev_cols == cols):
+                plane = torch.empty(mq.mq_q8_bytes(cols), dtype=torch.uint8, device=device)
+                yp = torch.empty(cols, dtype=torch.float32, device=device)
+                if producer == "rms":
+                    x = self._input(synth.normal(g, cols))
+                    gain = torch.from_numpy(synth.normal(g, cols, 1.0, 0.1)).to(device)
+                    self.ops.append(("rms", x, gain, yp, plane, cols))
+                elif producer == "swiglu":
+                    if len(prev_outputs) >= 2 and prev_outputs[-1].numel() == cols and \
+                            prev_outputs[-2].numel() == cols:
+                        gv, uv = prev_outputs[-2], prev_outputs[-1]     # gate, up outputs
+                    else:
+                        gv = self._input(synth.normal(g, cols))
+                        uv = self._input(synth.normal(g, cols))
+                    self.ops.append(("swiglu", gv, uv, yp, plane, cols))
+                else:
+                    x = self._input(synth.normal(g, cols))
+                    self.ops.append(("quant", x, plane, cols))
+            prev_kind, prev_cols = producer, cols
+            W0 = base[(fmt, rows, cols)][1]
+            copies = [W0.clone() for _ in range(self.n_copies)]
+            y = torch.empty(rows, dtype=torch.float32, device=device)
+            ws = mq.mq_gemv_workspace(rows, cols, device=device)
+            self.ops.append(("gemv", fmt, copies, plane, y, rows, cols, ws, gname))
+            prev_outputs.append(y)
+        self.output = self.ops[-1][4]
+        self.n_gemv = sum(1 for o in self.ops if o[0] == "gemv")
+        self.n_kernels = len(self.ops)
+        self.gemv_bytes = [self._gemv_alg_bytes(o) for o in self.ops if o[0] == "gemv"]
+
+    def _input(self, arr: np.ndarray):
+        import torch
+        t = torch.from_numpy(arr).to(self.dev)
+        self.inputs.append((t, torch.from_numpy(arr).pin_memory()))
+        return t
+
+    @staticmethod
+    def _gemv_alg_bytes(o) -> int:
+        _, fmt, _, plane, _, rows, cols, _, _ = o
+        wb = rows * (cols // 256) * (210 if fmt == "q6k" else 144)
+        act = (cols // 32) * (34 if fmt == "q6k" else 38)      # codes + fp16 d (+ int32 sum)
+        return wb + act + 4 * rows
+
+    def run(self, k: int, events=None):
+        """Enqueue step k (weights copy k % n_copies) on the current stream."""
+        mq = self.mq
+        c = k % self.n_copies
+        gi = 0
+        for o in self.ops:
+            kind = o[0]
+            if kind == "rms":
+                mq.mq_rmsnorm_quant_q8(o[1], o[2], 1e-6, y=o[3], q8=o[4])
+            elif kind == "swiglu":
+                mq.mq_swiglu_quant_q8(o[1], o[2], y=o[3], q8=o[4])
+            elif kind == "quant":
+                mq.mq_quantize_q8(o[1], q8=o[2])
+            else:
+                _, fmt, copies, plane, y, rows, cols, ws, _ = o
+                if events is not None:
+                    events[gi][0].record()
+                fn = mq.mq_gemv_q6k_q8 if fmt == "q6k" else mq.mq_gemv_q4k_q8
+                fn(copies[c], plane, rows, cols, y=y, ws=ws)
+                if events is not None:
+                    events[gi][1].record()
+                gi += 1
+
+
+def make_event(timing=True, external=False):
+    import torch
+    if external:
+        return torch.cuda.Event(enable_timing=timing, external=True)
+    return torch.cuda.Event(enable_timing=timing)
+
+
+def bench_mq(args, ws_, rank, local) -> dict | None:
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(ws_, "nccl")
+    from quant_quantized_gemv_gb300 import build as _b
+    if rank == 0 or ws_ == 1:
+        _b.build()
+    if dist is not None:
+        dist.barrier()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    wl = DeviceWorkload(args.workload, dev, l2)
+    n_graphs = max(wl.n_copies, 16)
+
+    # ---- capture one graph per step slot; external events bracket each GEMV
+    external = True
+    graphs, evs = [], []
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        wl.run(0)                                   # first launches outside capture
+    torch.cuda.synchronize()
+    for i in range(n_graphs):
+        try:
+            e = [(make_event(external=external), make_event(external=external)) for _ in range(wl.n_gemv)]
+        except TypeError:
+            external, e = False, None
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            wl.run(i, e if external else None)
+        graphs.append(g)
+        evs.append(e)
+    torch.cuda.synchronize()
+
+    # ---- warm-up, then a clock-sampled window: soak / timed K steps / soak
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % n_graphs].replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local) if rank == 0 or ws_ == 1 else None
+    t_win0 = time.perf_counter()
+
+    def soak(seconds):
+        t_end = time.perf_counter() + seconds
+        i = 0
+        with torch.cuda.stream(stream):
+            while time.perf_counter() < t_end:
+                for _ in range(64):
+                    graphs[i % n_graphs].replay()
+                    i += 1
+                torch.cuda.synchronize()
+
+    soak(args.soak)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start, stop = make_event(), make_event()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(args.steps):
+            graphs[i % n_graphs].replay()
+        stop.record(stream)
+    stop.synchronize()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    ms_total = start.elapsed_time(stop)
+    t_timed1 = time.perf_counter()
+    # per-GEMV durations of the last replay of every graph slot (the final
+    # n_graphs steps of the timed region)
+    gemv_ms = None
+    if external:
+        per_slot = []
+        for i in range(n_graphs):
+            if i >= args.steps:
+                continue
+            per_slot.append([a.elapsed_time(b) for a, b in evs[i]])
+        if per_slot:
+            gemv_ms = np.array(per_slot).mean(0)
+    soak(args.soak)
+    t_win1 = time.perf_counter()
+    if sampler is not None:
+        sampler.stop()
+    max_ms = reduce_max(ms_total, dist)
+    ms_per_step = max_ms / args.steps
+
+    # ---- e2e: the public API, pinned host inputs in, result out, every step
+    out_host = torch.empty(wl.output.numel(), dtype=torch.float32).pin_memory()
+    h2d = sum(h.numel() * h.element_size() for _, h in wl.inputs)
+    d2h = out_host.numel() * 4
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            for d_, h_ in wl.inputs:
+                d_.copy_(h_, non_blocking=True)
+            wl.run(i)
+            out_host.copy_(wl.output, non_blocking=True)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            for d_, h_ in wl.inputs:
+                d_.copy_(h_, non_blocking=True)
+            wl.run(i)
+            out_host.copy_(wl.output, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max((time.perf_counter() - t0) * 1e3, dist) / e2e_steps
+
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_peak_gbs()
+    value = weak_scaling_value(wl.weight_bytes, args.steps, max_ms, ws_)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws_,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "i8", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCR[args.workload]}",
+                   "weight_content_bytes_per_step": wl.weight_bytes,
+                   "gemvs_per_step": wl.n_gemv,
+                   "l2": f"{wl.n_copies} rotated weight copies "
+                         f"({wl.n_copies * wl.weight_bytes / 1e6:.0f} MB >= 4 x L2 {l2 / 1e6:.0f} MB)",
+                   "timing": "CUDA graph per step, CUDA events on the launching stream",
+                   "parallelism": f"replicas{ws_}" if ws_ > 1 else "single GPU"},
+        "compute": "int8 x (6-bit|4-bit) dp4a dots, int32 sub-block sums, f32 scale combine",
+        "pct_of_hbm_peak": round(100 * value / ws_ / peak, 2),
+    }
+    if gemv_ms is not None:
+        gsum_ms = float(gemv_ms.sum())
+        alg = float(sum(wl.gemv_bytes))
+        achieved = alg / (gsum_ms * 1e-3) / 1e9
+        traffic = profiled_traffic(args.workload) if wl.n_gemv == 1 else None
+        line["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                            "unit": "GB/s", "frac": round(achieved / peak, 4),
+                            "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs (copy)",
+                            "algorithmic_bytes_per_step": int(alg),
+                            "kernel": "gemv_kernel (q6_K/q4_K x q8)",
+                            "gemv_us_per_step": round(gsum_ms * 1e3, 3),
+                            "samples": int(min(n_graphs, args.steps))}
+        line["kernel_us"] = {"gemv_total": round(gsum_ms * 1e3, 3),
+                             "rest_of_step": round(ms_per_step * 1e3 - gsum_ms * 1e3, 3)}
+    line["e2e"] = {"value": round(wl.weight_bytes / (e2e_ms * 1e-3) / 1e9 * ws_, 2), "unit": "GB/s",
+                   "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
+                   "d2h_bytes_per_step": int(d2h),
+                   "how": "eager Python API calls per step: pinned H2D inputs, producers + GEMVs, "
+                          "D2H of the last GEMV output; wall clock, synchronize at both ends"}
+    line["gpu_launches"] = wl.n_kernels * args.steps
+    clocks = sampler.summary(t_win0, t_win1) if sampler else None
+    line["clocks"] = clocks or {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+    line["clocks_window"] = (f"{args.soak:.1f}s soak + timed steps + {args.soak:.1f}s soak of the same "
+                             f"graphs ({(t_timed1 - t_win0):.2f}s to end of timed region)")
+    if ws_ == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+    return line
+
+
+# ---------------------------------------------------------------- oracle (CPU) legs
+def oracle_sample(workload: str, rows_cap: int):
+    """Host inputs for the oracle: each GEMV of the workload truncated to its
+    first rows_cap rows, with its producer's f32 inputs."""
+    wl = synth.WORKLOADS[workload]
+    g = synth.rng("bench", workload)
+    items, seen = [], {}
+    for gname, fmt, rows, cols, producer in wl.gemvs:
+        key = (fmt, rows, cols)
+        if key in seen:
+            continue
+        r = min(rows, rows_cap)
+        W = synth.blocks(fmt, g, rows, cols)[:r].copy()
+        if producer == "rms":
+            inp = (synth.normal(g, cols), synth.normal(g, cols, 1.0, 0.1))
+        elif producer == "swiglu":
+            inp = (synth.normal(g, cols), synth.normal(g, cols))
+        else:
+            inp = (synth.normal(g, cols),)
+        seen[key] = True
+        items.append((fmt, r, cols, producer, W, inp))
+    return items
+
+
+def oracle_step(items):
+    import oracle
+    nbytes = 0
+    for fmt, r, cols, producer, W, inp in items:
+        if producer == "rms":
+            x = oracle.rmsnorm(inp[0], inp[1], 1e-6).astype(np.float32)
+        elif producer == "swiglu":
+            x = oracle.swiglu(inp[0], inp[1]).astype(np.float32)
+        else:
+            x = inp[0]
+        d, q, _ = oracle.quantize_q8(x)
+        oracle.gemv(fmt, W, d, q, r, cols)
+        nbytes += W.nbytes
+    return nbytes
+
+
+def cpu_baseline(workload: str, seconds: float) -> dict:
+    items = oracle_sample(workload, 512)
+    oracle_step(items)                                   # warm (page-in, build)
+    done, t0 = 0, time.perf_counter()
+    n = 0
+    while True:
+        done += oracle_step(items)
+        n += 1
+        if time.perf_counter() - t0 >= seconds or n >= 10000:
+            break
+    dt = time.perf_counter() - t0
+    rows = ", ".join(f"{fmt} {r}x{cols}" for fmt, r, cols, _, _, _ in items)
+    return {"value": round(done / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} passes over the first <=512 rows of each distinct GEMV ({rows}) with "
+                      f"its producer, single-threaded C oracle, {dt:.1f} s"}
+
+
+def bench_reference(args, ws_, rank) -> dict | None:
+    if rank != 0:
+        return None
+    items = oracle_sample(args.workload, 512)
+    for _ in range(args.warmup):
+        oracle_step(items)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        nbytes += oracle_step(items)
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    rows = ", ".join(f"{fmt} {r}x{cols}" for fmt, r, cols, _, _, _ in items)
+    sample = f"each step: the first <=512 rows of each distinct GEMV ({rows}) with its producer"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "i8", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {DESCR[args.workload]}", "sample": sample},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="mq", choices=["mq", "reference"])
+    ap.add_argument("--workload", default="ffn_down_7b", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--soak", type=float, default=0.6, help="seconds of identical load around the timed steps")
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+    ws_, rank, local = dist_env()
+    if args.impl == "reference":
+        line = bench_reference(args, ws_, rank)
+    else:
+        line = bench_mq(args, ws_, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+/*
+ * mq.h -- C ABI of the GB300 (sm_103a) k-quant batch-1 decode GEMV library.
+ *
+ * What it computes (the minfer engineering log, cited by page and section):
+ *   "76 · D4-4 — dpl dense split-plane q6_K decode MMVQ"      [D4-4]
+ *   "74 · D4-2 — B0 latent correctness fix"                   [D4-2]
+ *   "67 · D3 — 14B decode attribution / bitwise MMVQ"         [D3]
+ *   "70 · D3-5 — fused-producer decode A-quantize"            [D3-5]
+ * y = W x_hat, W a k-quantized matrix (GGUF q6_K or q4_K super-blocks of 256
+ * weights), x_hat an activation row quantized to int8 in 32-value blocks
+ * (the q8 plane), computed with integer sub-block dot products and an f32
+ * scale combine.  The q8 plane is written by one of three producers.
+ *
+ * Conventions for every entry point:
+ *   - All pointers are owned by the caller.  The library allocates and frees
+ *     nothing.  "device" pointers must be CUDA device (or managed) memory of
+ *     the current device; "host" pointers are ordinary host memory.
+ *   - GPU entry points are asynchronous on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) and return after the launch.
+ *   - Every call validates its arguments before launching anything and
+ *     returns an mq_status: MQ_OK, or an error with nothing launched, or
+ *     MQ_ERR_CUDA when the launch itself failed (cudaGetLastError()).
+ *   - Shapes: cols % 256 == 0 (whole super-blocks, the gate of [D4-4] §3.1),
+ *     n % 32 == 0 for the producers ([D3-5] §3.1), rows >= 1, all sizes
+ *     below 2^31 elements.
+ *   - Alignment: every device pointer must be 16-byte aligned (the vector
+ *     loads of [D4-4] §3.3 "the dpl row base is not naturally 16B aligned").
+ *   - Not thread-safe for the same workspace: calls that share a workspace
+ *     must be ordered on one stream.
+ */
+#ifndef MQ_H
+#define MQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MQ_OK = 0,
+    MQ_ERR_SHAPE = 1,      /* a size breaks the shape rules above            */
+    MQ_ERR_ALIGN = 2,      /* a device pointer is not 16-byte aligned         */
+    MQ_ERR_NULL = 3,       /* a required pointer is NULL                      */
+    MQ_ERR_COVERAGE = 4,   /* a dispatch plan would leave work uncovered or
+                              cover it twice; nothing was launched ([D4-2] §6
+                              lesson 1: a gate must bound both sides)         */
+    MQ_ERR_WORKSPACE = 5,  /* split-K needs a larger workspace               */
+    MQ_ERR_CUDA = 6        /* the CUDA launch failed                          */
+} mq_status;
+
+/* Static message for a status code. */
+const char *mq_strerror(int status);
+
+/* Library version string. */
+const char *mq_version(void);
+
+/* ------------------------------------------------------------------------
+ * Weight repack (host, once at load).  [D4-4] §2-§3.1: the GGUF q6_K block
+ * (210 B: ql 128 | qh 64 | sc 16 | d 2) is rearranged once so that every byte
+ * a decode GEMV streams from HBM is content.  The repacked form here groups
+ * rows in tiles of 8 and columns in chunks of 4 super-blocks and stores each
+ * tile-chunk as planes in the order the kernel's lanes read them; it is a
+ * lossless permutation of the block's bits (exactly rows*cols/256 * 210 B of
+ * content; rows are padded to a multiple of 8 with zero rows, which decode to
+ * zero).  q4_K (144 B: d | dmin | scales 12 | qs 128, the GGUF q4_K block) is
+ * treated the same way.  The repacked layout is private to this library.
+ *
+ * mq_repacked_bytes_*: bytes of the repacked matrix (0 on a bad shape).
+ * mq_repack_*:   gguf (host, rows x cols/256 blocks, row-major, GGUF order)
+ *                -> dst (host, mq_repacked_bytes_* bytes).  Overwrites dst.
+ * mq_unrepack_*: the exact inverse: dst -> gguf.  Used to prove the repack is
+ *                a permutation (round trip is the identity).
+ * Errors: MQ_ERR_NULL, MQ_ERR_SHAPE.  Host only, synchronous, thread-safe.
+ * ------------------------------------------------------------------------ */
+size_t mq_repacked_bytes_q6k(int rows, int cols);
+size_t mq_repacked_bytes_q4k(int rows, int cols);
+int mq_repack_q6k(const void *gguf, void *dst, int rows, int cols);
+int mq_repack_q4k(const void *gguf, void *dst, int rows, int cols);
+int mq_unrepack_q6k(const void *packed, void *gguf, int rows, int cols);
+int mq_unrepack_q4k(const void *packed, void *gguf, int rows, int cols);
+
+/* ------------------------------------------------------------------------
+ * The q8 activation plane ([D3-5] §3.2, the pad40 block's fields): for each
+ * block of 32 values an fp16 scale d, 32 int8 values and their int32 sum.
+ * The plane is stored split by field (qs | d | sum, each 16-byte aligned); it
+ * is opaque to callers, who size it with mq_q8_bytes and read it (for tests)
+ * with mq_q8_unpack_host.
+ *
+ * mq_q8_bytes(n): bytes of the plane for n values (0 unless n % 32 == 0).
+ * mq_q8_unpack_host: plane (host copy) -> d[n/32] (fp16 bits), qs[n],
+ *                    sum[n/32].  Any output pointer may be NULL.
+ * ------------------------------------------------------------------------ */
+size_t mq_q8_bytes(int n);
+int mq_q8_unpack_host(const void *plane, int n, uint16_t *d, int8_t *qs, int32_t *sum);
+
+/* ------------------------------------------------------------------------
+ * Producers (device).  Each writes the q8 plane of n values, quantized per
+ * 32-value block exactly as [D3-5] §3.2 prints it: am = max|v|, d = am/127,
+ * di = d != 0 ? 1/d : 0 (IEEE f32), q = clamp(rint(v * di), -128, 127)
+ * (rint rounds half to even), d stored as fp16 (round to nearest even), sum =
+ * sum of q.  The q8 bytes are a per-element function of the f32 values that
+ * were quantized ([D3-5] §2.3), so a fused producer's plane equals the
+ * standalone quantizer applied to the f32 output it wrote.
+ *
+ * mq_quantize_q8:      x[n] (device f32) -> q8.
+ * mq_rmsnorm_quant_q8: y = x / sqrt(mean(x^2) + eps) * gain (f32; the rms arm
+ *                      of [D3-5] §3.2, body not printed there), writes y[n]
+ *                      (device f32) and q8.  One row; y must not alias x or
+ *                      gain.
+ * mq_swiglu_quant_q8:  y = (g / (1 + exp(-g))) * u ([D3-5] §3.2), writes y[n]
+ *                      and q8.  g, u, y device f32; y may alias g or u.
+ * Errors: MQ_ERR_NULL, MQ_ERR_SHAPE (n <= 0 or n % 32), MQ_ERR_ALIGN,
+ *         MQ_ERR_CUDA.
+ * ------------------------------------------------------------------------ */
+int mq_quantize_q8(const float *x, void *q8, int n, void *stream);
+int mq_rmsnorm_quant_q8(const float *x, const float *gain, float eps, float *y, void *q8,
+                        int n, void *stream);
+int mq_swiglu_quant_q8(const float *g, const float *u, float *y, void *q8, int n, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Decode GEMV (device): y[rows] = W x_hat.
+ *   q6_K ([D4-2] §3.2 Excerpt C): y_r = sum over blocks b and 16-weight
+ *        sub-blocks s of f16(d_b) * sc_s * f16(d8) * isum_s,
+ *        isum_s = sum (q - 32) * q8 (int32).
+ *   q4_K: y_r = sum over 32-weight sub-blocks k of
+ *        f16(d8_k) * (f16(d) * sc_k * isum_k - f16(dmin) * m_k * qsum_k),
+ *        isum_k = sum q * q8, qsum_k = the q8 block's sum.
+ * Wp: repacked weights (device, mq_repack_* output).  q8: plane of cols
+ * values (device).  y: rows f32 (device).  The f32 combine order is fixed
+ * (ascending chunks within a split, a fixed butterfly across lanes, splits
+ * summed in ascending order), so results are deterministic run to run.
+ *
+ * Rows are cut into tiles of 8 and each tile's columns into S contiguous
+ * ranges of 4-super-block chunks ("split-K", [D4-2] §2's tall-row case).
+ * When S > 1 each split writes 8 partial sums to `ws` and the last split of a
+ * tile to finish adds the S partials in ascending order; nothing spins.  The
+ * host checks before launch that the splits cover every chunk exactly once
+ * (MQ_ERR_COVERAGE otherwise).
+ *
+ * mq_gemv_workspace_bytes(rows, cols): workspace the plan on the current
+ *   device needs (0 when S == 1).  ws must be device memory, zero-filled
+ *   before its first use; every completed call leaves it zero-filled again.
+ * mq_gemv_splits(rows, cols): the S the plan picks on the current device
+ *   (it uses ceil(nchunks / S) chunks per split, nchunks = ceil(cols/1024)).
+ * mq_gemv_*_q8_plan: the same GEMV with an explicit plan (S, chunks per
+ *   split); the coverage check is the only thing between a wrong plan and
+ *   dropped work, and it rejects the plan with MQ_ERR_COVERAGE.
+ * Errors: MQ_ERR_NULL, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_WORKSPACE,
+ *         MQ_ERR_COVERAGE, MQ_ERR_CUDA.
+ * ------------------------------------------------------------------------ */
+size_t mq_gemv_workspace_bytes(int rows, int cols);
+int mq_gemv_splits(int rows, int cols);
+int mq_gemv_q6k_q8(const void *Wp, const void *q8, float *y, int rows, int cols, void *ws,
+                   size_t ws_bytes, void *stream);
+int mq_gemv_q4k_q8(const void *Wp, const void *q8, float *y, int rows, int cols, void *ws,
+                   size_t ws_bytes, void *stream);
+int mq_gemv_q6k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int cols,
+                        int splits, int chunks_per_split, void *ws, size_t ws_bytes,
+                        void *stream);
+int mq_gemv_q4k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int cols,
+                        int splits, int chunks_per_split, void *ws, size_t ws_bytes,
+                        void *stream);
+/* Workspace for an explicit split count (0 when splits == 1). */
+size_t mq_gemv_workspace_bytes_for(int rows, int splits);
+
+/* The plan the dispatch would pick for (rows, cols) on a device with `sms`
+ * streaming multiprocessors: writes S and chunks per split.  Host only. */
+int mq_gemv_plan_for(int rows, int cols, int sms, int *splits, int *chunks_per_split);
+
+/* Coverage check used by every GEMV dispatch, exposed for tests: returns
+ * MQ_OK iff splits * chunks_per_split >= nchunks (nothing dropped) and
+ * (splits - 1) * chunks_per_split < nchunks (no empty split), all >= 1. */
+int mq_check_coverage(int nchunks, int splits, int chunks_per_split);
+
+/* ------------------------------------------------------------------------
+ * Integer sub-block dots (device), for bit-exact testing of the GEMV's
+ * integer path: the same kernel and lane mapping as the GEMV, writing
+ * isums[r][b][s] (int32) instead of accumulating: 16 per block (q6_K,
+ * isum_s = sum (q - 32) * q8) or 8 per block (q4_K, isum_k = sum q * q8).
+ * isums: rows * cols/256 * {16, 8} int32 (device).
+ * ------------------------------------------------------------------------ */
+int mq_gemv_q6k_q8_subdots(const void *Wp, const void *q8, int32_t *isums, int rows, int cols,
+                           void *stream);
+int mq_gemv_q4k_q8_subdots(const void *Wp, const void *q8, int32_t *isums, int rows, int cols,
+                           void *stream);
+
+/* Number of streaming multiprocessors of the current device (0 on error);
+ * the dispatch plan sizes its grid from it. */
+int mq_device_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MQ_H */

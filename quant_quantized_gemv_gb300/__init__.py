@@ -1,0 +1,299 @@
+"""GB300-native k-quant batch-1 decode GEMV (q6_K / q4_K x q8) and its q8
+producers, behind the C ABI of include/mq.h (libmq.so, built in-tree).
+
+This module is a thin binding: the functions carry the C entry points' names
+and only marshal arguments (torch tensors -> pointers, the current CUDA
+stream).  Every step of the path runs in the library's CUDA kernels; there is
+no CPU or PyTorch fallback, and a missing library raises.
+
+Typical decode use:
+    Wp  = to_device(mq_repack_q6k(gguf_rows, rows, cols))   # once, at load
+    ws  = mq_gemv_workspace(rows, cols)                      # once, zeroed
+    y, q8 = mq_swiglu_quant_q8(g, u)                         # producer
+    out = mq_gemv_q6k_q8(Wp, q8, rows, cols, ws=ws)          # GEMV
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_SO = os.path.join(_PKG, "_build", "libmq.so")
+_lib = None
+
+MQ_OK, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_NULL, MQ_ERR_COVERAGE, MQ_ERR_WORKSPACE, MQ_ERR_CUDA = range(7)
+
+# every symbol include/mq.h declares
+EXPORTS = [
+    "mq_strerror", "mq_version", "mq_repacked_bytes_q6k", "mq_repacked_bytes_q4k",
+    "mq_repack_q6k", "mq_repack_q4k", "mq_unrepack_q6k", "mq_unrepack_q4k", "mq_q8_bytes",
+    "mq_q8_unpack_host", "mq_quantize_q8", "mq_rmsnorm_quant_q8", "mq_swiglu_quant_q8",
+    "mq_gemv_workspace_bytes", "mq_gemv_splits", "mq_gemv_q6k_q8", "mq_gemv_q4k_q8",
+    "mq_gemv_q6k_q8_plan", "mq_gemv_q4k_q8_plan", "mq_gemv_workspace_bytes_for",
+    "mq_check_coverage", "mq_gemv_plan_for", "mq_gemv_q6k_q8_subdots", "mq_gemv_q4k_q8_subdots", "mq_device_sms",
+]
+
+
+class MQError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {lib().mq_strerror(status).decode()} (status {status})")
+
+
+def library_path() -> str:
+    return _SO
+
+
+def lib():
+    """Load libmq.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_SO):
+        raise RuntimeError(f"{_SO} is missing: build it with "
+                           "`python -m quant_quantized_gemv_gb300.build` (or __graft_entry__.build())")
+    L = ctypes.CDLL(_SO)
+    P, I, S, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+    sig = {
+        "mq_strerror": ([I], ctypes.c_char_p),
+        "mq_version": ([], ctypes.c_char_p),
+        "mq_repacked_bytes_q6k": ([I, I], S),
+        "mq_repacked_bytes_q4k": ([I, I], S),
+        "mq_repack_q6k": ([P, P, I, I], I),
+        "mq_repack_q4k": ([P, P, I, I], I),
+        "mq_unrepack_q6k": ([P, P, I, I], I),
+        "mq_unrepack_q4k": ([P, P, I, I], I),
+        "mq_q8_bytes": ([I], S),
+        "mq_q8_unpack_host": ([P, I, P, P, P], I),
+        "mq_quantize_q8": ([P, P, I, P], I),
+        "mq_rmsnorm_quant_q8": ([P, P, F, P, P, I, P], I),
+        "mq_swiglu_quant_q8": ([P, P, P, P, I, P], I),
+        "mq_gemv_workspace_bytes": ([I, I], S),
+        "mq_gemv_splits": ([I, I], I),
+        "mq_gemv_q6k_q8": ([P, P, P, I, I, P, S, P], I),
+        "mq_gemv_q4k_q8": ([P, P, P, I, I, P, S, P], I),
+        "mq_gemv_q6k_q8_plan": ([P, P, P, I, I, I, I, P, S, P], I),
+        "mq_gemv_q4k_q8_plan": ([P, P, P, I, I, I, I, P, S, P], I),
+        "mq_gemv_workspace_bytes_for": ([I, I], S),
+        "mq_check_coverage": ([I, I, I], I),
+        "mq_gemv_plan_for": ([I, I, I, P, P], I),
+        "mq_gemv_q6k_q8_subdots": ([P, P, P, I, I, P], I),
+        "mq_gemv_q4k_q8_subdots": ([P, P, P, I, I, P], I),
+        "mq_device_sms": ([], I),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = L
+    return L
+
+
+def _check(status: int, where: str):
+    if status != MQ_OK:
+        raise MQError(status, where)
+
+
+# ------------------------------------------------------------------ helpers
+def _np_ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _dev(t, dtype=None):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("expected a CUDA tensor (the library has no CPU path)")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ------------------------------------------------------------------ repack (host)
+def mq_repacked_bytes_q6k(rows: int, cols: int) -> int:
+    return lib().mq_repacked_bytes_q6k(rows, cols)
+
+
+def mq_repacked_bytes_q4k(rows: int, cols: int) -> int:
+    return lib().mq_repacked_bytes_q4k(rows, cols)
+
+
+def _repack(fn, size_fn, gguf: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    gguf = np.ascontiguousarray(gguf, dtype=np.uint8)
+    out = np.empty(size_fn(rows, cols), np.uint8)
+    _check(fn(_np_ptr(gguf), _np_ptr(out), rows, cols), fn.__name__)
+    return out
+
+
+def mq_repack_q6k(gguf: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    """GGUF q6_K rows (host) -> repacked bytes (host numpy)."""
+    return _repack(lib().mq_repack_q6k, mq_repacked_bytes_q6k, gguf, rows, cols)
+
+
+def mq_repack_q4k(gguf: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    return _repack(lib().mq_repack_q4k, mq_repacked_bytes_q4k, gguf, rows, cols)
+
+
+def mq_unrepack_q6k(packed: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    out = np.empty(rows * (cols // 256) * 210, np.uint8)
+    _check(lib().mq_unrepack_q6k(_np_ptr(packed), _np_ptr(out), rows, cols), "mq_unrepack_q6k")
+    return out.reshape(rows, -1)
+
+
+def mq_unrepack_q4k(packed: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    out = np.empty(rows * (cols // 256) * 144, np.uint8)
+    _check(lib().mq_unrepack_q4k(_np_ptr(packed), _np_ptr(out), rows, cols), "mq_unrepack_q4k")
+    return out.reshape(rows, -1)
+
+
+# ------------------------------------------------------------------ q8 plane
+def mq_q8_bytes(n: int) -> int:
+    return lib().mq_q8_bytes(n)
+
+
+def mq_q8_unpack_host(plane: np.ndarray, n: int):
+    """Host copy of a q8 plane -> (d fp16 bits [n/32], qs int8 [n], sum int32 [n/32])."""
+    plane = np.ascontiguousarray(plane, dtype=np.uint8)
+    d = np.empty(n // 32, np.uint16)
+    qs = np.empty(n, np.int8)
+    s = np.empty(n // 32, np.int32)
+    _check(lib().mq_q8_unpack_host(_np_ptr(plane), n, _np_ptr(d), _np_ptr(qs), _np_ptr(s)),
+           "mq_q8_unpack_host")
+    return d, qs, s
+
+
+def _q8_out(n: int, like, q8):
+    import torch
+    if q8 is None:
+        q8 = torch.empty(mq_q8_bytes(n), dtype=torch.uint8, device=like.device)
+    return q8
+
+
+# ------------------------------------------------------------------ producers
+def mq_quantize_q8(x, q8=None, stream=None):
+    import torch
+    n = x.numel()
+    q8 = _q8_out(n, x, q8)
+    _check(lib().mq_quantize_q8(_dev(x, torch.float32), _dev(q8), n, _stream(stream)),
+           "mq_quantize_q8")
+    return q8
+
+
+def mq_rmsnorm_quant_q8(x, gain, eps: float, y=None, q8=None, stream=None):
+    import torch
+    n = x.numel()
+    y = torch.empty_like(x) if y is None else y
+    q8 = _q8_out(n, x, q8)
+    _check(lib().mq_rmsnorm_quant_q8(_dev(x, torch.float32), _dev(gain, torch.float32), float(eps),
+                                     _dev(y, torch.float32), _dev(q8), n, _stream(stream)),
+           "mq_rmsnorm_quant_q8")
+    return y, q8
+
+
+def mq_swiglu_quant_q8(g, u, y=None, q8=None, stream=None):
+    import torch
+    n = g.numel()
+    y = torch.empty_like(g) if y is None else y
+    q8 = _q8_out(n, g, q8)
+    _check(lib().mq_swiglu_quant_q8(_dev(g, torch.float32), _dev(u, torch.float32),
+                                    _dev(y, torch.float32), _dev(q8), n, _stream(stream)),
+           "mq_swiglu_quant_q8")
+    return y, q8
+
+
+# ------------------------------------------------------------------ GEMV
+def mq_gemv_workspace_bytes(rows: int, cols: int) -> int:
+    return lib().mq_gemv_workspace_bytes(rows, cols)
+
+
+def mq_gemv_workspace_bytes_for(rows: int, splits: int) -> int:
+    return lib().mq_gemv_workspace_bytes_for(rows, splits)
+
+
+def mq_gemv_splits(rows: int, cols: int) -> int:
+    return lib().mq_gemv_splits(rows, cols)
+
+
+def mq_check_coverage(nchunks: int, splits: int, chunks_per_split: int) -> int:
+    return lib().mq_check_coverage(nchunks, splits, chunks_per_split)
+
+
+def mq_gemv_plan_for(rows: int, cols: int, sms: int):
+    """(splits, chunks_per_split) the dispatch picks on a device with `sms` SMs."""
+    s, c = ctypes.c_int(), ctypes.c_int()
+    _check(lib().mq_gemv_plan_for(rows, cols, sms, ctypes.byref(s), ctypes.byref(c)),
+           "mq_gemv_plan_for")
+    return s.value, c.value
+
+
+def mq_device_sms() -> int:
+    return lib().mq_device_sms()
+
+
+def mq_gemv_workspace(rows: int, cols: int, splits: int | None = None, device=None):
+    """A zero-filled split-K workspace for (rows, cols) (None when not needed)."""
+    import torch
+    nbytes = (mq_gemv_workspace_bytes(rows, cols) if splits is None
+              else mq_gemv_workspace_bytes_for(rows, splits))
+    if nbytes == 0:
+        return None
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def _ws_args(ws):
+    if ws is None:
+        return ctypes.c_void_p(0), 0
+    return _dev(ws), ws.numel() * ws.element_size()
+
+
+def _gemv(name: str, Wp, q8, rows: int, cols: int, y, ws, stream, plan=None):
+    import torch
+    y = torch.empty(rows, dtype=torch.float32, device=Wp.device) if y is None else y
+    wsp, wsb = _ws_args(ws)
+    L = lib()
+    if plan is None:
+        st = getattr(L, name)(_dev(Wp), _dev(q8), _dev(y, torch.float32), rows, cols, wsp, wsb,
+                              _stream(stream))
+    else:
+        st = getattr(L, name + "_plan")(_dev(Wp), _dev(q8), _dev(y, torch.float32), rows, cols,
+                                        int(plan[0]), int(plan[1]), wsp, wsb, _stream(stream))
+    _check(st, name)
+    return y
+
+
+def mq_gemv_q6k_q8(Wp, q8, rows: int, cols: int, y=None, ws=None, stream=None, plan=None):
+    """y = W x_hat for repacked q6_K weights Wp (device) and a q8 plane."""
+    return _gemv("mq_gemv_q6k_q8", Wp, q8, rows, cols, y, ws, stream, plan)
+
+
+def mq_gemv_q4k_q8(Wp, q8, rows: int, cols: int, y=None, ws=None, stream=None, plan=None):
+    """y = W x_hat for repacked q4_K weights Wp (device) and a q8 plane."""
+    return _gemv("mq_gemv_q4k_q8", Wp, q8, rows, cols, y, ws, stream, plan)
+
+
+def _subdots(name: str, per: int, Wp, q8, rows: int, cols: int, stream):
+    import torch
+    out = torch.empty(rows * (cols // 256) * per, dtype=torch.int32, device=Wp.device)
+    _check(getattr(lib(), name)(_dev(Wp), _dev(q8), _dev(out), rows, cols, _stream(stream)), name)
+    return out.view(rows, cols // 256, per)
+
+
+def mq_gemv_q6k_q8_subdots(Wp, q8, rows: int, cols: int, stream=None):
+    """Integer sub-block dots rows x nb x 16 (int32) through the GEMV's lane mapping."""
+    return _subdots("mq_gemv_q6k_q8_subdots", 16, Wp, q8, rows, cols, stream)
+
+
+def mq_gemv_q4k_q8_subdots(Wp, q8, rows: int, cols: int, stream=None):
+    return _subdots("mq_gemv_q4k_q8_subdots", 8, Wp, q8, rows, cols, stream)

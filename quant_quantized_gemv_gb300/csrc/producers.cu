@@ -1,0 +1,183 @@
+// producers.cu -- the q8 activation producers for sm_103a: standalone
+// quantize, rms_norm -> q8 and SwiGLU -> q8 (page "70 · D3-5 — fused-producer
+// decode A-quantize", §2-§3).
+//
+// Quantization (§3.2 of that page, per 32-value block): am = max|v|,
+// d = am / 127, di = d != 0 ? 1/d : 0, q = clamp(rint(v * di), -128, 127),
+// fp16(d) stored, sum of q stored.  Built without fast-math, so the division,
+// the reciprocal and the rounding are IEEE f32 exactly as the host computes
+// them.  Here 8 consecutive lanes share a block (4 values each, one float4
+// load): the max and the sum are taken with 3 xor-shuffles, which is exact for
+// both (max is associative; integer addition too), so the bytes do not
+// depend on the thread geometry.  Shuffles run on every lane unconditionally
+// and only loads/stores are guarded (the page's §3.3 barrier pitfall).
+//
+// The fused producers quantize the f32 values they have just computed, in
+// registers, so the q8 bytes are by construction the quantization of the f32
+// output they write (the page's "constructive bitwise", §2.3).
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+
+namespace mq {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ int q8_code(float v, float di)
+{
+    int q = __float2int_rn(v * di);  // round half to even, like rintf
+    return max(-128, min(127, q));
+}
+
+// Quantize 4 values held by this lane; 8 lanes (aligned group) form a block.
+// gid = global index of this lane's 4-value group (block = gid / 8).
+__device__ __forceinline__ void quantize4(float4 v, bool valid, long long gid, uint8_t *q8,
+                                          unsigned d_off, unsigned sum_off)
+{
+    float am = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    am = fmaxf(am, __shfl_xor_sync(kFull, am, 1));
+    am = fmaxf(am, __shfl_xor_sync(kFull, am, 2));
+    am = fmaxf(am, __shfl_xor_sync(kFull, am, 4));
+    const float d = am / 127.0f;
+    const float di = (d != 0.0f) ? 1.0f / d : 0.0f;
+    const int q0 = q8_code(v.x, di), q1 = q8_code(v.y, di);
+    const int q2 = q8_code(v.z, di), q3 = q8_code(v.w, di);
+    int s = q0 + q1 + q2 + q3;
+    s += __shfl_xor_sync(kFull, s, 1);
+    s += __shfl_xor_sync(kFull, s, 2);
+    s += __shfl_xor_sync(kFull, s, 4);
+    if (!valid) return;
+    const uint32_t packed = (uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8) |
+                            ((uint32_t)(q2 & 0xff) << 16) | ((uint32_t)(q3 & 0xff) << 24);
+    reinterpret_cast<uint32_t *>(q8)[gid] = packed;
+    if ((gid & 7) == 0) {
+        const long long b = gid >> 3;
+        reinterpret_cast<__half *>(q8 + d_off)[b] = __float2half_rn(d);
+        reinterpret_cast<int *>(q8 + sum_off)[b] = s;
+    }
+}
+
+__global__ void __launch_bounds__(256) quantize_q8_kernel(const float *__restrict__ x,
+                                                          uint8_t *__restrict__ q8, int n4,
+                                                          unsigned d_off, unsigned sum_off)
+{
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const bool valid = gid < n4;
+    const float4 v = valid ? __ldg(reinterpret_cast<const float4 *>(x) + gid)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    quantize4(v, valid, gid, q8, d_off, sum_off);
+}
+
+// y = (g / (1 + exp(-g))) * u, the swiglu body of the D3-5 page §3.2; y may
+// alias g or u (each lane reads its 4 values before writing them).
+__global__ void __launch_bounds__(256) swiglu_quant_q8_kernel(const float *g, const float *u,
+                                                              float *y, uint8_t *__restrict__ q8,
+                                                              int n4, unsigned d_off,
+                                                              unsigned sum_off)
+{
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const bool valid = gid < n4;
+    float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (valid) {
+        const float4 gv = reinterpret_cast<const float4 *>(g)[gid];
+        const float4 uv = reinterpret_cast<const float4 *>(u)[gid];
+        out.x = (gv.x / (1.0f + expf(-gv.x))) * uv.x;
+        out.y = (gv.y / (1.0f + expf(-gv.y))) * uv.y;
+        out.z = (gv.z / (1.0f + expf(-gv.z))) * uv.z;
+        out.w = (gv.w / (1.0f + expf(-gv.w))) * uv.w;
+        reinterpret_cast<float4 *>(y)[gid] = out;
+    }
+    quantize4(out, valid, gid, q8, d_off, sum_off);
+}
+
+// One row, one CTA of kRmsThreads: ss = sum x^2 (per-lane serial, then a
+// fixed shuffle tree and a fixed cross-warp order), scale = 1/sqrt(ss/n+eps)
+// (IEEE sqrt and division), y = (x * scale) * gain, then quantize.
+constexpr int kRmsThreads = 1024;
+
+__global__ void __launch_bounds__(kRmsThreads) rmsnorm_quant_q8_kernel(
+    const float *__restrict__ x, const float *__restrict__ gain, float eps, float *__restrict__ y,
+    uint8_t *__restrict__ q8, int n, unsigned d_off, unsigned sum_off)
+{
+    __shared__ float warp_ss[kRmsThreads / 32];
+    __shared__ float scale_sh;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int n4 = n >> 2;
+    const float4 *x4 = reinterpret_cast<const float4 *>(x);
+    const float4 *g4 = reinterpret_cast<const float4 *>(gain);
+
+    float ss = 0.0f;
+    for (int i = tid; i < n4; i += kRmsThreads) {
+        const float4 v = __ldg(x4 + i);
+        ss = fmaf(v.x, v.x, ss);
+        ss = fmaf(v.y, v.y, ss);
+        ss = fmaf(v.z, v.z, ss);
+        ss = fmaf(v.w, v.w, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
+    if (lane == 0) warp_ss[wid] = ss;
+    __syncthreads();
+    if (wid == 0) {
+        float t = warp_ss[lane];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+        if (lane == 0) scale_sh = 1.0f / sqrtf(t / (float)n + eps);
+    }
+    __syncthreads();
+    const float scale = scale_sh;
+
+    // Every thread runs the same number of iterations, so the quantizer's
+    // shuffles always see full warps.
+    for (int base = 0; base < n4; base += kRmsThreads) {
+        const int i = base + tid;
+        const bool valid = i < n4;
+        float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (valid) {
+            const float4 v = __ldg(x4 + i);
+            const float4 gv = __ldg(g4 + i);
+            out.x = (v.x * scale) * gv.x;
+            out.y = (v.y * scale) * gv.y;
+            out.z = (v.z * scale) * gv.z;
+            out.w = (v.w * scale) * gv.w;
+            reinterpret_cast<float4 *>(y)[i] = out;
+        }
+        quantize4(out, valid, i, q8, d_off, sum_off);
+    }
+}
+
+inline unsigned blocks_for(long long threads, int per_block)
+{
+    return (unsigned)((threads + per_block - 1) / per_block);
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_q8(const float *x, uint8_t *q8, int n, unsigned d_off,
+                               unsigned sum_off, cudaStream_t st)
+{
+    const int n4 = n / 4;
+    quantize_q8_kernel<<<blocks_for(n4, 256), 256, 0, st>>>(x, q8, n4, d_off, sum_off);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_quant_q8(const float *g, const float *u, float *y, uint8_t *q8, int n,
+                                   unsigned d_off, unsigned sum_off, cudaStream_t st)
+{
+    const int n4 = n / 4;
+    swiglu_quant_q8_kernel<<<blocks_for(n4, 256), 256, 0, st>>>(g, u, y, q8, n4, d_off, sum_off);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_quant_q8(const float *x, const float *gain, float eps, float *y,
+                                    uint8_t *q8, int n, unsigned d_off, unsigned sum_off,
+                                    cudaStream_t st)
+{
+    rmsnorm_quant_q8_kernel<<<1, kRmsThreads, 0, st>>>(x, gain, eps, y, q8, n, d_off, sum_off);
+    return cudaGetLastError();
+}
+
+}  // namespace mq

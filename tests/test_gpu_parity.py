@@ -1,0 +1,277 @@
+"""Parity of the CUDA path (through the C ABI) against the oracle.
+
+Bar (written here, from the arithmetic of the method):
+  * q8 planes, integer sub-block dots: bit-exact.
+  * f32 GEMV outputs: |y_gpu - y_oracle| <= 1e-4 * sum_terms |term| per row.
+  * f32 producer outputs: |y_gpu - y_oracle| <= 1e-4 * |y_oracle| per element
+    (+1e-30 absolute for exact zeros).
+A fused producer's q8 must equal the oracle quantizer applied to the f32
+output the producer wrote (the q8 bytes are a per-element function of it).
+"""
+import numpy as np
+import pytest
+
+import synth
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def mq():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quant_quantized_gemv_gb300 import build
+    build.build()
+    import quant_quantized_gemv_gb300 as m
+    m.lib()
+    return m
+
+
+def dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    import torch
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def repack_dev(mq, fmt, W, rows, cols):
+    rep = mq.mq_repack_q6k if fmt == "q6k" else mq.mq_repack_q4k
+    return dev(rep(W, rows, cols))
+
+
+def q8_fields(mq, plane, n):
+    return mq.mq_q8_unpack_host(host(plane), n)
+
+
+def gemv(mq, fmt, Wp, q8, rows, cols, plan=None, ws=None):
+    if plan is not None and plan[0] > 1 and ws is None:
+        ws = mq.mq_gemv_workspace(rows, cols, splits=plan[0])
+    elif plan is None and ws is None:
+        ws = mq.mq_gemv_workspace(rows, cols)
+    fn = mq.mq_gemv_q6k_q8 if fmt == "q6k" else mq.mq_gemv_q4k_q8
+    return fn(Wp, q8, rows, cols, ws=ws, plan=plan)
+
+
+def assert_gemv_close(y, yref, absum):
+    err = np.abs(y.astype(np.float64) - yref)
+    bad = err > TOL * absum
+    assert not bad.any(), f"{bad.sum()} rows out of tolerance; worst {np.max(err / np.maximum(absum, 1e-300))}"
+
+
+def special_activation(n, seed):
+    """N(0,1) with hand-placed blocks: zeros, exact ties, one-hots, tiny and
+    huge scales (subnormal and large fp16 d)."""
+    g = synth.rng("act", seed, n)
+    x = synth.normal(g, n)
+    nb = n // 32
+    if nb >= 6:
+        x[0:32] = 0.0
+        x[32:64] = 0.0
+        x[32:42] = [127, 2.5, 3.5, -2.5, 0.5, 1.5, -0.5, 126.5, -3.5, 5.5]
+        x[64:96] = 0.0
+        x[64 + 7] = -1.0
+        x[96:128] *= np.float32(1e-4)
+        x[128:160] *= np.float32(3e3)
+    return x
+
+
+# ------------------------------------------------------------------ producers
+@pytest.mark.parametrize("n", [32, 96, 2048, 4128, 18944])
+def test_quantize_q8_bit_exact(mq, orc, n):
+    x = special_activation(n, "quant")
+    plane = mq.mq_quantize_q8(dev(x))
+    d, q, s = q8_fields(mq, plane, n)
+    d0, q0, s0 = orc.quantize_q8(x)
+    assert np.array_equal(d, d0) and np.array_equal(q, q0) and np.array_equal(s, s0)
+
+
+@pytest.mark.parametrize("n", [64, 5120, 13824, 18944])
+def test_swiglu_quant_q8(mq, orc, n):
+    g = synth.rng("swiglu", n)
+    gv = synth.normal(g, n)
+    uv = synth.normal(g, n)
+    y, plane = mq.mq_swiglu_quant_q8(dev(gv), dev(uv))
+    yh = host(y)
+    yref = orc.swiglu(gv, uv)
+    assert np.all(np.abs(yh - yref) <= TOL * np.abs(yref) + 1e-30)
+    d, q, s = q8_fields(mq, plane, n)
+    d0, q0, s0 = orc.quantize_q8(yh)          # the plane is the quantization of y as written
+    assert np.array_equal(d, d0) and np.array_equal(q, q0) and np.array_equal(s, s0)
+
+
+def test_swiglu_in_place(mq, orc):
+    n = 4096
+    g = synth.rng("swiglu-inplace")
+    gv, uv = synth.normal(g, n), synth.normal(g, n)
+    gd = dev(gv)
+    y, plane = mq.mq_swiglu_quant_q8(gd, dev(uv), y=gd)
+    assert np.all(np.abs(host(gd) - orc.swiglu(gv, uv)) <= TOL * np.abs(orc.swiglu(gv, uv)) + 1e-30)
+
+
+@pytest.mark.parametrize("n", [32, 5120, 13824, 40960])
+def test_rmsnorm_quant_q8(mq, orc, n):
+    g = synth.rng("rms", n)
+    x = synth.normal(g, n)
+    gain = synth.normal(g, n, 1.0, 0.1)
+    y, plane = mq.mq_rmsnorm_quant_q8(dev(x), dev(gain), 1e-6)
+    yh = host(y)
+    yref = orc.rmsnorm(x, gain, 1e-6)
+    assert np.all(np.abs(yh - yref) <= TOL * np.abs(yref) + 1e-30)
+    d, q, s = q8_fields(mq, plane, n)
+    d0, q0, s0 = orc.quantize_q8(yh)
+    assert np.array_equal(d, d0) and np.array_equal(q, q0) and np.array_equal(s, s0)
+
+
+# ------------------------------------------------------------------ integer path
+@pytest.mark.parametrize("fmt", ["q6k", "q4k"])
+@pytest.mark.parametrize("rows,cols", [(16, 2048), (13, 1280), (9, 18944), (1, 256)])
+def test_subdots_bit_exact(mq, orc, fmt, rows, cols):
+    g = synth.rng("subdots", fmt, rows, cols)
+    W = synth.blocks(fmt, g, rows, cols)
+    x = special_activation(cols, "subdots")
+    Wp = repack_dev(mq, fmt, W, rows, cols)
+    plane = mq.mq_quantize_q8(dev(x))
+    fn = mq.mq_gemv_q6k_q8_subdots if fmt == "q6k" else mq.mq_gemv_q4k_q8_subdots
+    got = host(fn(Wp, plane, rows, cols))
+    _, q0, _ = orc.quantize_q8(x)
+    want = orc.subdots(fmt, W, q0, rows, cols)
+    assert np.array_equal(got, want)
+
+
+# ------------------------------------------------------------------ GEMV
+SHAPES = [(512, 2048), (13, 1280), (1, 256), (37, 4608), (64, 18944), (8, 32768), (200, 5120)]
+
+
+@pytest.mark.parametrize("fmt", ["q6k", "q4k"])
+@pytest.mark.parametrize("rows,cols", SHAPES)
+def test_gemv_matches_oracle(mq, orc, fmt, rows, cols):
+    g = synth.rng("gemv", fmt, rows, cols)
+    W = synth.blocks(fmt, g, rows, cols)
+    x = special_activation(cols, "gemv")
+    Wp = repack_dev(mq, fmt, W, rows, cols)
+    plane = mq.mq_quantize_q8(dev(x))
+    y = host(gemv(mq, fmt, Wp, plane, rows, cols))
+    d0, q0, _ = orc.quantize_q8(x)
+    yref, absum = orc.gemv(fmt, W, d0, q0, rows, cols, threads=8)
+    assert_gemv_close(y, yref, absum)
+
+
+@pytest.mark.parametrize("fmt", ["q6k", "q4k"])
+def test_every_split_plan_agrees_and_is_deterministic(mq, orc, fmt):
+    import torch
+    rows, cols = 24, 18944                                  # 19 chunks per row
+    g = synth.rng("splits", fmt)
+    W = synth.blocks(fmt, g, rows, cols)
+    x = synth.normal(g, cols)
+    Wp = repack_dev(mq, fmt, W, rows, cols)
+    plane = mq.mq_quantize_q8(dev(x))
+    d0, q0, _ = orc.quantize_q8(x)
+    yref, absum = orc.gemv(fmt, W, d0, q0, rows, cols)
+    nchunks = 19
+    for s in range(1, nchunks + 1):
+        cps = -(-nchunks // s)
+        if (s - 1) * cps >= nchunks:
+            continue
+        ws = mq.mq_gemv_workspace(rows, cols, splits=s)
+        y1 = host(gemv(mq, fmt, Wp, plane, rows, cols, plan=(s, cps), ws=ws))
+        y2 = host(gemv(mq, fmt, Wp, plane, rows, cols, plan=(s, cps), ws=ws))
+        assert_gemv_close(y1, yref, absum)
+        assert np.array_equal(y1, y2)                       # fixed combine order
+        if ws is not None:                                  # counters back to zero
+            ntiles = -(-rows // 8)
+            assert torch.count_nonzero(ws[:4 * ntiles]).item() == 0
+
+
+def test_bad_plan_is_refused_and_nothing_runs(mq):
+    import torch
+    rows, cols = 16, 18944
+    g = synth.rng("badplan")
+    W = synth.q6k_blocks(g, rows, cols)
+    Wp = repack_dev(mq, "q6k", W, rows, cols)
+    plane = mq.mq_quantize_q8(dev(synth.normal(g, cols)))
+    y = torch.full((rows,), float("nan"), device="cuda")
+    ws = mq.mq_gemv_workspace(rows, cols, splits=5)
+    with pytest.raises(mq.MQError) as e:
+        mq.mq_gemv_q6k_q8(Wp, plane, rows, cols, y=y, ws=ws, plan=(5, 3))   # 15 of 19 chunks
+    assert e.value.status == mq.MQ_ERR_COVERAGE
+    assert torch.isnan(y).all().item()
+
+
+# ------------------------------------------------------------------ chains
+def test_swiglu_to_gemv_chain(mq, orc):
+    """The 7B ffn_down chain at reduced rows: swiglu -> q8 -> q6_K split-K GEMV,
+    against the oracle chain computed from the same f32 inputs only."""
+    rows, cols = 256, 18944
+    g = synth.rng("chain-swiglu")
+    W = synth.q6k_blocks(g, rows, cols)
+    gv, uv = synth.normal(g, cols), synth.normal(g, cols)
+    Wp = repack_dev(mq, "q6k", W, rows, cols)
+    _, plane = mq.mq_swiglu_quant_q8(dev(gv), dev(uv))
+    y = host(gemv(mq, "q6k", Wp, plane, rows, cols))
+    d0, q0, _ = orc.quantize_q8(orc.swiglu(gv, uv).astype(np.float32))
+    yref, absum = orc.gemv("q6k", W, d0, q0, rows, cols, threads=8)
+    assert_gemv_close(y, yref, absum)
+
+
+def test_rms_to_gemv_chain(mq, orc):
+    rows, cols = 320, 5120
+    g = synth.rng("chain-rms")
+    W = synth.q4k_blocks(g, rows, cols)
+    x, gain = synth.normal(g, cols), synth.normal(g, cols, 1.0, 0.1)
+    Wp = repack_dev(mq, "q4k", W, rows, cols)
+    _, plane = mq.mq_rmsnorm_quant_q8(dev(x), dev(gain), 1e-6)
+    y = host(gemv(mq, "q4k", Wp, plane, rows, cols))
+    d0, q0, _ = orc.quantize_q8(orc.rmsnorm(x, gain, 1e-6).astype(np.float32))
+    yref, absum = orc.gemv("q4k", W, d0, q0, rows, cols, threads=8)
+    assert_gemv_close(y, yref, absum)
+
+
+# ------------------------------------------------------------------ full sizes
+def sampled_rows(rows, k, seed):
+    g = synth.rng("sample", seed, rows)
+    pick = set(g.choice(rows, size=min(k, rows), replace=False).tolist())
+    pick |= set(range(min(8, rows))) | set(range(max(0, rows - 8), rows))
+    return np.array(sorted(pick))
+
+
+FULL = [("ffn_down_7b", "q6k", 3584, 18944, "swiglu"),
+        ("attn_v_14b", "q6k", 1024, 5120, "rms"),
+        ("ffn_down_14b", "q6k", 5120, 13824, "rms"),
+        ("attn_q_14b", "q4k", 5120, 5120, "rms"),
+        ("attn_k_14b", "q4k", 1024, 5120, "rms"),
+        ("ffn_gate_14b", "q4k", 13824, 5120, "rms"),
+        ("lm_head_14b", "q6k", 152064, 5120, "rms")]
+
+
+@pytest.mark.parametrize("name,fmt,rows,cols,producer", FULL)
+def test_full_size_sampled_rows(mq, orc, name, fmt, rows, cols, producer):
+    """Full-size matrices in the launch configuration the benchmark times;
+    sampled rows (plus the first and last tile) against the oracle, and every
+    output finite and identical across two runs."""
+    g = synth.rng("full", name)
+    W = synth.blocks(fmt, g, rows, cols)
+    Wp = repack_dev(mq, fmt, W, rows, cols)
+    if producer == "swiglu":
+        gv, uv = synth.normal(g, cols), synth.normal(g, cols)
+        yprod, plane = mq.mq_swiglu_quant_q8(dev(gv), dev(uv))
+    else:
+        x, gain = synth.normal(g, cols), synth.normal(g, cols, 1.0, 0.1)
+        yprod, plane = mq.mq_rmsnorm_quant_q8(dev(x), dev(gain), 1e-6)
+    ws = mq.mq_gemv_workspace(rows, cols)
+    y1 = host(gemv(mq, fmt, Wp, plane, rows, cols, ws=ws))
+    y2 = host(gemv(mq, fmt, Wp, plane, rows, cols, ws=ws))
+    assert np.all(np.isfinite(y1)) and np.array_equal(y1, y2)
+    # the oracle on sampled rows, fed the oracle's own quantization of the
+    # producer output (checked bit-exact against the plane above)
+    d, q, _ = orc.quantize_q8(host(yprod))
+    dg, qg, _ = q8_fields(mq, plane, cols)
+    assert np.array_equal(d, dg) and np.array_equal(q, qg)
+    idx = sampled_rows(rows, 384, name)
+    yref, absum = orc.gemv(fmt, np.ascontiguousarray(W[idx]), d, q, len(idx), cols, threads=8)
+    assert_gemv_close(y1[idx], yref, absum)

@@ -1,0 +1,163 @@
+"""Host-side logic of the C-ABI library, no GPU needed: the library loads and
+exports every symbol include/mq.h declares; the repack is a lossless,
+content-dense permutation; the dispatch plan always covers every chunk
+exactly once; argument validation rejects bad calls before any launch."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def mq():
+    from quant_quantized_gemv_gb300 import build
+    build.build()
+    import quant_quantized_gemv_gb300 as m
+    m.lib()
+    return m
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "mq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mq_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(mq):
+    names = header_functions()
+    assert len(names) >= 20
+    L = ctypes.CDLL(mq.library_path())
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(mq.EXPORTS) == names
+
+
+@pytest.mark.parametrize("fmt", ["q6k", "q4k"])
+@pytest.mark.parametrize("rows,cols", [(1, 256), (7, 512), (8, 1024), (13, 1280), (24, 4608), (9, 18944)])
+def test_repack_round_trip_and_size(mq, fmt, rows, cols):
+    g = synth.rng("host", "repack", fmt, rows, cols)
+    W = synth.blocks(fmt, g, rows, cols)
+    bb = 210 if fmt == "q6k" else 144
+    rep = mq.mq_repack_q6k if fmt == "q6k" else mq.mq_repack_q4k
+    unrep = mq.mq_unrepack_q6k if fmt == "q6k" else mq.mq_unrepack_q4k
+    P = rep(W, rows, cols)
+    nb = cols // 256
+    tiles = -(-rows // 8)
+    assert P.size == tiles * 8 * nb * bb                  # zero padding beyond whole tiles
+    assert np.array_equal(unrep(P, rows, cols), W)         # lossless
+    # a permutation of bits: the same number of set bits
+    assert np.unpackbits(P).sum() == np.unpackbits(W.reshape(-1)).sum()
+    if rows % 8 == 0:
+        assert P.size == W.size                            # exactly the content bytes
+
+
+def test_repack_differs_only_by_bit_permutation(mq):
+    """Flipping one source bit flips exactly one repacked bit, and distinct
+    source bits map to distinct repacked bits (an injective bit map)."""
+    rows, cols = 8, 1024
+    W = np.zeros((rows, cols // 256 * 210), np.uint8)
+    seen = set()
+    rng = synth.rng("host", "bits")
+    for pos in rng.choice(W.size * 8, 400, replace=False):
+        Wb = W.copy().reshape(-1)
+        Wb[pos // 8] = 1 << (pos % 8)
+        P = mq.mq_repack_q6k(Wb.reshape(rows, -1), rows, cols)
+        on = np.flatnonzero(np.unpackbits(P))
+        assert on.size == 1
+        assert on[0] not in seen
+        seen.add(int(on[0]))
+
+
+def test_q8_plane_size_and_unpack(mq):
+    assert mq.mq_q8_bytes(33) == 0 and mq.mq_q8_bytes(0) == 0
+    n = 2048
+    nb = mq.mq_q8_bytes(n)
+    assert nb >= n + n // 32 * 6 and nb % 16 == 0
+    plane = np.arange(nb, dtype=np.uint32).astype(np.uint8)
+    d, qs, s = mq.mq_q8_unpack_host(plane, n)
+    assert np.array_equal(qs.view(np.uint8), plane[:n])
+
+
+def test_coverage_check_rejects_the_pages_dropped_work(mq, facts):
+    """The pipelined kernel of the D4-2 page covered 2 units x 256 threads =
+    512 units; npair 592 lost 80 units (13.5%).  The same plan must be refused."""
+    npair, covered = facts["npair_q6k_18944"], facts["pf_units_covered"]
+    assert npair == 18944 // facts["q6k_weights_per_unit"]
+    assert npair - covered == facts["dropped_units_18944"]
+    assert round(100 * (npair - covered) / npair, 1) == facts["dropped_percent_18944"]
+    assert mq.mq_check_coverage(npair, 256, 2) == mq.MQ_ERR_COVERAGE
+    assert mq.mq_check_coverage(npair, 296, 2) == mq.MQ_OK
+    assert mq.mq_check_coverage(19, 5, 4) == mq.MQ_OK
+    assert mq.mq_check_coverage(19, 5, 3) == mq.MQ_ERR_COVERAGE     # 15 < 19: dropped chunks
+    assert mq.mq_check_coverage(19, 11, 2) == mq.MQ_ERR_COVERAGE    # split 10 would be empty
+    assert mq.mq_check_coverage(19, 0, 19) == mq.MQ_ERR_COVERAGE
+    assert mq.mq_check_coverage(1, 1, 1) == mq.MQ_OK
+
+
+def test_unit_counts_match_pages(facts):
+    assert 5120 // facts["q6k_weights_per_unit"] == facts["npair_q6k_5120"]
+    assert 13824 // facts["q6k_weights_per_unit"] == facts["npair_q6k_13824"]
+    assert 5120 // facts["q4k_weights_per_unit"] == facts["npair_q4k_5120"]
+    assert 13824 // facts["q4k_weights_per_unit"] == facts["npair_q4k_13824"]
+    # the padded layout the repack removes, and the page's dense-row example
+    assert facts["dpl_nbe_example"] * facts["q6k_block_bytes"] == facts["dpl_row_content"]
+    assert (facts["dpl_row_content"] + 15) & ~15 == facts["dpl_row_stride"]
+    assert 1024 * (5120 // 256) * facts["q6k_padded_stride"] == facts["attn_v_padded_bytes"]
+
+
+@pytest.mark.parametrize("sms", [1, 8, 76, 148, 152, 160])
+def test_plan_always_covers(mq, sms):
+    shapes = [(r, c) for r in (1, 5, 8, 64, 512, 1024, 3584, 5120, 13824, 152064)
+              for c in (256, 1024, 1280, 2048, 5120, 13824, 18944, 32768)]
+    for rows, cols in shapes:
+        s, cps = mq.mq_gemv_plan_for(rows, cols, sms)
+        nchunks = -(-(cols // 256) // 4)
+        assert mq.mq_check_coverage(nchunks, s, cps) == mq.MQ_OK, (rows, cols, sms, s, cps)
+        assert s * cps >= nchunks and (s - 1) * cps < nchunks
+        assert s == 1 or mq.mq_gemv_workspace_bytes_for(rows, s) > 0
+
+
+def test_workspace_sizes(mq):
+    assert mq.mq_gemv_workspace_bytes_for(100, 1) == 0
+    tiles = 13
+    assert mq.mq_gemv_workspace_bytes_for(100, 3) == 64 + 3 * tiles * 8 * 4
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="fake device pointers are only passed where no GPU exists")
+def test_validation_rejects_before_launch(mq):
+    L = mq.lib()
+    A = ctypes.c_void_p(0x10000)       # aligned, never dereferenced: every call below
+    B = ctypes.c_void_p(0x20000)       # must fail validation before any launch
+    Y = ctypes.c_void_p(0x30000)
+    N = ctypes.c_void_p(0)
+    S = ctypes.c_void_p(0)
+    assert L.mq_gemv_q6k_q8(N, B, Y, 8, 1024, N, 0, S) == mq.MQ_ERR_NULL
+    assert L.mq_gemv_q6k_q8(A, B, Y, 8, 1000, N, 0, S) == mq.MQ_ERR_SHAPE
+    assert L.mq_gemv_q6k_q8(A, B, Y, 0, 1024, N, 0, S) == mq.MQ_ERR_SHAPE
+    assert L.mq_gemv_q4k_q8(ctypes.c_void_p(0x10008), B, Y, 8, 1024, N, 0, S) == mq.MQ_ERR_ALIGN
+    # explicit plans that drop or duplicate work never launch
+    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 5, 3, N, 0, S) == mq.MQ_ERR_COVERAGE
+    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 19, 2, N, 0, S) == mq.MQ_ERR_COVERAGE
+    # a split plan without (enough) workspace never launches
+    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 5, 4, N, 0, S) == mq.MQ_ERR_NULL
+    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 5, 4, ctypes.c_void_p(0x40000), 16, S) == \
+        mq.MQ_ERR_WORKSPACE
+    assert L.mq_quantize_q8(A, B, 48, S) == mq.MQ_ERR_SHAPE
+    assert L.mq_swiglu_quant_q8(A, B, N, Y, 64, S) == mq.MQ_ERR_NULL
+    assert L.mq_rmsnorm_quant_q8(A, ctypes.c_void_p(0x20004), ctypes.c_float(1e-6), Y, B, 64, S) == \
+        mq.MQ_ERR_ALIGN
+    assert L.mq_repack_q6k(N, A, 8, 1024) == mq.MQ_ERR_NULL
+    assert mq.mq_repacked_bytes_q6k(8, 1000) == 0
+
+
+def test_binding_refuses_cpu_tensors(mq):
+    import torch
+    with pytest.raises(TypeError):
+        mq.mq_quantize_q8(torch.zeros(64))
