@@ -264,6 +264,14 @@ def make_event(timing=True, external=False):
     return torch.cuda.Event(enable_timing=timing)
 
 
+def capture(fn, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
 def bench_mq(args, ws_, rank, local) -> dict | None:
     import torch
     torch.cuda.set_device(local)
@@ -274,47 +282,58 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
         _b.build()
     if dist is not None:
         dist.barrier()
+    import quant_quantized_gemv_gb300 as mq
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
     wl = DeviceWorkload(args.workload, dev, l2)
-    n_graphs = max(wl.n_copies, 16)
-
-    # ---- capture one graph per step slot; external events bracket each GEMV
-    external = True
-    graphs, evs = [], []
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         wl.run(0)                                   # first launches outside capture
     torch.cuda.synchronize()
-    for i in range(n_graphs):
-        try:
-            e = [(make_event(external=external), make_event(external=external)) for _ in range(wl.n_gemv)]
-        except TypeError:
-            external, e = False, None
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            wl.run(i, e if external else None)
-        graphs.append(g)
-        evs.append(e)
+
+    # ---- step graphs: m consecutive steps per graph (PDL edges between all
+    # kernels when enabled), rotating through the weight copies
+    mq.mq_set_pdl(args.pdl)
+    m = max(1, min(args.steps_per_graph, args.steps))
+    n_big = max(1, math.ceil(wl.n_copies / m))
+    big = [capture(lambda j=j: [wl.run(j * m + s) for s in range(m)], stream) for j in range(n_big)]
+    single = [capture(lambda i=i: wl.run(i), stream) for i in range(wl.n_copies)]
+    # ---- kernel-timing graphs: one step each, external events around each
+    # GEMV, no PDL (so each event pair brackets exactly one kernel)
+    mq.mq_set_pdl(False)
+    n_ev = max(wl.n_copies, 16)
+    ev_graphs, evs = [], []
+    try:
+        for i in range(n_ev):
+            e = [(make_event(external=True), make_event(external=True)) for _ in range(wl.n_gemv)]
+            ev_graphs.append(capture(lambda i=i, e=e: wl.run(i, e), stream))
+            evs.append(e)
+    except TypeError:
+        ev_graphs, evs = [], []
+    mq.mq_set_pdl(args.pdl)
     torch.cuda.synchronize()
+
+    def run_steps(k):
+        """Enqueue exactly k steps: whole multi-step graphs, then single steps."""
+        nb_, rest = divmod(k, m)
+        for j in range(nb_):
+            big[j % n_big].replay()
+        for i in range(rest):
+            single[i % wl.n_copies].replay()
 
     # ---- warm-up, then a clock-sampled window: soak / timed K steps / soak
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            graphs[i % n_graphs].replay()
+        run_steps(args.warmup)
     torch.cuda.synchronize()
     sampler = ClockSampler(local) if rank == 0 or ws_ == 1 else None
     t_win0 = time.perf_counter()
 
     def soak(seconds):
         t_end = time.perf_counter() + seconds
-        i = 0
         with torch.cuda.stream(stream):
             while time.perf_counter() < t_end:
-                for _ in range(64):
-                    graphs[i % n_graphs].replay()
-                    i += 1
+                run_steps(16 * m)
                 torch.cuda.synchronize()
 
     soak(args.soak)
@@ -324,8 +343,7 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     start, stop = make_event(), make_event()
     with torch.cuda.stream(stream):
         start.record(stream)
-        for i in range(args.steps):
-            graphs[i % n_graphs].replay()
+        run_steps(args.steps)
         stop.record(stream)
     stop.synchronize()
     torch.cuda.synchronize()
@@ -333,17 +351,6 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
         dist.barrier()
     ms_total = start.elapsed_time(stop)
     t_timed1 = time.perf_counter()
-    # per-GEMV durations of the last replay of every graph slot (the final
-    # n_graphs steps of the timed region)
-    gemv_ms = None
-    if external:
-        per_slot = []
-        for i in range(n_graphs):
-            if i >= args.steps:
-                continue
-            per_slot.append([a.elapsed_time(b) for a, b in evs[i]])
-        if per_slot:
-            gemv_ms = np.array(per_slot).mean(0)
     soak(args.soak)
     t_win1 = time.perf_counter()
     if sampler is not None:
@@ -351,30 +358,42 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     max_ms = reduce_max(ms_total, dist)
     ms_per_step = max_ms / args.steps
 
+    # ---- kernel timing: the GEMV launches of n_ev steps, events per launch
+    gemv_ms = None
+    if ev_graphs:
+        with torch.cuda.stream(stream):
+            for rep in range(3):
+                for g in ev_graphs:
+                    g.replay()
+        torch.cuda.synchronize()
+        gemv_ms = np.array([[a.elapsed_time(b) for a, b in e] for e in evs]).mean(0)
+
     # ---- e2e: the public API, pinned host inputs in, result out, every step
     out_host = torch.empty(wl.output.numel(), dtype=torch.float32).pin_memory()
     h2d = sum(h.numel() * h.element_size() for _, h in wl.inputs)
     d2h = out_host.numel() * 4
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
     torch.cuda.synchronize()
+
+    def e2e_step(i):
+        for d_, h_ in wl.inputs:
+            d_.copy_(h_, non_blocking=True)
+        wl.run(i)
+        out_host.copy_(wl.output, non_blocking=True)
+
     with torch.cuda.stream(stream):
         for i in range(3):
-            for d_, h_ in wl.inputs:
-                d_.copy_(h_, non_blocking=True)
-            wl.run(i)
-            out_host.copy_(wl.output, non_blocking=True)
+            e2e_step(i)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(e2e_steps):
-            for d_, h_ in wl.inputs:
-                d_.copy_(h_, non_blocking=True)
-            wl.run(i)
-            out_host.copy_(wl.output, non_blocking=True)
+            e2e_step(i)
     torch.cuda.synchronize()
     e2e_ms = reduce_max((time.perf_counter() - t0) * 1e3, dist) / e2e_steps
+    mq.mq_set_pdl(False)
 
     if rank != 0:
         return None
@@ -387,10 +406,11 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
         "dtype": "i8", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {DESCR[args.workload]}",
                    "weight_content_bytes_per_step": wl.weight_bytes,
-                   "gemvs_per_step": wl.n_gemv,
+                   "gemvs_per_step": wl.n_gemv, "kernels_per_step": wl.n_kernels,
                    "l2": f"{wl.n_copies} rotated weight copies "
                          f"({wl.n_copies * wl.weight_bytes / 1e6:.0f} MB >= 4 x L2 {l2 / 1e6:.0f} MB)",
-                   "timing": "CUDA graph per step, CUDA events on the launching stream",
+                   "timing": f"CUDA graphs of {m} steps (+ single-step graphs for a remainder), "
+                             f"CUDA events on the launching stream; PDL {'on' if args.pdl else 'off'}",
                    "parallelism": f"replicas{ws_}" if ws_ > 1 else "single GPU"},
         "compute": "int8 x (6-bit|4-bit) dp4a dots, int32 sub-block sums, f32 scale combine",
         "pct_of_hbm_peak": round(100 * value / ws_ / peak, 2),
@@ -406,9 +426,10 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
                             "algorithmic_bytes_per_step": int(alg),
                             "kernel": "gemv_kernel (q6_K/q4_K x q8)",
                             "gemv_us_per_step": round(gsum_ms * 1e3, 3),
-                            "samples": int(min(n_graphs, args.steps))}
-        line["kernel_us"] = {"gemv_total": round(gsum_ms * 1e3, 3),
-                             "rest_of_step": round(ms_per_step * 1e3 - gsum_ms * 1e3, 3)}
+                            "how": f"events around every GEMV in {n_ev} single-step graphs "
+                                   f"(PDL off), 3 replays each, rotated copies"}
+        line["kernel_us"] = {"gemv_total_isolated": round(gsum_ms * 1e3, 3),
+                             "step": round(ms_per_step * 1e3, 3)}
     line["e2e"] = {"value": round(wl.weight_bytes / (e2e_ms * 1e-3) / 1e9 * ws_, 2), "unit": "GB/s",
                    "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
                    "d2h_bytes_per_step": int(d2h),
@@ -515,6 +536,9 @@ def main(argv=None):
     ap.add_argument("--workload", default="ffn_down_7b", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--soak", type=float, default=0.6, help="seconds of identical load around the timed steps")
     ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--steps-per-graph", type=int, default=16)
+    ap.add_argument("--no-pdl", dest="pdl", action="store_false",
+                    help="launch without programmatic dependent launch")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

@@ -129,50 +129,76 @@ int mq_swiglu_quant_q8(const float *g, const float *u, float *y, void *q8, int n
  *        isum_k = sum q * q8, qsum_k = the q8 block's sum.
  * Wp: repacked weights (device, mq_repack_* output).  q8: plane of cols
  * values (device).  y: rows f32 (device).  The f32 combine order is fixed
- * (ascending chunks within a split, a fixed butterfly across lanes, splits
- * summed in ascending order), so results are deterministic run to run.
+ * (ascending chunks within a work item, a fixed butterfly across lanes,
+ * splits summed in ascending order), so results are deterministic run to run.
  *
- * Rows are cut into tiles of 8 and each tile's columns into S contiguous
- * ranges of 4-super-block chunks ("split-K", [D4-2] §2's tall-row case).
- * When S > 1 each split writes 8 partial sums to `ws` and the last split of a
- * tile to finish adds the S partials in ascending order; nothing spins.  The
- * host checks before launch that the splits cover every chunk exactly once
- * (MQ_ERR_COVERAGE otherwise).
+ * Work decomposition.  Rows are cut into tiles of 8 and each tile's columns
+ * into nchunks = ceil(cols/1024) chunks of 4 super-blocks.  A plan is
+ * (splits, chunks_per_split, tiles_per_item); one warp per work item:
+ *   splits > 1 ("split-K", the tall-row case of [D4-2] §2): every tile is cut
+ *     into `splits` tile-aligned ranges of chunks_per_split chunks (the last
+ *     may be shorter); tiles_per_item must be 1.  Each split leaves its 8
+ *     partial row sums in `ws`; the split that finishes last adds all of them
+ *     in ascending split order (an atomic ticket; nothing waits or spins).
+ *   splits == 1: every item covers tiles_per_item whole tiles, no workspace;
+ *     chunks_per_split must still cover a row (>= nchunks).
+ * Before any launch the host checks the plan: splits * chunks_per_split >=
+ * nchunks (no chunk dropped) and (splits - 1) * chunks_per_split < nchunks
+ * (no empty split), else MQ_ERR_COVERAGE ([D4-2] §6 lesson 1: a gate must
+ * bound both sides).  The default plan fills one resident wave of warps on
+ * the current device: tiles_per_item = ceil(tiles / wave) when tiles exceed
+ * the wave, else as many splits as the wave has room for.
  *
- * mq_gemv_workspace_bytes(rows, cols): workspace the plan on the current
- *   device needs (0 when S == 1).  ws must be device memory, zero-filled
- *   before its first use; every completed call leaves it zero-filled again.
- * mq_gemv_splits(rows, cols): the S the plan picks on the current device
- *   (it uses ceil(nchunks / S) chunks per split, nchunks = ceil(cols/1024)).
- * mq_gemv_*_q8_plan: the same GEMV with an explicit plan (S, chunks per
- *   split); the coverage check is the only thing between a wrong plan and
- *   dropped work, and it rejects the plan with MQ_ERR_COVERAGE.
+ * mq_gemv_workspace_bytes(rows, cols): workspace the default plans (q6_K and
+ *   q4_K) need on the current device (0 when splits == 1).  ws must be device
+ *   memory, zero-filled before its first use; every completed call leaves it
+ *   zero-filled again.  ws may be NULL when 0 bytes are needed.
+ * mq_gemv_workspace_bytes_for: the same for an explicit plan (0 if invalid).
+ * mq_gemv_plan: the default plan for format 6 (q6_K) or 4 (q4_K) on the
+ *   current device.
+ * mq_gemv_plan_for: the default plan for a device with `sms` SMs holding
+ *   `warps_per_sm` GEMV warps each.  Host only.
+ * mq_gemv_*_q8_plan: the GEMV with an explicit plan.
  * Errors: MQ_ERR_NULL, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_WORKSPACE,
  *         MQ_ERR_COVERAGE, MQ_ERR_CUDA.
  * ------------------------------------------------------------------------ */
 size_t mq_gemv_workspace_bytes(int rows, int cols);
-int mq_gemv_splits(int rows, int cols);
+size_t mq_gemv_workspace_bytes_for(int rows, int cols, int splits, int chunks_per_split,
+                                   int tiles_per_item);
+int mq_gemv_plan(int rows, int cols, int fmt, int *splits, int *chunks_per_split,
+                 int *tiles_per_item);
+int mq_gemv_plan_for(int rows, int cols, int sms, int warps_per_sm, int *splits,
+                     int *chunks_per_split, int *tiles_per_item);
 int mq_gemv_q6k_q8(const void *Wp, const void *q8, float *y, int rows, int cols, void *ws,
                    size_t ws_bytes, void *stream);
 int mq_gemv_q4k_q8(const void *Wp, const void *q8, float *y, int rows, int cols, void *ws,
                    size_t ws_bytes, void *stream);
-int mq_gemv_q6k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int cols,
-                        int splits, int chunks_per_split, void *ws, size_t ws_bytes,
+int mq_gemv_q6k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int cols, int splits,
+                        int chunks_per_split, int tiles_per_item, void *ws, size_t ws_bytes,
                         void *stream);
-int mq_gemv_q4k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int cols,
-                        int splits, int chunks_per_split, void *ws, size_t ws_bytes,
+int mq_gemv_q4k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int cols, int splits,
+                        int chunks_per_split, int tiles_per_item, void *ws, size_t ws_bytes,
                         void *stream);
-/* Workspace for an explicit split count (0 when splits == 1). */
-size_t mq_gemv_workspace_bytes_for(int rows, int splits);
 
-/* The plan the dispatch would pick for (rows, cols) on a device with `sms`
- * streaming multiprocessors: writes S and chunks per split.  Host only. */
-int mq_gemv_plan_for(int rows, int cols, int sms, int *splits, int *chunks_per_split);
-
-/* Coverage check used by every GEMV dispatch, exposed for tests: returns
- * MQ_OK iff splits * chunks_per_split >= nchunks (nothing dropped) and
- * (splits - 1) * chunks_per_split < nchunks (no empty split), all >= 1. */
+/* Coverage check used by every GEMV dispatch, exposed for tests: MQ_OK iff
+ * all arguments are >= 1, splits * chunks_per_split >= nchunks (nothing
+ * dropped) and (splits - 1) * chunks_per_split < nchunks (no empty split);
+ * else MQ_ERR_COVERAGE. */
 int mq_check_coverage(int nchunks, int splits, int chunks_per_split);
+
+/* ------------------------------------------------------------------------
+ * Programmatic dependent launch (process-wide switch, default off; returns
+ * the previous setting).  When on, every kernel is launched with CUDA's
+ * programmatic stream serialization, so it may start while the previous
+ * kernel in the stream drains: producers then wait (griddepcontrol.wait)
+ * before reading anything, and a GEMV issues its first weight loads BEFORE
+ * waiting and touches the q8 plane, y and ws only after.  This hides launch
+ * and ramp latency in a producer -> GEMV -> producer chain (the retry
+ * condition of [D4-4] §5 for PDL: a purely bandwidth-bound chain).  Turn it
+ * on only when the kernel that directly precedes a GEMV in the stream does
+ * not write that GEMV's weight matrix.
+ * ------------------------------------------------------------------------ */
+int mq_set_pdl(int enable);
 
 /* ------------------------------------------------------------------------
  * Integer sub-block dots (device), for bit-exact testing of the GEMV's

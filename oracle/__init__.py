@@ -11,6 +11,7 @@ C source carries the full statement of each formula.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -42,34 +43,63 @@ def build(force: bool = False) -> str:
     return _SO
 
 
+def _bind(L):
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    L.mqo_f16_to_f32.argtypes = [ctypes.c_uint16]
+    L.mqo_f16_to_f32.restype = ctypes.c_float
+    L.mqo_f32_to_f16.argtypes = [ctypes.c_float]
+    L.mqo_f32_to_f16.restype = ctypes.c_uint16
+    L.mqo_quantize_q8.argtypes = [P, I, P, P, P]
+    L.mqo_dequant_q6k.argtypes = [P, ctypes.c_long, P]
+    L.mqo_dequant_q4k.argtypes = [P, ctypes.c_long, P]
+    L.mqo_q4k_scale_min.argtypes = [P, I, P, P]
+    L.mqo_subdots_q6k.argtypes = [P, P, I, I, P]
+    L.mqo_subdots_q4k.argtypes = [P, P, I, I, P]
+    L.mqo_gemv_q6k.argtypes = [P, P, P, I, I, I, P, P]
+    L.mqo_gemv_q4k.argtypes = [P, P, P, I, I, I, P, P]
+    L.mqo_rmsnorm.argtypes = [P, P, ctypes.c_float, I, P]
+    L.mqo_swiglu.argtypes = [P, P, I, P]
+    for f in ("mqo_quantize_q8", "mqo_dequant_q6k", "mqo_dequant_q4k", "mqo_q4k_scale_min",
+              "mqo_subdots_q6k", "mqo_subdots_q4k", "mqo_gemv_q6k", "mqo_gemv_q4k",
+              "mqo_rmsnorm", "mqo_swiglu"):
+        getattr(L, f).restype = None
+    return L
+
+
 def lib():
     global _lib
     with _lock:
         if _lib is None:
             build()
-            L = ctypes.CDLL(_SO)
-            P = ctypes.c_void_p
-            I = ctypes.c_int
-            L.mqo_f16_to_f32.argtypes = [ctypes.c_uint16]
-            L.mqo_f16_to_f32.restype = ctypes.c_float
-            L.mqo_f32_to_f16.argtypes = [ctypes.c_float]
-            L.mqo_f32_to_f16.restype = ctypes.c_uint16
-            L.mqo_quantize_q8.argtypes = [P, I, P, P, P]
-            L.mqo_dequant_q6k.argtypes = [P, ctypes.c_long, P]
-            L.mqo_dequant_q4k.argtypes = [P, ctypes.c_long, P]
-            L.mqo_q4k_scale_min.argtypes = [P, I, P, P]
-            L.mqo_subdots_q6k.argtypes = [P, P, I, I, P]
-            L.mqo_subdots_q4k.argtypes = [P, P, I, I, P]
-            L.mqo_gemv_q6k.argtypes = [P, P, P, I, I, I, P, P]
-            L.mqo_gemv_q4k.argtypes = [P, P, P, I, I, I, P, P]
-            L.mqo_rmsnorm.argtypes = [P, P, ctypes.c_float, I, P]
-            L.mqo_swiglu.argtypes = [P, P, I, P]
-            for f in ("mqo_quantize_q8", "mqo_dequant_q6k", "mqo_dequant_q4k", "mqo_q4k_scale_min",
-                      "mqo_subdots_q6k", "mqo_subdots_q4k", "mqo_gemv_q6k", "mqo_gemv_q4k",
-                      "mqo_rmsnorm", "mqo_swiglu"):
-                getattr(L, f).restype = None
-            _lib = L
+            _lib = _bind(ctypes.CDLL(_SO))
     return _lib
+
+
+@contextlib.contextmanager
+def variant(source: str, workdir: str):
+    """Temporarily run every oracle function from another C source text (used
+    by the mutation tests to show that the pins catch planted mistakes)."""
+    global _lib
+    src = os.path.join(workdir, "variant.c")
+    so = os.path.join(workdir, "libvariant.so")
+    with open(src, "w") as f:
+        f.write(source)
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+                           "-fPIC", "-shared", "-o", so, src, "-lm"])
+    saved = lib()
+    with _lock:
+        _lib = _bind(ctypes.CDLL(so))
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = saved
+
+
+def source() -> str:
+    with open(_SRC) as f:
+        return f.read()
 
 
 def _p(a: np.ndarray):

@@ -30,9 +30,10 @@ EXPORTS = [
     "mq_strerror", "mq_version", "mq_repacked_bytes_q6k", "mq_repacked_bytes_q4k",
     "mq_repack_q6k", "mq_repack_q4k", "mq_unrepack_q6k", "mq_unrepack_q4k", "mq_q8_bytes",
     "mq_q8_unpack_host", "mq_quantize_q8", "mq_rmsnorm_quant_q8", "mq_swiglu_quant_q8",
-    "mq_gemv_workspace_bytes", "mq_gemv_splits", "mq_gemv_q6k_q8", "mq_gemv_q4k_q8",
+    "mq_gemv_workspace_bytes", "mq_gemv_plan", "mq_gemv_q6k_q8", "mq_gemv_q4k_q8",
     "mq_gemv_q6k_q8_plan", "mq_gemv_q4k_q8_plan", "mq_gemv_workspace_bytes_for",
-    "mq_check_coverage", "mq_gemv_plan_for", "mq_gemv_q6k_q8_subdots", "mq_gemv_q4k_q8_subdots", "mq_device_sms",
+    "mq_check_coverage", "mq_gemv_plan_for", "mq_set_pdl", "mq_gemv_q6k_q8_subdots",
+    "mq_gemv_q4k_q8_subdots", "mq_device_sms",
 ]
 
 
@@ -55,7 +56,7 @@ def lib():
         raise RuntimeError(f"{_SO} is missing: build it with "
                            "`python -m quant_quantized_gemv_gb300.build` (or __graft_entry__.build())")
     L = ctypes.CDLL(_SO)
-    P, I, S, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+    P, I, S, F, LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float, ctypes.c_longlong
     sig = {
         "mq_strerror": ([I], ctypes.c_char_p),
         "mq_version": ([], ctypes.c_char_p),
@@ -71,14 +72,15 @@ def lib():
         "mq_rmsnorm_quant_q8": ([P, P, F, P, P, I, P], I),
         "mq_swiglu_quant_q8": ([P, P, P, P, I, P], I),
         "mq_gemv_workspace_bytes": ([I, I], S),
-        "mq_gemv_splits": ([I, I], I),
+        "mq_gemv_plan": ([I, I, I, P, P, P], I),
         "mq_gemv_q6k_q8": ([P, P, P, I, I, P, S, P], I),
         "mq_gemv_q4k_q8": ([P, P, P, I, I, P, S, P], I),
-        "mq_gemv_q6k_q8_plan": ([P, P, P, I, I, I, I, P, S, P], I),
-        "mq_gemv_q4k_q8_plan": ([P, P, P, I, I, I, I, P, S, P], I),
-        "mq_gemv_workspace_bytes_for": ([I, I], S),
+        "mq_gemv_q6k_q8_plan": ([P, P, P, I, I, I, I, I, P, S, P], I),
+        "mq_gemv_q4k_q8_plan": ([P, P, P, I, I, I, I, I, P, S, P], I),
+        "mq_gemv_workspace_bytes_for": ([I, I, I, I, I], S),
         "mq_check_coverage": ([I, I, I], I),
-        "mq_gemv_plan_for": ([I, I, I, P, P], I),
+        "mq_gemv_plan_for": ([I, I, I, I, P, P, P], I),
+        "mq_set_pdl": ([I], I),
         "mq_gemv_q6k_q8_subdots": ([P, P, P, I, I, P], I),
         "mq_gemv_q4k_q8_subdots": ([P, P, P, I, I, P], I),
         "mq_device_sms": ([], I),
@@ -218,35 +220,47 @@ def mq_gemv_workspace_bytes(rows: int, cols: int) -> int:
     return lib().mq_gemv_workspace_bytes(rows, cols)
 
 
-def mq_gemv_workspace_bytes_for(rows: int, splits: int) -> int:
-    return lib().mq_gemv_workspace_bytes_for(rows, splits)
-
-
-def mq_gemv_splits(rows: int, cols: int) -> int:
-    return lib().mq_gemv_splits(rows, cols)
+def mq_gemv_workspace_bytes_for(rows: int, cols: int, plan) -> int:
+    """Workspace bytes for an explicit plan (splits, chunks_per_split, tiles_per_item)."""
+    return lib().mq_gemv_workspace_bytes_for(rows, cols, *map(int, plan))
 
 
 def mq_check_coverage(nchunks: int, splits: int, chunks_per_split: int) -> int:
     return lib().mq_check_coverage(nchunks, splits, chunks_per_split)
 
 
-def mq_gemv_plan_for(rows: int, cols: int, sms: int):
-    """(splits, chunks_per_split) the dispatch picks on a device with `sms` SMs."""
-    s, c = ctypes.c_int(), ctypes.c_int()
-    _check(lib().mq_gemv_plan_for(rows, cols, sms, ctypes.byref(s), ctypes.byref(c)),
-           "mq_gemv_plan_for")
-    return s.value, c.value
+def _plan_out(fn, *args):
+    s, c, t = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(fn(*args, ctypes.byref(s), ctypes.byref(c), ctypes.byref(t)), fn.__name__)
+    return s.value, c.value, t.value
+
+
+def mq_gemv_plan(rows: int, cols: int, fmt: str = "q6k"):
+    """Default (splits, chunks_per_split, tiles_per_item) on the current device."""
+    return _plan_out(lib().mq_gemv_plan, rows, cols, 6 if fmt == "q6k" else 4)
+
+
+def mq_gemv_plan_for(rows: int, cols: int, sms: int, warps_per_sm: int):
+    """Default plan for a device with `sms` SMs x `warps_per_sm` GEMV warps."""
+    return _plan_out(lib().mq_gemv_plan_for, rows, cols, sms, warps_per_sm)
+
+
+def mq_set_pdl(enable: bool) -> bool:
+    """Programmatic dependent launch for every later launch (process-wide)."""
+    return bool(lib().mq_set_pdl(1 if enable else 0))
 
 
 def mq_device_sms() -> int:
     return lib().mq_device_sms()
 
 
-def mq_gemv_workspace(rows: int, cols: int, splits: int | None = None, device=None):
-    """A zero-filled split-K workspace for (rows, cols) (None when not needed)."""
+def mq_gemv_workspace(rows: int, cols: int, plan=None, device=None):
+    """A zero-filled workspace for (rows, cols) under the default plans, or
+    under an explicit plan (splits, chunks_per_split, tiles_per_item); None
+    when not needed."""
     import torch
-    nbytes = (mq_gemv_workspace_bytes(rows, cols) if splits is None
-              else mq_gemv_workspace_bytes_for(rows, splits))
+    nbytes = (mq_gemv_workspace_bytes(rows, cols) if plan is None
+              else mq_gemv_workspace_bytes_for(rows, cols, plan))
     if nbytes == 0:
         return None
     return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
@@ -268,7 +282,8 @@ def _gemv(name: str, Wp, q8, rows: int, cols: int, y, ws, stream, plan=None):
                               _stream(stream))
     else:
         st = getattr(L, name + "_plan")(_dev(Wp), _dev(q8), _dev(y, torch.float32), rows, cols,
-                                        int(plan[0]), int(plan[1]), wsp, wsb, _stream(stream))
+                                        int(plan[0]), int(plan[1]), int(plan[2]), wsp, wsb,
+                                        _stream(stream))
     _check(st, name)
     return y
 

@@ -16,6 +16,8 @@ using namespace mq;
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sms[kMaxDevices];
+std::atomic<int> g_warps[kMaxDevices][2];  // resident GEMV warps per SM: [q6_K, q4_K]
+std::atomic<int> g_pdl{0};
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -26,10 +28,17 @@ bool gemv_shape_ok(int rows, int cols)
 
 bool vec_shape_ok(int n) { return n > 0 && n % 32 == 0; }
 
-int device_sms()
+int current_device()
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+int device_sms()
+{
+    const int dev = current_device();
+    if (dev < 0) return 0;
     int v = g_sms[dev].load(std::memory_order_relaxed);
     if (v > 0) return v;
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
@@ -37,25 +46,47 @@ int device_sms()
     return v;
 }
 
-// Split count for a (rows, cols) GEMV: enough warps in flight to keep HBM
-// busy, and no more splits than that (each split adds a partial write and a
-// share of a combine).  A warp streams ~6.7 KB (q6_K) per chunk; about 16
-// resident warp-items per SM keep >= 20 MB of loads queued GPU-wide.
-int plan_splits(int ntiles, int nchunks, int sms)
+int resident_warps(int fmt)
 {
-    if (sms <= 0) sms = 1;
-    const long long target = (long long)sms * 16;
-    if (ntiles >= target) return 1;
-    long long s = (target + ntiles - 1) / ntiles;
-    if (s > nchunks) s = nchunks;
-    const int cps = ceil_div(nchunks, (int)s);
-    return ceil_div(nchunks, cps);
+    const int dev = current_device();
+    if (dev < 0) return 0;
+    std::atomic<int> &slot = g_warps[dev][fmt == 6 ? 0 : 1];
+    int v = slot.load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    v = gemv_resident_warps_per_sm(fmt);
+    if (v > 0) slot.store(v, std::memory_order_relaxed);
+    return v;
 }
 
-size_t ws_bytes_for(int ntiles, int splits)
+struct Plan {
+    int splits, cps, tpi;
+};
+
+// One resident wave of warps.  More tiles than warps: whole tiles per warp
+// (tpi of them, no combine).  Fewer: cut each tile's chunks into as many
+// tile-aligned splits as the wave has room for.
+Plan plan_for(int ntiles, int nchunks, int sms, int warps_per_sm)
 {
-    if (splits <= 1) return 0;
-    return round16((size_t)ntiles * 4) + (size_t)splits * ntiles * 8 * sizeof(float);
+    if (sms <= 0) sms = 1;
+    if (warps_per_sm <= 0) warps_per_sm = 12;
+    const long long cap = (long long)sms * warps_per_sm;
+    if (ntiles >= cap) return Plan{1, nchunks, (int)((ntiles + cap - 1) / cap)};
+    long long s = cap / ntiles;
+    if (s > nchunks) s = nchunks;
+    if (s < 1) s = 1;
+    const int cps = ceil_div(nchunks, (int)s);
+    return Plan{ceil_div(nchunks, cps), cps, 1};
+}
+
+long long plan_items(int ntiles, const Plan &p)
+{
+    return p.splits > 1 ? (long long)ntiles * p.splits : (ntiles + p.tpi - 1) / p.tpi;
+}
+
+size_t ws_bytes_for(int ntiles, const Plan &p)
+{
+    if (p.splits <= 1) return 0;
+    return round16((size_t)ntiles * 4) + (size_t)plan_items(ntiles, p) * 8 * sizeof(float);
 }
 
 int check_coverage(int nchunks, int splits, int cps)
@@ -68,25 +99,33 @@ int check_coverage(int nchunks, int splits, int cps)
     return MQ_OK;
 }
 
+int check_plan(const Geom &g, const Plan &p)
+{
+    if (p.tpi < 1 || (p.splits > 1 && p.tpi != 1)) return MQ_ERR_COVERAGE;
+    const int cov = check_coverage(g.nchunks, p.splits, p.cps);
+    if (cov != MQ_OK) return cov;
+    if (plan_items(g.ntiles, p) >= (1LL << 31)) return MQ_ERR_SHAPE;
+    return MQ_OK;
+}
+
 int gemv_common(int fmt, const void *Wp, const void *q8, float *y, int rows, int cols,
-                int splits, int cps, void *ws, size_t ws_bytes, void *stream)
+                const Plan *explicit_plan, void *ws, size_t ws_bytes, void *stream)
 {
     if (!Wp || !q8 || !y) return MQ_ERR_NULL;
     if (!gemv_shape_ok(rows, cols)) return MQ_ERR_SHAPE;
     if (!aligned16(Wp) || !aligned16(q8) || !aligned16(y)) return MQ_ERR_ALIGN;
     const Geom g = make_geom(rows, cols, fmt == 6 ? kQ6kBytes : kQ4kBytes);
-    if (splits <= 0) {
-        splits = plan_splits(g.ntiles, g.nchunks, device_sms());
-        cps = ceil_div(g.nchunks, splits);
-    }
-    const int cov = check_coverage(g.nchunks, splits, cps);
+    const Plan p = explicit_plan ? *explicit_plan
+                                 : plan_for(g.ntiles, g.nchunks, device_sms(), resident_warps(fmt));
+    const int cov = check_plan(g, p);
     if (cov != MQ_OK) return cov;
     GemvLaunch a;
     memset(&a, 0, sizeof a);
-    if (splits > 1) {
+    const size_t need = ws_bytes_for(g.ntiles, p);
+    if (need > 0) {
         if (!ws) return MQ_ERR_NULL;
         if (!aligned16(ws)) return MQ_ERR_ALIGN;
-        if (ws_bytes < ws_bytes_for(g.ntiles, splits)) return MQ_ERR_WORKSPACE;
+        if (ws_bytes < need) return MQ_ERR_WORKSPACE;
         a.ws_cnt = (unsigned *)ws;
         a.ws_part = (float *)((uint8_t *)ws + round16((size_t)g.ntiles * 4));
     }
@@ -97,12 +136,14 @@ int gemv_common(int fmt, const void *Wp, const void *q8, float *y, int rows, int
     a.nb = g.nb;
     a.ntiles = g.ntiles;
     a.nchunks = g.nchunks;
-    a.splits = splits;
-    a.cps = cps;
-    a.n_items = (long long)g.ntiles * splits;
+    a.splits = p.splits;
+    a.cps = p.cps;
+    a.tpi = p.tpi;
+    a.n_items = (int)plan_items(g.ntiles, p);
     a.tile_bytes = g.tile_bytes;
     a.q8_d_off = (unsigned)q8_d_offset(cols);
     a.q8_sum_off = (unsigned)q8_sum_offset(cols);
+    a.pdl = g_pdl.load(std::memory_order_relaxed);
     const cudaError_t e = fmt == 6 ? launch_gemv_q6k(a, (cudaStream_t)stream)
                                    : launch_gemv_q4k(a, (cudaStream_t)stream);
     return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
@@ -124,12 +165,15 @@ int subdots_common(int fmt, const void *Wp, const void *q8, int32_t *isums, int 
     a.nb = g.nb;
     a.ntiles = g.ntiles;
     a.nchunks = g.nchunks;
+    if ((long long)g.ntiles * g.nchunks >= (1LL << 31)) return MQ_ERR_SHAPE;
     a.splits = g.nchunks;  // one chunk per work item
     a.cps = 1;
-    a.n_items = (long long)g.ntiles * g.nchunks;
+    a.tpi = 1;
+    a.n_items = g.ntiles * g.nchunks;
     a.tile_bytes = g.tile_bytes;
     a.q8_d_off = (unsigned)q8_d_offset(cols);
     a.q8_sum_off = (unsigned)q8_sum_offset(cols);
+    a.pdl = g_pdl.load(std::memory_order_relaxed);
     const cudaError_t e = fmt == 6 ? launch_subdots_q6k(a, (cudaStream_t)stream)
                                    : launch_subdots_q4k(a, (cudaStream_t)stream);
     return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
@@ -176,7 +220,8 @@ int mq_quantize_q8(const float *x, void *q8, int n, void *stream)
     if (!vec_shape_ok(n)) return MQ_ERR_SHAPE;
     if (!aligned16(x) || !aligned16(q8)) return MQ_ERR_ALIGN;
     const cudaError_t e = launch_quantize_q8(x, (uint8_t *)q8, n, (unsigned)q8_d_offset(n),
-                                             (unsigned)q8_sum_offset(n), (cudaStream_t)stream);
+                                             (unsigned)q8_sum_offset(n), g_pdl.load(std::memory_order_relaxed),
+                                             (cudaStream_t)stream);
     return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
 }
 
@@ -188,7 +233,8 @@ int mq_rmsnorm_quant_q8(const float *x, const float *gain, float eps, float *y, 
     if (!aligned16(x) || !aligned16(gain) || !aligned16(y) || !aligned16(q8)) return MQ_ERR_ALIGN;
     const cudaError_t e = launch_rmsnorm_quant_q8(x, gain, eps, y, (uint8_t *)q8, n,
                                                   (unsigned)q8_d_offset(n),
-                                                  (unsigned)q8_sum_offset(n), (cudaStream_t)stream);
+                                                  (unsigned)q8_sum_offset(n), g_pdl.load(std::memory_order_relaxed),
+                                             (cudaStream_t)stream);
     return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
 }
 
@@ -199,7 +245,8 @@ int mq_swiglu_quant_q8(const float *g, const float *u, float *y, void *q8, int n
     if (!aligned16(g) || !aligned16(u) || !aligned16(y) || !aligned16(q8)) return MQ_ERR_ALIGN;
     const cudaError_t e = launch_swiglu_quant_q8(g, u, y, (uint8_t *)q8, n,
                                                  (unsigned)q8_d_offset(n),
-                                                 (unsigned)q8_sum_offset(n), (cudaStream_t)stream);
+                                                 (unsigned)q8_sum_offset(n), g_pdl.load(std::memory_order_relaxed),
+                                             (cudaStream_t)stream);
     return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
 }
 
@@ -208,60 +255,80 @@ int mq_check_coverage(int nchunks, int splits, int chunks_per_split)
     return check_coverage(nchunks, splits, chunks_per_split);
 }
 
-int mq_gemv_plan_for(int rows, int cols, int sms, int *splits, int *chunks_per_split)
+int mq_gemv_plan_for(int rows, int cols, int sms, int warps_per_sm, int *splits,
+                     int *chunks_per_split, int *tiles_per_item)
 {
-    if (!splits || !chunks_per_split) return MQ_ERR_NULL;
+    if (!splits || !chunks_per_split || !tiles_per_item) return MQ_ERR_NULL;
     if (!gemv_shape_ok(rows, cols)) return MQ_ERR_SHAPE;
     const Geom g = make_geom(rows, cols, kQ6kBytes);
-    *splits = plan_splits(g.ntiles, g.nchunks, sms);
-    *chunks_per_split = ceil_div(g.nchunks, *splits);
+    const Plan p = plan_for(g.ntiles, g.nchunks, sms, warps_per_sm);
+    *splits = p.splits;
+    *chunks_per_split = p.cps;
+    *tiles_per_item = p.tpi;
     return MQ_OK;
 }
 
-int mq_gemv_splits(int rows, int cols)
+int mq_gemv_plan(int rows, int cols, int fmt, int *splits, int *chunks_per_split,
+                 int *tiles_per_item)
+{
+    if (fmt != 6 && fmt != 4) return MQ_ERR_SHAPE;
+    return mq_gemv_plan_for(rows, cols, device_sms(), resident_warps(fmt), splits,
+                            chunks_per_split, tiles_per_item);
+}
+
+size_t mq_gemv_workspace_bytes_for(int rows, int cols, int splits, int chunks_per_split,
+                                   int tiles_per_item)
 {
     if (!gemv_shape_ok(rows, cols)) return 0;
     const Geom g = make_geom(rows, cols, kQ6kBytes);
-    return plan_splits(g.ntiles, g.nchunks, device_sms());
+    const Plan p{splits, chunks_per_split, tiles_per_item};
+    if (check_plan(g, p) != MQ_OK) return 0;
+    return ws_bytes_for(g.ntiles, p);
 }
 
 size_t mq_gemv_workspace_bytes(int rows, int cols)
 {
-    if (!gemv_shape_ok(rows, cols)) return 0;
-    const Geom g = make_geom(rows, cols, kQ6kBytes);
-    return ws_bytes_for(g.ntiles, plan_splits(g.ntiles, g.nchunks, device_sms()));
+    size_t need = 0;
+    for (int fmt : {6, 4}) {
+        int s = 0, c = 0, t = 0;
+        if (mq_gemv_plan(rows, cols, fmt, &s, &c, &t) != MQ_OK) return 0;
+        const size_t b = mq_gemv_workspace_bytes_for(rows, cols, s, c, t);
+        if (b > need) need = b;
+    }
+    return need;
 }
 
-size_t mq_gemv_workspace_bytes_for(int rows, int splits)
+int mq_set_pdl(int enable)
 {
-    if (rows < 1) return 0;
-    return ws_bytes_for(ceil_div(rows, kTileRows), splits);
+    return g_pdl.exchange(enable ? 1 : 0);
 }
 
 int mq_gemv_q6k_q8(const void *Wp, const void *q8, float *y, int rows, int cols, void *ws,
                    size_t ws_bytes, void *stream)
 {
-    return gemv_common(6, Wp, q8, y, rows, cols, 0, 0, ws, ws_bytes, stream);
+    return gemv_common(6, Wp, q8, y, rows, cols, nullptr, ws, ws_bytes, stream);
 }
 
 int mq_gemv_q4k_q8(const void *Wp, const void *q8, float *y, int rows, int cols, void *ws,
                    size_t ws_bytes, void *stream)
 {
-    return gemv_common(4, Wp, q8, y, rows, cols, 0, 0, ws, ws_bytes, stream);
+    return gemv_common(4, Wp, q8, y, rows, cols, nullptr, ws, ws_bytes, stream);
 }
 
 int mq_gemv_q6k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int cols, int splits,
-                        int chunks_per_split, void *ws, size_t ws_bytes, void *stream)
+                        int chunks_per_split, int tiles_per_item, void *ws, size_t ws_bytes,
+                        void *stream)
 {
-    if (splits < 1 || chunks_per_split < 1) return MQ_ERR_COVERAGE;
-    return gemv_common(6, Wp, q8, y, rows, cols, splits, chunks_per_split, ws, ws_bytes, stream);
+    const Plan p{splits, chunks_per_split, tiles_per_item};
+    return gemv_common(6, Wp, q8, y, rows, cols, &p, ws, ws_bytes, stream);
 }
 
 int mq_gemv_q4k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int cols, int splits,
-                        int chunks_per_split, void *ws, size_t ws_bytes, void *stream)
+                        int chunks_per_split, int tiles_per_item, void *ws, size_t ws_bytes,
+                        void *stream)
 {
-    if (splits < 1 || chunks_per_split < 1) return MQ_ERR_COVERAGE;
-    return gemv_common(4, Wp, q8, y, rows, cols, splits, chunks_per_split, ws, ws_bytes, stream);
+    const Plan p{splits, chunks_per_split, tiles_per_item};
+    return gemv_common(4, Wp, q8, y, rows, cols, &p, ws, ws_bytes, stream);
 }
 
 int mq_gemv_q6k_q8_subdots(const void *Wp, const void *q8, int32_t *isums, int rows, int cols,

@@ -11,25 +11,33 @@
 //   * The work is a pure HBM stream (page "67 · D3", §2.1: 93.4% of decode
 //     kernel time is weight streaming), so there are no tensor cores and no
 //     shared-memory staging: each lane issues 14 (q6_K) or 13 (q4_K)
-//     independent 16-byte loads per chunk (224 B in flight per lane), every
-//     warp-wide load instruction covers 512 contiguous bytes, and the weight
-//     loads bypass L1 (ld.global.nc.L1::no_allocate) because each byte is used
-//     once.
-//   * A warp owns one work item: 8 rows (a tile) x a contiguous range of
-//     4-super-block chunks.  Lane i owns unit i of every chunk for all 8 rows,
-//     so its activation codes (32 B + fp16 scale) are loaded once per chunk
-//     and reused 8 times from registers.
-//   * Per row the lane accumulates in f32 over its chunks in ascending order;
-//     the 8 row sums are then reduced across the warp with a fixed butterfly
-//     (9 shuffles).  With S > 1 splits per tile the warp writes its 8
-//     partials to a workspace and the split that arrives last (atomic ticket,
-//     no waiting) adds the S partials in ascending split order: the result
-//     does not depend on which split finishes first.  Page "74 · D4-2" (§2,
-//     §6) is why the host proves, before launch, that the splits cover every
-//     chunk exactly once.
+//     independent 16-byte loads per chunk, every warp-wide load instruction
+//     covers 512 contiguous bytes, and the weight loads bypass L1
+//     (ld.global.nc.L1::no_allocate) because each byte is used once.
+//   * Two register buffers per lane: chunk u+1 is in flight while chunk u is
+//     being computed, so a warp always has ~7 KB of loads outstanding.
+//   * One resident wave of warps: the host sizes the grid to the number of
+//     warps the SMs can hold.  A warp's work item is a contiguous run of
+//     chunk units: whole 8-row tiles when there are more tiles than warps,
+//     else one of `splits` tile-aligned column ranges of a tile ("split-K",
+//     the tall-row case of page "74 · D4-2", §2).  Lane i owns unit i of each
+//     chunk for the tile's 8 rows, so its activation codes are loaded once
+//     per chunk and reused 8 times.
+//   * A whole tile is reduced (fixed 9-shuffle butterfly) and written
+//     directly.  A split leaves its 8 partial sums in the workspace; the split
+//     that arrives last (atomic ticket, no waiting) loads all of them at once
+//     and adds them in ascending split order, so the result does not depend
+//     on arrival order.  The host proves before launch that the splits cover
+//     every chunk exactly once (the page's §6 lesson).
+//   * With programmatic dependent launch the first chunk's weight loads are
+//     issued before griddepcontrol.wait, so the weight stream starts while
+//     the preceding kernel (the q8 producer) drains; the activation, the
+//     output and the workspace are touched only after the wait.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 #include "kernels.h"
 #include "layout.h"
@@ -45,15 +53,15 @@ constexpr uint32_t kOnes = 0x01010101u;
 __device__ __forceinline__ uint4 ld_stream16(const uint8_t *p)
 {
     uint4 v;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
     return v;
 }
 __device__ __forceinline__ uint32_t ld_stream4(const uint8_t *p)
 {
     uint32_t v;
-    asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
     return v;
 }
 
@@ -71,24 +79,6 @@ __device__ __forceinline__ float half_hi(uint32_t w)
     return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
 }
 
-// Activation unit: the 32 int8 codes of q8 block U and its fp16 scale.
-struct Act {
-    uint4 xa, xb;  // codes 0..15, 16..31
-    float d8;
-};
-
-__device__ __forceinline__ Act load_act(const GemvLaunch &a, int U)
-{
-    Act x;
-    const uint4 *qs = reinterpret_cast<const uint4 *>(a.q8 + (size_t)U * 32);
-    x.xa = __ldg(qs);
-    x.xb = __ldg(qs + 1);
-    const unsigned short dh =
-        __ldg(reinterpret_cast<const unsigned short *>(a.q8 + a.q8_d_off) + U);
-    x.d8 = __half2float(__ushort_as_half(dh));
-    return x;
-}
-
 __device__ __forceinline__ int sum16(const uint4 &v)
 {
     int s = __dp4a((int)v.x, (int)kOnes, 0);
@@ -97,105 +87,182 @@ __device__ __forceinline__ int sum16(const uint4 &v)
     return __dp4a((int)v.w, (int)kOnes, s);
 }
 
-// ---- q6_K: one lane, one chunk, 8 rows --------------------------------------
+// Where chunk (t, c) of the matrix lives, for this lane.
+struct Unit {
+    const uint8_t *seg;  // chunk base
+    int t, c, cb;        // tile, chunk within the tile, blocks in the chunk
+    bool active;         // this lane owns a unit of the chunk
+};
+
+__device__ __forceinline__ Unit locate(const GemvLaunch &a, int t, int c, int lane, int chunk_bytes)
+{
+    Unit x;
+    x.t = t;
+    x.c = c;
+    x.cb = min(kChunkBlocks, a.nb - kChunkBlocks * c);
+    x.seg = a.W + (size_t)t * a.tile_bytes + (size_t)c * chunk_bytes;
+    x.active = lane < 8 * x.cb;
+    return x;
+}
+
+// ---- q6_K ------------------------------------------------------------------
 // Unit codes for row r: QL word m holds the low 4 bits of weights 4m..4m+3
 // (low nibbles) and 16+4m..16+4m+3 (high nibbles); QH word h byte k holds
 // the 2-bit highs of weights 16h+4m+k at bits 2m.  q - 32 is never formed:
 // isum = dot(q, x) - 32 * sum(x) is the same integer.
-template <bool SUBDOTS>
-__device__ __forceinline__ void q6k_chunk(const GemvLaunch &a, const uint8_t *seg, int cb,
-                                          int lane, int c, int t, float (&acc)[8])
+struct Q6kRegs {
+    uint4 ql[8], qh[4], sc, dd;  // weights of one chunk (8 rows)
+    uint4 xa, xb;                // activation codes 0..15, 16..31 of the unit
+    unsigned short dh;           // activation fp16 scale
+};
+
+__device__ __forceinline__ void load_w(const Unit &x, int lane, Q6kRegs &R)
 {
-    const int nu = 8 * cb;
-    const Act x = load_act(a, 32 * c + lane);
-    const int xs0 = sum16(x.xa), xs1 = sum16(x.xb);
-
-    uint4 ql[8], qh[4];
+    const int nu = 8 * x.cb, cb = x.cb;
+    if (x.active) {
 #pragma unroll
-    for (int r = 0; r < 8; ++r) ql[r] = ld_stream16(seg + ((size_t)r * nu + lane) * 16);
+        for (int r = 0; r < 8; ++r) R.ql[r] = ld_stream16(x.seg + ((size_t)r * nu + lane) * 16);
 #pragma unroll
-    for (int p = 0; p < 4; ++p)
-        qh[p] = ld_stream16(seg + (size_t)kQ6kQH * cb + ((size_t)p * nu + lane) * 16);
-    const uint4 sc = ld_stream16(seg + (size_t)kQ6kSC * cb + (size_t)lane * 16);
-    const uint4 dd = ld_stream16(seg + (size_t)kQ6kD * cb + (size_t)(lane >> 3) * 16);
+        for (int p = 0; p < 4; ++p)
+            R.qh[p] = ld_stream16(x.seg + (size_t)kQ6kQH * cb + ((size_t)p * nu + lane) * 16);
+        R.sc = ld_stream16(x.seg + (size_t)kQ6kSC * cb + (size_t)lane * 16);
+        R.dd = ld_stream16(x.seg + (size_t)kQ6kD * cb + (size_t)(lane >> 3) * 16);
+    } else {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) R.ql[r] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) R.qh[p] = make_uint4(0, 0, 0, 0);
+        R.sc = R.dd = make_uint4(0, 0, 0, 0);
+    }
+}
 
+__device__ __forceinline__ void load_x(const GemvLaunch &a, const Unit &x, int lane, Q6kRegs &R)
+{
+    if (x.active) {
+        const int U = 32 * x.c + lane;
+        const uint4 *qs = reinterpret_cast<const uint4 *>(a.q8 + (size_t)U * 32);
+        R.xa = __ldg(qs);
+        R.xb = __ldg(qs + 1);
+        R.dh = __ldg(reinterpret_cast<const unsigned short *>(a.q8 + a.q8_d_off) + U);
+    } else {
+        R.xa = R.xb = make_uint4(0, 0, 0, 0);
+        R.dh = 0;
+    }
+}
+
+template <bool SUBDOTS>
+__device__ __forceinline__ void compute(const GemvLaunch &a, const Q6kRegs &R, const Unit &x,
+                                        int lane, float (&acc)[8])
+{
+    const float d8 = __half2float(__ushort_as_half(R.dh));
+    const int xs0 = sum16(R.xa), xs1 = sum16(R.xb);
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-        const uint32_t h0 = (r & 1) ? qh[r >> 1].z : qh[r >> 1].x;
-        const uint32_t h1 = (r & 1) ? qh[r >> 1].w : qh[r >> 1].y;
+        const uint32_t h0 = (r & 1) ? R.qh[r >> 1].z : R.qh[r >> 1].x;
+        const uint32_t h1 = (r & 1) ? R.qh[r >> 1].w : R.qh[r >> 1].y;
         int dot0 = 0, dot1 = 0;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            const uint32_t w = word(ql[r], m);
+            const uint32_t w = word(R.ql[r], m);
             const uint32_t q0 = (w & kLo4) | (((h0 >> (2 * m)) & 0x03030303u) << 4);
             const uint32_t q1 = ((w >> 4) & kLo4) | (((h1 >> (2 * m)) & 0x03030303u) << 4);
-            dot0 = __dp4a((int)q0, (int)word(x.xa, m), dot0);
-            dot1 = __dp4a((int)q1, (int)word(x.xb, m), dot1);
+            dot0 = __dp4a((int)q0, (int)word(R.xa, m), dot0);
+            dot1 = __dp4a((int)q1, (int)word(R.xb, m), dot1);
         }
         const int isum0 = dot0 - 32 * xs0;
         const int isum1 = dot1 - 32 * xs1;
-        const uint32_t scw = word(sc, r >> 1) >> (16 * (r & 1));
+        const uint32_t scw = word(R.sc, r >> 1) >> (16 * (r & 1));
         const int sc0 = (int)(int8_t)(scw & 0xffu);
         const int sc1 = (int)(int8_t)((scw >> 8) & 0xffu);
         if (SUBDOTS) {
-            const int row = t * kTileRows + r;
-            if (row < a.rows) {
-                const int blk = kChunkBlocks * c + (lane >> 3), p = lane & 7;
+            const int row = x.t * kTileRows + r;
+            if (x.active && row < a.rows) {
+                const int blk = kChunkBlocks * x.c + (lane >> 3), p = lane & 7;
                 int32_t *o = a.isums + ((size_t)row * a.nb + blk) * 16 + 2 * p;
                 o[0] = isum0;
                 o[1] = isum1;
             }
         } else {
-            const float d = (r & 1) ? half_hi(word(dd, r >> 1)) : half_lo(word(dd, r >> 1));
-            acc[r] = fmaf(d * x.d8, (float)(sc0 * isum0 + sc1 * isum1), acc[r]);
+            const float d = (r & 1) ? half_hi(word(R.dd, r >> 1)) : half_lo(word(R.dd, r >> 1));
+            acc[r] = fmaf(d * d8, (float)(sc0 * isum0 + sc1 * isum1), acc[r]);
         }
     }
 }
 
-// ---- q4_K: one lane, one chunk, 8 rows --------------------------------------
-template <bool SUBDOTS>
-__device__ __forceinline__ void q4k_chunk(const GemvLaunch &a, const uint8_t *seg, int cb,
-                                          int lane, int c, int t, float (&acc)[8])
+// ---- q4_K ------------------------------------------------------------------
+struct Q4kRegs {
+    uint4 qs[8], dm0, dm1;       // nibbles of 8 rows; (d, dmin) of 8 rows
+    uint32_t s0, s1, s2;         // 6-bit scales and mins of 8 rows, packed
+    uint4 xa, xb;
+    unsigned short dh;
+    int qsum;
+};
+
+__device__ __forceinline__ void load_w(const Unit &x, int lane, Q4kRegs &R)
 {
-    const int nu = 8 * cb;
-    const int U = 32 * c + lane;
-    const Act x = load_act(a, U);
-    const int qsum = __ldg(reinterpret_cast<const int *>(a.q8 + a.q8_sum_off) + U);
-
-    uint4 qs[8];
+    const int nu = 8 * x.cb, cb = x.cb;
+    if (x.active) {
 #pragma unroll
-    for (int r = 0; r < 8; ++r) qs[r] = ld_stream16(seg + ((size_t)r * nu + lane) * 16);
-    const uint8_t *smp = seg + (size_t)kQ4kSM * cb + (size_t)lane * 4;
-    const uint32_t s0 = ld_stream4(smp);
-    const uint32_t s1 = ld_stream4(smp + (size_t)nu * 4);
-    const uint32_t s2 = ld_stream4(smp + (size_t)nu * 8);
-    const uint8_t *dmp = seg + (size_t)kQ4kDM * cb + (size_t)(lane >> 3) * 32;
-    const uint4 dm0 = ld_stream16(dmp);
-    const uint4 dm1 = ld_stream16(dmp + 16);
+        for (int r = 0; r < 8; ++r) R.qs[r] = ld_stream16(x.seg + ((size_t)r * nu + lane) * 16);
+        const uint8_t *smp = x.seg + (size_t)kQ4kSM * cb + (size_t)lane * 4;
+        R.s0 = ld_stream4(smp);
+        R.s1 = ld_stream4(smp + (size_t)nu * 4);
+        R.s2 = ld_stream4(smp + (size_t)nu * 8);
+        const uint8_t *dmp = x.seg + (size_t)kQ4kDM * cb + (size_t)(lane >> 3) * 32;
+        R.dm0 = ld_stream16(dmp);
+        R.dm1 = ld_stream16(dmp + 16);
+    } else {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) R.qs[r] = make_uint4(0, 0, 0, 0);
+        R.s0 = R.s1 = R.s2 = 0;
+        R.dm0 = R.dm1 = make_uint4(0, 0, 0, 0);
+    }
+}
 
+__device__ __forceinline__ void load_x(const GemvLaunch &a, const Unit &x, int lane, Q4kRegs &R)
+{
+    if (x.active) {
+        const int U = 32 * x.c + lane;
+        const uint4 *qs = reinterpret_cast<const uint4 *>(a.q8 + (size_t)U * 32);
+        R.xa = __ldg(qs);
+        R.xb = __ldg(qs + 1);
+        R.dh = __ldg(reinterpret_cast<const unsigned short *>(a.q8 + a.q8_d_off) + U);
+        R.qsum = __ldg(reinterpret_cast<const int *>(a.q8 + a.q8_sum_off) + U);
+    } else {
+        R.xa = R.xb = make_uint4(0, 0, 0, 0);
+        R.dh = 0;
+        R.qsum = 0;
+    }
+}
+
+template <bool SUBDOTS>
+__device__ __forceinline__ void compute(const GemvLaunch &a, const Q4kRegs &R, const Unit &x,
+                                        int lane, float (&acc)[8])
+{
+    const float d8 = __half2float(__ushort_as_half(R.dh));
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
         int dot = 0;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            const uint32_t w = word(qs[r], m);
-            dot = __dp4a((int)(w & kLo4), (int)word(x.xa, m), dot);
-            dot = __dp4a((int)((w >> 4) & kLo4), (int)word(x.xb, m), dot);
+            const uint32_t w = word(R.qs[r], m);
+            dot = __dp4a((int)(w & kLo4), (int)word(R.xa, m), dot);
+            dot = __dp4a((int)((w >> 4) & kLo4), (int)word(R.xb, m), dot);
         }
         if (SUBDOTS) {
-            const int row = t * kTileRows + r;
-            if (row < a.rows) {
-                const int blk = kChunkBlocks * c + (lane >> 3), k = lane & 7;
+            const int row = x.t * kTileRows + r;
+            if (x.active && row < a.rows) {
+                const int blk = kChunkBlocks * x.c + (lane >> 3), k = lane & 7;
                 a.isums[((size_t)row * a.nb + blk) * 8 + k] = dot;
             }
         } else {
-            const int hi = (int)((s2 >> (4 * r)) & 15u);
-            const int sc = (int)((s0 >> (4 * r)) & 15u) | ((hi & 3) << 4);
-            const int mn = (int)((s1 >> (4 * r)) & 15u) | ((hi >> 2) << 4);
-            const uint32_t dmw = word(r < 4 ? dm0 : dm1, r & 3);
+            const int hi = (int)((R.s2 >> (4 * r)) & 15u);
+            const int sc = (int)((R.s0 >> (4 * r)) & 15u) | ((hi & 3) << 4);
+            const int mn = (int)((R.s1 >> (4 * r)) & 15u) | ((hi >> 2) << 4);
+            const uint32_t dmw = word(r < 4 ? R.dm0 : R.dm1, r & 3);
             const float d = half_lo(dmw), dmin = half_hi(dmw);
-            const float term = fmaf(d, (float)(sc * dot), -dmin * (float)(mn * qsum));
-            acc[r] = fmaf(x.d8, term, acc[r]);
+            const float term = fmaf(d, (float)(sc * dot), -dmin * (float)(mn * R.qsum));
+            acc[r] = fmaf(d8, term, acc[r]);
         }
     }
 }
@@ -227,49 +294,30 @@ __device__ __forceinline__ float reduce8(const float (&acc)[8], int lane)
     return v;
 }
 
-template <int FMT, bool SUBDOTS>  // FMT 6 = q6_K, 4 = q4_K
-__global__ void __launch_bounds__(32 * kGemvWarpsPerBlock) gemv_kernel(const GemvLaunch a)
+// Tile t is finished for this warp (work item `item`, covering units
+// [u0, u1)): write it, or hand its partial to the tile's last arriver.
+__device__ __forceinline__ void flush_tile(const GemvLaunch &a, int t, float (&acc)[8], int item,
+                                           int u0, int u1, int lane)
 {
-    const int lane = threadIdx.x & 31;
-    const long long item = (long long)blockIdx.x * kGemvWarpsPerBlock + (threadIdx.x >> 5);
-    if (item >= a.n_items) return;  // whole warp; the kernel has no block barrier
-    const int t = (int)(item / a.splits);
-    const int s = (int)(item - (long long)t * a.splits);
-    const int c0 = s * a.cps;
-    const int c1 = min(c0 + a.cps, a.nchunks);
-    const uint8_t *tile = a.W + (size_t)t * a.tile_bytes;
-    constexpr int kChunkBytes = (FMT == 6 ? kQ6kChunkPerBlock : kQ4kChunkPerBlock) * kChunkBlocks;
-
-    float acc[8];
+    const float v = reduce8(acc, lane);
 #pragma unroll
     for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
-    for (int c = c0; c < c1; ++c) {
-        const int cb = min(kChunkBlocks, a.nb - kChunkBlocks * c);
-        if (lane < 8 * cb) {
-            const uint8_t *seg = tile + (size_t)c * kChunkBytes;
-            if (FMT == 6)
-                q6k_chunk<SUBDOTS>(a, seg, cb, lane, c, t, acc);
-            else
-                q4k_chunk<SUBDOTS>(a, seg, cb, lane, c, t, acc);
-        }
-    }
-    if (SUBDOTS) return;
-
-    const float v = reduce8(acc, lane);
     const int row0 = t * kTileRows;
-    if (a.splits == 1) {
+    const int tu0 = t * a.nchunks, tu1 = tu0 + a.nchunks;
+    if (tu0 >= u0 && tu1 <= u1) {  // whole tile in this range
         if ((lane & 3) == 0 && row0 + (lane >> 2) < a.rows) a.y[row0 + (lane >> 2)] = v;
         return;
     }
-    // split-K: lane 0 publishes the 8 partials, then takes a ticket.
-    float part[8];
+    // one split of tile t (splits > 1): lane 0 publishes the 8 partials,
+    // fences them and takes a ticket (writer and ticket holder are one thread)
+    float *dst = a.ws_part + (size_t)item * 8;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) part[k] = __shfl_sync(kFull, v, 4 * k);
+    for (int k = 0; k < 8; ++k) {
+        const float pk = __shfl_sync(kFull, v, 4 * k);
+        if (lane == 0) dst[k] = pk;
+    }
     int last = 0;
     if (lane == 0) {
-        float4 *dst = reinterpret_cast<float4 *>(a.ws_part + ((size_t)s * a.ntiles + t) * 8);
-        dst[0] = make_float4(part[0], part[1], part[2], part[3]);
-        dst[1] = make_float4(part[4], part[5], part[6], part[7]);
         __threadfence();
         const unsigned prev = atomicAdd(a.ws_cnt + t, 1u);
         last = prev == (unsigned)(a.splits - 1);
@@ -277,21 +325,82 @@ __global__ void __launch_bounds__(32 * kGemvWarpsPerBlock) gemv_kernel(const Gem
     last = __shfl_sync(kFull, last, 0);
     if (!last) return;
     __threadfence();
-    if (lane < 8) {
-        float sum = 0.0f;
-        for (int k = 0; k < a.splits; ++k)
-            sum += __ldcg(a.ws_part + ((size_t)k * a.ntiles + t) * 8 + lane);
-        if (row0 + lane < a.rows) a.y[row0 + lane] = sum;
+    // last arriver: lane (4g + ...) loads split base+g of row lane&7, four
+    // splits per round trip; lanes 0..7 add them in ascending split order.
+    const float *base_ptr = a.ws_part + (size_t)t * a.splits * 8;
+    float sum = 0.0f;
+    for (int base = 0; base < a.splits; base += 4) {
+        const int s = base + (lane >> 3);
+        const float p = s < a.splits ? __ldcg(base_ptr + (size_t)s * 8 + (lane & 7)) : 0.0f;
+        const float p1 = __shfl_down_sync(kFull, p, 8);
+        const float p2 = __shfl_down_sync(kFull, p, 16);
+        const float p3 = __shfl_down_sync(kFull, p, 24);
+        sum = (((sum + p) + p1) + p2) + p3;
     }
+    if (lane < 8 && row0 + lane < a.rows) a.y[row0 + lane] = sum;
     if (lane == 0) a.ws_cnt[t] = 0u;  // ready for the next call
+}
+
+template <int FMT, bool SUBDOTS>  // FMT 6 = q6_K, 4 = q4_K
+__global__ void __launch_bounds__(32 * kGemvWarpsPerBlock, 3) gemv_kernel(const GemvLaunch a)
+{
+    using Regs = typename std::conditional<FMT == 6, Q6kRegs, Q4kRegs>::type;
+    constexpr int kChunkBytes = (FMT == 6 ? kQ6kChunkPerBlock : kQ4kChunkPerBlock) * kChunkBlocks;
+    const int lane = threadIdx.x & 31;
+    const int item = blockIdx.x * kGemvWarpsPerBlock + (threadIdx.x >> 5);
+    griddep_launch_dependents();
+    if (item >= a.n_items) return;  // whole warp; the kernel has no block barrier
+    const int nch = a.nchunks;
+    int u0, u1;
+    if (a.splits > 1) {
+        const int tt = item / a.splits, s = item - tt * a.splits;
+        u0 = tt * nch + s * a.cps;
+        u1 = tt * nch + min(s * a.cps + a.cps, nch);
+    } else {
+        u0 = item * a.tpi * nch;
+        u1 = min(u0 + a.tpi * nch, a.ntiles * nch);
+    }
+
+    Regs A, B;
+    int t = u0 / nch, c = u0 - t * nch;  // position of the next chunk to load
+    Unit xa = locate(a, t, c, lane, kChunkBytes), xb;
+    load_w(xa, lane, A);   // weights do not depend on the preceding kernel
+    griddep_wait();        // the q8 plane, y and the workspace do
+    load_x(a, xa, lane, A);
+    if (++c == nch) { c = 0; ++t; }
+
+    float acc[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
+    for (int u = u0; u < u1; u += 2) {
+        const bool has_b = u + 1 < u1;
+        if (has_b) {
+            xb = locate(a, t, c, lane, kChunkBytes);
+            load_w(xb, lane, B);
+            load_x(a, xb, lane, B);
+            if (++c == nch) { c = 0; ++t; }
+        }
+        compute<SUBDOTS>(a, A, xa, lane, acc);
+        if (!SUBDOTS && (!has_b || xb.t != xa.t)) flush_tile(a, xa.t, acc, item, u0, u1, lane);
+        if (!has_b) break;
+        const bool has_a = u + 2 < u1;
+        if (has_a) {
+            xa = locate(a, t, c, lane, kChunkBytes);
+            load_w(xa, lane, A);
+            load_x(a, xa, lane, A);
+            if (++c == nch) { c = 0; ++t; }
+        }
+        compute<SUBDOTS>(a, B, xb, lane, acc);
+        if (!SUBDOTS && (!has_a || xa.t != xb.t)) flush_tile(a, xb.t, acc, item, u0, u1, lane);
+    }
 }
 
 template <int FMT, bool SUBDOTS>
 cudaError_t launch(const GemvLaunch &a, cudaStream_t st)
 {
     const long long blocks = (a.n_items + kGemvWarpsPerBlock - 1) / kGemvWarpsPerBlock;
-    gemv_kernel<FMT, SUBDOTS><<<(unsigned)blocks, 32 * kGemvWarpsPerBlock, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_maybe_pdl(gemv_kernel<FMT, SUBDOTS>, dim3((unsigned)blocks),
+                            dim3(32 * kGemvWarpsPerBlock), a.pdl, st, a);
 }
 
 }  // namespace
@@ -300,5 +409,16 @@ cudaError_t launch_gemv_q6k(const GemvLaunch &a, cudaStream_t st) { return launc
 cudaError_t launch_gemv_q4k(const GemvLaunch &a, cudaStream_t st) { return launch<4, false>(a, st); }
 cudaError_t launch_subdots_q6k(const GemvLaunch &a, cudaStream_t st) { return launch<6, true>(a, st); }
 cudaError_t launch_subdots_q4k(const GemvLaunch &a, cudaStream_t st) { return launch<4, true>(a, st); }
+
+int gemv_resident_warps_per_sm(int fmt)
+{
+    int blocks = 0;
+    const cudaError_t e =
+        fmt == 6 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemv_kernel<6, false>,
+                                                                 32 * kGemvWarpsPerBlock, 0)
+                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemv_kernel<4, false>,
+                                                                 32 * kGemvWarpsPerBlock, 0);
+    return e == cudaSuccess ? blocks * kGemvWarpsPerBlock : 0;
+}
 
 }  // namespace mq

@@ -64,6 +64,8 @@ __global__ void __launch_bounds__(256) quantize_q8_kernel(const float *__restric
                                                           uint8_t *__restrict__ q8, int n4,
                                                           unsigned d_off, unsigned sum_off)
 {
+    griddep_launch_dependents();
+    griddep_wait();  // x may come from the preceding kernel
     const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const bool valid = gid < n4;
     const float4 v = valid ? __ldg(reinterpret_cast<const float4 *>(x) + gid)
@@ -78,6 +80,8 @@ __global__ void __launch_bounds__(256) swiglu_quant_q8_kernel(const float *g, co
                                                               int n4, unsigned d_off,
                                                               unsigned sum_off)
 {
+    griddep_launch_dependents();
+    griddep_wait();  // g and u may come from the preceding kernels
     const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const bool valid = gid < n4;
     float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -104,6 +108,8 @@ __global__ void __launch_bounds__(kRmsThreads) rmsnorm_quant_q8_kernel(
 {
     __shared__ float warp_ss[kRmsThreads / 32];
     __shared__ float scale_sh;
+    griddep_launch_dependents();
+    griddep_wait();  // x may come from the preceding kernel
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int n4 = n >> 2;
     const float4 *x4 = reinterpret_cast<const float4 *>(x);
@@ -157,27 +163,27 @@ inline unsigned blocks_for(long long threads, int per_block)
 }  // namespace
 
 cudaError_t launch_quantize_q8(const float *x, uint8_t *q8, int n, unsigned d_off,
-                               unsigned sum_off, cudaStream_t st)
+                               unsigned sum_off, int pdl, cudaStream_t st)
 {
     const int n4 = n / 4;
-    quantize_q8_kernel<<<blocks_for(n4, 256), 256, 0, st>>>(x, q8, n4, d_off, sum_off);
-    return cudaGetLastError();
+    return launch_maybe_pdl(quantize_q8_kernel, dim3(blocks_for(n4, 256)), dim3(256), pdl, st, x, q8,
+                            n4, d_off, sum_off);
 }
 
 cudaError_t launch_swiglu_quant_q8(const float *g, const float *u, float *y, uint8_t *q8, int n,
-                                   unsigned d_off, unsigned sum_off, cudaStream_t st)
+                                   unsigned d_off, unsigned sum_off, int pdl, cudaStream_t st)
 {
     const int n4 = n / 4;
-    swiglu_quant_q8_kernel<<<blocks_for(n4, 256), 256, 0, st>>>(g, u, y, q8, n4, d_off, sum_off);
-    return cudaGetLastError();
+    return launch_maybe_pdl(swiglu_quant_q8_kernel, dim3(blocks_for(n4, 256)), dim3(256), pdl, st,
+                            g, u, y, q8, n4, d_off, sum_off);
 }
 
 cudaError_t launch_rmsnorm_quant_q8(const float *x, const float *gain, float eps, float *y,
-                                    uint8_t *q8, int n, unsigned d_off, unsigned sum_off,
+                                    uint8_t *q8, int n, unsigned d_off, unsigned sum_off, int pdl,
                                     cudaStream_t st)
 {
-    rmsnorm_quant_q8_kernel<<<1, kRmsThreads, 0, st>>>(x, gain, eps, y, q8, n, d_off, sum_off);
-    return cudaGetLastError();
+    return launch_maybe_pdl(rmsnorm_quant_q8_kernel, dim3(1), dim3(kRmsThreads), pdl, st, x, gain,
+                            eps, y, q8, n, d_off, sum_off);
 }
 
 }  // namespace mq

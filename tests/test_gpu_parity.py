@@ -50,10 +50,8 @@ def q8_fields(mq, plane, n):
 
 
 def gemv(mq, fmt, Wp, q8, rows, cols, plan=None, ws=None):
-    if plan is not None and plan[0] > 1 and ws is None:
-        ws = mq.mq_gemv_workspace(rows, cols, splits=plan[0])
-    elif plan is None and ws is None:
-        ws = mq.mq_gemv_workspace(rows, cols)
+    if ws is None:
+        ws = mq.mq_gemv_workspace(rows, cols, plan=plan)
     fn = mq.mq_gemv_q6k_q8 if fmt == "q6k" else mq.mq_gemv_q4k_q8
     return fn(Wp, q8, rows, cols, ws=ws, plan=plan)
 
@@ -162,10 +160,22 @@ def test_gemv_matches_oracle(mq, orc, fmt, rows, cols):
     assert_gemv_close(y, yref, absum)
 
 
+def all_plans(ntiles, nch):
+    plans = []
+    for s in range(2, nch + 1):
+        cps = -(-nch // s)
+        if (s - 1) * cps < nch:
+            plans.append((s, cps, 1))
+    plans += [(1, nch, tpi) for tpi in range(1, ntiles + 1)]
+    return plans
+
+
 @pytest.mark.parametrize("fmt", ["q6k", "q4k"])
-def test_every_split_plan_agrees_and_is_deterministic(mq, orc, fmt):
+def test_every_plan_agrees_and_is_deterministic(mq, orc, fmt):
+    """Every valid plan of a 5-tile x 19-chunk matrix (every split count,
+    every tiles-per-item) against the oracle, twice, bitwise repeatable."""
     import torch
-    rows, cols = 24, 18944                                  # 19 chunks per row
+    rows, cols = 37, 18944                                  # 5 tiles (ragged) x 19 chunks
     g = synth.rng("splits", fmt)
     W = synth.blocks(fmt, g, rows, cols)
     x = synth.normal(g, cols)
@@ -173,33 +183,32 @@ def test_every_split_plan_agrees_and_is_deterministic(mq, orc, fmt):
     plane = mq.mq_quantize_q8(dev(x))
     d0, q0, _ = orc.quantize_q8(x)
     yref, absum = orc.gemv(fmt, W, d0, q0, rows, cols)
-    nchunks = 19
-    for s in range(1, nchunks + 1):
-        cps = -(-nchunks // s)
-        if (s - 1) * cps >= nchunks:
-            continue
-        ws = mq.mq_gemv_workspace(rows, cols, splits=s)
-        y1 = host(gemv(mq, fmt, Wp, plane, rows, cols, plan=(s, cps), ws=ws))
-        y2 = host(gemv(mq, fmt, Wp, plane, rows, cols, plan=(s, cps), ws=ws))
+    for plan in all_plans(5, 19):
+        ws = mq.mq_gemv_workspace(rows, cols, plan=plan)
+        y1 = host(gemv(mq, fmt, Wp, plane, rows, cols, plan=plan, ws=ws))
+        y2 = host(gemv(mq, fmt, Wp, plane, rows, cols, plan=plan, ws=ws))
         assert_gemv_close(y1, yref, absum)
-        assert np.array_equal(y1, y2)                       # fixed combine order
+        assert np.array_equal(y1, y2), plan                 # fixed combine order
         if ws is not None:                                  # counters back to zero
-            ntiles = -(-rows // 8)
-            assert torch.count_nonzero(ws[:4 * ntiles]).item() == 0
+            assert torch.count_nonzero(ws[:4 * 5]).item() == 0
 
 
 def test_bad_plan_is_refused_and_nothing_runs(mq):
     import torch
-    rows, cols = 16, 18944
+    rows, cols = 16, 18944                                  # 2 tiles x 19 chunks
     g = synth.rng("badplan")
     W = synth.q6k_blocks(g, rows, cols)
     Wp = repack_dev(mq, "q6k", W, rows, cols)
     plane = mq.mq_quantize_q8(dev(synth.normal(g, cols)))
     y = torch.full((rows,), float("nan"), device="cuda")
-    ws = mq.mq_gemv_workspace(rows, cols, splits=5)
-    with pytest.raises(mq.MQError) as e:
-        mq.mq_gemv_q6k_q8(Wp, plane, rows, cols, y=y, ws=ws, plan=(5, 3))   # 15 of 19 chunks
-    assert e.value.status == mq.MQ_ERR_COVERAGE
+    ws = mq.mq_gemv_workspace(rows, cols, plan=(19, 1, 1))
+    # 15 of 19 chunks; an empty split; a one-split plan short of the row;
+    # splits together with multi-tile items
+    for bad in ((5, 3, 1), (10, 2, 2), (1, 18, 1), (4, 5, 2)):
+        with pytest.raises(mq.MQError) as e:
+            mq.mq_gemv_q6k_q8(Wp, plane, rows, cols, y=y, ws=ws, plan=bad)
+        assert e.value.status == mq.MQ_ERR_COVERAGE, bad
+    torch.cuda.synchronize()
     assert torch.isnan(y).all().item()
 
 

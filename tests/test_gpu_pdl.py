@@ -1,0 +1,113 @@
+"""Programmatic dependent launch: a decode chain whose kernels overlap must
+give exactly the results of the same chain launched without PDL, eagerly and
+under CUDA-graph capture, including the hazards PDL opens (a GEMV's output
+read by the next producer; a q8 plane rewritten by the next step's producer
+while the previous GEMV may still be reading it)."""
+import numpy as np
+import pytest
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mq():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quant_quantized_gemv_gb300 import build
+    build.build()
+    import quant_quantized_gemv_gb300 as m
+    m.lib()
+    yield m
+    m.mq_set_pdl(False)
+
+
+def dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+class FfnChain:
+    """rms -> gate, up (q4_K) -> swiglu -> down (q6_K): the FFN half of a
+    14B-shaped layer at reduced width, all buffers preallocated."""
+
+    def __init__(self, mq, hidden=2048, inter=5376):
+        import torch
+        g = synth.rng("pdl-chain")
+        self.mq, self.h, self.i = mq, hidden, inter
+        self.Wg_h = synth.q4k_blocks(g, inter, hidden)
+        self.Wu_h = synth.q4k_blocks(g, inter, hidden)
+        self.Wd_h = synth.q6k_blocks(g, hidden, inter)
+        self.Wg = dev(mq.mq_repack_q4k(self.Wg_h, inter, hidden))
+        self.Wu = dev(mq.mq_repack_q4k(self.Wu_h, inter, hidden))
+        self.Wd = dev(mq.mq_repack_q6k(self.Wd_h, hidden, inter))
+        self.x = torch.empty(hidden, device="cuda")
+        self.gain = dev(synth.normal(g, hidden, 1.0, 0.1))
+        self.xn = torch.empty(hidden, device="cuda")
+        self.q8a = torch.empty(mq.mq_q8_bytes(hidden), dtype=torch.uint8, device="cuda")
+        self.yg = torch.empty(inter, device="cuda")
+        self.yu = torch.empty(inter, device="cuda")
+        self.act = torch.empty(inter, device="cuda")
+        self.q8b = torch.empty(mq.mq_q8_bytes(inter), dtype=torch.uint8, device="cuda")
+        self.out = torch.empty(hidden, device="cuda")
+        self.wsg = mq.mq_gemv_workspace(inter, hidden)
+        self.wsd = mq.mq_gemv_workspace(hidden, inter)
+
+    def step(self):
+        mq = self.mq
+        mq.mq_rmsnorm_quant_q8(self.x, self.gain, 1e-6, y=self.xn, q8=self.q8a)
+        mq.mq_gemv_q4k_q8(self.Wg, self.q8a, self.i, self.h, y=self.yg, ws=self.wsg)
+        mq.mq_gemv_q4k_q8(self.Wu, self.q8a, self.i, self.h, y=self.yu, ws=self.wsg)
+        mq.mq_swiglu_quant_q8(self.yg, self.yu, y=self.act, q8=self.q8b)
+        mq.mq_gemv_q6k_q8(self.Wd, self.q8b, self.h, self.i, y=self.out, ws=self.wsd)
+
+
+def run_steps(mq, chain, xs, pdl, graph):
+    import torch
+    mq.mq_set_pdl(pdl)
+    outs = []
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        if graph:
+            chain.x.copy_(xs[0])
+            chain.step()                          # warm-up outside capture
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                chain.step()
+        for x in xs:
+            chain.x.copy_(x)
+            if graph:
+                g.replay()
+            else:
+                chain.step()
+            outs.append(chain.out.clone())
+    torch.cuda.synchronize()
+    mq.mq_set_pdl(False)
+    return [o.cpu().numpy() for o in outs]
+
+
+def test_pdl_chain_is_bitwise_identical(mq, orc):
+    chain = FfnChain(mq)
+    g = synth.rng("pdl-inputs")
+    xs = [dev(synth.normal(g, chain.h)) for _ in range(4)]
+    ref = run_steps(mq, chain, xs, pdl=False, graph=False)
+    for pdl, graph in ((True, False), (False, True), (True, True)):
+        got = run_steps(mq, chain, xs, pdl=pdl, graph=graph)
+        for a, b in zip(ref, got):
+            assert np.array_equal(a, b), (pdl, graph)
+    # and the chain itself against the oracle chain (from the f32 inputs only)
+    x0 = xs[-1].cpu().numpy()
+    xn = orc.rmsnorm(x0, chain.gain.cpu().numpy(), 1e-6).astype(np.float32)
+    d, q, _ = orc.quantize_q8(xn)
+    yg, _ = orc.gemv("q4k", chain.Wg_h, d, q, chain.i, chain.h, threads=8)
+    yu, _ = orc.gemv("q4k", chain.Wu_h, d, q, chain.i, chain.h, threads=8)
+    act = orc.swiglu(yg.astype(np.float32), yu.astype(np.float32)).astype(np.float32)
+    d2, q2, _ = orc.quantize_q8(act)
+    y, absum = orc.gemv("q6k", chain.Wd_h, d2, q2, chain.h, chain.i, threads=8)
+    # two f32 GEMV layers and a re-quantization sit between input and output:
+    # allow a few q8 code flips' worth (each |flip| <= d8 * |w|) beyond 1e-4
+    err = np.abs(ref[-1] - y)
+    assert np.all(err <= 1e-3 * absum), float(np.max(err / absum))

@@ -111,22 +111,30 @@ def test_unit_counts_match_pages(facts):
     assert 1024 * (5120 // 256) * facts["q6k_padded_stride"] == facts["attn_v_padded_bytes"]
 
 
-@pytest.mark.parametrize("sms", [1, 8, 76, 148, 152, 160])
-def test_plan_always_covers(mq, sms):
+@pytest.mark.parametrize("sms,warps", [(1, 4), (8, 12), (76, 12), (148, 8), (152, 12), (160, 16)])
+def test_plan_always_covers(mq, sms, warps):
     shapes = [(r, c) for r in (1, 5, 8, 64, 512, 1024, 3584, 5120, 13824, 152064)
               for c in (256, 1024, 1280, 2048, 5120, 13824, 18944, 32768)]
     for rows, cols in shapes:
-        s, cps = mq.mq_gemv_plan_for(rows, cols, sms)
-        nchunks = -(-(cols // 256) // 4)
-        assert mq.mq_check_coverage(nchunks, s, cps) == mq.MQ_OK, (rows, cols, sms, s, cps)
-        assert s * cps >= nchunks and (s - 1) * cps < nchunks
-        assert s == 1 or mq.mq_gemv_workspace_bytes_for(rows, s) > 0
+        s, cps, tpi = mq.mq_gemv_plan_for(rows, cols, sms, warps)
+        ntiles, nch = -(-rows // 8), -(-(cols // 256) // 4)
+        assert mq.mq_check_coverage(nch, s, cps) == mq.MQ_OK, (rows, cols, sms, s, cps)
+        assert s * cps >= nch and (s - 1) * cps < nch
+        items = ntiles * s if s > 1 else -(-ntiles // tpi)
+        assert items <= sms * warps                             # one resident wave
+        assert s == 1 or tpi == 1
+        ws = mq.mq_gemv_workspace_bytes_for(rows, cols, (s, cps, tpi))
+        assert (ws > 0) == (s > 1)
 
 
 def test_workspace_sizes(mq):
-    assert mq.mq_gemv_workspace_bytes_for(100, 1) == 0
-    tiles = 13
-    assert mq.mq_gemv_workspace_bytes_for(100, 3) == 64 + 3 * tiles * 8 * 4
+    # 100 rows -> 13 tiles; 4096 cols -> 4 chunks
+    assert mq.mq_gemv_workspace_bytes_for(100, 4096, (1, 4, 1)) == 0
+    assert mq.mq_gemv_workspace_bytes_for(100, 4096, (1, 4, 5)) == 0
+    assert mq.mq_gemv_workspace_bytes_for(100, 4096, (4, 1, 1)) == 64 + 13 * 4 * 8 * 4
+    assert mq.mq_gemv_workspace_bytes_for(100, 4096, (2, 2, 1)) == 64 + 13 * 2 * 8 * 4
+    assert mq.mq_gemv_workspace_bytes_for(100, 4096, (2, 1, 1)) == 0      # invalid: drops chunks
+    assert mq.mq_gemv_workspace_bytes_for(100, 4096, (2, 2, 3)) == 0      # invalid: splits with tpi
 
 
 @pytest.mark.skipif(__import__("torch").cuda.is_available(),
@@ -142,12 +150,16 @@ def test_validation_rejects_before_launch(mq):
     assert L.mq_gemv_q6k_q8(A, B, Y, 8, 1000, N, 0, S) == mq.MQ_ERR_SHAPE
     assert L.mq_gemv_q6k_q8(A, B, Y, 0, 1024, N, 0, S) == mq.MQ_ERR_SHAPE
     assert L.mq_gemv_q4k_q8(ctypes.c_void_p(0x10008), B, Y, 8, 1024, N, 0, S) == mq.MQ_ERR_ALIGN
-    # explicit plans that drop or duplicate work never launch
-    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 5, 3, N, 0, S) == mq.MQ_ERR_COVERAGE
-    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 19, 2, N, 0, S) == mq.MQ_ERR_COVERAGE
-    # a split plan without (enough) workspace never launches
-    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 5, 4, N, 0, S) == mq.MQ_ERR_NULL
-    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 5, 4, ctypes.c_void_p(0x40000), 16, S) == \
+    # 64 x 18944: 8 tiles x 19 chunks.  Plans that drop or duplicate work
+    # never launch
+    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 5, 3, 1, N, 0, S) == mq.MQ_ERR_COVERAGE
+    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 11, 2, 1, N, 0, S) == mq.MQ_ERR_COVERAGE
+    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 1, 18, 1, N, 0, S) == mq.MQ_ERR_COVERAGE
+    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 4, 5, 2, N, 0, S) == mq.MQ_ERR_COVERAGE
+    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 1, 19, 0, N, 0, S) == mq.MQ_ERR_COVERAGE
+    # a split plan needs (enough) workspace, or it never launches
+    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 4, 5, 1, N, 0, S) == mq.MQ_ERR_NULL
+    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 4, 5, 1, ctypes.c_void_p(0x40000), 16, S) == \
         mq.MQ_ERR_WORKSPACE
     assert L.mq_quantize_q8(A, B, 48, S) == mq.MQ_ERR_SHAPE
     assert L.mq_swiglu_quant_q8(A, B, N, Y, 64, S) == mq.MQ_ERR_NULL
