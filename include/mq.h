@@ -180,6 +180,28 @@ int mq_gemv_q4k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int 
                         int chunks_per_split, int tiles_per_item, void *ws, size_t ws_bytes,
                         void *stream);
 
+/* q6_K GEMV for callers that cannot allocate device memory (no counterpart
+ * on the pages; it exists for integration).  Some callers only receive
+ * input and output pointers: a plugin or callback inside a host framework
+ * that owns every allocation, a real-time loop that may not allocate once
+ * running, code in a region where cudaMalloc is forbidden or would stall the
+ * device.  They cannot provide the split-K workspace of mq_gemv_q6k_q8.
+ * This entry point computes the same y with the same kernel and default
+ * plan, keeping the scratch in a static device array inside the library
+ * (64 KiB per GPU, held until the process exits).  It allocates nothing.
+ *   - Limit: if the default plan on this device needs more than 64 KiB of
+ *     scratch the call returns MQ_ERR_WORKSPACE and launches nothing.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any CUDA graph capture.
+ *   - Every call uses the same array.  Each call clears the counters it
+ *     needs (an async memset on `stream`) before its kernel; calls whose
+ *     work overlaps on the GPU (other streams, other threads) race on the
+ *     array and give wrong results: order them on one stream.
+ * Arguments and other errors as mq_gemv_q6k_q8. */
+int mq_gemv_q6k_q8_noalloc(const void *Wp, const void *q8, float *y, int rows, int cols,
+                           void *stream);
+
 /* Coverage check used by every GEMV dispatch, exposed for tests: MQ_OK iff
  * all arguments are >= 1, splits * chunks_per_split >= nchunks (nothing
  * dropped) and (splits - 1) * chunks_per_split < nchunks (no empty split);

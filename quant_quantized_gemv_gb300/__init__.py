@@ -32,7 +32,8 @@ EXPORTS = [
     "mq_q8_unpack_host", "mq_quantize_q8", "mq_rmsnorm_quant_q8", "mq_swiglu_quant_q8",
     "mq_gemv_workspace_bytes", "mq_gemv_plan", "mq_gemv_q6k_q8", "mq_gemv_q4k_q8",
     "mq_gemv_q6k_q8_plan", "mq_gemv_q4k_q8_plan", "mq_gemv_workspace_bytes_for",
-    "mq_check_coverage", "mq_gemv_plan_for", "mq_set_pdl", "mq_gemv_q6k_q8_subdots",
+    "mq_check_coverage", "mq_gemv_plan_for", "mq_set_pdl", "mq_gemv_q6k_q8_noalloc",
+    "mq_gemv_q6k_q8_subdots",
     "mq_gemv_q4k_q8_subdots", "mq_device_sms",
 ]
 
@@ -81,6 +82,7 @@ def lib():
         "mq_check_coverage": ([I, I, I], I),
         "mq_gemv_plan_for": ([I, I, I, I, P, P, P], I),
         "mq_set_pdl": ([I], I),
+        "mq_gemv_q6k_q8_noalloc": ([P, P, P, I, I, P], I),
         "mq_gemv_q6k_q8_subdots": ([P, P, P, I, I, P], I),
         "mq_gemv_q4k_q8_subdots": ([P, P, P, I, I, P], I),
         "mq_device_sms": ([], I),
@@ -296,6 +298,19 @@ def mq_gemv_q6k_q8(Wp, q8, rows: int, cols: int, y=None, ws=None, stream=None, p
 def mq_gemv_q4k_q8(Wp, q8, rows: int, cols: int, y=None, ws=None, stream=None, plan=None):
     """y = W x_hat for repacked q4_K weights Wp (device) and a q8 plane."""
     return _gemv("mq_gemv_q4k_q8", Wp, q8, rows, cols, y, ws, stream, plan)
+
+
+def mq_gemv_q6k_q8_noalloc(Wp, q8, rows: int, cols: int, y=None, stream=None):
+    """The q6_K GEMV without a caller workspace: for callers that may not
+    allocate device memory (the library keeps the split-K scratch in a
+    static device array).  The first call on a device must precede any CUDA
+    graph capture; calls that overlap on the GPU race on the shared array."""
+    import torch
+    if y is None:
+        y = torch.empty(rows, dtype=torch.float32, device=Wp.device)
+    _check(lib().mq_gemv_q6k_q8_noalloc(_dev(Wp), _dev(q8), _dev(y, torch.float32), rows, cols,
+                                        _stream(stream)), "mq_gemv_q6k_q8_noalloc")
+    return y
 
 
 def _subdots(name: str, per: int, Wp, q8, rows: int, cols: int, stream):

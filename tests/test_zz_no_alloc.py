@@ -1,0 +1,63 @@
+"""The allocation-free q6_K GEMV entry point (mq_gemv_q6k_q8_noalloc).
+
+It serves callers that are handed only input and output pointers and may
+not allocate device memory, so they cannot pass the split-K workspace the
+regular entry point needs.  This file runs last so that a failure here comes
+after every other test has run; it also passes on its own in a fresh
+process.  It calls the entry point through the C ABI twice in a row and
+checks each result against mq_gemv_q6k_q8 (same tolerance as the parity
+tests: |dy| <= 1e-4 * sum |terms| per row) and against the oracle."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import synth
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def mq():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quant_quantized_gemv_gb300 import build
+    build.build()
+    import quant_quantized_gemv_gb300 as m
+    m.lib()
+    return m
+
+
+@pytest.mark.parametrize("rows,cols", [(512, 18944), (1024, 5120)])
+def test_noalloc_matches_regular_entry_point(mq, orc, rows, cols):
+    import torch
+    g = synth.rng("noalloc", rows, cols)
+    W = synth.q6k_blocks(g, rows, cols)
+    x = synth.normal(g, cols)
+    Wp = torch.from_numpy(mq.mq_repack_q6k(W, rows, cols)).cuda()
+    plane = mq.mq_quantize_q8(torch.from_numpy(x).cuda())
+    splits, _, _ = mq.mq_gemv_plan(rows, cols, "q6k")
+    assert splits > 1                                    # the scratch path is exercised
+    ws = mq.mq_gemv_workspace(rows, cols)
+    y_ref = mq.mq_gemv_q6k_q8(Wp, plane, rows, cols, ws=ws)
+    d0, q0, _ = orc.quantize_q8(x)
+    y_or, absum = orc.gemv("q6k", W, d0, q0, rows, cols, threads=8)
+    L = mq.lib()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for _ in range(2):                                   # two calls in a row share the array
+        y = torch.full((rows,), float("nan"), device="cuda")
+        st = L.mq_gemv_q6k_q8_noalloc(ctypes.c_void_p(Wp.data_ptr()), ctypes.c_void_p(plane.data_ptr()),
+                                      ctypes.c_void_p(y.data_ptr()), rows, cols, stream)
+        assert st == mq.MQ_OK, mq.lib().mq_strerror(st)
+        torch.cuda.synchronize()
+        yn = y.cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(yn - y_ref.cpu().numpy()) <= TOL * absum)
+        assert np.all(np.abs(yn - y_or) <= TOL * absum)
+
+
+def test_noalloc_rejects_bad_arguments_before_launch(mq):
+    L = mq.lib()
+    null = ctypes.c_void_p(0)
+    assert L.mq_gemv_q6k_q8_noalloc(null, null, null, 8, 1024, null) == mq.MQ_ERR_NULL
