@@ -135,29 +135,34 @@ int mq_swiglu_quant_q8(const float *g, const float *u, float *y, void *q8, int n
  * Work decomposition.  Rows are cut into tiles of 8 and each tile's columns
  * into nchunks = ceil(cols/1024) chunks of 4 super-blocks.  A plan is
  * (splits, chunks_per_split, tiles_per_item); one warp per work item:
+ *   splits == 1: every item covers tiles_per_item whole tiles;
+ *     chunks_per_split must still cover a row (>= nchunks).
  *   splits > 1 ("split-K", the tall-row case of [D4-2] §2): every tile is cut
  *     into `splits` tile-aligned ranges of chunks_per_split chunks (the last
- *     may be shorter); tiles_per_item must be 1.  Each split leaves its 8
- *     partial row sums in `ws`; the split that finishes last adds all of them
- *     in ascending split order (an atomic ticket; nothing waits or spins).
- *   splits == 1: every item covers tiles_per_item whole tiles, no workspace;
- *     chunks_per_split must still cover a row (>= nchunks).
+ *     may be shorter); tiles_per_item must be 1.  With splits <= 12 the
+ *     splits of a tile are the warps of one CTA and add their partial row
+ *     sums in shared memory in ascending split order.  With splits > 12 each
+ *     split leaves its partials in `ws` and the split that finishes last adds
+ *     all of them in ascending split order (an atomic ticket; nothing waits
+ *     or spins).
  * Before any launch the host checks the plan: splits * chunks_per_split >=
  * nchunks (no chunk dropped) and (splits - 1) * chunks_per_split < nchunks
  * (no empty split), else MQ_ERR_COVERAGE ([D4-2] §6 lesson 1: a gate must
- * bound both sides).  The default plan fills one resident wave of warps on
- * the current device: tiles_per_item = ceil(tiles / wave) when tiles exceed
- * the wave, else as many splits as the wave has room for.
+ * bound both sides).  The default plan fills one resident wave of the GPU:
+ * whole tiles when there are more tiles than warps, else the largest CTA
+ * split count whose one-CTA-per-tile grid fits the wave, and workspace splits
+ * only when that still leaves the wave less than half full (very few tiles,
+ * rows longer than 12 chunks).
  *
  * mq_gemv_workspace_bytes(rows, cols): workspace the default plans (q6_K and
- *   q4_K) need on the current device (0 when splits == 1).  ws must be device
- *   memory, zero-filled before its first use; every completed call leaves it
- *   zero-filled again.  ws may be NULL when 0 bytes are needed.
+ *   q4_K) need on the current device (0 unless splits > 12).  ws must be
+ *   device memory, zero-filled before its first use; every completed call
+ *   leaves it zero-filled again.  ws may be NULL when 0 bytes are needed.
  * mq_gemv_workspace_bytes_for: the same for an explicit plan (0 if invalid).
  * mq_gemv_plan: the default plan for format 6 (q6_K) or 4 (q4_K) on the
- *   current device.
- * mq_gemv_plan_for: the default plan for a device with `sms` SMs holding
- *   `warps_per_sm` GEMV warps each.  Host only.
+ *   current device (from the kernel's measured occupancy).
+ * mq_gemv_plan_for: the default plan for a device with `sms` SMs and a
+ *   kernel using regs_per_thread registers (64K registers per SM).  Host only.
  * mq_gemv_*_q8_plan: the GEMV with an explicit plan.
  * Errors: MQ_ERR_NULL, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_WORKSPACE,
  *         MQ_ERR_COVERAGE, MQ_ERR_CUDA.
@@ -167,7 +172,7 @@ size_t mq_gemv_workspace_bytes_for(int rows, int cols, int splits, int chunks_pe
                                    int tiles_per_item);
 int mq_gemv_plan(int rows, int cols, int fmt, int *splits, int *chunks_per_split,
                  int *tiles_per_item);
-int mq_gemv_plan_for(int rows, int cols, int sms, int warps_per_sm, int *splits,
+int mq_gemv_plan_for(int rows, int cols, int sms, int regs_per_thread, int *splits,
                      int *chunks_per_split, int *tiles_per_item);
 int mq_gemv_q6k_q8(const void *Wp, const void *q8, float *y, int rows, int cols, void *ws,
                    size_t ws_bytes, void *stream);
@@ -187,8 +192,9 @@ int mq_gemv_q4k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int 
  * running, code in a region where cudaMalloc is forbidden or would stall the
  * device.  They cannot provide the split-K workspace of mq_gemv_q6k_q8.
  * This entry point computes the same y with the same kernel and default
- * plan, keeping the scratch in a static device array inside the library
- * (64 KiB per GPU, held until the process exits).  It allocates nothing.
+ * plan; when that plan needs scratch (more than 12 splits per tile) it is
+ * kept in a static device array inside the library (64 KiB per GPU, held
+ * until the process exits).  It allocates nothing.
  *   - Limit: if the default plan on this device needs more than 64 KiB of
  *     scratch the call returns MQ_ERR_WORKSPACE and launches nothing.
  *   - The first call on each device looks up the array's device address

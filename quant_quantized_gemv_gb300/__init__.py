@@ -242,9 +242,9 @@ def mq_gemv_plan(rows: int, cols: int, fmt: str = "q6k"):
     return _plan_out(lib().mq_gemv_plan, rows, cols, 6 if fmt == "q6k" else 4)
 
 
-def mq_gemv_plan_for(rows: int, cols: int, sms: int, warps_per_sm: int):
-    """Default plan for a device with `sms` SMs x `warps_per_sm` GEMV warps."""
-    return _plan_out(lib().mq_gemv_plan_for, rows, cols, sms, warps_per_sm)
+def mq_gemv_plan_for(rows: int, cols: int, sms: int, regs_per_thread: int = 168):
+    """Default plan for a device with `sms` SMs and a kernel of regs_per_thread registers."""
+    return _plan_out(lib().mq_gemv_plan_for, rows, cols, sms, regs_per_thread)
 
 
 def mq_set_pdl(enable: bool) -> bool:

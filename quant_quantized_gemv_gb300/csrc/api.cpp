@@ -16,7 +16,8 @@ using namespace mq;
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sms[kMaxDevices];
-std::atomic<int> g_warps[kMaxDevices][2];  // resident GEMV warps per SM: [q6_K, q4_K]
+// resident GEMV CTAs per SM: [device][q6_K, q4_K][warps per CTA]
+std::atomic<int> g_ctas[kMaxDevices][2][kMaxCtaSplits + 1];
 std::atomic<int> g_pdl{0};
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -46,36 +47,75 @@ int device_sms()
     return v;
 }
 
-int resident_warps(int fmt)
+// ctas[w], w = 1..kMaxCtaSplits: resident GEMV CTAs per SM with w warps each.
+struct Occupancy {
+    int ctas[kMaxCtaSplits + 1];
+};
+
+bool device_occupancy(int fmt, Occupancy *o)
 {
     const int dev = current_device();
-    if (dev < 0) return 0;
-    std::atomic<int> &slot = g_warps[dev][fmt == 6 ? 0 : 1];
-    int v = slot.load(std::memory_order_relaxed);
-    if (v > 0) return v;
-    v = gemv_resident_warps_per_sm(fmt);
-    if (v > 0) slot.store(v, std::memory_order_relaxed);
-    return v;
+    if (dev < 0) return false;
+    for (int w = 1; w <= kMaxCtaSplits; ++w) {
+        std::atomic<int> &slot = g_ctas[dev][fmt == 6 ? 0 : 1][w];
+        int v = slot.load(std::memory_order_relaxed);
+        if (v <= 0) {
+            v = gemv_ctas_per_sm(fmt, w);
+            if (v <= 0) return false;
+            slot.store(v, std::memory_order_relaxed);
+        }
+        o->ctas[w] = v;
+    }
+    return true;
+}
+
+// The same from a register count (host-only planning, tests): 64K registers
+// per SM, at most 2048 threads and 32 CTAs.
+Occupancy model_occupancy(int regs_per_thread)
+{
+    Occupancy o;
+    const int regs = ((regs_per_thread + 7) / 8) * 8;
+    for (int w = 1; w <= kMaxCtaSplits; ++w) {
+        int c = 65536 / (w * 32 * regs);
+        if (c > 2048 / (32 * w)) c = 2048 / (32 * w);
+        if (c > 32) c = 32;
+        o.ctas[w] = c;
+    }
+    return o;
 }
 
 struct Plan {
     int splits, cps, tpi;
 };
 
-// One resident wave of warps.  More tiles than warps: whole tiles per warp
-// (tpi of them, no combine).  Fewer: cut each tile's chunks into as many
-// tile-aligned splits as the wave has room for.
-Plan plan_for(int ntiles, int nchunks, int sms, int warps_per_sm)
+// One resident wave.  Enough tiles: whole tiles per warp.  Fewer: one CTA
+// per tile whose warps are the tile's splits (the largest split count whose
+// grid still fits one wave).  Very few tiles with long rows: warp splits
+// that meet in the workspace, as many as the wave holds.
+Plan plan_for(int ntiles, int nchunks, int sms, const Occupancy &o)
 {
     if (sms <= 0) sms = 1;
-    if (warps_per_sm <= 0) warps_per_sm = 12;
-    const long long cap = (long long)sms * warps_per_sm;
-    if (ntiles >= cap) return Plan{1, nchunks, (int)((ntiles + cap - 1) / cap)};
-    long long s = cap / ntiles;
-    if (s > nchunks) s = nchunks;
-    if (s < 1) s = 1;
-    const int cps = ceil_div(nchunks, (int)s);
-    return Plan{ceil_div(nchunks, cps), cps, 1};
+    const long long wave = (long long)sms * (o.ctas[kGemvWarpsPerBlock] > 0 ? o.ctas[kGemvWarpsPerBlock] : 1) *
+                           kGemvWarpsPerBlock;  // warps in one wave of 4-warp CTAs
+    if (ntiles >= wave || nchunks == 1)
+        return Plan{1, nchunks, (int)((ntiles + wave - 1) / wave)};
+    int best = 1;
+    for (int sp = 2; sp <= kMaxCtaSplits && sp <= nchunks; ++sp)
+        if ((long long)ntiles <= (long long)sms * o.ctas[sp]) best = sp;
+    Plan p{1, nchunks, 1};
+    if (best > 1) {
+        p.cps = ceil_div(nchunks, best);
+        p.splits = ceil_div(nchunks, p.cps);
+        if (p.splits == 1) p.cps = nchunks;
+    }
+    if (nchunks > kMaxCtaSplits && (long long)ntiles * p.splits * 2 < wave) {
+        long long s2 = wave / ntiles;
+        if (s2 > nchunks) s2 = nchunks;
+        const int cps2 = ceil_div(nchunks, (int)s2);
+        const int sp2 = ceil_div(nchunks, cps2);
+        if (sp2 > kMaxCtaSplits) return Plan{sp2, cps2, 1};
+    }
+    return p;
 }
 
 long long plan_items(int ntiles, const Plan &p)
@@ -85,7 +125,7 @@ long long plan_items(int ntiles, const Plan &p)
 
 size_t ws_bytes_for(int ntiles, const Plan &p)
 {
-    if (p.splits <= 1) return 0;
+    if (p.splits <= kMaxCtaSplits) return 0;  // splits meet in shared memory (or none)
     return round16((size_t)ntiles * 4) + (size_t)plan_items(ntiles, p) * 8 * sizeof(float);
 }
 
@@ -115,8 +155,14 @@ int gemv_common(int fmt, const void *Wp, const void *q8, float *y, int rows, int
     if (!gemv_shape_ok(rows, cols)) return MQ_ERR_SHAPE;
     if (!aligned16(Wp) || !aligned16(q8) || !aligned16(y)) return MQ_ERR_ALIGN;
     const Geom g = make_geom(rows, cols, fmt == 6 ? kQ6kBytes : kQ4kBytes);
-    const Plan p = explicit_plan ? *explicit_plan
-                                 : plan_for(g.ntiles, g.nchunks, device_sms(), resident_warps(fmt));
+    Plan p;
+    if (explicit_plan) {
+        p = *explicit_plan;
+    } else {
+        Occupancy o;
+        if (!device_occupancy(fmt, &o)) return MQ_ERR_CUDA;
+        p = plan_for(g.ntiles, g.nchunks, device_sms(), o);
+    }
     const int cov = check_plan(g, p);
     if (cov != MQ_OK) return cov;
     GemvLaunch a;
@@ -255,13 +301,13 @@ int mq_check_coverage(int nchunks, int splits, int chunks_per_split)
     return check_coverage(nchunks, splits, chunks_per_split);
 }
 
-int mq_gemv_plan_for(int rows, int cols, int sms, int warps_per_sm, int *splits,
+int mq_gemv_plan_for(int rows, int cols, int sms, int regs_per_thread, int *splits,
                      int *chunks_per_split, int *tiles_per_item)
 {
     if (!splits || !chunks_per_split || !tiles_per_item) return MQ_ERR_NULL;
-    if (!gemv_shape_ok(rows, cols)) return MQ_ERR_SHAPE;
+    if (!gemv_shape_ok(rows, cols) || regs_per_thread < 1 || regs_per_thread > 255) return MQ_ERR_SHAPE;
     const Geom g = make_geom(rows, cols, kQ6kBytes);
-    const Plan p = plan_for(g.ntiles, g.nchunks, sms, warps_per_sm);
+    const Plan p = plan_for(g.ntiles, g.nchunks, sms, model_occupancy(regs_per_thread));
     *splits = p.splits;
     *chunks_per_split = p.cps;
     *tiles_per_item = p.tpi;
@@ -271,9 +317,17 @@ int mq_gemv_plan_for(int rows, int cols, int sms, int warps_per_sm, int *splits,
 int mq_gemv_plan(int rows, int cols, int fmt, int *splits, int *chunks_per_split,
                  int *tiles_per_item)
 {
+    if (!splits || !chunks_per_split || !tiles_per_item) return MQ_ERR_NULL;
     if (fmt != 6 && fmt != 4) return MQ_ERR_SHAPE;
-    return mq_gemv_plan_for(rows, cols, device_sms(), resident_warps(fmt), splits,
-                            chunks_per_split, tiles_per_item);
+    if (!gemv_shape_ok(rows, cols)) return MQ_ERR_SHAPE;
+    Occupancy o;
+    if (!device_occupancy(fmt, &o)) return MQ_ERR_CUDA;
+    const Geom g = make_geom(rows, cols, kQ6kBytes);
+    const Plan p = plan_for(g.ntiles, g.nchunks, device_sms(), o);
+    *splits = p.splits;
+    *chunks_per_split = p.cps;
+    *tiles_per_item = p.tpi;
+    return MQ_OK;
 }
 
 size_t mq_gemv_workspace_bytes_for(int rows, int cols, int splits, int chunks_per_split,

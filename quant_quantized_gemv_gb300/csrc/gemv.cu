@@ -24,11 +24,14 @@
 //     chunk for the tile's 8 rows, so its activation codes are loaded once
 //     per chunk and reused 8 times.
 //   * A whole tile is reduced (fixed 9-shuffle butterfly) and written
-//     directly.  A split leaves its 8 partial sums in the workspace; the split
-//     that arrives last (atomic ticket, no waiting) loads all of them at once
-//     and adds them in ascending split order, so the result does not depend
-//     on arrival order.  The host proves before launch that the splits cover
-//     every chunk exactly once (the page's §6 lesson).
+//     directly.  With 2..12 splits the splits of a tile are the warps of one
+//     CTA and meet in shared memory (one __syncthreads, ascending split
+//     order).  With more splits (very few tiles, very long rows) each split
+//     leaves its 8 partial sums in the workspace and the split that arrives
+//     last (atomic ticket, no waiting) loads all of them at once and adds
+//     them in ascending split order.  Either way the result does not depend
+//     on arrival order, and the host proves before launch that the splits
+//     cover every chunk exactly once (the page's §6 lesson).
 //   * With programmatic dependent launch the first chunk's weight loads are
 //     issued before griddepcontrol.wait, so the weight stream starts while
 //     the preceding kernel (the q8 producer) drains; the activation, the
@@ -295,10 +298,11 @@ __device__ __forceinline__ float reduce8(const float (&acc)[8], int lane)
 }
 
 // Tile t is finished for this warp (work item `item`, covering units
-// [u0, u1)): write it, or hand its partial to the tile's last arriver.
+// [u0, u1)): write it, or combine it with the tile's other splits.
 __device__ __forceinline__ void flush_tile(const GemvLaunch &a, int t, float (&acc)[8], int item,
                                            int u0, int u1, int lane)
 {
+    __shared__ float cta_part[kMaxCtaSplits][8];
     const float v = reduce8(acc, lane);
 #pragma unroll
     for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
@@ -308,8 +312,26 @@ __device__ __forceinline__ void flush_tile(const GemvLaunch &a, int t, float (&a
         if ((lane & 3) == 0 && row0 + (lane >> 2) < a.rows) a.y[row0 + (lane >> 2)] = v;
         return;
     }
-    // one split of tile t (splits > 1): lane 0 publishes the 8 partials,
-    // fences them and takes a ticket (writer and ticket holder are one thread)
+    if (a.splits <= kMaxCtaSplits) {
+        // the splits of tile t are the warps of this CTA (one flush each):
+        // combine through shared memory in ascending split order
+        const int s = threadIdx.x >> 5;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float pk = __shfl_sync(kFull, v, 4 * k);
+            if (lane == k) cta_part[s][k] = pk;
+        }
+        __syncthreads();
+        if (s == 0 && lane < 8) {
+            float sum = 0.0f;
+            for (int j = 0; j < a.splits; ++j) sum += cta_part[j][lane];
+            if (row0 + lane < a.rows) a.y[row0 + lane] = sum;
+        }
+        return;
+    }
+    // more splits than a CTA holds: lane 0 publishes the 8 partials to the
+    // workspace, fences them and takes a ticket (writer and ticket holder are
+    // one thread); the last of the tile's splits adds them all
     float *dst = a.ws_part + (size_t)item * 8;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -325,8 +347,8 @@ __device__ __forceinline__ void flush_tile(const GemvLaunch &a, int t, float (&a
     last = __shfl_sync(kFull, last, 0);
     if (!last) return;
     __threadfence();
-    // last arriver: lane (4g + ...) loads split base+g of row lane&7, four
-    // splits per round trip; lanes 0..7 add them in ascending split order.
+    // last arriver: lane (8g + r) loads split base+g of row r, four splits
+    // per round trip; lanes 0..7 add them in ascending split order
     const float *base_ptr = a.ws_part + (size_t)t * a.splits * 8;
     float sum = 0.0f;
     for (int base = 0; base < a.splits; base += 4) {
@@ -341,15 +363,20 @@ __device__ __forceinline__ void flush_tile(const GemvLaunch &a, int t, float (&a
     if (lane == 0) a.ws_cnt[t] = 0u;  // ready for the next call
 }
 
+// CTA shapes: splits == 1 (whole tiles) and splits > kMaxCtaSplits use CTAs
+// of kGemvWarpsPerBlock independent warps; 2..kMaxCtaSplits splits use one
+// CTA per tile whose warps are its splits.
 template <int FMT, bool SUBDOTS>  // FMT 6 = q6_K, 4 = q4_K
-__global__ void __launch_bounds__(32 * kGemvWarpsPerBlock, 3) gemv_kernel(const GemvLaunch a)
+__global__ void __launch_bounds__(32 * kMaxCtaSplits, 1) gemv_kernel(const GemvLaunch a)
 {
     using Regs = typename std::conditional<FMT == 6, Q6kRegs, Q4kRegs>::type;
     constexpr int kChunkBytes = (FMT == 6 ? kQ6kChunkPerBlock : kQ4kChunkPerBlock) * kChunkBlocks;
     const int lane = threadIdx.x & 31;
-    const int item = blockIdx.x * kGemvWarpsPerBlock + (threadIdx.x >> 5);
+    const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     griddep_launch_dependents();
-    if (item >= a.n_items) return;  // whole warp; the kernel has no block barrier
+    // a whole warp leaves; CTAs that combine in shared memory are launched
+    // exact (every warp has an item), so none of their warps leaves early
+    if (item >= a.n_items) return;
     const int nch = a.nchunks;
     int u0, u1;
     if (a.splits > 1) {
@@ -398,9 +425,10 @@ __global__ void __launch_bounds__(32 * kGemvWarpsPerBlock, 3) gemv_kernel(const 
 template <int FMT, bool SUBDOTS>
 cudaError_t launch(const GemvLaunch &a, cudaStream_t st)
 {
-    const long long blocks = (a.n_items + kGemvWarpsPerBlock - 1) / kGemvWarpsPerBlock;
-    return launch_maybe_pdl(gemv_kernel<FMT, SUBDOTS>, dim3((unsigned)blocks),
-                            dim3(32 * kGemvWarpsPerBlock), a.pdl, st, a);
+    const int warps = gemv_cta_warps(a.splits, SUBDOTS);
+    const long long blocks = (a.n_items + warps - 1) / warps;
+    return launch_maybe_pdl(gemv_kernel<FMT, SUBDOTS>, dim3((unsigned)blocks), dim3(32 * warps),
+                            a.pdl, st, a);
 }
 
 }  // namespace
@@ -410,15 +438,15 @@ cudaError_t launch_gemv_q4k(const GemvLaunch &a, cudaStream_t st) { return launc
 cudaError_t launch_subdots_q6k(const GemvLaunch &a, cudaStream_t st) { return launch<6, true>(a, st); }
 cudaError_t launch_subdots_q4k(const GemvLaunch &a, cudaStream_t st) { return launch<4, true>(a, st); }
 
-int gemv_resident_warps_per_sm(int fmt)
+int gemv_ctas_per_sm(int fmt, int warps_per_cta)
 {
     int blocks = 0;
     const cudaError_t e =
         fmt == 6 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemv_kernel<6, false>,
-                                                                 32 * kGemvWarpsPerBlock, 0)
+                                                                 32 * warps_per_cta, 0)
                  : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemv_kernel<4, false>,
-                                                                 32 * kGemvWarpsPerBlock, 0);
-    return e == cudaSuccess ? blocks * kGemvWarpsPerBlock : 0;
+                                                                 32 * warps_per_cta, 0);
+    return e == cudaSuccess ? blocks : 0;
 }
 
 }  // namespace mq

@@ -111,30 +111,50 @@ def test_unit_counts_match_pages(facts):
     assert 1024 * (5120 // 256) * facts["q6k_padded_stride"] == facts["attn_v_padded_bytes"]
 
 
-@pytest.mark.parametrize("sms,warps", [(1, 4), (8, 12), (76, 12), (148, 8), (152, 12), (160, 16)])
-def test_plan_always_covers(mq, sms, warps):
+def model_ctas(w, regs=168):
+    return min(65536 // (w * 32 * regs), 2048 // (32 * w), 32)
+
+
+@pytest.mark.parametrize("sms,regs", [(1, 168), (8, 168), (76, 128), (148, 200), (152, 168), (160, 96)])
+def test_plan_always_covers(mq, sms, regs):
     shapes = [(r, c) for r in (1, 5, 8, 64, 512, 1024, 3584, 5120, 13824, 152064)
               for c in (256, 1024, 1280, 2048, 5120, 13824, 18944, 32768)]
     for rows, cols in shapes:
-        s, cps, tpi = mq.mq_gemv_plan_for(rows, cols, sms, warps)
+        s, cps, tpi = mq.mq_gemv_plan_for(rows, cols, sms, regs)
         ntiles, nch = -(-rows // 8), -(-(cols // 256) // 4)
         assert mq.mq_check_coverage(nch, s, cps) == mq.MQ_OK, (rows, cols, sms, s, cps)
         assert s * cps >= nch and (s - 1) * cps < nch
-        items = ntiles * s if s > 1 else -(-ntiles // tpi)
-        assert items <= sms * warps                             # one resident wave
         assert s == 1 or tpi == 1
+        wave = sms * model_ctas(4, regs) * 4
+        if s == 1:
+            assert -(-ntiles // tpi) <= wave                     # one resident wave
+        elif s <= 12:
+            assert ntiles <= sms * model_ctas(s, regs)           # one CTA per tile, one wave
+        else:
+            assert ntiles * s <= wave and nch > 12               # workspace splits
         ws = mq.mq_gemv_workspace_bytes_for(rows, cols, (s, cps, tpi))
-        assert (ws > 0) == (s > 1)
+        assert (ws > 0) == (s > 12)
+
+
+def test_plans_of_the_benchmark_shapes(mq):
+    """GB300: 152 SMs, 168 registers -> 3 four-warp CTAs (12 warps) per SM."""
+    assert mq.mq_gemv_plan_for(3584, 18944, 152, 168) == (4, 5, 1)     # 448 tiles x 4 splits
+    assert mq.mq_gemv_plan_for(152064, 5120, 152, 168) == (1, 5, 11)   # 11 whole tiles per warp
+    assert mq.mq_gemv_plan_for(5120, 13824, 152, 168) == (2, 7, 1)
+    assert mq.mq_gemv_plan_for(1024, 5120, 152, 168) == (5, 1, 1)
+    assert mq.mq_gemv_plan_for(13824, 5120, 152, 168) == (1, 5, 1)
+    assert mq.mq_gemv_plan_for(512, 18944, 152, 168) == (19, 1, 1)     # few tiles: workspace splits
 
 
 def test_workspace_sizes(mq):
-    # 100 rows -> 13 tiles; 4096 cols -> 4 chunks
-    assert mq.mq_gemv_workspace_bytes_for(100, 4096, (1, 4, 1)) == 0
-    assert mq.mq_gemv_workspace_bytes_for(100, 4096, (1, 4, 5)) == 0
-    assert mq.mq_gemv_workspace_bytes_for(100, 4096, (4, 1, 1)) == 64 + 13 * 4 * 8 * 4
-    assert mq.mq_gemv_workspace_bytes_for(100, 4096, (2, 2, 1)) == 64 + 13 * 2 * 8 * 4
-    assert mq.mq_gemv_workspace_bytes_for(100, 4096, (2, 1, 1)) == 0      # invalid: drops chunks
-    assert mq.mq_gemv_workspace_bytes_for(100, 4096, (2, 2, 3)) == 0      # invalid: splits with tpi
+    # 100 rows -> 13 tiles; 16384 cols -> 16 chunks
+    assert mq.mq_gemv_workspace_bytes_for(100, 16384, (1, 16, 1)) == 0
+    assert mq.mq_gemv_workspace_bytes_for(100, 16384, (1, 16, 5)) == 0
+    assert mq.mq_gemv_workspace_bytes_for(100, 16384, (4, 4, 1)) == 0           # CTA splits
+    assert mq.mq_gemv_workspace_bytes_for(100, 16384, (12, 2, 1)) == 0          # (8 would do; valid)
+    assert mq.mq_gemv_workspace_bytes_for(100, 16384, (16, 1, 1)) == 64 + 13 * 16 * 8 * 4
+    assert mq.mq_gemv_workspace_bytes_for(100, 16384, (2, 7, 1)) == 0           # invalid: drops chunks
+    assert mq.mq_gemv_workspace_bytes_for(100, 16384, (16, 1, 3)) == 0          # invalid: splits with tpi
 
 
 @pytest.mark.skipif(__import__("torch").cuda.is_available(),
@@ -157,9 +177,9 @@ def test_validation_rejects_before_launch(mq):
     assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 1, 18, 1, N, 0, S) == mq.MQ_ERR_COVERAGE
     assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 4, 5, 2, N, 0, S) == mq.MQ_ERR_COVERAGE
     assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 1, 19, 0, N, 0, S) == mq.MQ_ERR_COVERAGE
-    # a split plan needs (enough) workspace, or it never launches
-    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 4, 5, 1, N, 0, S) == mq.MQ_ERR_NULL
-    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 4, 5, 1, ctypes.c_void_p(0x40000), 16, S) == \
+    # a workspace plan (> 12 splits) needs (enough) workspace, or it never launches
+    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 19, 1, 1, N, 0, S) == mq.MQ_ERR_NULL
+    assert L.mq_gemv_q6k_q8_plan(A, B, Y, 64, 18944, 19, 1, 1, ctypes.c_void_p(0x40000), 16, S) == \
         mq.MQ_ERR_WORKSPACE
     assert L.mq_quantize_q8(A, B, 48, S) == mq.MQ_ERR_SHAPE
     assert L.mq_swiglu_quant_q8(A, B, N, Y, 64, S) == mq.MQ_ERR_NULL
