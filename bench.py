@@ -167,7 +167,7 @@ def profiled_traffic(workload: str):
 class DeviceWorkload:
     """Ops of one decode step: producers writing q8 planes, GEMVs reading them."""
 
-    def __init__(self, name: str, device, l2_bytes: int, min_graphs: int = 16):
+    def __init__(self, name: str, device, l2_bytes: int, group: bool = True):
         import torch
         import quant_quantized_gemv_gb300 as mq
         self.mq = mq
@@ -212,13 +212,23 @@ class DeviceWorkload:
             W0 = base[(fmt, rows, cols)][1]
             copies = [W0.clone() for _ in range(self.n_copies)]
             y = torch.empty(rows, dtype=torch.float32, device=device)
-            ws = mq.mq_gemv_workspace(rows, cols, device=device)
-            self.ops.append(("gemv", fmt, copies, plane, y, rows, cols, ws, gname))
+            part = (fmt, copies, rows, y, gname)
+            last = self.ops[-1] if self.ops else None
+            if group and last is not None and last[0] == "gemv" and last[1] is plane and \
+                    len(last[3]) < mq.MQ_MAX_GROUP:
+                last[3].append(part)             # same q8 plane: one launch for the group
+            else:
+                self.ops.append(["gemv", plane, cols, [part], None])
             prev_outputs.append(y)
-        self.output = self.ops[-1][4]
-        self.n_gemv = sum(1 for o in self.ops if o[0] == "gemv")
+        for o in self.ops:                       # workspace per GEMV launch (default plan)
+            if o[0] == "gemv":
+                o[4] = mq.mq_gemv_group_workspace(self._spec(o), o[2], device=device)
+        self.output = self.ops[-1][3][-1][3]
+        self.n_gemv = sum(len(o[3]) for o in self.ops if o[0] == "gemv")
+        self.n_gemv_launches = sum(1 for o in self.ops if o[0] == "gemv")
         self.n_kernels = len(self.ops)
-        self.gemv_bytes = [self._gemv_alg_bytes(o) for o in self.ops if o[0] == "gemv"]
+        self.gemv_bytes = [self._part_alg_bytes(p[0], p[2], o[2]) for o in self.ops if o[0] == "gemv"
+                           for p in o[3]]
 
     def _input(self, arr: np.ndarray):
         import torch
@@ -227,27 +237,36 @@ class DeviceWorkload:
         return t
 
     @staticmethod
-    def _gemv_alg_bytes(o) -> int:
-        _, fmt, _, plane, _, rows, cols, _, _ = o
+    def _part_alg_bytes(fmt, rows, cols) -> int:
         wb = rows * (cols // 256) * (210 if fmt == "q6k" else 144)
         act = (cols // 32) * (34 if fmt == "q6k" else 38)      # codes + fp16 d (+ int32 sum)
         return wb + act + 4 * rows
 
-    def run_gemvs(self, k: int):
-        """Enqueue only the GEMVs of step k (for kernel timing)."""
+    @staticmethod
+    def _spec(o, c=0):
+        return [(fmt, copies[c], rows) for fmt, copies, rows, _, _ in o[3]]
+
+    def _launch(self, o, c):
+        _, plane, cols, parts, ws = o
         mq = self.mq
+        if len(parts) == 1:
+            fmt, copies, rows, y, _ = parts[0]
+            fn = mq.mq_gemv_q6k_q8 if fmt == "q6k" else mq.mq_gemv_q4k_q8
+            fn(copies[c], plane, rows, cols, y=y, ws=ws)
+        else:
+            mq.mq_gemv_group_q8(self._spec(o, c), plane, cols, ys=[p[3] for p in parts], ws=ws)
+
+    def run_gemvs(self, k: int):
+        """Enqueue only the GEMV launches of step k (for kernel timing)."""
         c = k % self.n_copies
         for o in self.ops:
             if o[0] == "gemv":
-                _, fmt, copies, plane, y, rows, cols, ws, _ = o
-                fn = mq.mq_gemv_q6k_q8 if fmt == "q6k" else mq.mq_gemv_q4k_q8
-                fn(copies[c], plane, rows, cols, y=y, ws=ws)
+                self._launch(o, c)
 
-    def run(self, k: int, events=None):
+    def run(self, k: int):
         """Enqueue step k (weights copy k % n_copies) on the current stream."""
         mq = self.mq
         c = k % self.n_copies
-        gi = 0
         for o in self.ops:
             kind = o[0]
             if kind == "rms":
@@ -257,14 +276,7 @@ class DeviceWorkload:
             elif kind == "quant":
                 mq.mq_quantize_q8(o[1], q8=o[2])
             else:
-                _, fmt, copies, plane, y, rows, cols, ws, _ = o
-                if events is not None:
-                    events[gi][0].record()
-                fn = mq.mq_gemv_q6k_q8 if fmt == "q6k" else mq.mq_gemv_q4k_q8
-                fn(copies[c], plane, rows, cols, y=y, ws=ws)
-                if events is not None:
-                    events[gi][1].record()
-                gi += 1
+                self._launch(o, c)
 
 
 def make_event(timing=True, external=False):
@@ -295,7 +307,7 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     import quant_quantized_gemv_gb300 as mq
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
-    wl = DeviceWorkload(args.workload, dev, l2)
+    wl = DeviceWorkload(args.workload, dev, l2, group=args.group)
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -414,7 +426,8 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
         "dtype": "i8", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {DESCR[args.workload]}",
                    "weight_content_bytes_per_step": wl.weight_bytes,
-                   "gemvs_per_step": wl.n_gemv, "kernels_per_step": wl.n_kernels,
+                   "gemvs_per_step": wl.n_gemv, "gemv_launches_per_step": wl.n_gemv_launches,
+                   "kernels_per_step": wl.n_kernels,
                    "l2": f"{wl.n_copies} rotated weight copies "
                          f"({wl.n_copies * wl.weight_bytes / 1e6:.0f} MB >= 4 x L2 {l2 / 1e6:.0f} MB)",
                    "timing": f"CUDA graphs of {m} steps (+ single-step graphs for a remainder), "
@@ -545,6 +558,8 @@ def main(argv=None):
     ap.add_argument("--steps-per-graph", type=int, default=16)
     ap.add_argument("--no-pdl", dest="pdl", action="store_false",
                     help="launch without programmatic dependent launch")
+    ap.add_argument("--no-group", dest="group", action="store_false",
+                    help="one launch per GEMV even when several read the same q8 plane")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

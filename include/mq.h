@@ -208,6 +208,39 @@ int mq_gemv_q4k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int 
 int mq_gemv_q6k_q8_noalloc(const void *Wp, const void *q8, float *y, int rows, int cols,
                            void *stream);
 
+/* ------------------------------------------------------------------------
+ * Grouped GEMV (device): up to MQ_MAX_GROUP matrices that read the same q8
+ * plane (same cols) in ONE launch, e.g. the q, k, v projections of a layer
+ * (q4_K, q4_K, q6_K) after one rms_norm->q8, or its gate and up (the
+ * gate||up pair of [D4-4] §2, L3).  Each part may be q6_K or q4_K and gets
+ * its own y; the arithmetic per part is exactly that of mq_gemv_q6k_q8 /
+ * mq_gemv_q4k_q8, and a group of one is that call.  One launch means one
+ * wave, one ramp and one tail for the group instead of one per matrix.
+ * The plan (and the workspace, when it needs one) is sized on the group's
+ * total tile count; work items never straddle two parts.
+ *   parts: host array of nparts descriptors (read during the call only).
+ *   mq_gemv_group_workspace_bytes: workspace for the default plan
+ *     (splits == 0) or an explicit one; the Wp / y fields may be NULL here.
+ * Errors: as mq_gemv_q6k_q8; MQ_ERR_SHAPE also for nparts outside
+ *         1..MQ_MAX_GROUP or a format other than 6 / 4.
+ * ------------------------------------------------------------------------ */
+#define MQ_MAX_GROUP 8
+
+typedef struct {
+    int fmt;            /* 6 = q6_K, 4 = q4_K                         */
+    int rows;           /* rows of this matrix (>= 1)                  */
+    const void *Wp;     /* its repacked weights (device)               */
+    float *y;           /* its rows f32 outputs (device)               */
+} mq_gemv_part;
+
+size_t mq_gemv_group_workspace_bytes(const mq_gemv_part *parts, int nparts, int cols, int splits,
+                                     int chunks_per_split, int tiles_per_item);
+int mq_gemv_group_q8(const mq_gemv_part *parts, int nparts, const void *q8, int cols, void *ws,
+                     size_t ws_bytes, void *stream);
+int mq_gemv_group_q8_plan(const mq_gemv_part *parts, int nparts, const void *q8, int cols,
+                          int splits, int chunks_per_split, int tiles_per_item, void *ws,
+                          size_t ws_bytes, void *stream);
+
 /* Coverage check used by every GEMV dispatch, exposed for tests: MQ_OK iff
  * all arguments are >= 1, splits * chunks_per_split >= nchunks (nothing
  * dropped) and (splits - 1) * chunks_per_split < nchunks (no empty split);

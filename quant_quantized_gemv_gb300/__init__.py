@@ -33,9 +33,19 @@ EXPORTS = [
     "mq_gemv_workspace_bytes", "mq_gemv_plan", "mq_gemv_q6k_q8", "mq_gemv_q4k_q8",
     "mq_gemv_q6k_q8_plan", "mq_gemv_q4k_q8_plan", "mq_gemv_workspace_bytes_for",
     "mq_check_coverage", "mq_gemv_plan_for", "mq_set_pdl", "mq_gemv_q6k_q8_noalloc",
+    "mq_gemv_group_workspace_bytes", "mq_gemv_group_q8", "mq_gemv_group_q8_plan",
     "mq_gemv_q6k_q8_subdots",
     "mq_gemv_q4k_q8_subdots", "mq_device_sms",
 ]
+
+
+class MQGemvPart(ctypes.Structure):
+    """mq_gemv_part of include/mq.h."""
+    _fields_ = [("fmt", ctypes.c_int), ("rows", ctypes.c_int), ("Wp", ctypes.c_void_p),
+                ("y", ctypes.c_void_p)]
+
+
+MQ_MAX_GROUP = 8
 
 
 class MQError(RuntimeError):
@@ -83,6 +93,9 @@ def lib():
         "mq_gemv_plan_for": ([I, I, I, I, P, P, P], I),
         "mq_set_pdl": ([I], I),
         "mq_gemv_q6k_q8_noalloc": ([P, P, P, I, I, P], I),
+        "mq_gemv_group_workspace_bytes": ([P, I, I, I, I, I], S),
+        "mq_gemv_group_q8": ([P, I, P, I, P, S, P], I),
+        "mq_gemv_group_q8_plan": ([P, I, P, I, I, I, I, P, S, P], I),
         "mq_gemv_q6k_q8_subdots": ([P, P, P, I, I, P], I),
         "mq_gemv_q4k_q8_subdots": ([P, P, P, I, I, P], I),
         "mq_device_sms": ([], I),
@@ -298,6 +311,53 @@ def mq_gemv_q6k_q8(Wp, q8, rows: int, cols: int, y=None, ws=None, stream=None, p
 def mq_gemv_q4k_q8(Wp, q8, rows: int, cols: int, y=None, ws=None, stream=None, plan=None):
     """y = W x_hat for repacked q4_K weights Wp (device) and a q8 plane."""
     return _gemv("mq_gemv_q4k_q8", Wp, q8, rows, cols, y, ws, stream, plan)
+
+
+def _parts_array(parts, ys=None):
+    """parts: [(fmt 'q6k'|'q4k', Wp tensor or None, rows)] -> ctypes array."""
+    arr = (MQGemvPart * len(parts))()
+    for i, (fmt, Wp, rows) in enumerate(parts):
+        arr[i].fmt = 6 if fmt == "q6k" else 4
+        arr[i].rows = int(rows)
+        arr[i].Wp = None if Wp is None else Wp.data_ptr()
+        arr[i].y = None if ys is None else ys[i].data_ptr()
+    return arr
+
+
+def mq_gemv_group_workspace_bytes(parts, cols: int, plan=None) -> int:
+    """Workspace bytes of a group (default plan, or plan = (splits, cps, tpi))."""
+    s, c, t = plan if plan is not None else (0, 0, 0)
+    return lib().mq_gemv_group_workspace_bytes(_parts_array(parts), len(parts), cols, s, c, t)
+
+
+def mq_gemv_group_workspace(parts, cols: int, plan=None, device=None):
+    import torch
+    nbytes = mq_gemv_group_workspace_bytes(parts, cols, plan)
+    if nbytes == 0:
+        return None
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def mq_gemv_group_q8(parts, q8, cols: int, ys=None, ws=None, stream=None, plan=None):
+    """One launch for several matrices reading the same q8 plane.
+
+    parts: [(fmt 'q6k'|'q4k', Wp device tensor, rows)]; returns the list of y."""
+    import torch
+    for _, Wp, _ in parts:
+        _dev(Wp)
+    if ys is None:
+        ys = [torch.empty(rows, dtype=torch.float32, device=q8.device) for _, _, rows in parts]
+    for y in ys:
+        _dev(y, torch.float32)
+    arr = _parts_array(parts, ys)
+    wsp, wsb = _ws_args(ws)
+    if plan is None:
+        st = lib().mq_gemv_group_q8(arr, len(parts), _dev(q8), cols, wsp, wsb, _stream(stream))
+    else:
+        st = lib().mq_gemv_group_q8_plan(arr, len(parts), _dev(q8), cols, int(plan[0]), int(plan[1]),
+                                         int(plan[2]), wsp, wsb, _stream(stream))
+    _check(st, "mq_gemv_group_q8")
+    return ys
 
 
 def mq_gemv_q6k_q8_noalloc(Wp, q8, rows: int, cols: int, y=None, stream=None):

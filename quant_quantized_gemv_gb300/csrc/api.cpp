@@ -14,10 +14,12 @@ namespace {
 
 using namespace mq;
 
+static_assert(kMaxParts == MQ_MAX_GROUP, "kernel part table and public group size differ");
+
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sms[kMaxDevices];
-// resident GEMV CTAs per SM: [device][q6_K, q4_K][warps per CTA]
-std::atomic<int> g_ctas[kMaxDevices][2][kMaxCtaSplits + 1];
+// resident GEMV CTAs per SM: [device][warps per CTA]
+std::atomic<int> g_ctas[kMaxDevices][kMaxCtaSplits + 1];
 std::atomic<int> g_pdl{0};
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -52,15 +54,15 @@ struct Occupancy {
     int ctas[kMaxCtaSplits + 1];
 };
 
-bool device_occupancy(int fmt, Occupancy *o)
+bool device_occupancy(Occupancy *o)
 {
     const int dev = current_device();
     if (dev < 0) return false;
     for (int w = 1; w <= kMaxCtaSplits; ++w) {
-        std::atomic<int> &slot = g_ctas[dev][fmt == 6 ? 0 : 1][w];
+        std::atomic<int> &slot = g_ctas[dev][w];
         int v = slot.load(std::memory_order_relaxed);
         if (v <= 0) {
-            v = gemv_ctas_per_sm(fmt, w);
+            v = gemv_ctas_per_sm(w);
             if (v <= 0) return false;
             slot.store(v, std::memory_order_relaxed);
         }
@@ -123,10 +125,10 @@ long long plan_items(int ntiles, const Plan &p)
     return p.splits > 1 ? (long long)ntiles * p.splits : (ntiles + p.tpi - 1) / p.tpi;
 }
 
-size_t ws_bytes_for(int ntiles, const Plan &p)
+size_t ws_bytes_for(long long total_tiles, long long n_items, const Plan &p)
 {
     if (p.splits <= kMaxCtaSplits) return 0;  // splits meet in shared memory (or none)
-    return round16((size_t)ntiles * 4) + (size_t)plan_items(ntiles, p) * 8 * sizeof(float);
+    return round16((size_t)total_tiles * 4) + (size_t)n_items * 8 * sizeof(float);
 }
 
 int check_coverage(int nchunks, int splits, int cps)
@@ -139,60 +141,106 @@ int check_coverage(int nchunks, int splits, int cps)
     return MQ_OK;
 }
 
-int check_plan(const Geom &g, const Plan &p)
+int check_plan(int nchunks, const Plan &p)
 {
     if (p.tpi < 1 || (p.splits > 1 && p.tpi != 1)) return MQ_ERR_COVERAGE;
-    const int cov = check_coverage(g.nchunks, p.splits, p.cps);
+    return check_coverage(nchunks, p.splits, p.cps);
+}
+
+struct Part {
+    int fmt, rows;
+    const void *Wp;
+    float *y;
+};
+
+// Validate a group, pick or check its plan, size the workspace.  On MQ_OK,
+// `a` holds everything but the workspace pointers, and *need the bytes.
+int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const Plan *explicit_plan,
+                  GemvLaunch *a, size_t *need, bool sizes_only = false)
+{
+    if (nparts < 1 || nparts > kMaxParts) return MQ_ERR_SHAPE;
+    if (!parts || (!q8 && !sizes_only)) return MQ_ERR_NULL;
+    if (cols < kQK || cols % kQK != 0) return MQ_ERR_SHAPE;
+    if (!aligned16(q8)) return MQ_ERR_ALIGN;
+    memset(a, 0, sizeof *a);
+    const int nb = cols / kQK, nchunks = ceil_div(nb, kChunkBlocks);
+    long long total_tiles = 0;
+    for (int p = 0; p < nparts; ++p) {
+        const Part &x = parts[p];
+        if (x.fmt != 6 && x.fmt != 4) return MQ_ERR_SHAPE;
+        if ((!x.Wp || !x.y) && !sizes_only) return MQ_ERR_NULL;
+        if (!gemv_shape_ok(x.rows, cols)) return MQ_ERR_SHAPE;
+        if (!aligned16(x.Wp) || !aligned16(x.y)) return MQ_ERR_ALIGN;
+        total_tiles += ceil_div(x.rows, kTileRows);
+    }
+    if (total_tiles * nchunks >= (1LL << 31)) return MQ_ERR_SHAPE;
+    Plan pl;
+    if (explicit_plan) {
+        pl = *explicit_plan;
+    } else {
+        Occupancy o;
+        if (!device_occupancy(&o)) return MQ_ERR_CUDA;
+        pl = plan_for((int)total_tiles, nchunks, device_sms(), o);
+    }
+    const int cov = check_plan(nchunks, pl);
     if (cov != MQ_OK) return cov;
-    if (plan_items(g.ntiles, p) >= (1LL << 31)) return MQ_ERR_SHAPE;
+    long long items = 0, tiles = 0;
+    for (int p = 0; p < nparts; ++p) {
+        const Part &x = parts[p];
+        const Geom g = make_geom(x.rows, cols, x.fmt == 6 ? kQ6kBytes : kQ4kBytes);
+        GemvPart &gp = a->part[p];
+        gp.W = (const uint8_t *)x.Wp;
+        gp.y = x.y;
+        gp.rows = x.rows;
+        gp.ntiles = g.ntiles;
+        gp.fmt = x.fmt;
+        gp.item0 = (int)items;
+        gp.tile0 = (int)tiles;
+        gp.tile_bytes_div16 = (int)(g.tile_bytes / 16);
+        items += plan_items(g.ntiles, pl);
+        tiles += g.ntiles;
+    }
+    if (items >= (1LL << 31)) return MQ_ERR_SHAPE;
+    a->nparts = nparts;
+    a->q8 = (const uint8_t *)q8;
+    a->nb = nb;
+    a->nchunks = nchunks;
+    a->splits = pl.splits;
+    a->cps = pl.cps;
+    a->tpi = pl.tpi;
+    a->n_items = (int)items;
+    a->q8_d_off = (unsigned)q8_d_offset(cols);
+    a->q8_sum_off = (unsigned)q8_sum_offset(cols);
+    a->pdl = g_pdl.load(std::memory_order_relaxed);
+    *need = ws_bytes_for(total_tiles, items, pl);
     return MQ_OK;
+}
+
+int gemv_group(const Part *parts, int nparts, const void *q8, int cols, const Plan *explicit_plan,
+               void *ws, size_t ws_bytes, void *stream)
+{
+    GemvLaunch a;
+    size_t need = 0;
+    const int st = prepare_group(parts, nparts, q8, cols, explicit_plan, &a, &need);
+    if (st != MQ_OK) return st;
+    if (need > 0) {
+        if (!ws) return MQ_ERR_NULL;
+        if (!aligned16(ws)) return MQ_ERR_ALIGN;
+        if (ws_bytes < need) return MQ_ERR_WORKSPACE;
+        long long total_tiles = 0;
+        for (int p = 0; p < nparts; ++p) total_tiles += a.part[p].ntiles;
+        a.ws_cnt = (unsigned *)ws;
+        a.ws_part = (float *)((uint8_t *)ws + round16((size_t)total_tiles * 4));
+    }
+    return launch_gemv(a, (cudaStream_t)stream) == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
 }
 
 int gemv_common(int fmt, const void *Wp, const void *q8, float *y, int rows, int cols,
                 const Plan *explicit_plan, void *ws, size_t ws_bytes, void *stream)
 {
     if (!Wp || !q8 || !y) return MQ_ERR_NULL;
-    if (!gemv_shape_ok(rows, cols)) return MQ_ERR_SHAPE;
-    if (!aligned16(Wp) || !aligned16(q8) || !aligned16(y)) return MQ_ERR_ALIGN;
-    const Geom g = make_geom(rows, cols, fmt == 6 ? kQ6kBytes : kQ4kBytes);
-    Plan p;
-    if (explicit_plan) {
-        p = *explicit_plan;
-    } else {
-        Occupancy o;
-        if (!device_occupancy(fmt, &o)) return MQ_ERR_CUDA;
-        p = plan_for(g.ntiles, g.nchunks, device_sms(), o);
-    }
-    const int cov = check_plan(g, p);
-    if (cov != MQ_OK) return cov;
-    GemvLaunch a;
-    memset(&a, 0, sizeof a);
-    const size_t need = ws_bytes_for(g.ntiles, p);
-    if (need > 0) {
-        if (!ws) return MQ_ERR_NULL;
-        if (!aligned16(ws)) return MQ_ERR_ALIGN;
-        if (ws_bytes < need) return MQ_ERR_WORKSPACE;
-        a.ws_cnt = (unsigned *)ws;
-        a.ws_part = (float *)((uint8_t *)ws + round16((size_t)g.ntiles * 4));
-    }
-    a.W = (const uint8_t *)Wp;
-    a.q8 = (const uint8_t *)q8;
-    a.y = y;
-    a.rows = rows;
-    a.nb = g.nb;
-    a.ntiles = g.ntiles;
-    a.nchunks = g.nchunks;
-    a.splits = p.splits;
-    a.cps = p.cps;
-    a.tpi = p.tpi;
-    a.n_items = (int)plan_items(g.ntiles, p);
-    a.tile_bytes = g.tile_bytes;
-    a.q8_d_off = (unsigned)q8_d_offset(cols);
-    a.q8_sum_off = (unsigned)q8_sum_offset(cols);
-    a.pdl = g_pdl.load(std::memory_order_relaxed);
-    const cudaError_t e = fmt == 6 ? launch_gemv_q6k(a, (cudaStream_t)stream)
-                                   : launch_gemv_q4k(a, (cudaStream_t)stream);
-    return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+    const Part part{fmt, rows, Wp, y};
+    return gemv_group(&part, 1, q8, cols, explicit_plan, ws, ws_bytes, stream);
 }
 
 int subdots_common(int fmt, const void *Wp, const void *q8, int32_t *isums, int rows, int cols,
@@ -202,27 +250,15 @@ int subdots_common(int fmt, const void *Wp, const void *q8, int32_t *isums, int 
     if (!gemv_shape_ok(rows, cols)) return MQ_ERR_SHAPE;
     if (!aligned16(Wp) || !aligned16(q8) || !aligned16(isums)) return MQ_ERR_ALIGN;
     const Geom g = make_geom(rows, cols, fmt == 6 ? kQ6kBytes : kQ4kBytes);
+    const Plan pl{g.nchunks, 1, 1};  // one chunk per work item
+    const Part part{fmt, rows, Wp, (float *)isums};
     GemvLaunch a;
-    memset(&a, 0, sizeof a);
-    a.W = (const uint8_t *)Wp;
-    a.q8 = (const uint8_t *)q8;
+    size_t need = 0;
+    const int st = prepare_group(&part, 1, q8, cols, &pl, &a, &need);
+    if (st != MQ_OK) return st;
+    a.part[0].y = nullptr;
     a.isums = isums;
-    a.rows = rows;
-    a.nb = g.nb;
-    a.ntiles = g.ntiles;
-    a.nchunks = g.nchunks;
-    if ((long long)g.ntiles * g.nchunks >= (1LL << 31)) return MQ_ERR_SHAPE;
-    a.splits = g.nchunks;  // one chunk per work item
-    a.cps = 1;
-    a.tpi = 1;
-    a.n_items = g.ntiles * g.nchunks;
-    a.tile_bytes = g.tile_bytes;
-    a.q8_d_off = (unsigned)q8_d_offset(cols);
-    a.q8_sum_off = (unsigned)q8_sum_offset(cols);
-    a.pdl = g_pdl.load(std::memory_order_relaxed);
-    const cudaError_t e = fmt == 6 ? launch_subdots_q6k(a, (cudaStream_t)stream)
-                                   : launch_subdots_q4k(a, (cudaStream_t)stream);
-    return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+    return launch_subdots(a, (cudaStream_t)stream) == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
 }
 
 }  // namespace
@@ -321,7 +357,7 @@ int mq_gemv_plan(int rows, int cols, int fmt, int *splits, int *chunks_per_split
     if (fmt != 6 && fmt != 4) return MQ_ERR_SHAPE;
     if (!gemv_shape_ok(rows, cols)) return MQ_ERR_SHAPE;
     Occupancy o;
-    if (!device_occupancy(fmt, &o)) return MQ_ERR_CUDA;
+    if (!device_occupancy(&o)) return MQ_ERR_CUDA;
     const Geom g = make_geom(rows, cols, kQ6kBytes);
     const Plan p = plan_for(g.ntiles, g.nchunks, device_sms(), o);
     *splits = p.splits;
@@ -336,20 +372,47 @@ size_t mq_gemv_workspace_bytes_for(int rows, int cols, int splits, int chunks_pe
     if (!gemv_shape_ok(rows, cols)) return 0;
     const Geom g = make_geom(rows, cols, kQ6kBytes);
     const Plan p{splits, chunks_per_split, tiles_per_item};
-    if (check_plan(g, p) != MQ_OK) return 0;
-    return ws_bytes_for(g.ntiles, p);
+    if (check_plan(g.nchunks, p) != MQ_OK) return 0;
+    return ws_bytes_for(g.ntiles, plan_items(g.ntiles, p), p);
 }
 
 size_t mq_gemv_workspace_bytes(int rows, int cols)
 {
+    int s = 0, c = 0, t = 0;
+    if (mq_gemv_plan(rows, cols, 6, &s, &c, &t) != MQ_OK) return 0;
+    return mq_gemv_workspace_bytes_for(rows, cols, s, c, t);
+}
+
+size_t mq_gemv_group_workspace_bytes(const mq_gemv_part *parts, int nparts, int cols, int splits,
+                                     int chunks_per_split, int tiles_per_item)
+{
+    if (!parts || nparts < 1 || nparts > kMaxParts) return 0;
+    Part ps[kMaxParts];
+    for (int p = 0; p < nparts; ++p) ps[p] = Part{parts[p].fmt, parts[p].rows, parts[p].Wp, parts[p].y};
+    const Plan pl{splits, chunks_per_split, tiles_per_item};
+    GemvLaunch a;
     size_t need = 0;
-    for (int fmt : {6, 4}) {
-        int s = 0, c = 0, t = 0;
-        if (mq_gemv_plan(rows, cols, fmt, &s, &c, &t) != MQ_OK) return 0;
-        const size_t b = mq_gemv_workspace_bytes_for(rows, cols, s, c, t);
-        if (b > need) need = b;
-    }
+    if (prepare_group(ps, nparts, nullptr, cols, splits > 0 ? &pl : nullptr, &a, &need, true) != MQ_OK)
+        return 0;
     return need;
+}
+
+int mq_gemv_group_q8(const mq_gemv_part *parts, int nparts, const void *q8, int cols, void *ws,
+                     size_t ws_bytes, void *stream)
+{
+    return mq_gemv_group_q8_plan(parts, nparts, q8, cols, 0, 0, 0, ws, ws_bytes, stream);
+}
+
+int mq_gemv_group_q8_plan(const mq_gemv_part *parts, int nparts, const void *q8, int cols,
+                          int splits, int chunks_per_split, int tiles_per_item, void *ws,
+                          size_t ws_bytes, void *stream)
+{
+    if (!parts) return MQ_ERR_NULL;
+    if (nparts < 1 || nparts > kMaxParts) return MQ_ERR_SHAPE;
+    Part ps[kMaxParts];
+    for (int p = 0; p < nparts; ++p) ps[p] = Part{parts[p].fmt, parts[p].rows, parts[p].Wp, parts[p].y};
+    const Plan pl{splits, chunks_per_split, tiles_per_item};
+    return gemv_group(ps, nparts, q8, cols, splits > 0 ? &pl : nullptr, ws, ws_bytes, stream);
 }
 
 int mq_set_pdl(int enable)
@@ -373,6 +436,7 @@ int mq_gemv_q6k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int 
                         int chunks_per_split, int tiles_per_item, void *ws, size_t ws_bytes,
                         void *stream)
 {
+    if (splits < 1) return MQ_ERR_COVERAGE;
     const Plan p{splits, chunks_per_split, tiles_per_item};
     return gemv_common(6, Wp, q8, y, rows, cols, &p, ws, ws_bytes, stream);
 }
@@ -381,6 +445,7 @@ int mq_gemv_q4k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int 
                         int chunks_per_split, int tiles_per_item, void *ws, size_t ws_bytes,
                         void *stream)
 {
+    if (splits < 1) return MQ_ERR_COVERAGE;
     const Plan p{splits, chunks_per_split, tiles_per_item};
     return gemv_common(4, Wp, q8, y, rows, cols, &p, ws, ws_bytes, stream);
 }

@@ -35,7 +35,10 @@
 //   * With programmatic dependent launch the first chunk's weight loads are
 //     issued before griddepcontrol.wait, so the weight stream starts while
 //     the preceding kernel (the q8 producer) drains; the activation, the
-//     output and the workspace are touched only after the wait.
+//     output and the workspace are touched only after the wait.  The
+//     activation is read with ld.global.cg, never the non-coherent path: the
+//     compiler treats non-coherent loads as invariant and may hoist them
+//     above the wait, and under PDL the plane is still being written then.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -97,13 +100,14 @@ struct Unit {
     bool active;         // this lane owns a unit of the chunk
 };
 
-__device__ __forceinline__ Unit locate(const GemvLaunch &a, int t, int c, int lane, int chunk_bytes)
+__device__ __forceinline__ Unit locate(const GemvLaunch &a, const GemvPart &P, int t, int c,
+                                      int lane, int chunk_bytes)
 {
     Unit x;
     x.t = t;
     x.c = c;
     x.cb = min(kChunkBlocks, a.nb - kChunkBlocks * c);
-    x.seg = a.W + (size_t)t * a.tile_bytes + (size_t)c * chunk_bytes;
+    x.seg = P.W + (size_t)t * P.tile_bytes_div16 * 16 + (size_t)c * chunk_bytes;
     x.active = lane < 8 * x.cb;
     return x;
 }
@@ -144,9 +148,9 @@ __device__ __forceinline__ void load_x(const GemvLaunch &a, const Unit &x, int l
     if (x.active) {
         const int U = 32 * x.c + lane;
         const uint4 *qs = reinterpret_cast<const uint4 *>(a.q8 + (size_t)U * 32);
-        R.xa = __ldg(qs);
-        R.xb = __ldg(qs + 1);
-        R.dh = __ldg(reinterpret_cast<const unsigned short *>(a.q8 + a.q8_d_off) + U);
+        R.xa = __ldcg(qs);
+        R.xb = __ldcg(qs + 1);
+        R.dh = __ldcg(reinterpret_cast<const unsigned short *>(a.q8 + a.q8_d_off) + U);
     } else {
         R.xa = R.xb = make_uint4(0, 0, 0, 0);
         R.dh = 0;
@@ -154,8 +158,8 @@ __device__ __forceinline__ void load_x(const GemvLaunch &a, const Unit &x, int l
 }
 
 template <bool SUBDOTS>
-__device__ __forceinline__ void compute(const GemvLaunch &a, const Q6kRegs &R, const Unit &x,
-                                        int lane, float (&acc)[8])
+__device__ __forceinline__ void compute(const GemvLaunch &a, const GemvPart &P, const Q6kRegs &R,
+                                        const Unit &x, int lane, float (&acc)[8])
 {
     const float d8 = __half2float(__ushort_as_half(R.dh));
     const int xs0 = sum16(R.xa), xs1 = sum16(R.xb);
@@ -179,7 +183,7 @@ __device__ __forceinline__ void compute(const GemvLaunch &a, const Q6kRegs &R, c
         const int sc1 = (int)(int8_t)((scw >> 8) & 0xffu);
         if (SUBDOTS) {
             const int row = x.t * kTileRows + r;
-            if (x.active && row < a.rows) {
+            if (x.active && row < P.rows) {
                 const int blk = kChunkBlocks * x.c + (lane >> 3), p = lane & 7;
                 int32_t *o = a.isums + ((size_t)row * a.nb + blk) * 16 + 2 * p;
                 o[0] = isum0;
@@ -227,10 +231,10 @@ __device__ __forceinline__ void load_x(const GemvLaunch &a, const Unit &x, int l
     if (x.active) {
         const int U = 32 * x.c + lane;
         const uint4 *qs = reinterpret_cast<const uint4 *>(a.q8 + (size_t)U * 32);
-        R.xa = __ldg(qs);
-        R.xb = __ldg(qs + 1);
-        R.dh = __ldg(reinterpret_cast<const unsigned short *>(a.q8 + a.q8_d_off) + U);
-        R.qsum = __ldg(reinterpret_cast<const int *>(a.q8 + a.q8_sum_off) + U);
+        R.xa = __ldcg(qs);
+        R.xb = __ldcg(qs + 1);
+        R.dh = __ldcg(reinterpret_cast<const unsigned short *>(a.q8 + a.q8_d_off) + U);
+        R.qsum = __ldcg(reinterpret_cast<const int *>(a.q8 + a.q8_sum_off) + U);
     } else {
         R.xa = R.xb = make_uint4(0, 0, 0, 0);
         R.dh = 0;
@@ -239,8 +243,8 @@ __device__ __forceinline__ void load_x(const GemvLaunch &a, const Unit &x, int l
 }
 
 template <bool SUBDOTS>
-__device__ __forceinline__ void compute(const GemvLaunch &a, const Q4kRegs &R, const Unit &x,
-                                        int lane, float (&acc)[8])
+__device__ __forceinline__ void compute(const GemvLaunch &a, const GemvPart &P, const Q4kRegs &R,
+                                        const Unit &x, int lane, float (&acc)[8])
 {
     const float d8 = __half2float(__ushort_as_half(R.dh));
 #pragma unroll
@@ -254,7 +258,7 @@ __device__ __forceinline__ void compute(const GemvLaunch &a, const Q4kRegs &R, c
         }
         if (SUBDOTS) {
             const int row = x.t * kTileRows + r;
-            if (x.active && row < a.rows) {
+            if (x.active && row < P.rows) {
                 const int blk = kChunkBlocks * x.c + (lane >> 3), k = lane & 7;
                 a.isums[((size_t)row * a.nb + blk) * 8 + k] = dot;
             }
@@ -297,10 +301,10 @@ __device__ __forceinline__ float reduce8(const float (&acc)[8], int lane)
     return v;
 }
 
-// Tile t is finished for this warp (work item `item`, covering units
-// [u0, u1)): write it, or combine it with the tile's other splits.
-__device__ __forceinline__ void flush_tile(const GemvLaunch &a, int t, float (&acc)[8], int item,
-                                           int u0, int u1, int lane)
+// Tile t of part P is finished for this warp (work item `item`, covering the
+// part's units [u0, u1)): write it, or combine it with the tile's other splits.
+__device__ __forceinline__ void flush_tile(const GemvLaunch &a, const GemvPart &P, int t,
+                                           float (&acc)[8], int item, int u0, int u1, int lane)
 {
     __shared__ float cta_part[kMaxCtaSplits][8];
     const float v = reduce8(acc, lane);
@@ -309,7 +313,7 @@ __device__ __forceinline__ void flush_tile(const GemvLaunch &a, int t, float (&a
     const int row0 = t * kTileRows;
     const int tu0 = t * a.nchunks, tu1 = tu0 + a.nchunks;
     if (tu0 >= u0 && tu1 <= u1) {  // whole tile in this range
-        if ((lane & 3) == 0 && row0 + (lane >> 2) < a.rows) a.y[row0 + (lane >> 2)] = v;
+        if ((lane & 3) == 0 && row0 + (lane >> 2) < P.rows) P.y[row0 + (lane >> 2)] = v;
         return;
     }
     if (a.splits <= kMaxCtaSplits) {
@@ -325,7 +329,7 @@ __device__ __forceinline__ void flush_tile(const GemvLaunch &a, int t, float (&a
         if (s == 0 && lane < 8) {
             float sum = 0.0f;
             for (int j = 0; j < a.splits; ++j) sum += cta_part[j][lane];
-            if (row0 + lane < a.rows) a.y[row0 + lane] = sum;
+            if (row0 + lane < P.rows) P.y[row0 + lane] = sum;
         }
         return;
     }
@@ -338,10 +342,11 @@ __device__ __forceinline__ void flush_tile(const GemvLaunch &a, int t, float (&a
         const float pk = __shfl_sync(kFull, v, 4 * k);
         if (lane == 0) dst[k] = pk;
     }
+    const int gt = P.tile0 + t;  // global tile
     int last = 0;
     if (lane == 0) {
         __threadfence();
-        const unsigned prev = atomicAdd(a.ws_cnt + t, 1u);
+        const unsigned prev = atomicAdd(a.ws_cnt + gt, 1u);
         last = prev == (unsigned)(a.splits - 1);
     }
     last = __shfl_sync(kFull, last, 0);
@@ -349,7 +354,7 @@ __device__ __forceinline__ void flush_tile(const GemvLaunch &a, int t, float (&a
     __threadfence();
     // last arriver: lane (8g + r) loads split base+g of row r, four splits
     // per round trip; lanes 0..7 add them in ascending split order
-    const float *base_ptr = a.ws_part + (size_t)t * a.splits * 8;
+    const float *base_ptr = a.ws_part + ((size_t)P.item0 + (size_t)t * a.splits) * 8;
     float sum = 0.0f;
     for (int base = 0; base < a.splits; base += 4) {
         const int s = base + (lane >> 3);
@@ -359,38 +364,21 @@ __device__ __forceinline__ void flush_tile(const GemvLaunch &a, int t, float (&a
         const float p3 = __shfl_down_sync(kFull, p, 24);
         sum = (((sum + p) + p1) + p2) + p3;
     }
-    if (lane < 8 && row0 + lane < a.rows) a.y[row0 + lane] = sum;
-    if (lane == 0) a.ws_cnt[t] = 0u;  // ready for the next call
+    if (lane < 8 && row0 + lane < P.rows) P.y[row0 + lane] = sum;
+    if (lane == 0) a.ws_cnt[gt] = 0u;  // ready for the next call
 }
 
-// CTA shapes: splits == 1 (whole tiles) and splits > kMaxCtaSplits use CTAs
-// of kGemvWarpsPerBlock independent warps; 2..kMaxCtaSplits splits use one
-// CTA per tile whose warps are its splits.
-template <int FMT, bool SUBDOTS>  // FMT 6 = q6_K, 4 = q4_K
-__global__ void __launch_bounds__(32 * kMaxCtaSplits, 1) gemv_kernel(const GemvLaunch a)
+// Stream the part's units [u0, u1) with two register buffers.
+template <int FMT, bool SUBDOTS>
+__device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P, int item, int u0,
+                                          int u1, int lane)
 {
     using Regs = typename std::conditional<FMT == 6, Q6kRegs, Q4kRegs>::type;
     constexpr int kChunkBytes = (FMT == 6 ? kQ6kChunkPerBlock : kQ4kChunkPerBlock) * kChunkBlocks;
-    const int lane = threadIdx.x & 31;
-    const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    griddep_launch_dependents();
-    // a whole warp leaves; CTAs that combine in shared memory are launched
-    // exact (every warp has an item), so none of their warps leaves early
-    if (item >= a.n_items) return;
     const int nch = a.nchunks;
-    int u0, u1;
-    if (a.splits > 1) {
-        const int tt = item / a.splits, s = item - tt * a.splits;
-        u0 = tt * nch + s * a.cps;
-        u1 = tt * nch + min(s * a.cps + a.cps, nch);
-    } else {
-        u0 = item * a.tpi * nch;
-        u1 = min(u0 + a.tpi * nch, a.ntiles * nch);
-    }
-
     Regs A, B;
     int t = u0 / nch, c = u0 - t * nch;  // position of the next chunk to load
-    Unit xa = locate(a, t, c, lane, kChunkBytes), xb;
+    Unit xa = locate(a, P, t, c, lane, kChunkBytes), xb;
     load_w(xa, lane, A);   // weights do not depend on the preceding kernel
     griddep_wait();        // the q8 plane, y and the workspace do
     load_x(a, xa, lane, A);
@@ -402,50 +390,81 @@ __global__ void __launch_bounds__(32 * kMaxCtaSplits, 1) gemv_kernel(const GemvL
     for (int u = u0; u < u1; u += 2) {
         const bool has_b = u + 1 < u1;
         if (has_b) {
-            xb = locate(a, t, c, lane, kChunkBytes);
+            xb = locate(a, P, t, c, lane, kChunkBytes);
             load_w(xb, lane, B);
             load_x(a, xb, lane, B);
             if (++c == nch) { c = 0; ++t; }
         }
-        compute<SUBDOTS>(a, A, xa, lane, acc);
-        if (!SUBDOTS && (!has_b || xb.t != xa.t)) flush_tile(a, xa.t, acc, item, u0, u1, lane);
+        compute<SUBDOTS>(a, P, A, xa, lane, acc);
+        if (!SUBDOTS && (!has_b || xb.t != xa.t)) flush_tile(a, P, xa.t, acc, item, u0, u1, lane);
         if (!has_b) break;
         const bool has_a = u + 2 < u1;
         if (has_a) {
-            xa = locate(a, t, c, lane, kChunkBytes);
+            xa = locate(a, P, t, c, lane, kChunkBytes);
             load_w(xa, lane, A);
             load_x(a, xa, lane, A);
             if (++c == nch) { c = 0; ++t; }
         }
-        compute<SUBDOTS>(a, B, xb, lane, acc);
-        if (!SUBDOTS && (!has_a || xa.t != xb.t)) flush_tile(a, xb.t, acc, item, u0, u1, lane);
+        compute<SUBDOTS>(a, P, B, xb, lane, acc);
+        if (!SUBDOTS && (!has_a || xa.t != xb.t)) flush_tile(a, P, xb.t, acc, item, u0, u1, lane);
     }
 }
 
-template <int FMT, bool SUBDOTS>
+// CTA shapes: splits == 1 (whole tiles) and splits > kMaxCtaSplits use CTAs
+// of kGemvWarpsPerBlock independent warps; 2..kMaxCtaSplits splits use one
+// CTA per tile whose warps are its splits.  The part of a work item is found
+// with constant indices (the part table stays in parameter space).
+template <bool SUBDOTS>
+__global__ void __launch_bounds__(32 * kMaxCtaSplits, 1)
+    gemv_kernel(const __grid_constant__ GemvLaunch a)
+{
+    const int lane = threadIdx.x & 31;
+    const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    griddep_launch_dependents();
+    // a whole warp leaves; CTAs that combine in shared memory are launched
+    // exact (every warp has an item), so none of their warps leaves early
+    if (item >= a.n_items) return;
+    int pi = 0;
+#pragma unroll
+    for (int k = 1; k < kMaxParts; ++k)
+        if (k < a.nparts && item >= a.part[k].item0) pi = k;
+    const GemvPart &P = a.part[pi];  // stays in the kernel's constant parameter space
+    const int li = item - P.item0;
+    const int nch = a.nchunks;
+    int u0, u1;
+    if (a.splits > 1) {
+        const int tt = li / a.splits, s = li - tt * a.splits;
+        u0 = tt * nch + s * a.cps;
+        u1 = tt * nch + min(s * a.cps + a.cps, nch);
+    } else {
+        u0 = li * a.tpi * nch;
+        u1 = min(u0 + a.tpi * nch, P.ntiles * nch);
+    }
+    if (P.fmt == 6)
+        run_range<6, SUBDOTS>(a, P, item, u0, u1, lane);
+    else
+        run_range<4, SUBDOTS>(a, P, item, u0, u1, lane);
+}
+
+template <bool SUBDOTS>
 cudaError_t launch(const GemvLaunch &a, cudaStream_t st)
 {
     const int warps = gemv_cta_warps(a.splits, SUBDOTS);
     const long long blocks = (a.n_items + warps - 1) / warps;
-    return launch_maybe_pdl(gemv_kernel<FMT, SUBDOTS>, dim3((unsigned)blocks), dim3(32 * warps),
-                            a.pdl, st, a);
+    return launch_maybe_pdl(gemv_kernel<SUBDOTS>, dim3((unsigned)blocks), dim3(32 * warps), a.pdl,
+                            st, a);
 }
 
 }  // namespace
 
-cudaError_t launch_gemv_q6k(const GemvLaunch &a, cudaStream_t st) { return launch<6, false>(a, st); }
-cudaError_t launch_gemv_q4k(const GemvLaunch &a, cudaStream_t st) { return launch<4, false>(a, st); }
-cudaError_t launch_subdots_q6k(const GemvLaunch &a, cudaStream_t st) { return launch<6, true>(a, st); }
-cudaError_t launch_subdots_q4k(const GemvLaunch &a, cudaStream_t st) { return launch<4, true>(a, st); }
+cudaError_t launch_gemv(const GemvLaunch &a, cudaStream_t st) { return launch<false>(a, st); }
+cudaError_t launch_subdots(const GemvLaunch &a, cudaStream_t st) { return launch<true>(a, st); }
 
-int gemv_ctas_per_sm(int fmt, int warps_per_cta)
+int gemv_ctas_per_sm(int warps_per_cta)
 {
     int blocks = 0;
-    const cudaError_t e =
-        fmt == 6 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemv_kernel<6, false>,
-                                                                 32 * warps_per_cta, 0)
-                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, gemv_kernel<4, false>,
-                                                                 32 * warps_per_cta, 0);
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &blocks, gemv_kernel<false>, 32 * warps_per_cta, 0);
     return e == cudaSuccess ? blocks : 0;
 }
 

@@ -7,35 +7,46 @@
 
 namespace mq {
 
-// One GEMV launch.  The matrix is ntiles x nchunks chunk units (tile = 8
-// rows, chunk = 4 super-blocks of those rows).  A work item (one warp)
-// streams a contiguous range of them:
-//   splits == 1: item i covers whole tiles [i*tpi, min((i+1)*tpi, ntiles));
-//   splits > 1 (tall rows): item i is split s = i % splits of tile
-//     t = i / splits and covers chunks [s*cps, min((s+1)*cps, nchunks)) of t.
-//     Up to kMaxCtaSplits splits the splits of a tile are the warps of one
-//     CTA and combine in shared memory; beyond that they combine through the
-//     workspace, where the last one to finish adds the partials in ascending
-//     split order.
-struct GemvLaunch {
+// One GEMV launch over a group of 1..kMaxParts matrices ("parts") that
+// share one q8 activation plane (the same cols): q, k, v of a layer, or its
+// gate and up.  Each part is cut into ntiles tiles of 8 rows x nchunks chunk
+// units (chunk = 4 super-blocks).  A work item (one warp) streams a
+// contiguous range of one part's units:
+//   splits == 1: whole tiles, tpi per item (a part's last item may hold fewer);
+//   splits > 1 (tall rows): one of `splits` tile-aligned column ranges of a
+//     tile, chunks [s*cps, min((s+1)*cps, nchunks)).  Up to kMaxCtaSplits the
+//     splits of a tile are the warps of one CTA and combine in shared memory;
+//     beyond that they combine through the workspace, where the last one to
+//     finish adds the partials in ascending split order.
+// Items are numbered part by part; part p owns items [item0, item0 + items)
+// and global tiles [tile0, tile0 + ntiles).
+constexpr int kMaxParts = 8;
+
+struct GemvPart {
     const uint8_t *W;       // repacked weights (layout.h)
-    const uint8_t *q8;      // q8 plane of cols values
     float *y;               // rows outputs
-    int32_t *isums;         // sub-dot mode: rows * nb * {16 | 8} int32, else null
-    unsigned *ws_cnt;       // arrival counters [ntiles] (splits > kMaxCtaSplits)
+    int rows, ntiles;
+    int fmt;                // 6 = q6_K, 4 = q4_K
+    int item0, tile0;       // first work item and first global tile of the part
+    int tile_bytes_div16;   // bytes of one 8-row tile / 16
+};
+
+struct GemvLaunch {
+    GemvPart part[kMaxParts];
+    int nparts;
+    const uint8_t *q8;      // q8 plane of cols values
+    int32_t *isums;         // sub-dot mode (one part): rows * nb * {16 | 8} int32, else null
+    unsigned *ws_cnt;       // arrival counters [total tiles] (splits > kMaxCtaSplits)
     float *ws_part;         // partials [n_items][8 rows] (splits > kMaxCtaSplits)
-    int rows, nb, ntiles, nchunks;
+    int nb, nchunks;        // super-blocks and chunks per row (all parts)
     int splits, cps, tpi;   // the plan (see above)
     int n_items;
-    size_t tile_bytes;
     unsigned q8_d_off, q8_sum_off;
     int pdl;                // launch with programmatic stream serialization
 };
 
-cudaError_t launch_gemv_q6k(const GemvLaunch &a, cudaStream_t st);
-cudaError_t launch_gemv_q4k(const GemvLaunch &a, cudaStream_t st);
-cudaError_t launch_subdots_q6k(const GemvLaunch &a, cudaStream_t st);
-cudaError_t launch_subdots_q4k(const GemvLaunch &a, cudaStream_t st);
+cudaError_t launch_gemv(const GemvLaunch &a, cudaStream_t st);
+cudaError_t launch_subdots(const GemvLaunch &a, cudaStream_t st);
 
 constexpr int kGemvWarpsPerBlock = 4;   // CTA of independent warps
 constexpr int kMaxCtaSplits = 12;       // largest CTA whose warps are one tile's splits
@@ -46,9 +57,9 @@ inline int gemv_cta_warps(int splits, bool subdots = false)
     return (!subdots && splits > 1 && splits <= kMaxCtaSplits) ? splits : kGemvWarpsPerBlock;
 }
 
-// Resident CTAs per SM of the GEMV kernel for format 6 (q6_K) or 4 (q4_K)
-// with `warps_per_cta` warps, on the current device (0 on error).
-int gemv_ctas_per_sm(int fmt, int warps_per_cta);
+// Resident CTAs per SM of the GEMV kernel with `warps_per_cta` warps, on the
+// current device (0 on error).
+int gemv_ctas_per_sm(int warps_per_cta);
 
 // Producers.  d_off / sum_off locate the q8 plane's fp16-scale and sum
 // sections (layout.h q8_d_offset / q8_sum_offset).

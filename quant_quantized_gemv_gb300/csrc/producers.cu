@@ -15,6 +15,11 @@
 // The fused producers quantize the f32 values they have just computed, in
 // registers, so the q8 bytes are by construction the quantization of the f32
 // output they write (the page's "constructive bitwise", §2.3).
+//
+// Inputs may be written by the preceding kernel, which under programmatic
+// dependent launch is still running when these kernels start: every input
+// is read after griddepcontrol.wait and with coherent loads (ld.global.cg),
+// never the non-coherent path the compiler may hoist above the wait.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -68,7 +73,7 @@ __global__ void __launch_bounds__(256) quantize_q8_kernel(const float *__restric
     griddep_wait();  // x may come from the preceding kernel
     const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const bool valid = gid < n4;
-    const float4 v = valid ? __ldg(reinterpret_cast<const float4 *>(x) + gid)
+    const float4 v = valid ? __ldcg(reinterpret_cast<const float4 *>(x) + gid)
                            : make_float4(0.f, 0.f, 0.f, 0.f);
     quantize4(v, valid, gid, q8, d_off, sum_off);
 }
@@ -117,7 +122,7 @@ __global__ void __launch_bounds__(kRmsThreads) rmsnorm_quant_q8_kernel(
 
     float ss = 0.0f;
     for (int i = tid; i < n4; i += kRmsThreads) {
-        const float4 v = __ldg(x4 + i);
+        const float4 v = __ldcg(x4 + i);
         ss = fmaf(v.x, v.x, ss);
         ss = fmaf(v.y, v.y, ss);
         ss = fmaf(v.z, v.z, ss);
@@ -143,8 +148,8 @@ __global__ void __launch_bounds__(kRmsThreads) rmsnorm_quant_q8_kernel(
         const bool valid = i < n4;
         float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
         if (valid) {
-            const float4 v = __ldg(x4 + i);
-            const float4 gv = __ldg(g4 + i);
+            const float4 v = __ldcg(x4 + i);
+            const float4 gv = __ldcg(g4 + i);
             out.x = (v.x * scale) * gv.x;
             out.y = (v.y * scale) * gv.y;
             out.z = (v.z * scale) * gv.z;

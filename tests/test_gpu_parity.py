@@ -284,3 +284,49 @@ def test_full_size_sampled_rows(mq, orc, name, fmt, rows, cols, producer):
     idx = sampled_rows(rows, 384, name)
     yref, absum = orc.gemv(fmt, np.ascontiguousarray(W[idx]), d, q, len(idx), cols, threads=8)
     assert_gemv_close(y1[idx], yref, absum)
+
+
+# ------------------------------------------------------------------ groups
+GROUPS = [
+    # q, k, v of a layer (q4_K, q4_K, q6_K), ragged rows, ragged last chunk
+    (4608, [("q4k", 40), ("q4k", 13), ("q6k", 24)]),
+    # a gate/up pair and a third part with long rows (19 chunks: > 12 splits possible)
+    (18944, [("q4k", 16), ("q4k", 16), ("q6k", 9)]),
+]
+
+
+@pytest.mark.parametrize("cols,spec", GROUPS)
+def test_group_matches_oracle_under_every_plan(mq, orc, cols, spec):
+    import torch
+    g = synth.rng("group", cols)
+    Ws = [synth.blocks(fmt, g, rows, cols) for fmt, rows in spec]
+    Wps = [repack_dev(mq, fmt, W, rows, cols) for (fmt, rows), W in zip(spec, Ws)]
+    x = special_activation(cols, "group")
+    plane = mq.mq_quantize_q8(dev(x))
+    d0, q0, _ = orc.quantize_q8(x)
+    refs = [orc.gemv(fmt, W, d0, q0, rows, cols) for (fmt, rows), W in zip(spec, Ws)]
+    parts = [(fmt, Wp, rows) for (fmt, rows), Wp in zip(spec, Wps)]
+    ntiles = sum(-(-rows // 8) for _, rows in spec)
+    nch = -(-(cols // 256) // 4)
+    plans = [None] + all_plans(ntiles, nch)
+    for plan in plans:
+        ws = mq.mq_gemv_group_workspace(parts, cols, plan=plan)
+        ys1 = mq.mq_gemv_group_q8(parts, plane, cols, ws=ws, plan=plan)
+        ys2 = mq.mq_gemv_group_q8(parts, plane, cols, ws=ws, plan=plan)
+        for y1, y2, (yref, absum) in zip(ys1, ys2, refs):
+            assert_gemv_close(host(y1), yref, absum)
+            assert np.array_equal(host(y1), host(y2)), plan
+        if ws is not None:
+            assert torch.count_nonzero(ws[:4 * ntiles]).item() == 0
+
+
+def test_group_of_one_is_the_single_gemv(mq):
+    rows, cols = 3584, 18944
+    g = synth.rng("group-one")
+    W = synth.q6k_blocks(g, rows, cols)
+    Wp = repack_dev(mq, "q6k", W, rows, cols)
+    plane = mq.mq_quantize_q8(dev(synth.normal(g, cols)))
+    y1 = host(gemv(mq, "q6k", Wp, plane, rows, cols))
+    (y2,) = mq.mq_gemv_group_q8([("q6k", Wp, rows)], plane, cols,
+                                ws=mq.mq_gemv_group_workspace([("q6k", Wp, rows)], cols))
+    assert np.array_equal(y1, host(y2))

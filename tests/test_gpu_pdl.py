@@ -33,8 +33,9 @@ class FfnChain:
     """rms -> gate, up (q4_K) -> swiglu -> down (q6_K): the FFN half of a
     14B-shaped layer at reduced width, all buffers preallocated."""
 
-    def __init__(self, mq, hidden=2048, inter=5376):
+    def __init__(self, mq, hidden=2048, inter=5376, grouped=False):
         import torch
+        self.grouped = grouped
         g = synth.rng("pdl-chain")
         self.mq, self.h, self.i = mq, hidden, inter
         self.Wg_h = synth.q4k_blocks(g, inter, hidden)
@@ -54,12 +55,18 @@ class FfnChain:
         self.out = torch.empty(hidden, device="cuda")
         self.wsg = mq.mq_gemv_workspace(inter, hidden)
         self.wsd = mq.mq_gemv_workspace(hidden, inter)
+        self.wsgu = mq.mq_gemv_group_workspace([("q4k", self.Wg, inter), ("q4k", self.Wu, inter)],
+                                               hidden)
 
     def step(self):
         mq = self.mq
         mq.mq_rmsnorm_quant_q8(self.x, self.gain, 1e-6, y=self.xn, q8=self.q8a)
-        mq.mq_gemv_q4k_q8(self.Wg, self.q8a, self.i, self.h, y=self.yg, ws=self.wsg)
-        mq.mq_gemv_q4k_q8(self.Wu, self.q8a, self.i, self.h, y=self.yu, ws=self.wsg)
+        if self.grouped:                          # gate and up in one launch
+            mq.mq_gemv_group_q8([("q4k", self.Wg, self.i), ("q4k", self.Wu, self.i)], self.q8a,
+                                self.h, ys=[self.yg, self.yu], ws=self.wsgu)
+        else:
+            mq.mq_gemv_q4k_q8(self.Wg, self.q8a, self.i, self.h, y=self.yg, ws=self.wsg)
+            mq.mq_gemv_q4k_q8(self.Wu, self.q8a, self.i, self.h, y=self.yu, ws=self.wsg)
         mq.mq_swiglu_quant_q8(self.yg, self.yu, y=self.act, q8=self.q8b)
         mq.mq_gemv_q6k_q8(self.Wd, self.q8b, self.h, self.i, y=self.out, ws=self.wsd)
 
@@ -89,10 +96,11 @@ def run_steps(mq, chain, xs, pdl, graph):
     return [o.cpu().numpy() for o in outs]
 
 
-def test_pdl_chain_is_bitwise_identical(mq, orc):
-    chain = FfnChain(mq)
+@pytest.mark.parametrize("grouped", [False, True])
+def test_pdl_chain_is_bitwise_identical(mq, orc, grouped):
+    chain = FfnChain(mq, grouped=grouped)
     g = synth.rng("pdl-inputs")
-    xs = [dev(synth.normal(g, chain.h)) for _ in range(4)]
+    xs = [dev(synth.normal(g, chain.h)) for _ in range(8)]
     ref = run_steps(mq, chain, xs, pdl=False, graph=False)
     for pdl, graph in ((True, False), (False, True), (True, True)):
         got = run_steps(mq, chain, xs, pdl=pdl, graph=graph)

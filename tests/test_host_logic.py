@@ -193,3 +193,34 @@ def test_binding_refuses_cpu_tensors(mq):
     import torch
     with pytest.raises(TypeError):
         mq.mq_quantize_q8(torch.zeros(64))
+
+
+def test_group_workspace_and_validation(mq):
+    qkv = [("q4k", None, 5120), ("q4k", None, 1024), ("q6k", None, 1024)]    # 640 + 128 + 128 tiles
+    assert mq.mq_gemv_group_workspace_bytes(qkv, 16384, (4, 4, 1)) == 0      # CTA splits
+    assert mq.mq_gemv_group_workspace_bytes(qkv, 16384, (16, 1, 1)) == 896 * 4 + 896 * 16 * 8 * 4
+    assert mq.mq_gemv_group_workspace_bytes(qkv, 16384, (1, 16, 3)) == 0     # whole tiles
+    assert mq.mq_gemv_group_workspace_bytes(qkv, 16384, (2, 7, 1)) == 0      # invalid plan
+    assert mq.mq_gemv_group_workspace_bytes([("q5k", None, 8)], 1024, (1, 1, 1)) == 0
+    assert mq.mq_gemv_group_workspace_bytes(qkv * 3, 1024, (1, 1, 1)) == 0   # 9 parts > MQ_MAX_GROUP
+    assert mq.MQ_MAX_GROUP == 8
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="fake device pointers are only passed where no GPU exists")
+def test_group_validation_rejects_before_launch(mq):
+    L = mq.lib()
+    arr = (mq.MQGemvPart * 3)()
+    for i, (fmt, rows) in enumerate(((4, 5120), (4, 1024), (6, 1024))):
+        arr[i].fmt, arr[i].rows, arr[i].Wp, arr[i].y = fmt, rows, 0x10000 * (i + 1), 0x100000 * (i + 1)
+    Q = ctypes.c_void_p(0x900000)
+    N = ctypes.c_void_p(0)
+    assert L.mq_gemv_group_q8(arr, 0, Q, 5120, N, 0, N) == mq.MQ_ERR_SHAPE
+    assert L.mq_gemv_group_q8(arr, 9, Q, 5120, N, 0, N) == mq.MQ_ERR_SHAPE
+    assert L.mq_gemv_group_q8(arr, 3, N, 5120, N, 0, N) == mq.MQ_ERR_NULL
+    assert L.mq_gemv_group_q8_plan(arr, 3, Q, 5120, 3, 1, 1, N, 0, N) == mq.MQ_ERR_COVERAGE
+    arr[2].fmt = 5
+    assert L.mq_gemv_group_q8(arr, 3, Q, 5120, N, 0, N) == mq.MQ_ERR_SHAPE
+    arr[2].fmt = 6
+    arr[1].y = 0x100008
+    assert L.mq_gemv_group_q8(arr, 3, Q, 5120, N, 0, N) == mq.MQ_ERR_ALIGN
