@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "kernels.h"
 #include "layout.h"
@@ -51,38 +52,79 @@ int device_sms()
 
 // ctas[w], w = 1..kMaxCtaSplits: resident GEMV CTAs per SM with w warps each.
 struct Occupancy {
-    int ctas[kMaxCtaSplits + 1];
+    int ctas[kMaxCtaSplits + 1];  // CTAs with w warps, no dynamic shared memory
+    int ctas_tiles;               // 4-warp whole-tile CTAs holding the staged plane
 };
 
-bool device_occupancy(Occupancy *o)
+struct DeviceLimits {
+    int smem_per_sm, smem_reserved;  // shared memory per SM, reserved per CTA
+    size_t max_plane;                // largest q8 plane the GEMV stages
+};
+std::atomic<bool> g_limits_ok[kMaxDevices];
+DeviceLimits g_limits[kMaxDevices];
+std::mutex g_limits_mutex;
+
+bool device_limits(DeviceLimits *out)
 {
     const int dev = current_device();
     if (dev < 0) return false;
+    if (!g_limits_ok[dev].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(g_limits_mutex);
+        if (!g_limits_ok[dev].load(std::memory_order_relaxed)) {
+            DeviceLimits l;
+            if (cudaDeviceGetAttribute(&l.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                       dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&l.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock,
+                                       dev) != cudaSuccess)
+                return false;
+            l.max_plane = gemv_max_plane_bytes();  // also opts the kernels in
+            if (l.max_plane == 0) return false;
+            g_limits[dev] = l;
+            g_limits_ok[dev].store(true, std::memory_order_release);
+        }
+    }
+    *out = g_limits[dev];
+    return true;
+}
+
+// CTAs per SM: the register limit (measured once per device and CTA shape)
+// and the shared-memory limit of a plane of `plane` bytes.
+bool device_occupancy(Occupancy *o, size_t plane)
+{
+    const int dev = current_device();
+    DeviceLimits lim;
+    if (dev < 0 || !device_limits(&lim)) return false;
+    const long long per_cta = (long long)plane + kGemvStaticSmem + lim.smem_reserved;
+    const int by_smem = (int)(lim.smem_per_sm / per_cta);
     for (int w = 1; w <= kMaxCtaSplits; ++w) {
         std::atomic<int> &slot = g_ctas[dev][w];
         int v = slot.load(std::memory_order_relaxed);
         if (v <= 0) {
-            v = gemv_ctas_per_sm(w);
+            v = gemv_ctas_per_sm(w, 0);
             if (v <= 0) return false;
             slot.store(v, std::memory_order_relaxed);
         }
-        o->ctas[w] = v;
+        o->ctas[w] = v;  // split CTAs stage nothing
     }
-    return true;
+    // whole-tile CTAs stage the plane in shared memory
+    o->ctas_tiles = o->ctas[kGemvWarpsPerBlock] < by_smem ? o->ctas[kGemvWarpsPerBlock] : by_smem;
+    return o->ctas_tiles > 0;
 }
 
 // The same from a register count (host-only planning, tests): 64K registers
 // per SM, at most 2048 threads and 32 CTAs.
-Occupancy model_occupancy(int regs_per_thread)
+Occupancy model_occupancy(int regs_per_thread, size_t plane)
 {
     Occupancy o;
     const int regs = ((regs_per_thread + 7) / 8) * 8;
+    const int by_smem = (int)(233472 / ((long long)plane + kGemvStaticSmem + 1024));
     for (int w = 1; w <= kMaxCtaSplits; ++w) {
         int c = 65536 / (w * 32 * regs);
         if (c > 2048 / (32 * w)) c = 2048 / (32 * w);
         if (c > 32) c = 32;
         o.ctas[w] = c;
     }
+    o.ctas_tiles = o.ctas[kGemvWarpsPerBlock] < by_smem ? o.ctas[kGemvWarpsPerBlock] : by_smem;
     return o;
 }
 
@@ -97,8 +139,8 @@ struct Plan {
 Plan plan_for(int ntiles, int nchunks, int sms, const Occupancy &o)
 {
     if (sms <= 0) sms = 1;
-    const long long wave = (long long)sms * (o.ctas[kGemvWarpsPerBlock] > 0 ? o.ctas[kGemvWarpsPerBlock] : 1) *
-                           kGemvWarpsPerBlock;  // warps in one wave of 4-warp CTAs
+    const long long wave = (long long)sms * (o.ctas_tiles > 0 ? o.ctas_tiles : 1) *
+                           kGemvWarpsPerBlock;  // warps in one wave of 4-warp whole-tile CTAs
     if (ntiles >= wave || nchunks == 1)
         return Plan{1, nchunks, (int)((ntiles + wave - 1) / wave)};
     int best = 1;
@@ -174,12 +216,22 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
         total_tiles += ceil_div(x.rows, kTileRows);
     }
     if (total_tiles * nchunks >= (1LL << 31)) return MQ_ERR_SHAPE;
+    const size_t plane = q8_plane_bytes(cols);
+    if (explicit_plan) {  // a wrong plan is refused before anything touches the device
+        const int cov = check_plan(nchunks, *explicit_plan);
+        if (cov != MQ_OK) return cov;
+    }
+    if (!sizes_only) {
+        DeviceLimits lim;
+        if (!device_limits(&lim)) return MQ_ERR_CUDA;
+        if (plane > lim.max_plane) return MQ_ERR_SHAPE;  // the plane must fit in shared memory
+    }
     Plan pl;
     if (explicit_plan) {
         pl = *explicit_plan;
     } else {
         Occupancy o;
-        if (!device_occupancy(&o)) return MQ_ERR_CUDA;
+        if (!device_occupancy(&o, plane)) return MQ_ERR_CUDA;
         pl = plan_for((int)total_tiles, nchunks, device_sms(), o);
     }
     const int cov = check_plan(nchunks, pl);
@@ -211,6 +263,7 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
     a->n_items = (int)items;
     a->q8_d_off = (unsigned)q8_d_offset(cols);
     a->q8_sum_off = (unsigned)q8_sum_offset(cols);
+    a->q8_bytes = (unsigned)plane;
     a->pdl = g_pdl.load(std::memory_order_relaxed);
     *need = ws_bytes_for(total_tiles, items, pl);
     return MQ_OK;
@@ -221,6 +274,12 @@ int gemv_group(const Part *parts, int nparts, const void *q8, int cols, const Pl
 {
     GemvLaunch a;
     size_t need = 0;
+    if (explicit_plan) {  // argument errors first, before anything asks the device
+        const int st0 = prepare_group(parts, nparts, q8, cols, explicit_plan, &a, &need, true);
+        if (st0 != MQ_OK) return st0;
+        if (need > 0 && !ws) return MQ_ERR_NULL;
+        if (need > 0 && ws_bytes < need) return MQ_ERR_WORKSPACE;
+    }
     const int st = prepare_group(parts, nparts, q8, cols, explicit_plan, &a, &need);
     if (st != MQ_OK) return st;
     if (need > 0) {
@@ -343,7 +402,7 @@ int mq_gemv_plan_for(int rows, int cols, int sms, int regs_per_thread, int *spli
     if (!splits || !chunks_per_split || !tiles_per_item) return MQ_ERR_NULL;
     if (!gemv_shape_ok(rows, cols) || regs_per_thread < 1 || regs_per_thread > 255) return MQ_ERR_SHAPE;
     const Geom g = make_geom(rows, cols, kQ6kBytes);
-    const Plan p = plan_for(g.ntiles, g.nchunks, sms, model_occupancy(regs_per_thread));
+    const Plan p = plan_for(g.ntiles, g.nchunks, sms, model_occupancy(regs_per_thread, q8_plane_bytes(cols)));
     *splits = p.splits;
     *chunks_per_split = p.cps;
     *tiles_per_item = p.tpi;
@@ -357,7 +416,7 @@ int mq_gemv_plan(int rows, int cols, int fmt, int *splits, int *chunks_per_split
     if (fmt != 6 && fmt != 4) return MQ_ERR_SHAPE;
     if (!gemv_shape_ok(rows, cols)) return MQ_ERR_SHAPE;
     Occupancy o;
-    if (!device_occupancy(&o)) return MQ_ERR_CUDA;
+    if (!device_occupancy(&o, q8_plane_bytes(cols))) return MQ_ERR_CUDA;
     const Geom g = make_geom(rows, cols, kQ6kBytes);
     const Plan p = plan_for(g.ntiles, g.nchunks, device_sms(), o);
     *splits = p.splits;

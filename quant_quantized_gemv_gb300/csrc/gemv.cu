@@ -32,13 +32,18 @@
 //     them in ascending split order.  Either way the result does not depend
 //     on arrival order, and the host proves before launch that the splits
 //     cover every chunk exactly once (the page's §6 lesson).
+//   * With whole-tile plans the q8 plane (a few KB to ~25 KB) is copied once
+//     per CTA into shared memory and every lane reads its activation codes
+//     from there: each plane byte leaves L2 once per CTA instead of once per
+//     warp and tile.  Split plans read each activation chunk from L2 with
+//     its weights, one chunk ahead (a CTA there reads each byte once).
 //   * With programmatic dependent launch the first chunk's weight loads are
 //     issued before griddepcontrol.wait, so the weight stream starts while
-//     the preceding kernel (the q8 producer) drains; the activation, the
-//     output and the workspace are touched only after the wait.  The
-//     activation is read with ld.global.cg, never the non-coherent path: the
-//     compiler treats non-coherent loads as invariant and may hoist them
-//     above the wait, and under PDL the plane is still being written then.
+//     the preceding kernel (the q8 producer) drains; the q8 plane, the
+//     output and the workspace are touched only after the wait.  The plane
+//     is read with ld.global.cg, never the non-coherent path: the compiler
+//     treats non-coherent loads as invariant and may hoist them above the
+//     wait, and under PDL the plane is still being written then.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -143,14 +148,22 @@ __device__ __forceinline__ void load_w(const Unit &x, int lane, Q6kRegs &R)
     }
 }
 
-__device__ __forceinline__ void load_x(const GemvLaunch &a, const Unit &x, int lane, Q6kRegs &R)
+__device__ __forceinline__ void load_x(const GemvLaunch &a, const uint8_t *xs, const Unit &x,
+                                       int lane, Q6kRegs &R)
 {
     if (x.active) {
         const int U = 32 * x.c + lane;
-        const uint4 *qs = reinterpret_cast<const uint4 *>(a.q8 + (size_t)U * 32);
-        R.xa = __ldcg(qs);
-        R.xb = __ldcg(qs + 1);
-        R.dh = __ldcg(reinterpret_cast<const unsigned short *>(a.q8 + a.q8_d_off) + U);
+        if (!xs) {  // split plans: straight from L2, coherent (see the file comment)
+            const uint4 *qs = reinterpret_cast<const uint4 *>(a.q8 + (size_t)U * 32);
+            R.xa = __ldcg(qs);
+            R.xb = __ldcg(qs + 1);
+            R.dh = __ldcg(reinterpret_cast<const unsigned short *>(a.q8 + a.q8_d_off) + U);
+            return;
+        }
+        const uint4 *qs = reinterpret_cast<const uint4 *>(xs + (size_t)U * 32);
+        R.xa = qs[0];
+        R.xb = qs[1];
+        R.dh = reinterpret_cast<const unsigned short *>(xs + a.q8_d_off)[U];
     } else {
         R.xa = R.xb = make_uint4(0, 0, 0, 0);
         R.dh = 0;
@@ -226,15 +239,24 @@ __device__ __forceinline__ void load_w(const Unit &x, int lane, Q4kRegs &R)
     }
 }
 
-__device__ __forceinline__ void load_x(const GemvLaunch &a, const Unit &x, int lane, Q4kRegs &R)
+__device__ __forceinline__ void load_x(const GemvLaunch &a, const uint8_t *xs, const Unit &x,
+                                       int lane, Q4kRegs &R)
 {
     if (x.active) {
         const int U = 32 * x.c + lane;
-        const uint4 *qs = reinterpret_cast<const uint4 *>(a.q8 + (size_t)U * 32);
-        R.xa = __ldcg(qs);
-        R.xb = __ldcg(qs + 1);
-        R.dh = __ldcg(reinterpret_cast<const unsigned short *>(a.q8 + a.q8_d_off) + U);
-        R.qsum = __ldcg(reinterpret_cast<const int *>(a.q8 + a.q8_sum_off) + U);
+        if (!xs) {  // split plans: straight from L2, coherent (see the file comment)
+            const uint4 *qs = reinterpret_cast<const uint4 *>(a.q8 + (size_t)U * 32);
+            R.xa = __ldcg(qs);
+            R.xb = __ldcg(qs + 1);
+            R.dh = __ldcg(reinterpret_cast<const unsigned short *>(a.q8 + a.q8_d_off) + U);
+            R.qsum = __ldcg(reinterpret_cast<const int *>(a.q8 + a.q8_sum_off) + U);
+            return;
+        }
+        const uint4 *qs = reinterpret_cast<const uint4 *>(xs + (size_t)U * 32);
+        R.xa = qs[0];
+        R.xb = qs[1];
+        R.dh = reinterpret_cast<const unsigned short *>(xs + a.q8_d_off)[U];
+        R.qsum = reinterpret_cast<const int *>(xs + a.q8_sum_off)[U];
     } else {
         R.xa = R.xb = make_uint4(0, 0, 0, 0);
         R.dh = 0;
@@ -368,10 +390,30 @@ __device__ __forceinline__ void flush_tile(const GemvLaunch &a, const GemvPart &
     if (lane == 0) a.ws_cnt[gt] = 0u;  // ready for the next call
 }
 
+// Wait for the producer.  Whole-tile plans (splits == 1) then copy the whole
+// q8 plane into shared memory once per CTA (coalesced 16-byte coherent
+// loads) and meet at named barrier 1: every warp of such a CTA calls this
+// exactly once, from whichever code path it is on (a named barrier counts
+// arrivals, not call sites).  Returns where the activation is read from:
+// the shared copy, or null for the global plane (split plans, whose CTAs
+// read each plane byte once anyway).
+__device__ __forceinline__ const uint8_t *stage_plane(const GemvLaunch &a, uint8_t *xs)
+{
+    griddep_wait();  // the q8 plane, y and the workspace depend on it
+    if (a.splits != 1) return nullptr;
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.q8);
+    uint4 *dst = reinterpret_cast<uint4 *>(xs);
+    const int n16 = (int)(a.q8_bytes >> 4);
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = __ldcg(src + i);
+    asm volatile("bar.sync 1, %0;" ::"r"(blockDim.x) : "memory");
+    return xs;
+}
+
 // Stream the part's units [u0, u1) with two register buffers.
 template <int FMT, bool SUBDOTS>
-__device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P, int item, int u0,
-                                          int u1, int lane)
+__device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P, uint8_t *smem,
+                                          int item, int u0, int u1, int lane)
 {
     using Regs = typename std::conditional<FMT == 6, Q6kRegs, Q4kRegs>::type;
     constexpr int kChunkBytes = (FMT == 6 ? kQ6kChunkPerBlock : kQ4kChunkPerBlock) * kChunkBlocks;
@@ -380,8 +422,8 @@ __device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P
     int t = u0 / nch, c = u0 - t * nch;  // position of the next chunk to load
     Unit xa = locate(a, P, t, c, lane, kChunkBytes), xb;
     load_w(xa, lane, A);   // weights do not depend on the preceding kernel
-    griddep_wait();        // the q8 plane, y and the workspace do
-    load_x(a, xa, lane, A);
+    const uint8_t *xs = stage_plane(a, smem);  // the q8 plane, y and the workspace do
+    load_x(a, xs, xa, lane, A);
     if (++c == nch) { c = 0; ++t; }
 
     float acc[8];
@@ -392,7 +434,7 @@ __device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P
         if (has_b) {
             xb = locate(a, P, t, c, lane, kChunkBytes);
             load_w(xb, lane, B);
-            load_x(a, xb, lane, B);
+            load_x(a, xs, xb, lane, B);
             if (++c == nch) { c = 0; ++t; }
         }
         compute<SUBDOTS>(a, P, A, xa, lane, acc);
@@ -402,7 +444,7 @@ __device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P
         if (has_a) {
             xa = locate(a, P, t, c, lane, kChunkBytes);
             load_w(xa, lane, A);
-            load_x(a, xa, lane, A);
+            load_x(a, xs, xa, lane, A);
             if (++c == nch) { c = 0; ++t; }
         }
         compute<SUBDOTS>(a, P, B, xb, lane, acc);
@@ -418,12 +460,17 @@ template <bool SUBDOTS>
 __global__ void __launch_bounds__(32 * kMaxCtaSplits, 1)
     gemv_kernel(const __grid_constant__ GemvLaunch a)
 {
+    extern __shared__ __align__(16) uint8_t xs[];  // the q8 plane, staged per CTA
     const int lane = threadIdx.x & 31;
     const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     griddep_launch_dependents();
-    // a whole warp leaves; CTAs that combine in shared memory are launched
-    // exact (every warp has an item), so none of their warps leaves early
-    if (item >= a.n_items) return;
+    if (item >= a.n_items) {
+        // no work item (only in the last CTA of a whole-tile or workspace
+        // grid): still help stage the plane, then leave.  CTAs that combine
+        // splits in shared memory are launched exact.
+        stage_plane(a, xs);
+        return;
+    }
     int pi = 0;
 #pragma unroll
     for (int k = 1; k < kMaxParts; ++k)
@@ -441,9 +488,9 @@ __global__ void __launch_bounds__(32 * kMaxCtaSplits, 1)
         u1 = min(u0 + a.tpi * nch, P.ntiles * nch);
     }
     if (P.fmt == 6)
-        run_range<6, SUBDOTS>(a, P, item, u0, u1, lane);
+        run_range<6, SUBDOTS>(a, P, xs, item, u0, u1, lane);
     else
-        run_range<4, SUBDOTS>(a, P, item, u0, u1, lane);
+        run_range<4, SUBDOTS>(a, P, xs, item, u0, u1, lane);
 }
 
 template <bool SUBDOTS>
@@ -451,8 +498,8 @@ cudaError_t launch(const GemvLaunch &a, cudaStream_t st)
 {
     const int warps = gemv_cta_warps(a.splits, SUBDOTS);
     const long long blocks = (a.n_items + warps - 1) / warps;
-    return launch_maybe_pdl(gemv_kernel<SUBDOTS>, dim3((unsigned)blocks), dim3(32 * warps), a.pdl,
-                            st, a);
+    return launch_maybe_pdl(gemv_kernel<SUBDOTS>, dim3((unsigned)blocks), dim3(32 * warps),
+                            a.splits == 1 ? (size_t)a.q8_bytes : 0, a.pdl, st, a);
 }
 
 }  // namespace
@@ -460,12 +507,27 @@ cudaError_t launch(const GemvLaunch &a, cudaStream_t st)
 cudaError_t launch_gemv(const GemvLaunch &a, cudaStream_t st) { return launch<false>(a, st); }
 cudaError_t launch_subdots(const GemvLaunch &a, cudaStream_t st) { return launch<true>(a, st); }
 
-int gemv_ctas_per_sm(int warps_per_cta)
+int gemv_ctas_per_sm(int warps_per_cta, size_t smem)
 {
     int blocks = 0;
     const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &blocks, gemv_kernel<false>, 32 * warps_per_cta, 0);
+        &blocks, gemv_kernel<false>, 32 * warps_per_cta, smem);
     return e == cudaSuccess ? blocks : 0;
+}
+
+size_t gemv_max_plane_bytes()
+{
+    int dev = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return 0;
+    const int limit = optin - 1024;  // room for the kernel's static shared memory
+    if (cudaFuncSetAttribute(gemv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(gemv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) !=
+            cudaSuccess)
+        return 0;
+    return (size_t)limit & ~(size_t)15;
 }
 
 }  // namespace mq

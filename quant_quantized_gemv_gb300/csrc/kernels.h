@@ -42,6 +42,7 @@ struct GemvLaunch {
     int splits, cps, tpi;   // the plan (see above)
     int n_items;
     unsigned q8_d_off, q8_sum_off;
+    unsigned q8_bytes;      // bytes of the q8 plane (multiple of 16), staged in shared memory
     int pdl;                // launch with programmatic stream serialization
 };
 
@@ -50,6 +51,7 @@ cudaError_t launch_subdots(const GemvLaunch &a, cudaStream_t st);
 
 constexpr int kGemvWarpsPerBlock = 4;   // CTA of independent warps
 constexpr int kMaxCtaSplits = 12;       // largest CTA whose warps are one tile's splits
+constexpr int kGemvStaticSmem = kMaxCtaSplits * 8 * 4;  // the split-combine buffer
 
 // Warps per CTA for a plan with `splits` splits.
 inline int gemv_cta_warps(int splits, bool subdots = false)
@@ -57,9 +59,13 @@ inline int gemv_cta_warps(int splits, bool subdots = false)
     return (!subdots && splits > 1 && splits <= kMaxCtaSplits) ? splits : kGemvWarpsPerBlock;
 }
 
-// Resident CTAs per SM of the GEMV kernel with `warps_per_cta` warps, on the
-// current device (0 on error).
-int gemv_ctas_per_sm(int warps_per_cta);
+// Resident CTAs per SM of the GEMV kernel with `warps_per_cta` warps and
+// `smem` bytes of dynamic shared memory, on the current device (0 on error).
+int gemv_ctas_per_sm(int warps_per_cta, size_t smem);
+
+// Largest q8 plane (bytes) the GEMV can stage in shared memory; makes the
+// kernels accept that much dynamic shared memory on the current device.
+size_t gemv_max_plane_bytes();
 
 // Producers.  d_off / sum_off locate the q8 plane's fp16-scale and sum
 // sections (layout.h q8_d_offset / q8_sum_offset).
@@ -75,13 +81,13 @@ cudaError_t launch_swiglu_quant_q8(const float *g, const float *u, float *y, uin
 // is set (the kernel then may start before its predecessor in the stream
 // finishes and must call griddep_wait() before touching dependent data).
 template <class... KArgs, class... Args>
-cudaError_t launch_maybe_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, int pdl,
+cudaError_t launch_maybe_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, int pdl,
                              cudaStream_t st, Args &&...args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -171,7 +171,7 @@ cudaError_t launch_quantize_q8(const float *x, uint8_t *q8, int n, unsigned d_of
                                unsigned sum_off, int pdl, cudaStream_t st)
 {
     const int n4 = n / 4;
-    return launch_maybe_pdl(quantize_q8_kernel, dim3(blocks_for(n4, 256)), dim3(256), pdl, st, x, q8,
+    return launch_maybe_pdl(quantize_q8_kernel, dim3(blocks_for(n4, 256)), dim3(256), 0, pdl, st, x, q8,
                             n4, d_off, sum_off);
 }
 
@@ -179,7 +179,7 @@ cudaError_t launch_swiglu_quant_q8(const float *g, const float *u, float *y, uin
                                    unsigned d_off, unsigned sum_off, int pdl, cudaStream_t st)
 {
     const int n4 = n / 4;
-    return launch_maybe_pdl(swiglu_quant_q8_kernel, dim3(blocks_for(n4, 256)), dim3(256), pdl, st,
+    return launch_maybe_pdl(swiglu_quant_q8_kernel, dim3(blocks_for(n4, 256)), dim3(256), 0, pdl, st,
                             g, u, y, q8, n4, d_off, sum_off);
 }
 
@@ -187,7 +187,7 @@ cudaError_t launch_rmsnorm_quant_q8(const float *x, const float *gain, float eps
                                     uint8_t *q8, int n, unsigned d_off, unsigned sum_off, int pdl,
                                     cudaStream_t st)
 {
-    return launch_maybe_pdl(rmsnorm_quant_q8_kernel, dim3(1), dim3(kRmsThreads), pdl, st, x, gain,
+    return launch_maybe_pdl(rmsnorm_quant_q8_kernel, dim3(1), dim3(kRmsThreads), 0, pdl, st, x, gain,
                             eps, y, q8, n, d_off, sum_off);
 }
 
