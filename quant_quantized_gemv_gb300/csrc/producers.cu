@@ -24,6 +24,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "kernels.h"
 
 namespace mq {
@@ -91,8 +93,8 @@ __global__ void __launch_bounds__(256) swiglu_quant_q8_kernel(const float *g, co
     const bool valid = gid < n4;
     float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
     if (valid) {
-        const float4 gv = reinterpret_cast<const float4 *>(g)[gid];
-        const float4 uv = reinterpret_cast<const float4 *>(u)[gid];
+        const float4 gv = __ldcg(reinterpret_cast<const float4 *>(g) + gid);
+        const float4 uv = __ldcg(reinterpret_cast<const float4 *>(u) + gid);
         out.x = (gv.x / (1.0f + expf(-gv.x))) * uv.x;
         out.y = (gv.y / (1.0f + expf(-gv.y))) * uv.y;
         out.z = (gv.z / (1.0f + expf(-gv.z))) * uv.z;
@@ -102,27 +104,35 @@ __global__ void __launch_bounds__(256) swiglu_quant_q8_kernel(const float *g, co
     quantize4(out, valid, gid, q8, d_off, sum_off);
 }
 
-// One row, one CTA of kRmsThreads: ss = sum x^2 (per-lane serial, then a
-// fixed shuffle tree and a fixed cross-warp order), scale = 1/sqrt(ss/n+eps)
-// (IEEE sqrt and division), y = (x * scale) * gain, then quantize.
-constexpr int kRmsThreads = 1024;
+// One row over a grid of CTAs with no inter-CTA communication: every CTA
+// computes the whole sum of squares itself (the row is a few tens of KB and
+// sits in L2, so the redundant reads cost less than a grid-wide exchange),
+// in one fixed order -- per-thread serial, a fixed shuffle tree, then the
+// per-warp partials added in warp order by every thread -- so all CTAs get
+// the same bits.  scale = 1/sqrt(ss/n + eps) (IEEE sqrt and division), then
+// each CTA writes y = (x * scale) * gain and its q8 blocks for its own slice.
+constexpr int kRmsThreads = 256;
+constexpr int kRmsMaxCtas = 64;
 
 __global__ void __launch_bounds__(kRmsThreads) rmsnorm_quant_q8_kernel(
     const float *__restrict__ x, const float *__restrict__ gain, float eps, float *__restrict__ y,
     uint8_t *__restrict__ q8, int n, unsigned d_off, unsigned sum_off)
 {
     __shared__ float warp_ss[kRmsThreads / 32];
-    __shared__ float scale_sh;
     griddep_launch_dependents();
     griddep_wait();  // x may come from the preceding kernel
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int n4 = n >> 2;
+    const int first = blockIdx.x * kRmsThreads;  // this CTA's first float4
     const float4 *x4 = reinterpret_cast<const float4 *>(x);
     const float4 *g4 = reinterpret_cast<const float4 *>(gain);
 
     float ss = 0.0f;
+    float4 own = make_float4(0.f, 0.f, 0.f, 0.f);  // x[first + tid], kept from the sum pass
+#pragma unroll 8
     for (int i = tid; i < n4; i += kRmsThreads) {
         const float4 v = __ldcg(x4 + i);
+        if (i == first + tid) own = v;
         ss = fmaf(v.x, v.x, ss);
         ss = fmaf(v.y, v.y, ss);
         ss = fmaf(v.z, v.z, ss);
@@ -132,23 +142,19 @@ __global__ void __launch_bounds__(kRmsThreads) rmsnorm_quant_q8_kernel(
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
     if (lane == 0) warp_ss[wid] = ss;
     __syncthreads();
-    if (wid == 0) {
-        float t = warp_ss[lane];
+    float t = 0.0f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
-        if (lane == 0) scale_sh = 1.0f / sqrtf(t / (float)n + eps);
-    }
-    __syncthreads();
-    const float scale = scale_sh;
+    for (int w = 0; w < kRmsThreads / 32; ++w) t += warp_ss[w];
+    const float scale = 1.0f / sqrtf(t / (float)n + eps);
 
-    // Every thread runs the same number of iterations, so the quantizer's
-    // shuffles always see full warps.
-    for (int base = 0; base < n4; base += kRmsThreads) {
+    // The slice loop's trip count is uniform across the CTA, so the
+    // quantizer's shuffles always see full warps.
+    for (int base = first; base < n4; base += gridDim.x * kRmsThreads) {
         const int i = base + tid;
         const bool valid = i < n4;
         float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
         if (valid) {
-            const float4 v = __ldcg(x4 + i);
+            const float4 v = base == first ? own : __ldcg(x4 + i);
             const float4 gv = __ldcg(g4 + i);
             out.x = (v.x * scale) * gv.x;
             out.y = (v.y * scale) * gv.y;
@@ -187,8 +193,9 @@ cudaError_t launch_rmsnorm_quant_q8(const float *x, const float *gain, float eps
                                     uint8_t *q8, int n, unsigned d_off, unsigned sum_off, int pdl,
                                     cudaStream_t st)
 {
-    return launch_maybe_pdl(rmsnorm_quant_q8_kernel, dim3(1), dim3(kRmsThreads), 0, pdl, st, x, gain,
-                            eps, y, q8, n, d_off, sum_off);
+    const unsigned ctas = std::min(blocks_for(n / 4, kRmsThreads), (unsigned)kRmsMaxCtas);
+    return launch_maybe_pdl(rmsnorm_quant_q8_kernel, dim3(ctas), dim3(kRmsThreads), 0, pdl, st, x,
+                            gain, eps, y, q8, n, d_off, sum_off);
 }
 
 }  // namespace mq
