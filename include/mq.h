@@ -241,6 +241,67 @@ int mq_gemv_group_q8_plan(const mq_gemv_part *parts, int nparts, const void *q8,
                           int splits, int chunks_per_split, int tiles_per_item, void *ws,
                           size_t ws_bytes, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Small-batch GEMV (device): nt = 1..MQ_MAX_TOKENS activation rows (the
+ * tokens of a batched or speculative decode step) against ONE pass over the
+ * weights.  The pages' MMVQ launch already takes a token count and gives
+ * each token a grid row, reading the weights once per token ([D4-2] §2);
+ * here every streamed weight byte is used for all nt tokens.  Per token the
+ * integer sub-block dots and the f32 combine are those of mq_gemv_q6k_q8 /
+ * mq_gemv_q4k_q8; the f32 reduction order is fixed (deterministic) but not
+ * the single-token kernel's, so results agree with it to rounding.
+ *   q8: nt planes of cols values, back to back: token t's plane starts at
+ *       q8 + t * mq_q8_bytes(cols) (what the _batch producers write).
+ *   y:  nt x rows f32, token-major: y[t * rows + r].
+ *   nt == 1 runs the same kernel for one token (no workspace, unlike
+ *   mq_gemv_q6k_q8, whose long-row plans may need one).
+ *   Every CTA stages all nt planes in shared memory: nt * mq_q8_bytes(cols)
+ *   must not exceed the device's per-CTA limit less 8 KiB (about 219 KiB on
+ *   GB300, i.e. cols <= 26368 at nt = 8), else MQ_ERR_SHAPE.
+ * Plans read differently from the single-token ones: splits S
+ * (1..8) cuts every row into S ranges of chunks_per_split chunks (coverage
+ * checked as above, no empty range); a CTA holds S warps for each of 8 / S
+ * tiles (a "group") and runs tiles_per_item consecutive groups, so the
+ * staged planes serve tiles_per_item * (8 / S) tiles.  A tile's S splits
+ * add their partial sums in shared memory in ascending split order; there
+ * is no workspace.  The default plan picks S and tiles_per_item so that the
+ * busiest warp streams the fewest chunks, scaled up when the grid leaves SMs
+ * idle.
+ * mq_gemv_batch_plan: the default plan for nt tokens on the current device
+ *   (both formats plan alike).
+ * mq_gemv_batch_plan_for: the same for a device with `sms` SMs and a kernel
+ *   of regs_per_thread registers.  Host only.
+ * mq_gemv_*_q8_batch_plan: the GEMV with an explicit plan.
+ * Errors: as mq_gemv_q6k_q8; MQ_ERR_SHAPE also for nt outside
+ *         1..MQ_MAX_TOKENS; MQ_ERR_COVERAGE for a bad plan.
+ * ------------------------------------------------------------------------ */
+#define MQ_MAX_TOKENS 8
+
+int mq_gemv_batch_plan(int rows, int cols, int nt, int *splits, int *chunks_per_split,
+                       int *tiles_per_item);
+int mq_gemv_batch_plan_for(int rows, int cols, int nt, int sms, int regs_per_thread, int *splits,
+                           int *chunks_per_split, int *tiles_per_item);
+int mq_gemv_q6k_q8_batch(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
+                         void *stream);
+int mq_gemv_q4k_q8_batch(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
+                         void *stream);
+int mq_gemv_q6k_q8_batch_plan(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
+                              int splits, int chunks_per_split, int tiles_per_item, void *stream);
+int mq_gemv_q4k_q8_batch_plan(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
+                              int splits, int chunks_per_split, int tiles_per_item, void *stream);
+
+/* Producers over nt rows (1..MQ_MAX_TOKENS) of n values each: x, g, u and y
+ * are nt x n row-major (device f32); q8 receives nt planes, token t's at
+ * q8 + t * mq_q8_bytes(n).  Each row is exactly what the single-row call
+ * computes on that row; rms_norm normalizes every row by its own mean
+ * square, with the one gain vector of n values.  Errors: as the single-row
+ * producers; MQ_ERR_SHAPE also for nt outside 1..MQ_MAX_TOKENS. */
+int mq_quantize_q8_batch(const float *x, void *q8, int n, int nt, void *stream);
+int mq_rmsnorm_quant_q8_batch(const float *x, const float *gain, float eps, float *y, void *q8,
+                              int n, int nt, void *stream);
+int mq_swiglu_quant_q8_batch(const float *g, const float *u, float *y, void *q8, int n, int nt,
+                             void *stream);
+
 /* Coverage check used by every GEMV dispatch, exposed for tests: MQ_OK iff
  * all arguments are >= 1, splits * chunks_per_split >= nchunks (nothing
  * dropped) and (splits - 1) * chunks_per_split < nchunks (no empty split);

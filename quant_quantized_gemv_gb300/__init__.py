@@ -36,6 +36,9 @@ EXPORTS = [
     "mq_gemv_group_workspace_bytes", "mq_gemv_group_q8", "mq_gemv_group_q8_plan",
     "mq_gemv_q6k_q8_subdots",
     "mq_gemv_q4k_q8_subdots", "mq_device_sms",
+    "mq_quantize_q8_batch", "mq_rmsnorm_quant_q8_batch", "mq_swiglu_quant_q8_batch",
+    "mq_gemv_batch_plan", "mq_gemv_batch_plan_for", "mq_gemv_q6k_q8_batch", "mq_gemv_q4k_q8_batch", "mq_gemv_q6k_q8_batch_plan",
+    "mq_gemv_q4k_q8_batch_plan",
 ]
 
 
@@ -46,6 +49,7 @@ class MQGemvPart(ctypes.Structure):
 
 
 MQ_MAX_GROUP = 8
+MQ_MAX_TOKENS = 8
 
 
 class MQError(RuntimeError):
@@ -99,6 +103,15 @@ def lib():
         "mq_gemv_q6k_q8_subdots": ([P, P, P, I, I, P], I),
         "mq_gemv_q4k_q8_subdots": ([P, P, P, I, I, P], I),
         "mq_device_sms": ([], I),
+        "mq_quantize_q8_batch": ([P, P, I, I, P], I),
+        "mq_rmsnorm_quant_q8_batch": ([P, P, F, P, P, I, I, P], I),
+        "mq_swiglu_quant_q8_batch": ([P, P, P, P, I, I, P], I),
+        "mq_gemv_batch_plan": ([I, I, I, P, P, P], I),
+        "mq_gemv_batch_plan_for": ([I, I, I, I, I, P, P, P], I),
+        "mq_gemv_q6k_q8_batch": ([P, P, I, P, I, I, P], I),
+        "mq_gemv_q4k_q8_batch": ([P, P, I, P, I, I, P], I),
+        "mq_gemv_q6k_q8_batch_plan": ([P, P, I, P, I, I, I, I, I, P], I),
+        "mq_gemv_q4k_q8_batch_plan": ([P, P, I, P, I, I, I, I, I, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -230,6 +243,49 @@ def mq_swiglu_quant_q8(g, u, y=None, q8=None, stream=None):
     return y, q8
 
 
+# ------------------------------------------------------------------ producers over nt rows
+def _q8_out_rows(n: int, nt: int, like, q8):
+    import torch
+    if q8 is None:
+        q8 = torch.empty(nt * mq_q8_bytes(n), dtype=torch.uint8, device=like.device)
+    return q8
+
+
+def mq_quantize_q8_batch(x, q8=None, stream=None):
+    """x: [nt, n] f32 -> nt q8 planes, back to back."""
+    import torch
+    nt, n = x.shape[0], x.shape[1]
+    q8 = _q8_out_rows(n, nt, x, q8)
+    _check(lib().mq_quantize_q8_batch(_dev(x, torch.float32), _dev(q8), n, nt, _stream(stream)),
+           "mq_quantize_q8_batch")
+    return q8
+
+
+def mq_rmsnorm_quant_q8_batch(x, gain, eps: float, y=None, q8=None, stream=None):
+    """x: [nt, n] f32, gain: [n] -> y [nt, n] and nt q8 planes."""
+    import torch
+    nt, n = x.shape[0], x.shape[1]
+    y = torch.empty_like(x) if y is None else y
+    q8 = _q8_out_rows(n, nt, x, q8)
+    _check(lib().mq_rmsnorm_quant_q8_batch(_dev(x, torch.float32), _dev(gain, torch.float32),
+                                           float(eps), _dev(y, torch.float32), _dev(q8), n, nt,
+                                           _stream(stream)),
+           "mq_rmsnorm_quant_q8_batch")
+    return y, q8
+
+
+def mq_swiglu_quant_q8_batch(g, u, y=None, q8=None, stream=None):
+    """g, u: [nt, n] f32 -> y [nt, n] and nt q8 planes."""
+    import torch
+    nt, n = g.shape[0], g.shape[1]
+    y = torch.empty_like(g) if y is None else y
+    q8 = _q8_out_rows(n, nt, g, q8)
+    _check(lib().mq_swiglu_quant_q8_batch(_dev(g, torch.float32), _dev(u, torch.float32),
+                                          _dev(y, torch.float32), _dev(q8), n, nt, _stream(stream)),
+           "mq_swiglu_quant_q8_batch")
+    return y, q8
+
+
 # ------------------------------------------------------------------ GEMV
 def mq_gemv_workspace_bytes(rows: int, cols: int) -> int:
     return lib().mq_gemv_workspace_bytes(rows, cols)
@@ -311,6 +367,41 @@ def mq_gemv_q6k_q8(Wp, q8, rows: int, cols: int, y=None, ws=None, stream=None, p
 def mq_gemv_q4k_q8(Wp, q8, rows: int, cols: int, y=None, ws=None, stream=None, plan=None):
     """y = W x_hat for repacked q4_K weights Wp (device) and a q8 plane."""
     return _gemv("mq_gemv_q4k_q8", Wp, q8, rows, cols, y, ws, stream, plan)
+
+
+# ------------------------------------------------------------------ small-batch GEMV
+def mq_gemv_batch_plan(rows: int, cols: int, nt: int):
+    """Default plan of the nt-token GEMV on the current device."""
+    return _plan_out(lib().mq_gemv_batch_plan, rows, cols, nt)
+
+
+def mq_gemv_batch_plan_for(rows: int, cols: int, nt: int, sms: int, regs_per_thread: int = 255):
+    """Default nt-token plan for a device with `sms` SMs (host-only model)."""
+    return _plan_out(lib().mq_gemv_batch_plan_for, rows, cols, nt, sms, regs_per_thread)
+
+
+def _gemv_batch(name: str, Wp, q8, nt: int, rows: int, cols: int, y, stream, plan=None):
+    import torch
+    y = torch.empty((nt, rows), dtype=torch.float32, device=Wp.device) if y is None else y
+    L = lib()
+    if plan is None:
+        st = getattr(L, name)(_dev(Wp), _dev(q8), nt, _dev(y, torch.float32), rows, cols,
+                              _stream(stream))
+    else:
+        st = getattr(L, name + "_plan")(_dev(Wp), _dev(q8), nt, _dev(y, torch.float32), rows, cols,
+                                        int(plan[0]), int(plan[1]), int(plan[2]), _stream(stream))
+    _check(st, name)
+    return y
+
+
+def mq_gemv_q6k_q8_batch(Wp, q8, nt: int, rows: int, cols: int, y=None, stream=None, plan=None):
+    """Y[nt, rows] = W x_hat_t for nt q8 planes (back to back), one pass over W."""
+    return _gemv_batch("mq_gemv_q6k_q8_batch", Wp, q8, nt, rows, cols, y, stream, plan)
+
+
+def mq_gemv_q4k_q8_batch(Wp, q8, nt: int, rows: int, cols: int, y=None, stream=None, plan=None):
+    """Y[nt, rows] = W x_hat_t for nt q8 planes (back to back), one pass over W."""
+    return _gemv_batch("mq_gemv_q4k_q8_batch", Wp, q8, nt, rows, cols, y, stream, plan)
 
 
 def _parts_array(parts, ys=None):

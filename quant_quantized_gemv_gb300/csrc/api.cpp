@@ -22,6 +22,8 @@ std::atomic<int> g_sms[kMaxDevices];
 // resident GEMV CTAs per SM: [device][warps per CTA]
 std::atomic<int> g_ctas[kMaxDevices][kMaxCtaSplits + 1];
 std::atomic<int> g_pdl{0};
+// resident small-batch CTAs per SM (register limit): [device][nt][warps per CTA]
+std::atomic<int> g_batch_ctas[kMaxDevices][kMaxTokens + 1][kBatchMaxCtaSplits + 1];
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -59,6 +61,7 @@ struct Occupancy {
 struct DeviceLimits {
     int smem_per_sm, smem_reserved;  // shared memory per SM, reserved per CTA
     size_t max_plane;                // largest q8 plane the GEMV stages
+    size_t max_batch_planes;         // largest nt planes the small-batch GEMV stages
 };
 std::atomic<bool> g_limits_ok[kMaxDevices];
 DeviceLimits g_limits[kMaxDevices];
@@ -78,7 +81,8 @@ bool device_limits(DeviceLimits *out)
                                        dev) != cudaSuccess)
                 return false;
             l.max_plane = gemv_max_plane_bytes();  // also opts the kernels in
-            if (l.max_plane == 0) return false;
+            l.max_batch_planes = gemv_batch_max_smem();
+            if (l.max_plane == 0 || l.max_batch_planes == 0) return false;
             g_limits[dev] = l;
             g_limits_ok[dev].store(true, std::memory_order_release);
         }
@@ -109,6 +113,29 @@ bool device_occupancy(Occupancy *o, size_t plane)
     // whole-tile CTAs stage the plane in shared memory
     o->ctas_tiles = o->ctas[kGemvWarpsPerBlock] < by_smem ? o->ctas[kGemvWarpsPerBlock] : by_smem;
     return o->ctas_tiles > 0;
+}
+
+// The small-batch kernel for nt tokens: every CTA stages all nt planes.
+bool batch_occupancy(Occupancy *o, int nt, size_t planes)
+{
+    const int dev = current_device();
+    DeviceLimits lim;
+    if (dev < 0 || !device_limits(&lim)) return false;
+    const long long per_cta = (long long)planes + kBatchStaticSmem + lim.smem_reserved;
+    const int by_smem = (int)(lim.smem_per_sm / per_cta);
+    for (int w = 1; w <= kBatchMaxCtaSplits; ++w) {
+        std::atomic<int> &slot = g_batch_ctas[dev][nt][w];
+        int v = slot.load(std::memory_order_relaxed);
+        if (v <= 0) {
+            v = gemv_batch_ctas_per_sm(nt, w, 0);
+            if (v <= 0) return false;
+            slot.store(v, std::memory_order_relaxed);
+        }
+        o->ctas[w] = v < by_smem ? v : by_smem;
+    }
+    for (int w = kBatchMaxCtaSplits + 1; w <= kMaxCtaSplits; ++w) o->ctas[w] = 0;
+    o->ctas_tiles = 0;  // unused by the small-batch plans
+    return o->ctas[kBatchMaxCtaSplits] > 0;
 }
 
 // The same from a register count (host-only planning, tests): 64K registers
@@ -162,11 +189,49 @@ Plan plan_for(int ntiles, int nchunks, int sms, const Occupancy &o)
     return p;
 }
 
+// Small-batch plan: S splits per tile (1..8, none empty), CTAs of S warps
+// per tile x 8 / S tiles, each CTA running tpi tile groups.  Every CTA
+// stages all nt planes, so the resident CTAs per SM come from the
+// occupancy with that much shared memory.  Choose the S whose busiest warp
+// streams the fewest chunks, scaled up when the grid leaves SMs idle.
+Plan batch_plan_for(int ntiles, int nchunks, int sms, const Occupancy &o)
+{
+    if (sms <= 0) sms = 1;
+    Plan best{1, nchunks, 1};
+    double best_score = -1.0;
+    for (int S = 1; S <= kBatchMaxCtaSplits && S <= nchunks; ++S) {
+        const int cps = ceil_div(nchunks, S);
+        if ((long long)(S - 1) * cps >= nchunks) continue;  // an empty split
+        const int G = kBatchMaxCtaSplits / S, W = S * G;
+        const long long resident = (long long)sms * o.ctas[W];
+        if (resident <= 0) continue;
+        const long long groups = (ntiles + G - 1) / G;
+        const long long tpc = (groups + resident - 1) / resident;
+        const long long ctas = (groups + tpc - 1) / tpc;
+        const double busy = ctas >= sms ? 1.0 : (double)ctas / sms;
+        const double score = (double)(tpc * cps) / busy;
+        if (best_score < 0 || score < best_score) {
+            best_score = score;
+            best = Plan{S, cps, (int)tpc};
+        }
+    }
+    return best;
+}
+
+long long batch_ctas(int ntiles, const Plan &p)
+{
+    const int G = kBatchMaxCtaSplits / p.splits;
+    const long long groups = (ntiles + G - 1) / G;
+    return (groups + p.tpi - 1) / p.tpi;
+}
+
 long long plan_items(int ntiles, const Plan &p)
 {
     return p.splits > 1 ? (long long)ntiles * p.splits : (ntiles + p.tpi - 1) / p.tpi;
 }
 
+// Workspace of a plan: arrival counters and 8 partials per work item, only
+// when the splits are too many to meet in one CTA.
 size_t ws_bytes_for(long long total_tiles, long long n_items, const Plan &p)
 {
     if (p.splits <= kMaxCtaSplits) return 0;  // splits meet in shared memory (or none)
@@ -183,6 +248,12 @@ int check_coverage(int nchunks, int splits, int cps)
     return MQ_OK;
 }
 
+int check_batch_plan(int nchunks, const Plan &p)
+{
+    if (p.splits < 1 || p.splits > kBatchMaxCtaSplits || p.tpi < 1) return MQ_ERR_COVERAGE;
+    return check_coverage(nchunks, p.splits, p.cps);
+}
+
 int check_plan(int nchunks, const Plan &p)
 {
     if (p.tpi < 1 || (p.splits > 1 && p.tpi != 1)) return MQ_ERR_COVERAGE;
@@ -197,10 +268,13 @@ struct Part {
 
 // Validate a group, pick or check its plan, size the workspace.  On MQ_OK,
 // `a` holds everything but the workspace pointers, and *need the bytes.
+// nt == 0: the single-token GEMV; nt >= 1: the small-batch kernel for nt tokens.
 int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const Plan *explicit_plan,
-                  GemvLaunch *a, size_t *need, bool sizes_only = false)
+                  GemvLaunch *a, size_t *need, bool sizes_only = false, int nt = 0)
 {
     if (nparts < 1 || nparts > kMaxParts) return MQ_ERR_SHAPE;
+    if (nt < 0 || nt > kMaxTokens) return MQ_ERR_SHAPE;
+    const bool batch = nt > 0;
     if (!parts || (!q8 && !sizes_only)) return MQ_ERR_NULL;
     if (cols < kQK || cols % kQK != 0) return MQ_ERR_SHAPE;
     if (!aligned16(q8)) return MQ_ERR_ALIGN;
@@ -217,24 +291,33 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
     }
     if (total_tiles * nchunks >= (1LL << 31)) return MQ_ERR_SHAPE;
     const size_t plane = q8_plane_bytes(cols);
+    if (batch && nparts != 1) return MQ_ERR_SHAPE;  // the small-batch kernel takes one matrix
     if (explicit_plan) {  // a wrong plan is refused before anything touches the device
-        const int cov = check_plan(nchunks, *explicit_plan);
+        const int cov = batch ? check_batch_plan(nchunks, *explicit_plan)
+                              : check_plan(nchunks, *explicit_plan);
         if (cov != MQ_OK) return cov;
     }
     if (!sizes_only) {
         DeviceLimits lim;
         if (!device_limits(&lim)) return MQ_ERR_CUDA;
-        if (plane > lim.max_plane) return MQ_ERR_SHAPE;  // the plane must fit in shared memory
+        // the plane(s) must fit in shared memory
+        if (!batch ? plane > lim.max_plane : (size_t)nt * plane > lim.max_batch_planes)
+            return MQ_ERR_SHAPE;
     }
     Plan pl;
     if (explicit_plan) {
         pl = *explicit_plan;
     } else {
         Occupancy o;
-        if (!device_occupancy(&o, plane)) return MQ_ERR_CUDA;
-        pl = plan_for((int)total_tiles, nchunks, device_sms(), o);
+        if (!batch) {
+            if (!device_occupancy(&o, plane)) return MQ_ERR_CUDA;
+            pl = plan_for((int)total_tiles, nchunks, device_sms(), o);
+        } else {
+            if (!batch_occupancy(&o, nt, (size_t)nt * plane)) return MQ_ERR_CUDA;
+            pl = batch_plan_for((int)total_tiles, nchunks, device_sms(), o);
+        }
     }
-    const int cov = check_plan(nchunks, pl);
+    const int cov = batch ? check_batch_plan(nchunks, pl) : check_plan(nchunks, pl);
     if (cov != MQ_OK) return cov;
     long long items = 0, tiles = 0;
     for (int p = 0; p < nparts; ++p) {
@@ -249,7 +332,7 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
         gp.item0 = (int)items;
         gp.tile0 = (int)tiles;
         gp.tile_bytes_div16 = (int)(g.tile_bytes / 16);
-        items += plan_items(g.ntiles, pl);
+        items += batch ? batch_ctas(g.ntiles, pl) : plan_items(g.ntiles, pl);
         tiles += g.ntiles;
     }
     if (items >= (1LL << 31)) return MQ_ERR_SHAPE;
@@ -265,22 +348,24 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
     a->q8_sum_off = (unsigned)q8_sum_offset(cols);
     a->q8_bytes = (unsigned)plane;
     a->pdl = g_pdl.load(std::memory_order_relaxed);
-    *need = ws_bytes_for(total_tiles, items, pl);
+    a->nt = batch ? nt : 1;
+    a->q8_stride = (unsigned)plane;
+    *need = batch ? 0 : ws_bytes_for(total_tiles, items, pl);  // small batch: splits meet in the CTA
     return MQ_OK;
 }
 
 int gemv_group(const Part *parts, int nparts, const void *q8, int cols, const Plan *explicit_plan,
-               void *ws, size_t ws_bytes, void *stream)
+               void *ws, size_t ws_bytes, void *stream, int nt = 0)
 {
     GemvLaunch a;
     size_t need = 0;
     if (explicit_plan) {  // argument errors first, before anything asks the device
-        const int st0 = prepare_group(parts, nparts, q8, cols, explicit_plan, &a, &need, true);
+        const int st0 = prepare_group(parts, nparts, q8, cols, explicit_plan, &a, &need, true, nt);
         if (st0 != MQ_OK) return st0;
         if (need > 0 && !ws) return MQ_ERR_NULL;
         if (need > 0 && ws_bytes < need) return MQ_ERR_WORKSPACE;
     }
-    const int st = prepare_group(parts, nparts, q8, cols, explicit_plan, &a, &need);
+    const int st = prepare_group(parts, nparts, q8, cols, explicit_plan, &a, &need, false, nt);
     if (st != MQ_OK) return st;
     if (need > 0) {
         if (!ws) return MQ_ERR_NULL;
@@ -291,15 +376,31 @@ int gemv_group(const Part *parts, int nparts, const void *q8, int cols, const Pl
         a.ws_cnt = (unsigned *)ws;
         a.ws_part = (float *)((uint8_t *)ws + round16((size_t)total_tiles * 4));
     }
-    return launch_gemv(a, (cudaStream_t)stream) == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+    const cudaError_t e = nt > 0 ? launch_gemv_batch(a, (cudaStream_t)stream)
+                                 : launch_gemv(a, (cudaStream_t)stream);
+    return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
 }
 
 int gemv_common(int fmt, const void *Wp, const void *q8, float *y, int rows, int cols,
-                const Plan *explicit_plan, void *ws, size_t ws_bytes, void *stream)
+                const Plan *explicit_plan, void *ws, size_t ws_bytes, void *stream, int nt = 0)
 {
     if (!Wp || !q8 || !y) return MQ_ERR_NULL;
     const Part part{fmt, rows, Wp, y};
-    return gemv_group(&part, 1, q8, cols, explicit_plan, ws, ws_bytes, stream);
+    return gemv_group(&part, 1, q8, cols, explicit_plan, ws, ws_bytes, stream, nt);
+}
+
+int batch_plan_of(int rows, int cols, int nt, Plan *p)
+{
+    if (!gemv_shape_ok(rows, cols) || nt < 1 || nt > kMaxTokens) return MQ_ERR_SHAPE;
+    const Geom g = make_geom(rows, cols, kQ6kBytes);
+    const size_t plane = q8_plane_bytes(cols);
+    Occupancy o;
+    DeviceLimits lim;
+    if (!device_limits(&lim)) return MQ_ERR_CUDA;
+    if ((size_t)nt * plane > lim.max_batch_planes) return MQ_ERR_SHAPE;
+    if (!batch_occupancy(&o, nt, (size_t)nt * plane)) return MQ_ERR_CUDA;
+    *p = batch_plan_for(g.ntiles, g.nchunks, device_sms(), o);
+    return MQ_OK;
 }
 
 int subdots_common(int fmt, const void *Wp, const void *q8, int32_t *isums, int rows, int cols,
@@ -360,7 +461,7 @@ int mq_quantize_q8(const float *x, void *q8, int n, void *stream)
     if (!x || !q8) return MQ_ERR_NULL;
     if (!vec_shape_ok(n)) return MQ_ERR_SHAPE;
     if (!aligned16(x) || !aligned16(q8)) return MQ_ERR_ALIGN;
-    const cudaError_t e = launch_quantize_q8(x, (uint8_t *)q8, n, (unsigned)q8_d_offset(n),
+    const cudaError_t e = launch_quantize_q8(x, (uint8_t *)q8, n, 1, 0, (unsigned)q8_d_offset(n),
                                              (unsigned)q8_sum_offset(n), g_pdl.load(std::memory_order_relaxed),
                                              (cudaStream_t)stream);
     return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
@@ -372,7 +473,7 @@ int mq_rmsnorm_quant_q8(const float *x, const float *gain, float eps, float *y, 
     if (!x || !gain || !y || !q8) return MQ_ERR_NULL;
     if (!vec_shape_ok(n)) return MQ_ERR_SHAPE;
     if (!aligned16(x) || !aligned16(gain) || !aligned16(y) || !aligned16(q8)) return MQ_ERR_ALIGN;
-    const cudaError_t e = launch_rmsnorm_quant_q8(x, gain, eps, y, (uint8_t *)q8, n,
+    const cudaError_t e = launch_rmsnorm_quant_q8(x, gain, eps, y, (uint8_t *)q8, n, 1, 0,
                                                   (unsigned)q8_d_offset(n),
                                                   (unsigned)q8_sum_offset(n), g_pdl.load(std::memory_order_relaxed),
                                              (cudaStream_t)stream);
@@ -384,7 +485,7 @@ int mq_swiglu_quant_q8(const float *g, const float *u, float *y, void *q8, int n
     if (!g || !u || !y || !q8) return MQ_ERR_NULL;
     if (!vec_shape_ok(n)) return MQ_ERR_SHAPE;
     if (!aligned16(g) || !aligned16(u) || !aligned16(y) || !aligned16(q8)) return MQ_ERR_ALIGN;
-    const cudaError_t e = launch_swiglu_quant_q8(g, u, y, (uint8_t *)q8, n,
+    const cudaError_t e = launch_swiglu_quant_q8(g, u, y, (uint8_t *)q8, n, 1, 0,
                                                  (unsigned)q8_d_offset(n),
                                                  (unsigned)q8_sum_offset(n), g_pdl.load(std::memory_order_relaxed),
                                              (cudaStream_t)stream);
@@ -472,6 +573,104 @@ int mq_gemv_group_q8_plan(const mq_gemv_part *parts, int nparts, const void *q8,
     for (int p = 0; p < nparts; ++p) ps[p] = Part{parts[p].fmt, parts[p].rows, parts[p].Wp, parts[p].y};
     const Plan pl{splits, chunks_per_split, tiles_per_item};
     return gemv_group(ps, nparts, q8, cols, splits > 0 ? &pl : nullptr, ws, ws_bytes, stream);
+}
+
+int mq_quantize_q8_batch(const float *x, void *q8, int n, int nt, void *stream)
+{
+    if (!x || !q8) return MQ_ERR_NULL;
+    if (!vec_shape_ok(n) || nt < 1 || nt > kMaxTokens) return MQ_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(q8)) return MQ_ERR_ALIGN;
+    const cudaError_t e = launch_quantize_q8(x, (uint8_t *)q8, n, nt, (unsigned)q8_plane_bytes(n),
+                                             (unsigned)q8_d_offset(n), (unsigned)q8_sum_offset(n),
+                                             g_pdl.load(std::memory_order_relaxed), (cudaStream_t)stream);
+    return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+}
+
+int mq_rmsnorm_quant_q8_batch(const float *x, const float *gain, float eps, float *y, void *q8,
+                              int n, int nt, void *stream)
+{
+    if (!x || !gain || !y || !q8) return MQ_ERR_NULL;
+    if (!vec_shape_ok(n) || nt < 1 || nt > kMaxTokens) return MQ_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(gain) || !aligned16(y) || !aligned16(q8)) return MQ_ERR_ALIGN;
+    const cudaError_t e = launch_rmsnorm_quant_q8(
+        x, gain, eps, y, (uint8_t *)q8, n, nt, (unsigned)q8_plane_bytes(n), (unsigned)q8_d_offset(n),
+        (unsigned)q8_sum_offset(n), g_pdl.load(std::memory_order_relaxed), (cudaStream_t)stream);
+    return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+}
+
+int mq_swiglu_quant_q8_batch(const float *g, const float *u, float *y, void *q8, int n, int nt,
+                             void *stream)
+{
+    if (!g || !u || !y || !q8) return MQ_ERR_NULL;
+    if (!vec_shape_ok(n) || nt < 1 || nt > kMaxTokens) return MQ_ERR_SHAPE;
+    if (!aligned16(g) || !aligned16(u) || !aligned16(y) || !aligned16(q8)) return MQ_ERR_ALIGN;
+    const cudaError_t e = launch_swiglu_quant_q8(
+        g, u, y, (uint8_t *)q8, n, nt, (unsigned)q8_plane_bytes(n), (unsigned)q8_d_offset(n),
+        (unsigned)q8_sum_offset(n), g_pdl.load(std::memory_order_relaxed), (cudaStream_t)stream);
+    return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+}
+
+int mq_gemv_batch_plan(int rows, int cols, int nt, int *splits, int *chunks_per_split,
+                       int *tiles_per_item)
+{
+    if (!splits || !chunks_per_split || !tiles_per_item) return MQ_ERR_NULL;
+    Plan p;
+    const int st = batch_plan_of(rows, cols, nt, &p);
+    if (st != MQ_OK) return st;
+    *splits = p.splits;
+    *chunks_per_split = p.cps;
+    *tiles_per_item = p.tpi;
+    return MQ_OK;
+}
+
+int mq_gemv_batch_plan_for(int rows, int cols, int nt, int sms, int regs_per_thread, int *splits,
+                           int *chunks_per_split, int *tiles_per_item)
+{
+    if (!splits || !chunks_per_split || !tiles_per_item) return MQ_ERR_NULL;
+    if (!gemv_shape_ok(rows, cols) || nt < 1 || nt > kMaxTokens || regs_per_thread < 1 ||
+        regs_per_thread > 255)
+        return MQ_ERR_SHAPE;
+    const Geom g = make_geom(rows, cols, kQ6kBytes);
+    const size_t planes = (size_t)nt * q8_plane_bytes(cols);
+    Occupancy o = model_occupancy(regs_per_thread, 0);
+    const int by_smem = (int)(233472 / ((long long)planes + kBatchStaticSmem + 1024));
+    for (int w = 1; w <= kMaxCtaSplits; ++w)
+        if (o.ctas[w] > by_smem) o.ctas[w] = by_smem;
+    const Plan p = batch_plan_for(g.ntiles, g.nchunks, sms, o);
+    *splits = p.splits;
+    *chunks_per_split = p.cps;
+    *tiles_per_item = p.tpi;
+    return MQ_OK;
+}
+
+int mq_gemv_q6k_q8_batch(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
+                         void *stream)
+{
+    if (nt < 1) return MQ_ERR_SHAPE;
+    return gemv_common(6, Wp, q8, y, rows, cols, nullptr, nullptr, 0, stream, nt);
+}
+
+int mq_gemv_q4k_q8_batch(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
+                         void *stream)
+{
+    if (nt < 1) return MQ_ERR_SHAPE;
+    return gemv_common(4, Wp, q8, y, rows, cols, nullptr, nullptr, 0, stream, nt);
+}
+
+int mq_gemv_q6k_q8_batch_plan(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
+                              int splits, int chunks_per_split, int tiles_per_item, void *stream)
+{
+    if (nt < 1) return MQ_ERR_SHAPE;
+    const Plan p{splits, chunks_per_split, tiles_per_item};
+    return gemv_common(6, Wp, q8, y, rows, cols, &p, nullptr, 0, stream, nt);
+}
+
+int mq_gemv_q4k_q8_batch_plan(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
+                              int splits, int chunks_per_split, int tiles_per_item, void *stream)
+{
+    if (nt < 1) return MQ_ERR_SHAPE;
+    const Plan p{splits, chunks_per_split, tiles_per_item};
+    return gemv_common(4, Wp, q8, y, rows, cols, &p, nullptr, 0, stream, nt);
 }
 
 int mq_set_pdl(int enable)

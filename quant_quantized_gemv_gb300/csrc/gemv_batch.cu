@@ -1,0 +1,415 @@
+// gemv_batch.cu -- small-batch decode GEMV: nt = 1..8 activation rows (the
+// tokens of a speculative or batched decode step) against one pass over the
+// repacked q6_K / q4_K weights.  The minfer pages' MMVQ kernels already carry
+// a token index for this (page "74 · D4-2 — B0 latent correctness fix", §2:
+// the launch takes nt and each token is a grid row); here every streamed
+// weight byte is used for all nt tokens instead of being read nt times.
+//
+// Per token the arithmetic is the single-token GEMV's (gemv.cu): the same
+// integer sub-block dots with dp4a, then the f32 combine with the block and
+// sub-block scales and the token's fp16 activation scale, reduced with the
+// same fixed butterfly and combined across splits in ascending split order.
+// Up to 4 tokens the f32 order is the single-token kernel's; beyond that the
+// butterfly runs once per chunk instead of once per tile (a different but
+// equally fixed order).
+//
+// What changes with nt:
+//   * All nt q8 planes are staged in shared memory once per CTA (after the
+//     grid-dependency wait), whatever the plan; each chunk's codes for a
+//     group of tokens (all of them up to 4, else pairs) are then read from
+//     there into registers.
+//   * A weight row's codes are decoded once per token group and used for
+//     every token of the group: the decode, not the dp4a, dominates the ALU
+//     work of a chunk.
+//   * CTAs hold at most 8 warps so the kernel may use up to 255 registers
+//     per thread (two chunks of weights, one token group's codes and the
+//     running sums).
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+#include "gemv_common.cuh"
+#include "kernels.h"
+#include "layout.h"
+
+namespace mq {
+namespace {
+
+using namespace gemv_detail;
+
+// Tokens whose activation codes are held in registers at once: all of them
+// up to kGroup; beyond that pairs (with two chunks of weights in flight,
+// larger groups of 5..8 tokens spill registers).
+constexpr int kGroup = 4;
+__host__ __device__ constexpr int group_size(int nt) { return nt <= kGroup ? nt : 2; }
+
+// Running sums of a work item.  Up to kGroup tokens each lane keeps its own
+// partial sums of the 8 rows (reduced across lanes when a tile is flushed,
+// as in the single-token kernel).  With more tokens that would take 8 x nt
+// registers, so each token group's chunk partials are reduced across lanes
+// at once and each lane keeps only the sum of its row (lane >> 2) per token.
+template <int NT>
+struct Acc {
+    static constexpr bool kEach = NT > kGroup;  // reduce every chunk
+    float v[kEach ? 1 : NT][8];                 // per-lane partials (not kEach)
+    float s[kEach ? NT : 1];                    // row (lane >> 2) sums (kEach)
+};
+
+// Activation codes of one unit for the tokens [t0, t0 + G) of a group.
+template <int G>
+struct XCodes {
+    uint4 xa[G], xb[G];  // codes 0..15 and 16..31 of the unit's q8 block
+    float d8[G];         // fp16 activation scale
+    int k0[G], k1[G];    // q6_K: -32 * sum(xa), -32 * sum(xb); q4_K: k0 = the block's sum
+};
+
+template <int FMT, int G>
+__device__ __forceinline__ void load_x_group(const GemvLaunch &a, const uint8_t *xs, int t0, int nt,
+                                             const Unit &x, int lane, XCodes<G> &X)
+{
+    const int U = 32 * x.c + lane;
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+        if (x.active && t0 + j < nt) {
+            const uint8_t *pl = xs + (size_t)(t0 + j) * a.q8_bytes;
+            const uint4 *qs = reinterpret_cast<const uint4 *>(pl + (size_t)U * 32);
+            X.xa[j] = qs[0];
+            X.xb[j] = qs[1];
+            X.d8[j] = __half2float(
+                __ushort_as_half(reinterpret_cast<const unsigned short *>(pl + a.q8_d_off)[U]));
+            if (FMT == 6) {
+                X.k0[j] = -32 * sum16(X.xa[j]);
+                X.k1[j] = -32 * sum16(X.xb[j]);
+            } else {
+                X.k0[j] = reinterpret_cast<const int *>(pl + a.q8_sum_off)[U];
+                X.k1[j] = 0;
+            }
+        } else {
+            X.xa[j] = X.xb[j] = make_uint4(0, 0, 0, 0);
+            X.d8[j] = 0.0f;
+            X.k0[j] = X.k1[j] = 0;
+        }
+    }
+}
+
+// q6_K: sub-block 0 of the unit is weights 0..15 against codes xa, sub-block
+// 1 is weights 16..31 against xb; isum_s = dot(q, x) - 32 * sum(x).  The two
+// sums are kept apart so each sub-block's integer is the single-token one.
+template <int NT, int G>
+__device__ __forceinline__ void compute_group(const Q6kW &W, const XCodes<G> &X, int t0,
+                                              float (&out)[G][8])
+{
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        uint32_t q0[4], q1[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) q6k_codes(W, r, m, q0[m], q1[m]);
+        int sc0, sc1;
+        float d;
+        q6k_scales(W, r, sc0, sc1, d);
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            if (t0 + j >= NT) break;
+            int dot0 = 0, dot1 = 0;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                dot0 = __dp4a((int)q0[m], (int)word(X.xa[j], m), dot0);
+                dot1 = __dp4a((int)q1[m], (int)word(X.xb[j], m), dot1);
+            }
+            const int isum0 = dot0 + X.k0[j];
+            const int isum1 = dot1 + X.k1[j];
+            out[j][r] = fmaf(d * X.d8[j], (float)(sc0 * isum0 + sc1 * isum1), out[j][r]);
+        }
+    }
+}
+
+// q4_K: the unit is one 32-weight sub-block; term = d*sc*isum - dmin*m*qsum.
+template <int NT, int G>
+__device__ __forceinline__ void compute_group(const Q4kW &W, const XCodes<G> &X, int t0,
+                                              float (&out)[G][8])
+{
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        uint32_t lo[4], hi[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const uint32_t w = word(W.qs[r], m);
+            lo[m] = w & kLo4;
+            hi[m] = (w >> 4) & kLo4;
+        }
+        int sc, mn;
+        float d, dmin;
+        q4k_scales(W, r, sc, mn, d, dmin);
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            if (t0 + j >= NT) break;
+            int dot = 0;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                dot = __dp4a((int)lo[m], (int)word(X.xa[j], m), dot);
+                dot = __dp4a((int)hi[m], (int)word(X.xb[j], m), dot);
+            }
+            const float term = fmaf(d, (float)(sc * dot), -dmin * (float)(mn * X.k0[j]));
+            out[j][r] = fmaf(X.d8[j], term, out[j][r]);
+        }
+    }
+}
+
+template <int FMT, int NT>
+__device__ __forceinline__ void compute(const GemvLaunch &a, const uint8_t *xs, const Unit &x,
+                                        int lane,
+                                        const typename std::conditional<FMT == 6, Q6kW, Q4kW>::type &W,
+                                        Acc<NT> &acc)
+{
+    constexpr int G = group_size(NT);
+    if (!Acc<NT>::kEach) {  // one group: accumulate straight into the per-lane partials
+        XCodes<G> X;
+        load_x_group<FMT, G>(a, xs, 0, NT, x, lane, X);
+        compute_group<NT, G>(W, X, 0, reinterpret_cast<float(&)[G][8]>(acc.v));
+        return;
+    }
+#pragma unroll
+    for (int t0 = 0; t0 < NT; t0 += G) {
+        XCodes<G> X;
+        load_x_group<FMT, G>(a, xs, t0, NT, x, lane, X);
+        float part[G][8];
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+#pragma unroll
+            for (int r = 0; r < 8; ++r) part[j][r] = 0.0f;
+        compute_group<NT, G>(W, X, t0, part);
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+            if (t0 + j < NT) acc.s[t0 + j] += reduce8(part[j], lane);
+    }
+}
+
+// Tile t is finished for this warp: reduce (or take) its nt x 8 sums and
+// write them, or -- with S > 1 -- leave them in shared memory, meet the
+// CTA's other warps at one barrier and let split 0 of each tile add the S
+// partials in ascending split order.  The exchange buffer alternates with the
+// tile iteration, so one barrier per tile suffices: a buffer is rewritten two
+// iterations later, after every warp has passed the barrier in between.
+template <int NT>
+__device__ __forceinline__ void flush_tile(const GemvLaunch &a, const GemvPart &P, int t, bool valid,
+                                           int iter, Acc<NT> &acc, int lane)
+{
+    __shared__ float xchg[2][kBatchMaxCtaSplits][NT][8];
+    float v[NT];
+#pragma unroll
+    for (int k = 0; k < NT; ++k) {
+        if (Acc<NT>::kEach) {
+            v[k] = acc.s[k];
+            acc.s[k] = 0.0f;
+        } else {
+            v[k] = reduce8(acc.v[k], lane);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) acc.v[k][r] = 0.0f;
+        }
+    }
+    const int row0 = t * kTileRows;
+    if (a.splits == 1) {
+        if (valid && (lane & 3) == 0 && row0 + (lane >> 2) < P.rows) {
+#pragma unroll
+            for (int k = 0; k < NT; ++k) P.y[(size_t)k * P.rows + row0 + (lane >> 2)] = v[k];
+        }
+        return;
+    }
+    const int w = threadIdx.x >> 5, sp = w % a.splits;
+    float(&buf)[kBatchMaxCtaSplits][NT][8] = xchg[iter & 1];
+#pragma unroll
+    for (int k = 0; k < NT; ++k) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const float pr = __shfl_sync(kFull, v[k], 4 * r);
+            if (lane == r) buf[w][k][r] = pr;
+        }
+    }
+    __syncthreads();
+    if (sp == 0 && valid && lane < 8 && row0 + lane < P.rows) {
+#pragma unroll
+        for (int k = 0; k < NT; ++k) {
+            float sum = 0.0f;
+            for (int j = 0; j < a.splits; ++j) sum += buf[w + j][k][lane];
+            P.y[(size_t)k * P.rows + row0 + lane] = sum;
+        }
+    }
+}
+
+// Wait for the producer, then stage the nt q8 planes in shared memory
+// (coalesced coherent 16-byte loads) and meet at named barrier 1.  Every
+// warp of the CTA calls this exactly once.
+__device__ __forceinline__ void stage_planes(const GemvLaunch &a, uint8_t *xs)
+{
+    griddep_wait();
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.q8);
+    uint4 *dst = reinterpret_cast<uint4 *>(xs);
+    const int per = (int)(a.q8_bytes >> 4), stride = (int)(a.q8_stride >> 4);
+    for (int t = 0; t < a.nt; ++t) {
+#pragma unroll 4
+        for (int i = threadIdx.x; i < per; i += blockDim.x)
+            dst[(size_t)t * per + i] = __ldcg(src + (size_t)t * stride + i);
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(blockDim.x) : "memory");
+}
+
+// Work decomposition.  A CTA has S * G warps (S = a.splits, G = 8 / S tiles
+// per group): warp w takes split w % S of tile w / S of each group.  The CTA
+// runs a.tpi consecutive groups, so the staged planes serve a.tpi * G tiles.
+// Split s covers chunks [s * cps, min((s + 1) * cps, nchunks)) of a row.  A
+// warp streams its (group, chunk) units in order with two register buffers,
+// loading unit u + 1 (possibly the next group's first chunk) while unit u
+// is computed.  Warps of a group past the last tile compute nothing but
+// still meet their CTA at every tile's barrier.
+struct Cursor {
+    int i, c;  // group iteration and chunk of the next unit to load
+};
+
+template <int FMT, int NT>
+__device__ __forceinline__ void run_batch(const GemvLaunch &a, const GemvPart &P, uint8_t *xs, int lane)
+{
+    using W = typename std::conditional<FMT == 6, Q6kW, Q4kW>::type;
+    constexpr int kChunkBytes = (FMT == 6 ? kQ6kChunkPerBlock : kQ4kChunkPerBlock) * kChunkBlocks;
+    const int S = a.splits, G = kBatchMaxCtaSplits / S;
+    const int w = threadIdx.x >> 5, sp = w % S, o = w / S;
+    const int c_lo = sp * a.cps, c_hi = min(c_lo + a.cps, a.nchunks);
+    const int group0 = blockIdx.x * a.tpi;
+    const int n_units = a.tpi * (c_hi - c_lo);
+    auto tile_of = [&](int i) { return (group0 + i) * G + o; };
+    auto unit_at = [&](const Cursor &k) {
+        const int t = tile_of(k.i);
+        Unit x = locate(a, P, t < P.ntiles ? t : 0, k.c, lane, kChunkBytes);
+        x.t = t;
+        x.active = x.active && t < P.ntiles;
+        return x;
+    };
+    auto advance = [&](Cursor &k) {
+        if (++k.c == c_hi) { k.c = c_lo; ++k.i; }
+    };
+
+    W A, B;
+    Cursor next{0, c_lo};
+    Unit xa = unit_at(next), xb;
+    load_w(xa, lane, A);  // weights do not depend on the preceding kernel
+    stage_planes(a, xs);  // the planes and y do
+    advance(next);
+
+    Acc<NT> acc;
+#pragma unroll
+    for (int k = 0; k < (Acc<NT>::kEach ? 1 : NT); ++k)
+#pragma unroll
+        for (int r = 0; r < 8; ++r) acc.v[k][r] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < (Acc<NT>::kEach ? NT : 1); ++k) acc.s[k] = 0.0f;
+
+    int done = 0;  // tiles flushed so far
+    for (int u = 0; u < n_units; u += 2) {
+        const bool has_b = u + 1 < n_units;
+        if (has_b) {
+            xb = unit_at(next);
+            load_w(xb, lane, B);
+            advance(next);
+        }
+        compute<FMT, NT>(a, xs, xa, lane, A, acc);
+        if (xa.c == c_hi - 1) {
+            flush_tile<NT>(a, P, xa.t, xa.t < P.ntiles, done, acc, lane);
+            ++done;
+        }
+        if (!has_b) break;
+        const bool has_a = u + 2 < n_units;
+        if (has_a) {
+            xa = unit_at(next);
+            load_w(xa, lane, A);
+            advance(next);
+        }
+        compute<FMT, NT>(a, xs, xb, lane, B, acc);
+        if (xb.c == c_hi - 1) {
+            flush_tile<NT>(a, P, xb.t, xb.t < P.ntiles, done, acc, lane);
+            ++done;
+        }
+    }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(32 * kBatchMaxCtaSplits, 1)
+    gemv_batch_kernel(const __grid_constant__ GemvLaunch a)
+{
+    extern __shared__ __align__(16) uint8_t xs[];  // the nt q8 planes
+    const int lane = threadIdx.x & 31;
+    griddep_launch_dependents();
+    const GemvPart &P = a.part[0];
+    if (P.fmt == 6)
+        run_batch<6, NT>(a, P, xs, lane);
+    else
+        run_batch<4, NT>(a, P, xs, lane);
+}
+
+template <int NT>
+cudaError_t launch_nt(const GemvLaunch &a, cudaStream_t st)
+{
+    const int warps = gemv_batch_cta_warps(a.splits);
+    return launch_maybe_pdl(gemv_batch_kernel<NT>, dim3((unsigned)a.n_items), dim3(32 * warps),
+                            (size_t)a.nt * a.q8_bytes, a.pdl, st, a);
+}
+
+using KernelFn = void (*)(GemvLaunch);
+
+KernelFn kernel_for(int nt)
+{
+    switch (nt) {
+    case 1: return gemv_batch_kernel<1>;
+    case 2: return gemv_batch_kernel<2>;
+    case 3: return gemv_batch_kernel<3>;
+    case 4: return gemv_batch_kernel<4>;
+    case 5: return gemv_batch_kernel<5>;
+    case 6: return gemv_batch_kernel<6>;
+    case 7: return gemv_batch_kernel<7>;
+    case 8: return gemv_batch_kernel<8>;
+    default: return nullptr;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_batch(const GemvLaunch &a, cudaStream_t st)
+{
+    switch (a.nt) {
+    case 1: return launch_nt<1>(a, st);
+    case 2: return launch_nt<2>(a, st);
+    case 3: return launch_nt<3>(a, st);
+    case 4: return launch_nt<4>(a, st);
+    case 5: return launch_nt<5>(a, st);
+    case 6: return launch_nt<6>(a, st);
+    case 7: return launch_nt<7>(a, st);
+    case 8: return launch_nt<8>(a, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int gemv_batch_ctas_per_sm(int nt, int warps_per_cta, size_t smem)
+{
+    const KernelFn k = kernel_for(nt);
+    int blocks = 0;
+    if (!k) return 0;
+    const cudaError_t e =
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k, 32 * warps_per_cta, smem);
+    return e == cudaSuccess ? blocks : 0;
+}
+
+size_t gemv_batch_max_smem()
+{
+    int dev = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return 0;
+    const int limit = optin - 8192;  // room for the split-exchange buffers
+    for (int nt = 1; nt <= kMaxTokens; ++nt)
+        if (cudaFuncSetAttribute(kernel_for(nt), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 limit) != cudaSuccess)
+            return 0;
+    return (size_t)limit & ~(size_t)15;
+}
+
+}  // namespace mq

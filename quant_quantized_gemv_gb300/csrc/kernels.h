@@ -44,20 +44,42 @@ struct GemvLaunch {
     unsigned q8_d_off, q8_sum_off;
     unsigned q8_bytes;      // bytes of the q8 plane (multiple of 16), staged in shared memory
     int pdl;                // launch with programmatic stream serialization
+    int nt;                 // activation rows (tokens) of the small-batch kernel
+    unsigned q8_stride;     // bytes from one token's plane to the next (small batch)
 };
 
 cudaError_t launch_gemv(const GemvLaunch &a, cudaStream_t st);
 cudaError_t launch_subdots(const GemvLaunch &a, cudaStream_t st);
+// Small-batch GEMV (gemv_batch.cu), 1 <= a.nt <= kMaxTokens, one part whose
+// y holds nt x rows outputs, token-major.  Its plan reads differently: each
+// CTA holds `splits` warps for each of kBatchMaxCtaSplits / splits tiles (a
+// group) and runs tpi consecutive groups; n_items is the number of CTAs.
+cudaError_t launch_gemv_batch(const GemvLaunch &a, cudaStream_t st);
 
 constexpr int kGemvWarpsPerBlock = 4;   // CTA of independent warps
 constexpr int kMaxCtaSplits = 12;       // largest CTA whose warps are one tile's splits
 constexpr int kGemvStaticSmem = kMaxCtaSplits * 8 * 4;  // the split-combine buffer
+constexpr int kMaxTokens = 8;           // activation rows of the small-batch GEMV
+constexpr int kBatchMaxCtaSplits = 8;   // its CTAs hold at most 8 warps (255 registers each)
+constexpr int kBatchStaticSmem = 2 * kBatchMaxCtaSplits * kMaxTokens * 8 * 4;  // split exchange
 
 // Warps per CTA for a plan with `splits` splits.
 inline int gemv_cta_warps(int splits, bool subdots = false)
 {
     return (!subdots && splits > 1 && splits <= kMaxCtaSplits) ? splits : kGemvWarpsPerBlock;
 }
+
+// Warps per CTA of the small-batch kernel: `splits` warps per tile times
+// kBatchMaxCtaSplits / splits tiles per group.
+inline int gemv_batch_cta_warps(int splits)
+{
+    return splits * (kBatchMaxCtaSplits / splits);
+}
+
+// Resident CTAs per SM of the small-batch kernel for nt tokens (0 on error),
+// and the largest dynamic shared memory (all nt planes) it accepts.
+int gemv_batch_ctas_per_sm(int nt, int warps_per_cta, size_t smem);
+size_t gemv_batch_max_smem();
 
 // Resident CTAs per SM of the GEMV kernel with `warps_per_cta` warps and
 // `smem` bytes of dynamic shared memory, on the current device (0 on error).
@@ -67,15 +89,17 @@ int gemv_ctas_per_sm(int warps_per_cta, size_t smem);
 // kernels accept that much dynamic shared memory on the current device.
 size_t gemv_max_plane_bytes();
 
-// Producers.  d_off / sum_off locate the q8 plane's fp16-scale and sum
-// sections (layout.h q8_d_offset / q8_sum_offset).
-cudaError_t launch_quantize_q8(const float *x, uint8_t *q8, int n, unsigned d_off,
-                               unsigned sum_off, int pdl, cudaStream_t st);
+// Producers over `rows` rows of n values (row-major), writing one q8 plane
+// per row, planes `stride` bytes apart.  d_off / sum_off locate a plane's
+// fp16-scale and sum sections (layout.h q8_d_offset / q8_sum_offset).
+cudaError_t launch_quantize_q8(const float *x, uint8_t *q8, int n, int rows, unsigned stride,
+                               unsigned d_off, unsigned sum_off, int pdl, cudaStream_t st);
 cudaError_t launch_rmsnorm_quant_q8(const float *x, const float *gain, float eps, float *y,
-                                    uint8_t *q8, int n, unsigned d_off, unsigned sum_off, int pdl,
-                                    cudaStream_t st);
+                                    uint8_t *q8, int n, int rows, unsigned stride, unsigned d_off,
+                                    unsigned sum_off, int pdl, cudaStream_t st);
 cudaError_t launch_swiglu_quant_q8(const float *g, const float *u, float *y, uint8_t *q8, int n,
-                                   unsigned d_off, unsigned sum_off, int pdl, cudaStream_t st);
+                                   int rows, unsigned stride, unsigned d_off, unsigned sum_off,
+                                   int pdl, cudaStream_t st);
 
 // Launch `kernel` on `st`, with programmatic stream serialization when pdl
 // is set (the kernel then may start before its predecessor in the stream

@@ -67,30 +67,46 @@ __device__ __forceinline__ void quantize4(float4 v, bool valid, long long gid, u
     }
 }
 
+// Rows of n values (n4 = n / 4 lane groups each) are quantized into planes
+// `stride` bytes apart.  n4 is a multiple of 8, so no 8-lane block straddles
+// two rows; lanes past the last row only join the shuffles.
+struct RowSplit {
+    long long row, w;  // row of this lane group and its index within the row
+};
+__device__ __forceinline__ RowSplit row_split(long long gid, int n4)
+{
+    const long long row = gid / n4;
+    return RowSplit{row, gid - row * n4};
+}
+
 __global__ void __launch_bounds__(256) quantize_q8_kernel(const float *__restrict__ x,
                                                           uint8_t *__restrict__ q8, int n4,
+                                                          int rows, unsigned stride,
                                                           unsigned d_off, unsigned sum_off)
 {
     griddep_launch_dependents();
     griddep_wait();  // x may come from the preceding kernel
     const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const bool valid = gid < n4;
+    const bool valid = gid < (long long)n4 * rows;
+    const RowSplit rs = row_split(gid, n4);
     const float4 v = valid ? __ldcg(reinterpret_cast<const float4 *>(x) + gid)
                            : make_float4(0.f, 0.f, 0.f, 0.f);
-    quantize4(v, valid, gid, q8, d_off, sum_off);
+    quantize4(v, valid, rs.w, q8 + rs.row * stride, d_off, sum_off);
 }
 
-// y = (g / (1 + exp(-g))) * u, the swiglu body of the D3-5 page §3.2; y may
-// alias g or u (each lane reads its 4 values before writing them).
+// y = (g / (1 + exp(-g))) * u, the swiglu body of the D3-5 page §3.2, over
+// rows of n values; y may alias g or u (each lane reads its 4 values before
+// writing them).
 __global__ void __launch_bounds__(256) swiglu_quant_q8_kernel(const float *g, const float *u,
                                                               float *y, uint8_t *__restrict__ q8,
-                                                              int n4, unsigned d_off,
-                                                              unsigned sum_off)
+                                                              int n4, int rows, unsigned stride,
+                                                              unsigned d_off, unsigned sum_off)
 {
     griddep_launch_dependents();
     griddep_wait();  // g and u may come from the preceding kernels
     const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const bool valid = gid < n4;
+    const bool valid = gid < (long long)n4 * rows;
+    const RowSplit rs = row_split(gid, n4);
     float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
     if (valid) {
         const float4 gv = __ldcg(reinterpret_cast<const float4 *>(g) + gid);
@@ -101,10 +117,10 @@ __global__ void __launch_bounds__(256) swiglu_quant_q8_kernel(const float *g, co
         out.w = (gv.w / (1.0f + expf(-gv.w))) * uv.w;
         reinterpret_cast<float4 *>(y)[gid] = out;
     }
-    quantize4(out, valid, gid, q8, d_off, sum_off);
+    quantize4(out, valid, rs.w, q8 + rs.row * stride, d_off, sum_off);
 }
 
-// One row over a grid of CTAs with no inter-CTA communication: every CTA
+// Each row (blockIdx.y) over a grid of CTAs with no inter-CTA communication: every CTA
 // computes the whole sum of squares itself (the row is a few tens of KB and
 // sits in L2, so the redundant reads cost less than a grid-wide exchange),
 // in one fixed order -- per-thread serial, a fixed shuffle tree, then the
@@ -116,7 +132,7 @@ constexpr int kRmsMaxCtas = 64;
 
 __global__ void __launch_bounds__(kRmsThreads) rmsnorm_quant_q8_kernel(
     const float *__restrict__ x, const float *__restrict__ gain, float eps, float *__restrict__ y,
-    uint8_t *__restrict__ q8, int n, unsigned d_off, unsigned sum_off)
+    uint8_t *__restrict__ q8, int n, unsigned stride, unsigned d_off, unsigned sum_off)
 {
     __shared__ float warp_ss[kRmsThreads / 32];
     griddep_launch_dependents();
@@ -124,8 +140,11 @@ __global__ void __launch_bounds__(kRmsThreads) rmsnorm_quant_q8_kernel(
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int n4 = n >> 2;
     const int first = blockIdx.x * kRmsThreads;  // this CTA's first float4
-    const float4 *x4 = reinterpret_cast<const float4 *>(x);
+    const size_t row = blockIdx.y;
+    const float4 *x4 = reinterpret_cast<const float4 *>(x + row * n);
     const float4 *g4 = reinterpret_cast<const float4 *>(gain);
+    y += row * n;
+    q8 += row * stride;
 
     float ss = 0.0f;
     float4 own = make_float4(0.f, 0.f, 0.f, 0.f);  // x[first + tid], kept from the sum pass
@@ -173,29 +192,30 @@ inline unsigned blocks_for(long long threads, int per_block)
 
 }  // namespace
 
-cudaError_t launch_quantize_q8(const float *x, uint8_t *q8, int n, unsigned d_off,
-                               unsigned sum_off, int pdl, cudaStream_t st)
+cudaError_t launch_quantize_q8(const float *x, uint8_t *q8, int n, int rows, unsigned stride,
+                               unsigned d_off, unsigned sum_off, int pdl, cudaStream_t st)
 {
     const int n4 = n / 4;
-    return launch_maybe_pdl(quantize_q8_kernel, dim3(blocks_for(n4, 256)), dim3(256), 0, pdl, st, x, q8,
-                            n4, d_off, sum_off);
+    return launch_maybe_pdl(quantize_q8_kernel, dim3(blocks_for((long long)n4 * rows, 256)), dim3(256),
+                            0, pdl, st, x, q8, n4, rows, stride, d_off, sum_off);
 }
 
 cudaError_t launch_swiglu_quant_q8(const float *g, const float *u, float *y, uint8_t *q8, int n,
-                                   unsigned d_off, unsigned sum_off, int pdl, cudaStream_t st)
+                                   int rows, unsigned stride, unsigned d_off, unsigned sum_off,
+                                   int pdl, cudaStream_t st)
 {
     const int n4 = n / 4;
-    return launch_maybe_pdl(swiglu_quant_q8_kernel, dim3(blocks_for(n4, 256)), dim3(256), 0, pdl, st,
-                            g, u, y, q8, n4, d_off, sum_off);
+    return launch_maybe_pdl(swiglu_quant_q8_kernel, dim3(blocks_for((long long)n4 * rows, 256)),
+                            dim3(256), 0, pdl, st, g, u, y, q8, n4, rows, stride, d_off, sum_off);
 }
 
 cudaError_t launch_rmsnorm_quant_q8(const float *x, const float *gain, float eps, float *y,
-                                    uint8_t *q8, int n, unsigned d_off, unsigned sum_off, int pdl,
-                                    cudaStream_t st)
+                                    uint8_t *q8, int n, int rows, unsigned stride, unsigned d_off,
+                                    unsigned sum_off, int pdl, cudaStream_t st)
 {
     const unsigned ctas = std::min(blocks_for(n / 4, kRmsThreads), (unsigned)kRmsMaxCtas);
-    return launch_maybe_pdl(rmsnorm_quant_q8_kernel, dim3(ctas), dim3(kRmsThreads), 0, pdl, st, x,
-                            gain, eps, y, q8, n, d_off, sum_off);
+    return launch_maybe_pdl(rmsnorm_quant_q8_kernel, dim3(ctas, (unsigned)rows), dim3(kRmsThreads),
+                            0, pdl, st, x, gain, eps, y, q8, n, stride, d_off, sum_off);
 }
 
 }  // namespace mq

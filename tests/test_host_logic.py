@@ -224,3 +224,49 @@ def test_group_validation_rejects_before_launch(mq):
     arr[2].fmt = 6
     arr[1].y = 0x100008
     assert L.mq_gemv_group_q8(arr, 3, Q, 5120, N, 0, N) == mq.MQ_ERR_ALIGN
+
+
+# ------------------------------------------------------------------ small batch
+@pytest.mark.parametrize("nt", [1, 2, 4, 8])
+@pytest.mark.parametrize("sms", [1, 20, 152])
+def test_batch_plan_always_covers(mq, nt, sms):
+    shapes = [(r, c) for r in (1, 8, 61, 512, 1024, 3584, 5120, 13824, 152064)
+              for c in (256, 1024, 1280, 5120, 13824, 18944)]
+    for rows, cols in shapes:
+        s, cps, tpi = mq.mq_gemv_batch_plan_for(rows, cols, nt, sms)
+        nch = -(-(cols // 256) // 4)
+        assert 1 <= s <= 8 and tpi >= 1
+        assert mq.mq_check_coverage(nch, s, cps) == mq.MQ_OK, (rows, cols, nt, s, cps)
+
+
+def test_batch_plans_of_the_benchmark_shapes(mq):
+    """GB300 model: 152 SMs, 255 registers -> one 8-warp CTA per SM.  Long
+    rows get 7 splits (one 7-warp CTA per tile, 3 tiles per CTA); lm_head
+    whole rows, 8 tiles per group, 16 groups per CTA."""
+    for nt in (2, 4, 8):
+        assert mq.mq_gemv_batch_plan_for(3584, 18944, nt, 152) == (7, 3, 3)
+        assert mq.mq_gemv_batch_plan_for(152064, 5120, nt, 152) == (1, 5, 16)
+        assert mq.mq_gemv_batch_plan_for(5120, 13824, nt, 152) == (7, 2, 5)
+        assert mq.mq_gemv_batch_plan_for(1024, 5120, nt, 152) == (5, 1, 1)
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="fake device pointers are only passed where no GPU exists")
+def test_batch_validation_rejects_before_launch(mq):
+    L = mq.lib()
+    A, B, Y = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30000)
+    N = ctypes.c_void_p(0)
+    # 64 x 4096: 8 tiles x 4 chunks
+    for nt in (0, 9, -1):
+        assert L.mq_gemv_q6k_q8_batch(A, B, nt, Y, 64, 4096, N) == mq.MQ_ERR_SHAPE
+        assert L.mq_gemv_q4k_q8_batch_plan(A, B, nt, Y, 64, 4096, 1, 4, 1, N) == mq.MQ_ERR_SHAPE
+    assert L.mq_gemv_q6k_q8_batch(N, B, 2, Y, 64, 4096, N) == mq.MQ_ERR_NULL
+    assert L.mq_gemv_q6k_q8_batch(A, B, 2, Y, 64, 4000, N) == mq.MQ_ERR_SHAPE
+    assert L.mq_gemv_q6k_q8_batch(A, ctypes.c_void_p(0x20008), 2, Y, 64, 4096, N) == mq.MQ_ERR_ALIGN
+    for plan in [(3, 1, 1), (4, 2, 1), (9, 1, 1), (0, 4, 1), (2, 2, 0)]:
+        assert L.mq_gemv_q6k_q8_batch_plan(A, B, 4, Y, 64, 4096, *plan, N) == mq.MQ_ERR_COVERAGE, plan
+    assert L.mq_quantize_q8_batch(A, B, 64, 0, N) == mq.MQ_ERR_SHAPE
+    assert L.mq_quantize_q8_batch(A, B, 48, 2, N) == mq.MQ_ERR_SHAPE
+    assert L.mq_swiglu_quant_q8_batch(A, B, N, Y, 64, 2, N) == mq.MQ_ERR_NULL
+    assert L.mq_rmsnorm_quant_q8_batch(A, B, ctypes.c_float(1e-6), Y, ctypes.c_void_p(0x40004), 64, 9,
+                                       N) == mq.MQ_ERR_SHAPE
