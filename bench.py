@@ -143,7 +143,7 @@ def measured_peak_gbs():
 
 def gemv_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("gemv.cu", "layout.h"):
+    for f in ("gemv.cu", "gemv_common.cuh", "layout.h"):
         with open(os.path.join(ROOT, "quant_quantized_gemv_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -259,10 +259,10 @@ int mq_gemv_group_q8_plan(const mq_gemv_part *parts, int nparts, const void *q8,
  *   must not exceed the device's per-CTA limit less 8 KiB (about 219 KiB on
  *   GB300, i.e. cols <= 26368 at nt = 8), else MQ_ERR_SHAPE.
  * Plans read differently from the single-token ones: splits S
- * (1..8) cuts every row into S ranges of chunks_per_split chunks (coverage
- * checked as above, no empty range); a CTA holds S warps for each of 8 / S
+ * (1..12) cuts every row into S ranges of chunks_per_split chunks (coverage
+ * checked as above, no empty range); a CTA holds S warps for each of 12 / S
  * tiles (a "group") and runs tiles_per_item consecutive groups, so the
- * staged planes serve tiles_per_item * (8 / S) tiles.  A tile's S splits
+ * staged planes serve tiles_per_item * (12 / S) tiles.  A tile's S splits
  * add their partial sums in shared memory in ascending split order; there
  * is no workspace.  The default plan picks S and tiles_per_item so that the
  * busiest warp streams the fewest chunks, scaled up when the grid leaves SMs

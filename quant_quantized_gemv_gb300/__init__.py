@@ -375,7 +375,7 @@ def mq_gemv_batch_plan(rows: int, cols: int, nt: int):
     return _plan_out(lib().mq_gemv_batch_plan, rows, cols, nt)
 
 
-def mq_gemv_batch_plan_for(rows: int, cols: int, nt: int, sms: int, regs_per_thread: int = 255):
+def mq_gemv_batch_plan_for(rows: int, cols: int, nt: int, sms: int, regs_per_thread: int = 168):
     """Default nt-token plan for a device with `sms` SMs (host-only model)."""
     return _plan_out(lib().mq_gemv_batch_plan_for, rows, cols, nt, sms, regs_per_thread)
 

@@ -189,8 +189,8 @@ Plan plan_for(int ntiles, int nchunks, int sms, const Occupancy &o)
     return p;
 }
 
-// Small-batch plan: S splits per tile (1..8, none empty), CTAs of S warps
-// per tile x 8 / S tiles, each CTA running tpi tile groups.  Every CTA
+// Small-batch plan: S splits per tile (1..12, none empty), CTAs of S warps
+// per tile x 12 / S tiles, each CTA running tpi tile groups.  Every CTA
 // stages all nt planes, so the resident CTAs per SM come from the
 // occupancy with that much shared memory.  Choose the S whose busiest warp
 // streams the fewest chunks, scaled up when the grid leaves SMs idle.

@@ -21,9 +21,8 @@
 //   * A weight row's codes are decoded once per token group and used for
 //     every token of the group: the decode, not the dp4a, dominates the ALU
 //     work of a chunk.
-//   * CTAs hold at most 8 warps so the kernel may use up to 255 registers
-//     per thread (two chunks of weights, one token group's codes and the
-//     running sums).
+//   * CTAs hold at most 12 warps of at most 168 registers: one CTA per SM
+//     stages the planes once for 12 warps.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -40,8 +39,8 @@ namespace {
 using namespace gemv_detail;
 
 // Tokens whose activation codes are held in registers at once: all of them
-// up to kGroup; beyond that pairs (with two chunks of weights in flight,
-// larger groups of 5..8 tokens spill registers).
+// up to kGroup; beyond that pairs (groups of 3 or 4 out of 5..8 tokens spill
+// more registers at the 168-register cap).
 constexpr int kGroup = 4;
 __host__ __device__ constexpr int group_size(int nt) { return nt <= kGroup ? nt : 2; }
 
@@ -255,17 +254,26 @@ __device__ __forceinline__ void stage_planes(const GemvLaunch &a, uint8_t *xs)
     asm volatile("bar.sync 1, %0;" ::"r"(blockDim.x) : "memory");
 }
 
-// Work decomposition.  A CTA has S * G warps (S = a.splits, G = 8 / S tiles
+// Work decomposition.  A CTA has S * G warps (S = a.splits, G = 12 / S tiles
 // per group): warp w takes split w % S of tile w / S of each group.  The CTA
 // runs a.tpi consecutive groups, so the staged planes serve a.tpi * G tiles.
 // Split s covers chunks [s * cps, min((s + 1) * cps, nchunks)) of a row.  A
 // warp streams its (group, chunk) units in order with two register buffers,
 // loading unit u + 1 (possibly the next group's first chunk) while unit u
-// is computed.  Warps of a group past the last tile compute nothing but
-// still meet their CTA at every tile's barrier.
+// is computed (one token), or right after it (more tokens).  Warps of a
+// group past the last tile compute nothing but still meet their CTA at
+// every tile's barrier.
 struct Cursor {
     int i, c;  // group iteration and chunk of the next unit to load
 };
+
+// Two register buffers of weights for one token (chunk u + 1 in flight while
+// chunk u is computed); with more tokens one buffer, issued as soon as the
+// previous chunk's compute is done: 12 warps per SM at 168 registers hide
+// each other's load latency better than 8 warps with two buffers (which
+// would need more registers than 168 and spill).
+template <int NT>
+constexpr bool kTwoBuffers = NT == 1;
 
 template <int FMT, int NT>
 __device__ __forceinline__ void run_batch(const GemvLaunch &a, const GemvPart &P, uint8_t *xs, int lane)
@@ -305,6 +313,23 @@ __device__ __forceinline__ void run_batch(const GemvLaunch &a, const GemvPart &P
     for (int k = 0; k < (Acc<NT>::kEach ? NT : 1); ++k) acc.s[k] = 0.0f;
 
     int done = 0;  // tiles flushed so far
+    if (!kTwoBuffers<NT>) {  // one buffer: the next chunk's loads follow its compute
+        for (int u = 0; u < n_units; ++u) {
+            compute<FMT, NT>(a, xs, xa, lane, A, acc);
+            const int t = xa.t;
+            const bool last = xa.c == c_hi - 1;
+            if (u + 1 < n_units) {
+                xa = unit_at(next);
+                load_w(xa, lane, A);
+                advance(next);
+            }
+            if (last) {
+                flush_tile<NT>(a, P, t, t < P.ntiles, done, acc, lane);
+                ++done;
+            }
+        }
+        return;
+    }
     for (int u = 0; u < n_units; u += 2) {
         const bool has_b = u + 1 < n_units;
         if (has_b) {

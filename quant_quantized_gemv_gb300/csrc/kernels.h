@@ -60,7 +60,7 @@ constexpr int kGemvWarpsPerBlock = 4;   // CTA of independent warps
 constexpr int kMaxCtaSplits = 12;       // largest CTA whose warps are one tile's splits
 constexpr int kGemvStaticSmem = kMaxCtaSplits * 8 * 4;  // the split-combine buffer
 constexpr int kMaxTokens = 8;           // activation rows of the small-batch GEMV
-constexpr int kBatchMaxCtaSplits = 8;   // its CTAs hold at most 8 warps (255 registers each)
+constexpr int kBatchMaxCtaSplits = 12;  // its CTAs hold at most 12 warps (168 registers each)
 constexpr int kBatchStaticSmem = 2 * kBatchMaxCtaSplits * kMaxTokens * 8 * 4;  // split exchange
 
 // Warps per CTA for a plan with `splits` splits.

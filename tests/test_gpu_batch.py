@@ -156,11 +156,11 @@ def test_batch_gemv_matches_oracle_per_token(mq, orc, fmt, nt, rows, cols):
 
 def valid_plans(nchunks, ntiles):
     out = []
-    for S in range(1, 9):
+    for S in range(1, 13):
         cps = -(-nchunks // S)
         if (S - 1) * cps >= nchunks:
             continue
-        G = 8 // S
+        G = 12 // S
         groups = -(-ntiles // G)
         for tpi in sorted({1, 2, 3, groups}):
             out.append((S, cps, tpi))
@@ -193,7 +193,7 @@ def test_batch_bad_plans_refused(mq):
     W, Wp, x = make(mq, "q6k", rows, cols, nt, 2)
     planes = mq.mq_quantize_q8_batch(dev(x))
     y = torch.full((nt, rows), 7.0, device="cuda")
-    for plan in [(3, 1, 1), (2, 1, 1), (9, 1, 1), (0, 4, 1), (2, 2, 0), (4, 2, 1)]:
+    for plan in [(3, 1, 1), (2, 1, 1), (9, 1, 1), (13, 1, 1), (0, 4, 1), (2, 2, 0), (4, 2, 1)]:
         with pytest.raises(mq.MQError) as e:
             mq.mq_gemv_q6k_q8_batch(Wp, planes, nt, rows, cols, y=y, plan=plan)
         assert e.value.status == mq.MQ_ERR_COVERAGE, plan

@@ -235,19 +235,20 @@ def test_batch_plan_always_covers(mq, nt, sms):
     for rows, cols in shapes:
         s, cps, tpi = mq.mq_gemv_batch_plan_for(rows, cols, nt, sms)
         nch = -(-(cols // 256) // 4)
-        assert 1 <= s <= 8 and tpi >= 1
+        assert 1 <= s <= 12 and tpi >= 1
         assert mq.mq_check_coverage(nch, s, cps) == mq.MQ_OK, (rows, cols, nt, s, cps)
 
 
 def test_batch_plans_of_the_benchmark_shapes(mq):
-    """GB300 model: 152 SMs, 255 registers -> one 8-warp CTA per SM.  Long
-    rows get 7 splits (one 7-warp CTA per tile, 3 tiles per CTA); lm_head
-    whole rows, 8 tiles per group, 16 groups per CTA."""
-    for nt in (2, 4, 8):
-        assert mq.mq_gemv_batch_plan_for(3584, 18944, nt, 152) == (7, 3, 3)
-        assert mq.mq_gemv_batch_plan_for(152064, 5120, nt, 152) == (1, 5, 16)
-        assert mq.mq_gemv_batch_plan_for(5120, 13824, nt, 152) == (7, 2, 5)
+    """GB300 model: 152 SMs, 168 registers -> one 12-warp CTA per SM.  7B
+    ffn_down: 4 splits x 3 tiles per CTA (150 CTAs); lm_head: whole rows, 12
+    tiles per group, 11 groups per CTA."""
+    for nt in (1, 2, 4, 8):
+        assert mq.mq_gemv_batch_plan_for(3584, 18944, nt, 152) == (4, 5, 1)
+        assert mq.mq_gemv_batch_plan_for(152064, 5120, nt, 152) == (1, 5, 11)
+        assert mq.mq_gemv_batch_plan_for(5120, 13824, nt, 152) == (2, 7, 1)
         assert mq.mq_gemv_batch_plan_for(1024, 5120, nt, 152) == (5, 1, 1)
+        assert mq.mq_gemv_batch_plan_for(13824, 5120, nt, 152) == (1, 5, 1)
 
 
 @pytest.mark.skipif(__import__("torch").cuda.is_available(),
@@ -263,7 +264,7 @@ def test_batch_validation_rejects_before_launch(mq):
     assert L.mq_gemv_q6k_q8_batch(N, B, 2, Y, 64, 4096, N) == mq.MQ_ERR_NULL
     assert L.mq_gemv_q6k_q8_batch(A, B, 2, Y, 64, 4000, N) == mq.MQ_ERR_SHAPE
     assert L.mq_gemv_q6k_q8_batch(A, ctypes.c_void_p(0x20008), 2, Y, 64, 4096, N) == mq.MQ_ERR_ALIGN
-    for plan in [(3, 1, 1), (4, 2, 1), (9, 1, 1), (0, 4, 1), (2, 2, 0)]:
+    for plan in [(3, 1, 1), (4, 2, 1), (9, 1, 1), (13, 1, 1), (0, 4, 1), (2, 2, 0)]:
         assert L.mq_gemv_q6k_q8_batch_plan(A, B, 4, Y, 64, 4096, *plan, N) == mq.MQ_ERR_COVERAGE, plan
     assert L.mq_quantize_q8_batch(A, B, 64, 0, N) == mq.MQ_ERR_SHAPE
     assert L.mq_quantize_q8_batch(A, B, 48, 2, N) == mq.MQ_ERR_SHAPE
