@@ -9,10 +9,12 @@ split-K).  L2 is defeated by rotating through enough device copies of the
 weights that one rotation exceeds 4x the L2 size.
 
     python bench.py [--gpus N --steps K --warmup W] [--impl mq|reference]
-                    [--workload NAME]
+                    [--workload NAME] [--tokens NT]
 
 Prints ONE JSON line (rank 0).  value = weight content bytes per step /
-device time per step (GB/s).  --impl reference times the oracle (plain C,
+device time per step (GB/s).  With --tokens NT > 1 every step decodes NT
+tokens through the small-batch producers and GEMV: the weights are still
+read once per step.  --impl reference times the oracle (plain C,
 one host core) on a bounded row sample of the same workload.
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (independent problems, weak scaling, no collective on the data path); the
@@ -167,11 +169,13 @@ def profiled_traffic(workload: str):
 class DeviceWorkload:
     """Ops of one decode step: producers writing q8 planes, GEMVs reading them."""
 
-    def __init__(self, name: str, device, l2_bytes: int, group: bool = True):
+    def __init__(self, name: str, device, l2_bytes: int, group: bool = True, nt: int = 1):
         import torch
         import quant_quantized_gemv_gb300 as mq
         self.mq = mq
         self.name = name
+        self.nt = nt                 # tokens per step (> 1: the small-batch kernels)
+        group = group and nt == 1    # the small-batch GEMV takes one matrix per launch
         self.wl = synth.WORKLOADS[name]
         self.dev = device
         self.weight_bytes = self.wl.weight_bytes()
@@ -189,29 +193,32 @@ class DeviceWorkload:
         self.ops = []
         self.inputs = []          # (device tensor, host pinned) pairs copied in by e2e
         prev_kind, prev_cols, plane, prev_outputs = None, None, None, []
+        def act(n):                              # nt token rows of n values
+            return np.stack([synth.normal(g, n) for _ in range(nt)]) if nt > 1 else synth.normal(g, n)
+
         for gname, fmt, rows, cols, producer in self.wl.gemvs:
             if not (producer == "rms" and prev_kind == "rms" and prev_cols == cols):
-                plane = torch.empty(mq.mq_q8_bytes(cols), dtype=torch.uint8, device=device)
-                yp = torch.empty(cols, dtype=torch.float32, device=device)
+                plane = torch.empty(nt * mq.mq_q8_bytes(cols), dtype=torch.uint8, device=device)
+                yp = torch.empty((nt, cols) if nt > 1 else cols, dtype=torch.float32, device=device)
                 if producer == "rms":
-                    x = self._input(synth.normal(g, cols))
+                    x = self._input(act(cols))
                     gain = torch.from_numpy(synth.normal(g, cols, 1.0, 0.1)).to(device)
                     self.ops.append(("rms", x, gain, yp, plane, cols))
                 elif producer == "swiglu":
-                    if len(prev_outputs) >= 2 and prev_outputs[-1].numel() == cols and \
-                            prev_outputs[-2].numel() == cols:
+                    if len(prev_outputs) >= 2 and prev_outputs[-1].numel() == nt * cols and \
+                            prev_outputs[-2].numel() == nt * cols:
                         gv, uv = prev_outputs[-2], prev_outputs[-1]     # gate, up outputs
                     else:
-                        gv = self._input(synth.normal(g, cols))
-                        uv = self._input(synth.normal(g, cols))
+                        gv = self._input(act(cols))
+                        uv = self._input(act(cols))
                     self.ops.append(("swiglu", gv, uv, yp, plane, cols))
                 else:
-                    x = self._input(synth.normal(g, cols))
+                    x = self._input(act(cols))
                     self.ops.append(("quant", x, plane, cols))
             prev_kind, prev_cols = producer, cols
             W0 = base[(fmt, rows, cols)][1]
             copies = [W0.clone() for _ in range(self.n_copies)]
-            y = torch.empty(rows, dtype=torch.float32, device=device)
+            y = torch.empty((nt, rows) if nt > 1 else rows, dtype=torch.float32, device=device)
             part = (fmt, copies, rows, y, gname)
             last = self.ops[-1] if self.ops else None
             if group and last is not None and last[0] == "gemv" and last[1] is plane and \
@@ -221,13 +228,13 @@ class DeviceWorkload:
                 self.ops.append(["gemv", plane, cols, [part], None])
             prev_outputs.append(y)
         for o in self.ops:                       # workspace per GEMV launch (default plan)
-            if o[0] == "gemv":
+            if o[0] == "gemv" and nt == 1:
                 o[4] = mq.mq_gemv_group_workspace(self._spec(o), o[2], device=device)
         self.output = self.ops[-1][3][-1][3]
         self.n_gemv = sum(len(o[3]) for o in self.ops if o[0] == "gemv")
         self.n_gemv_launches = sum(1 for o in self.ops if o[0] == "gemv")
         self.n_kernels = len(self.ops)
-        self.gemv_bytes = [self._part_alg_bytes(p[0], p[2], o[2]) for o in self.ops if o[0] == "gemv"
+        self.gemv_bytes = [self._part_alg_bytes(p[0], p[2], o[2], nt) for o in self.ops if o[0] == "gemv"
                            for p in o[3]]
 
     def _input(self, arr: np.ndarray):
@@ -237,10 +244,10 @@ class DeviceWorkload:
         return t
 
     @staticmethod
-    def _part_alg_bytes(fmt, rows, cols) -> int:
+    def _part_alg_bytes(fmt, rows, cols, nt=1) -> int:
         wb = rows * (cols // 256) * (210 if fmt == "q6k" else 144)
         act = (cols // 32) * (34 if fmt == "q6k" else 38)      # codes + fp16 d (+ int32 sum)
-        return wb + act + 4 * rows
+        return wb + nt * (act + 4 * rows)
 
     @staticmethod
     def _spec(o, c=0):
@@ -249,7 +256,11 @@ class DeviceWorkload:
     def _launch(self, o, c):
         _, plane, cols, parts, ws = o
         mq = self.mq
-        if len(parts) == 1:
+        if self.nt > 1:
+            fmt, copies, rows, y, _ = parts[0]
+            fn = mq.mq_gemv_q6k_q8_batch if fmt == "q6k" else mq.mq_gemv_q4k_q8_batch
+            fn(copies[c], plane, self.nt, rows, cols, y=y)
+        elif len(parts) == 1:
             fmt, copies, rows, y, _ = parts[0]
             fn = mq.mq_gemv_q6k_q8 if fmt == "q6k" else mq.mq_gemv_q4k_q8
             fn(copies[c], plane, rows, cols, y=y, ws=ws)
@@ -269,12 +280,14 @@ class DeviceWorkload:
         c = k % self.n_copies
         for o in self.ops:
             kind = o[0]
+            b = self.nt > 1
             if kind == "rms":
-                mq.mq_rmsnorm_quant_q8(o[1], o[2], 1e-6, y=o[3], q8=o[4])
+                (mq.mq_rmsnorm_quant_q8_batch if b else mq.mq_rmsnorm_quant_q8)(o[1], o[2], 1e-6, y=o[3],
+                                                                                q8=o[4])
             elif kind == "swiglu":
-                mq.mq_swiglu_quant_q8(o[1], o[2], y=o[3], q8=o[4])
+                (mq.mq_swiglu_quant_q8_batch if b else mq.mq_swiglu_quant_q8)(o[1], o[2], y=o[3], q8=o[4])
             elif kind == "quant":
-                mq.mq_quantize_q8(o[1], q8=o[2])
+                (mq.mq_quantize_q8_batch if b else mq.mq_quantize_q8)(o[1], q8=o[2])
             else:
                 self._launch(o, c)
 
@@ -307,7 +320,7 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     import quant_quantized_gemv_gb300 as mq
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
-    wl = DeviceWorkload(args.workload, dev, l2, group=args.group)
+    wl = DeviceWorkload(args.workload, dev, l2, group=args.group, nt=args.tokens)
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -389,7 +402,7 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     gemv_step_ms = float(np.median(kt))
 
     # ---- e2e: the public API, pinned host inputs in, result out, every step
-    out_host = torch.empty(wl.output.numel(), dtype=torch.float32).pin_memory()
+    out_host = torch.empty(wl.output.shape, dtype=torch.float32).pin_memory()
     h2d = sum(h.numel() * h.element_size() for _, h in wl.inputs)
     d2h = out_host.numel() * 4
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
@@ -425,6 +438,7 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "i8", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {DESCR[args.workload]}",
+                   "tokens_per_step": args.tokens,
                    "weight_content_bytes_per_step": wl.weight_bytes,
                    "gemvs_per_step": wl.n_gemv, "gemv_launches_per_step": wl.n_gemv_launches,
                    "kernels_per_step": wl.n_kernels,
@@ -435,15 +449,17 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
                    "parallelism": f"replicas{ws_}" if ws_ > 1 else "single GPU"},
         "compute": "int8 x (6-bit|4-bit) dp4a dots, int32 sub-block sums, f32 scale combine",
         "pct_of_hbm_peak": round(100 * value / ws_ / peak, 2),
+        "tokens_per_s": round(ws_ * args.tokens * args.steps / (max_ms * 1e-3), 1),
     }
     alg = float(sum(wl.gemv_bytes))
     achieved = alg / (gemv_step_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(args.workload) if wl.n_gemv == 1 else None
+    traffic = profiled_traffic(args.workload) if wl.n_gemv == 1 and args.tokens == 1 else None
     line["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                         "unit": "GB/s", "frac": round(achieved / peak, 4),
                         "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
                         "algorithmic_bytes_per_step": int(alg),
-                        "kernel": "gemv_kernel (q6_K/q4_K x q8)",
+                        "kernel": ("gemv_kernel (q6_K/q4_K x q8)" if args.tokens == 1 else
+                                   f"gemv_batch_kernel<{args.tokens}> (q6_K/q4_K x {args.tokens} q8 rows)"),
                         "gemv_us_per_step": round(gemv_step_ms * 1e3, 3),
                         "how": f"GEMV launches of {n_kt} steps back to back in one CUDA graph "
                                f"(PDL off, rotated copies), CUDA events around 5 replays, median"}
@@ -460,14 +476,14 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     line["clocks_window"] = (f"{args.soak:.1f}s soak + timed steps + {args.soak:.1f}s soak of the same "
                              f"graphs ({(t_timed1 - t_win0):.2f}s to end of timed region)")
     if ws_ == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds, args.tokens)
     return line
 
 
 # ---------------------------------------------------------------- oracle (CPU) legs
-def oracle_sample(workload: str, rows_cap: int):
+def oracle_sample(workload: str, rows_cap: int, nt: int = 1):
     """Host inputs for the oracle: each GEMV of the workload truncated to its
-    first rows_cap rows, with its producer's f32 inputs."""
+    first rows_cap rows, with its producer's f32 inputs for nt tokens."""
     wl = synth.WORKLOADS[workload]
     g = synth.rng("bench", workload)
     items, seen = [], {}
@@ -477,35 +493,40 @@ def oracle_sample(workload: str, rows_cap: int):
             continue
         r = min(rows, rows_cap)
         W = synth.blocks(fmt, g, rows, cols)[:r].copy()
-        if producer == "rms":
-            inp = (synth.normal(g, cols), synth.normal(g, cols, 1.0, 0.1))
-        elif producer == "swiglu":
-            inp = (synth.normal(g, cols), synth.normal(g, cols))
-        else:
-            inp = (synth.normal(g, cols),)
+        inps = []
+        for _ in range(nt):
+            if producer == "rms":
+                inps.append((synth.normal(g, cols), synth.normal(g, cols, 1.0, 0.1)))
+            elif producer == "swiglu":
+                inps.append((synth.normal(g, cols), synth.normal(g, cols)))
+            else:
+                inps.append((synth.normal(g, cols),))
         seen[key] = True
-        items.append((fmt, r, cols, producer, W, inp))
+        items.append((fmt, r, cols, producer, W, inps))
     return items
 
 
 def oracle_step(items):
+    """One step: every token's producer and GEMV; returns the weight bytes
+    (read once per step, as on the GPU)."""
     import oracle
     nbytes = 0
-    for fmt, r, cols, producer, W, inp in items:
-        if producer == "rms":
-            x = oracle.rmsnorm(inp[0], inp[1], 1e-6).astype(np.float32)
-        elif producer == "swiglu":
-            x = oracle.swiglu(inp[0], inp[1]).astype(np.float32)
-        else:
-            x = inp[0]
-        d, q, _ = oracle.quantize_q8(x)
-        oracle.gemv(fmt, W, d, q, r, cols)
+    for fmt, r, cols, producer, W, inps in items:
+        for inp in inps:
+            if producer == "rms":
+                x = oracle.rmsnorm(inp[0], inp[1], 1e-6).astype(np.float32)
+            elif producer == "swiglu":
+                x = oracle.swiglu(inp[0], inp[1]).astype(np.float32)
+            else:
+                x = inp[0]
+            d, q, _ = oracle.quantize_q8(x)
+            oracle.gemv(fmt, W, d, q, r, cols)
         nbytes += W.nbytes
     return nbytes
 
 
-def cpu_baseline(workload: str, seconds: float) -> dict:
-    items = oracle_sample(workload, 512)
+def cpu_baseline(workload: str, seconds: float, nt: int = 1) -> dict:
+    items = oracle_sample(workload, 512, nt)
     oracle_step(items)                                   # warm (page-in, build)
     done, t0 = 0, time.perf_counter()
     n = 0
@@ -518,13 +539,13 @@ def cpu_baseline(workload: str, seconds: float) -> dict:
     rows = ", ".join(f"{fmt} {r}x{cols}" for fmt, r, cols, _, _, _ in items)
     return {"value": round(done / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{n} passes over the first <=512 rows of each distinct GEMV ({rows}) with "
-                      f"its producer, single-threaded C oracle, {dt:.1f} s"}
+                      f"its producer, {nt} token(s) per pass, single-threaded C oracle, {dt:.1f} s"}
 
 
 def bench_reference(args, ws_, rank) -> dict | None:
     if rank != 0:
         return None
-    items = oracle_sample(args.workload, 512)
+    items = oracle_sample(args.workload, 512, args.tokens)
     for _ in range(args.warmup):
         oracle_step(items)
     t0 = time.perf_counter()
@@ -534,12 +555,14 @@ def bench_reference(args, ws_, rank) -> dict | None:
     dt = time.perf_counter() - t0
     value = nbytes / dt / 1e9
     rows = ", ".join(f"{fmt} {r}x{cols}" for fmt, r, cols, _, _, _ in items)
-    sample = f"each step: the first <=512 rows of each distinct GEMV ({rows}) with its producer"
+    sample = (f"each step: the first <=512 rows of each distinct GEMV ({rows}) with its producer, "
+              f"{args.tokens} token(s)")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "i8", "data": "synthetic",
-            "config": {"workload": f"{args.workload}: {DESCR[args.workload]}", "sample": sample},
+            "config": {"workload": f"{args.workload}: {DESCR[args.workload]}",
+                       "tokens_per_step": args.tokens, "sample": sample},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -560,6 +583,8 @@ def main(argv=None):
                     help="launch without programmatic dependent launch")
     ap.add_argument("--no-group", dest="group", action="store_false",
                     help="one launch per GEMV even when several read the same q8 plane")
+    ap.add_argument("--tokens", type=int, default=1, choices=range(1, 9), metavar="NT",
+                    help="tokens per step (1..8); > 1 uses the small-batch producers and GEMV")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
