@@ -49,6 +49,8 @@ DESCR = {
     "layer_14b": "Qwen2.5-14B attn_v q6_K 1024x5120 + ffn_down q6_K 5120x13824, each fed by "
                  "rms_norm->q8, batch 1",
     "lm_head_14b": "Qwen2.5-14B output head q6_K 152064x5120, rms_norm->q8, batch 1",
+    "ffn_14b": "Qwen2.5-14B FFN: rms_norm->q8 -> gate, up q4_K 13824x5120 -> SwiGLU->q8 -> "
+               "down q6_K 5120x13824, batch 1",
     "sweep_14b": "Qwen2.5-14B decode weight sweep: 48 layers x {q,k,o,gate,up q4_K; v,down q6_K} "
                  "+ q6_K head, fused rms/swiglu/quantize producers, batch 1",
 }
@@ -169,7 +171,8 @@ def profiled_traffic(workload: str):
 class DeviceWorkload:
     """Ops of one decode step: producers writing q8 planes, GEMVs reading them."""
 
-    def __init__(self, name: str, device, l2_bytes: int, group: bool = True, nt: int = 1):
+    def __init__(self, name: str, device, l2_bytes: int, group: bool = True, nt: int = 1,
+                 fuse: bool = True):
         import torch
         import quant_quantized_gemv_gb300 as mq
         self.mq = mq
@@ -227,15 +230,36 @@ class DeviceWorkload:
             else:
                 self.ops.append(["gemv", plane, cols, [part], None])
             prev_outputs.append(y)
+        if fuse and group and nt == 1:
+            self._fuse_gateup()
         for o in self.ops:                       # workspace per GEMV launch (default plan)
             if o[0] == "gemv" and nt == 1:
                 o[4] = mq.mq_gemv_group_workspace(self._spec(o), o[2], device=device)
         self.output = self.ops[-1][3][-1][3]
-        self.n_gemv = sum(len(o[3]) for o in self.ops if o[0] == "gemv")
-        self.n_gemv_launches = sum(1 for o in self.ops if o[0] == "gemv")
+        gemv_ops = [o for o in self.ops if o[0] in ("gemv", "gateup")]
+        self.n_gemv = sum(len(o[3]) for o in gemv_ops)
+        self.n_gemv_launches = len(gemv_ops)
         self.n_kernels = len(self.ops)
-        self.gemv_bytes = [self._part_alg_bytes(p[0], p[2], o[2], nt) for o in self.ops if o[0] == "gemv"
-                           for p in o[3]]
+        self.gemv_bytes = [self._part_alg_bytes(p[0], p[2], o[2], nt) for o in gemv_ops for p in o[3]]
+
+    def _fuse_gateup(self):
+        """A two-matrix GEMV launch (gate, up) whose outputs feed the next
+        op's SwiGLU becomes one gate||up launch with the SwiGLU -> q8 epilogue."""
+        out = []
+        i = 0
+        while i < len(self.ops):
+            o = self.ops[i]
+            nxt = self.ops[i + 1] if i + 1 < len(self.ops) else None
+            if o[0] == "gemv" and len(o[3]) == 2 and nxt is not None and nxt[0] == "swiglu":
+                (f0, c0, r0, y0, _), (f1, c1, r1, y1, _) = o[3]
+                if f0 == f1 and r0 == r1 and r0 % 32 == 0 and nxt[1] is y0 and nxt[2] is y1:
+                    # ("gateup", plane_in, cols, parts, act, plane_out)
+                    out.append(["gateup", o[1], o[2], o[3], nxt[3], nxt[4]])
+                    i += 2
+                    continue
+            out.append(o)
+            i += 1
+        self.ops = out
 
     def _input(self, arr: np.ndarray):
         import torch
@@ -267,12 +291,19 @@ class DeviceWorkload:
         else:
             mq.mq_gemv_group_q8(self._spec(o, c), plane, cols, ys=[p[3] for p in parts], ws=ws)
 
+    def _launch_gateup(self, o, c):
+        _, plane, cols, parts, act, plane_out = o
+        (fmt, cg, rows, _, _), (_, cu, _, _, _) = parts
+        self.mq.mq_gemv_gateup_swiglu_q8(fmt, cg[c], cu[c], plane, rows, cols, act=act, q8_out=plane_out)
+
     def run_gemvs(self, k: int):
         """Enqueue only the GEMV launches of step k (for kernel timing)."""
         c = k % self.n_copies
         for o in self.ops:
             if o[0] == "gemv":
                 self._launch(o, c)
+            elif o[0] == "gateup":
+                self._launch_gateup(o, c)
 
     def run(self, k: int):
         """Enqueue step k (weights copy k % n_copies) on the current stream."""
@@ -288,6 +319,8 @@ class DeviceWorkload:
                 (mq.mq_swiglu_quant_q8_batch if b else mq.mq_swiglu_quant_q8)(o[1], o[2], y=o[3], q8=o[4])
             elif kind == "quant":
                 (mq.mq_quantize_q8_batch if b else mq.mq_quantize_q8)(o[1], q8=o[2])
+            elif kind == "gateup":
+                self._launch_gateup(o, c)
             else:
                 self._launch(o, c)
 
@@ -320,7 +353,7 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     import quant_quantized_gemv_gb300 as mq
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
-    wl = DeviceWorkload(args.workload, dev, l2, group=args.group, nt=args.tokens)
+    wl = DeviceWorkload(args.workload, dev, l2, group=args.group, nt=args.tokens, fuse=args.fuse)
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -441,6 +474,7 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
                    "tokens_per_step": args.tokens,
                    "weight_content_bytes_per_step": wl.weight_bytes,
                    "gemvs_per_step": wl.n_gemv, "gemv_launches_per_step": wl.n_gemv_launches,
+                   "fused_gateup_launches_per_step": sum(1 for o in wl.ops if o[0] == "gateup"),
                    "kernels_per_step": wl.n_kernels,
                    "l2": f"{wl.n_copies} rotated weight copies "
                          f"({wl.n_copies * wl.weight_bytes / 1e6:.0f} MB >= 4 x L2 {l2 / 1e6:.0f} MB)",
@@ -583,6 +617,9 @@ def main(argv=None):
                     help="launch without programmatic dependent launch")
     ap.add_argument("--no-group", dest="group", action="store_false",
                     help="one launch per GEMV even when several read the same q8 plane")
+    ap.add_argument("--no-fuse", dest="fuse", action="store_false",
+                    help="gate and up as a grouped GEMV plus a separate SwiGLU producer instead of "
+                         "one gate||up launch with the SwiGLU -> q8 epilogue")
     ap.add_argument("--tokens", type=int, default=1, choices=range(1, 9), metavar="NT",
                     help="tokens per step (1..8); > 1 uses the small-batch producers and GEMV")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -302,6 +302,38 @@ int mq_rmsnorm_quant_q8_batch(const float *x, const float *gain, float eps, floa
 int mq_swiglu_quant_q8_batch(const float *g, const float *u, float *y, void *q8, int n, int nt,
                              void *stream);
 
+/* ------------------------------------------------------------------------
+ * FFN gate||up GEMV with the SwiGLU -> q8 producer fused in (device).
+ * One launch computes, for r < rows,
+ *     act[r] = silu(g_r) * u_r = (g_r / (1 + exp(-g_r))) * u_r,
+ *     g = Wg x_hat, u = Wu x_hat  (each exactly as mq_gemv_q6k_q8 /
+ *                                  mq_gemv_q4k_q8 with a whole-tile plan),
+ * writes act (f32) and act's q8 plane (rows values, quantized as by
+ * mq_quantize_q8), i.e. what GEMV(gate), GEMV(up) and mq_swiglu_quant_q8
+ * produce in three launches, bit for bit.  This is the concatenated
+ * gate||up launch with a SwiGLU epilogue that [D4-4] §2 and §5 closed on
+ * GB10 for running 1.5 waves; here the grid is one resident wave.
+ *   fmt: 6 (q6_K) or 4 (q4_K), for both matrices.  Wg, Wu: repacked
+ *   weights, rows x cols each (device).  q8: plane of cols values (device).
+ *   act: rows f32 (device).  q8_out: mq_q8_bytes(rows) bytes (device).
+ *   rows must be a multiple of 32 (q8 blocks of act are whole).
+ * Plan: CTAs of warps_per_cta warps (1..8) each take whole 32-row blocks,
+ * the block's 4 gate and 4 up tiles shared among the warps; `ctas` CTAs
+ * (1..rows/32) stride over the blocks.  The default takes the most warps per
+ * CTA whose one-CTA-per-block grid fits one resident wave.
+ * mq_gemv_gateup_plan_for: that plan for `sms` SMs and regs_per_thread
+ *   registers (host only).
+ * Errors: MQ_ERR_NULL, MQ_ERR_SHAPE (fmt, cols % 256, rows % 32, a plane too
+ *   large for shared memory), MQ_ERR_ALIGN, MQ_ERR_COVERAGE (a plan outside
+ *   the ranges above), MQ_ERR_CUDA.
+ * ------------------------------------------------------------------------ */
+int mq_gemv_gateup_swiglu_q8(int fmt, const void *Wg, const void *Wu, const void *q8, int rows,
+                             int cols, float *act, void *q8_out, void *stream);
+int mq_gemv_gateup_swiglu_q8_plan(int fmt, const void *Wg, const void *Wu, const void *q8, int rows,
+                                  int cols, float *act, void *q8_out, int warps_per_cta, int ctas,
+                                  void *stream);
+int mq_gemv_gateup_plan_for(int rows, int sms, int regs_per_thread, int *warps_per_cta, int *ctas);
+
 /* Coverage check used by every GEMV dispatch, exposed for tests: MQ_OK iff
  * all arguments are >= 1, splits * chunks_per_split >= nchunks (nothing
  * dropped) and (splits - 1) * chunks_per_split < nchunks (no empty split);

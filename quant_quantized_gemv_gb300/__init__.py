@@ -38,7 +38,8 @@ EXPORTS = [
     "mq_gemv_q4k_q8_subdots", "mq_device_sms",
     "mq_quantize_q8_batch", "mq_rmsnorm_quant_q8_batch", "mq_swiglu_quant_q8_batch",
     "mq_gemv_batch_plan", "mq_gemv_batch_plan_for", "mq_gemv_q6k_q8_batch", "mq_gemv_q4k_q8_batch", "mq_gemv_q6k_q8_batch_plan",
-    "mq_gemv_q4k_q8_batch_plan",
+    "mq_gemv_q4k_q8_batch_plan", "mq_gemv_gateup_swiglu_q8", "mq_gemv_gateup_swiglu_q8_plan",
+    "mq_gemv_gateup_plan_for",
 ]
 
 
@@ -112,6 +113,9 @@ def lib():
         "mq_gemv_q4k_q8_batch": ([P, P, I, P, I, I, P], I),
         "mq_gemv_q6k_q8_batch_plan": ([P, P, I, P, I, I, I, I, I, P], I),
         "mq_gemv_q4k_q8_batch_plan": ([P, P, I, P, I, I, I, I, I, P], I),
+        "mq_gemv_gateup_swiglu_q8": ([I, P, P, P, I, I, P, P, P], I),
+        "mq_gemv_gateup_swiglu_q8_plan": ([I, P, P, P, I, I, P, P, I, I, P], I),
+        "mq_gemv_gateup_plan_for": ([I, I, I, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -402,6 +406,35 @@ def mq_gemv_q6k_q8_batch(Wp, q8, nt: int, rows: int, cols: int, y=None, stream=N
 def mq_gemv_q4k_q8_batch(Wp, q8, nt: int, rows: int, cols: int, y=None, stream=None, plan=None):
     """Y[nt, rows] = W x_hat_t for nt q8 planes (back to back), one pass over W."""
     return _gemv_batch("mq_gemv_q4k_q8_batch", Wp, q8, nt, rows, cols, y, stream, plan)
+
+
+# ------------------------------------------------------------------ gate||up + SwiGLU -> q8
+def mq_gemv_gateup_swiglu_q8(fmt: str, Wg, Wu, q8, rows: int, cols: int, act=None, q8_out=None,
+                             stream=None, plan=None):
+    """act = silu(Wg x_hat) * (Wu x_hat) and its q8 plane, in one launch.
+    plan: None (default) or (warps_per_cta, ctas).  Returns (act, q8_out)."""
+    import torch
+    act = torch.empty(rows, dtype=torch.float32, device=Wg.device) if act is None else act
+    q8_out = _q8_out(rows, act, q8_out)
+    L = lib()
+    f = 6 if fmt == "q6k" else 4
+    if plan is None:
+        st = L.mq_gemv_gateup_swiglu_q8(f, _dev(Wg), _dev(Wu), _dev(q8), rows, cols,
+                                        _dev(act, torch.float32), _dev(q8_out), _stream(stream))
+    else:
+        st = L.mq_gemv_gateup_swiglu_q8_plan(f, _dev(Wg), _dev(Wu), _dev(q8), rows, cols,
+                                             _dev(act, torch.float32), _dev(q8_out), int(plan[0]),
+                                             int(plan[1]), _stream(stream))
+    _check(st, "mq_gemv_gateup_swiglu_q8")
+    return act, q8_out
+
+
+def mq_gemv_gateup_plan_for(rows: int, sms: int, regs_per_thread: int = 168):
+    """Default (warps_per_cta, ctas) of the gate||up kernel (host-only model)."""
+    w, c = ctypes.c_int(), ctypes.c_int()
+    _check(lib().mq_gemv_gateup_plan_for(rows, sms, regs_per_thread, ctypes.byref(w), ctypes.byref(c)),
+           "mq_gemv_gateup_plan_for")
+    return w.value, c.value
 
 
 def _parts_array(parts, ys=None):

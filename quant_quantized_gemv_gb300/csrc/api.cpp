@@ -24,6 +24,9 @@ std::atomic<int> g_ctas[kMaxDevices][kMaxCtaSplits + 1];
 std::atomic<int> g_pdl{0};
 // resident small-batch CTAs per SM (register limit): [device][nt][warps per CTA]
 std::atomic<int> g_batch_ctas[kMaxDevices][kMaxTokens + 1][kBatchMaxCtaSplits + 1];
+// resident gate||up CTAs per SM (register limit): [device][warps per CTA]
+constexpr int kGateUpMaxWarps = 8;
+std::atomic<int> g_gateup_ctas[kMaxDevices][kGateUpMaxWarps + 1];
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -82,7 +85,8 @@ bool device_limits(DeviceLimits *out)
                 return false;
             l.max_plane = gemv_max_plane_bytes();  // also opts the kernels in
             l.max_batch_planes = gemv_batch_max_smem();
-            if (l.max_plane == 0 || l.max_batch_planes == 0) return false;
+            if (l.max_plane == 0 || l.max_batch_planes == 0 || !gateup_opt_in(l.max_plane))
+                return false;
             g_limits[dev] = l;
             g_limits_ok[dev].store(true, std::memory_order_release);
         }
@@ -403,6 +407,87 @@ int batch_plan_of(int rows, int cols, int nt, Plan *p)
     return MQ_OK;
 }
 
+// Gate||up + SwiGLU -> q8 plan: W warps per CTA (1..8) and the grid.  The
+// largest W whose one-CTA-per-block grid fits one resident wave; failing
+// that (very many blocks) 4 warps and a one-wave grid that strides over the
+// blocks.  sms/ctas_of give the machine.
+struct GateUpPlan {
+    int wpb, ctas;
+};
+
+template <class CtasOf>
+GateUpPlan gateup_plan_for(int nblk, int sms, CtasOf ctas_of)
+{
+    if (sms <= 0) sms = 1;
+    for (int w = kGateUpMaxWarps; w >= 1; --w) {
+        const long long resident = (long long)sms * ctas_of(w);
+        if (resident > 0 && nblk <= resident) return GateUpPlan{w, nblk};
+    }
+    long long resident = (long long)sms * ctas_of(4);
+    if (resident < 1) resident = 1;
+    return GateUpPlan{4, (int)(nblk < resident ? nblk : resident)};
+}
+
+int gateup_device_ctas(int w, size_t plane)
+{
+    const int dev = current_device();
+    DeviceLimits lim;
+    if (dev < 0 || !device_limits(&lim)) return 0;
+    std::atomic<int> &slot = g_gateup_ctas[dev][w];
+    int v = slot.load(std::memory_order_relaxed);
+    if (v <= 0) {
+        v = gateup_ctas_per_sm(w, 0);
+        if (v <= 0) return 0;
+        slot.store(v, std::memory_order_relaxed);
+    }
+    const long long per_cta = (long long)plane + 2 * 8 * 8 * 4 + lim.smem_reserved;
+    const int by_smem = (int)(lim.smem_per_sm / per_cta);
+    return v < by_smem ? v : by_smem;
+}
+
+int gateup_common(int fmt, const void *Wg, const void *Wu, const void *q8, int rows, int cols,
+                  float *act, void *q8o, const GateUpPlan *explicit_plan, void *stream)
+{
+    if (!Wg || !Wu || !q8 || !act || !q8o) return MQ_ERR_NULL;
+    if (fmt != 6 && fmt != 4) return MQ_ERR_SHAPE;
+    if (!gemv_shape_ok(rows, cols) || rows % 32 != 0) return MQ_ERR_SHAPE;
+    if (!aligned16(act) || !aligned16(q8o)) return MQ_ERR_ALIGN;
+    const int nblk = rows / 32;
+    if (explicit_plan && (explicit_plan->wpb < 1 || explicit_plan->wpb > kGateUpMaxWarps ||
+                          explicit_plan->ctas < 1 || explicit_plan->ctas > nblk))
+        return MQ_ERR_COVERAGE;
+    const Part parts[2] = {Part{fmt, rows, Wg, nullptr}, Part{fmt, rows, Wu, nullptr}};
+    GateUpLaunch L;
+    memset(&L, 0, sizeof L);
+    size_t need = 0;
+    const int nchunks = ceil_div(cols / kQK, kChunkBlocks);
+    const Plan whole{1, nchunks, 1};  // fills the geometry; the gate||up kernel has its own plan
+    Part checked[2] = {parts[0], parts[1]};
+    checked[0].y = checked[1].y = act;  // stand-ins: prepare_group requires an output pointer
+    const int st = prepare_group(checked, 2, q8, cols, &whole, &L.g, &need);
+    if (st != MQ_OK) return st;
+    GateUpPlan pl;
+    if (explicit_plan) {
+        pl = *explicit_plan;
+    } else {
+        bool ok = true;
+        const size_t plane = q8_plane_bytes(cols);
+        pl = gateup_plan_for(nblk, device_sms(), [&](int w) {
+            const int c = gateup_device_ctas(w, plane);
+            if (c <= 0) ok = false;
+            return c;
+        });
+        if (!ok) return MQ_ERR_CUDA;
+    }
+    L.act = act;
+    L.q8o = (uint8_t *)q8o;
+    L.o_d_off = (unsigned)q8_d_offset(rows);
+    L.o_sum_off = (unsigned)q8_sum_offset(rows);
+    L.nblk = nblk;
+    L.wpb = pl.wpb;
+    return launch_gateup(L, pl.ctas, (cudaStream_t)stream) == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+}
+
 int subdots_common(int fmt, const void *Wp, const void *q8, int32_t *isums, int rows, int cols,
                    void *stream)
 {
@@ -671,6 +756,31 @@ int mq_gemv_q4k_q8_batch_plan(const void *Wp, const void *q8, int nt, float *y, 
     if (nt < 1) return MQ_ERR_SHAPE;
     const Plan p{splits, chunks_per_split, tiles_per_item};
     return gemv_common(4, Wp, q8, y, rows, cols, &p, nullptr, 0, stream, nt);
+}
+
+int mq_gemv_gateup_swiglu_q8(int fmt, const void *Wg, const void *Wu, const void *q8, int rows,
+                             int cols, float *act, void *q8_out, void *stream)
+{
+    return gateup_common(fmt, Wg, Wu, q8, rows, cols, act, q8_out, nullptr, stream);
+}
+
+int mq_gemv_gateup_swiglu_q8_plan(int fmt, const void *Wg, const void *Wu, const void *q8, int rows,
+                                  int cols, float *act, void *q8_out, int warps_per_cta, int ctas,
+                                  void *stream)
+{
+    const GateUpPlan p{warps_per_cta, ctas};
+    return gateup_common(fmt, Wg, Wu, q8, rows, cols, act, q8_out, &p, stream);
+}
+
+int mq_gemv_gateup_plan_for(int rows, int sms, int regs_per_thread, int *warps_per_cta, int *ctas)
+{
+    if (!warps_per_cta || !ctas) return MQ_ERR_NULL;
+    if (rows < 32 || rows % 32 != 0 || regs_per_thread < 1 || regs_per_thread > 255) return MQ_ERR_SHAPE;
+    const Occupancy o = model_occupancy(regs_per_thread, 0);
+    const GateUpPlan p = gateup_plan_for(rows / 32, sms, [&](int w) { return o.ctas[w]; });
+    *warps_per_cta = p.wpb;
+    *ctas = p.ctas;
+    return MQ_OK;
 }
 
 int mq_set_pdl(int enable)

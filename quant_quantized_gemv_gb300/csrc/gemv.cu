@@ -59,131 +59,6 @@ namespace {
 
 using namespace gemv_detail;
 
-// ---- q6_K ------------------------------------------------------------------
-struct Q6kRegs : Q6kW {
-    uint4 xa, xb;        // activation codes 0..15, 16..31 of the unit
-    unsigned short dh;   // activation fp16 scale
-};
-
-__device__ __forceinline__ void load_x(const GemvLaunch &a, const uint8_t *xs, const Unit &x,
-                                       int lane, Q6kRegs &R)
-{
-    if (x.active) {
-        const int U = 32 * x.c + lane;
-        if (!xs) {  // split plans: straight from L2, coherent (see the file comment)
-            const uint4 *qs = reinterpret_cast<const uint4 *>(a.q8 + (size_t)U * 32);
-            R.xa = __ldcg(qs);
-            R.xb = __ldcg(qs + 1);
-            R.dh = __ldcg(reinterpret_cast<const unsigned short *>(a.q8 + a.q8_d_off) + U);
-            return;
-        }
-        const uint4 *qs = reinterpret_cast<const uint4 *>(xs + (size_t)U * 32);
-        R.xa = qs[0];
-        R.xb = qs[1];
-        R.dh = reinterpret_cast<const unsigned short *>(xs + a.q8_d_off)[U];
-    } else {
-        R.xa = R.xb = make_uint4(0, 0, 0, 0);
-        R.dh = 0;
-    }
-}
-
-template <bool SUBDOTS>
-__device__ __forceinline__ void compute(const GemvLaunch &a, const GemvPart &P, const Q6kRegs &R,
-                                        const Unit &x, int lane, float (&acc)[8])
-{
-    const float d8 = __half2float(__ushort_as_half(R.dh));
-    const int xs0 = sum16(R.xa), xs1 = sum16(R.xb);
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        int dot0 = 0, dot1 = 0;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            uint32_t q0, q1;
-            q6k_codes(R, r, m, q0, q1);
-            dot0 = __dp4a((int)q0, (int)word(R.xa, m), dot0);
-            dot1 = __dp4a((int)q1, (int)word(R.xb, m), dot1);
-        }
-        const int isum0 = dot0 - 32 * xs0;
-        const int isum1 = dot1 - 32 * xs1;
-        int sc0, sc1;
-        float d;
-        q6k_scales(R, r, sc0, sc1, d);
-        if (SUBDOTS) {
-            const int row = x.t * kTileRows + r;
-            if (x.active && row < P.rows) {
-                const int blk = kChunkBlocks * x.c + (lane >> 3), p = lane & 7;
-                int32_t *o = a.isums + ((size_t)row * a.nb + blk) * 16 + 2 * p;
-                o[0] = isum0;
-                o[1] = isum1;
-            }
-        } else {
-            acc[r] = fmaf(d * d8, (float)(sc0 * isum0 + sc1 * isum1), acc[r]);
-        }
-    }
-}
-
-// ---- q4_K ------------------------------------------------------------------
-struct Q4kRegs : Q4kW {
-    uint4 xa, xb;
-    unsigned short dh;
-    int qsum;
-};
-
-__device__ __forceinline__ void load_x(const GemvLaunch &a, const uint8_t *xs, const Unit &x,
-                                       int lane, Q4kRegs &R)
-{
-    if (x.active) {
-        const int U = 32 * x.c + lane;
-        if (!xs) {  // split plans: straight from L2, coherent (see the file comment)
-            const uint4 *qs = reinterpret_cast<const uint4 *>(a.q8 + (size_t)U * 32);
-            R.xa = __ldcg(qs);
-            R.xb = __ldcg(qs + 1);
-            R.dh = __ldcg(reinterpret_cast<const unsigned short *>(a.q8 + a.q8_d_off) + U);
-            R.qsum = __ldcg(reinterpret_cast<const int *>(a.q8 + a.q8_sum_off) + U);
-            return;
-        }
-        const uint4 *qs = reinterpret_cast<const uint4 *>(xs + (size_t)U * 32);
-        R.xa = qs[0];
-        R.xb = qs[1];
-        R.dh = reinterpret_cast<const unsigned short *>(xs + a.q8_d_off)[U];
-        R.qsum = reinterpret_cast<const int *>(xs + a.q8_sum_off)[U];
-    } else {
-        R.xa = R.xb = make_uint4(0, 0, 0, 0);
-        R.dh = 0;
-        R.qsum = 0;
-    }
-}
-
-template <bool SUBDOTS>
-__device__ __forceinline__ void compute(const GemvLaunch &a, const GemvPart &P, const Q4kRegs &R,
-                                        const Unit &x, int lane, float (&acc)[8])
-{
-    const float d8 = __half2float(__ushort_as_half(R.dh));
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        int dot = 0;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const uint32_t w = word(R.qs[r], m);
-            dot = __dp4a((int)(w & kLo4), (int)word(R.xa, m), dot);
-            dot = __dp4a((int)((w >> 4) & kLo4), (int)word(R.xb, m), dot);
-        }
-        if (SUBDOTS) {
-            const int row = x.t * kTileRows + r;
-            if (x.active && row < P.rows) {
-                const int blk = kChunkBlocks * x.c + (lane >> 3), k = lane & 7;
-                a.isums[((size_t)row * a.nb + blk) * 8 + k] = dot;
-            }
-        } else {
-            int sc, mn;
-            float d, dmin;
-            q4k_scales(R, r, sc, mn, d, dmin);
-            const float term = fmaf(d, (float)(sc * dot), -dmin * (float)(mn * R.qsum));
-            acc[r] = fmaf(d8, term, acc[r]);
-        }
-    }
-}
-
 // Tile t of part P is finished for this warp (work item `item`, covering the
 // part's units [u0, u1)): write it, or combine it with the tile's other splits.
 __device__ __forceinline__ void flush_tile(const GemvLaunch &a, const GemvPart &P, int t,

@@ -163,25 +163,25 @@ __device__ __forceinline__ void compute(const GemvLaunch &a, const uint8_t *xs, 
                                         Acc<NT> &acc)
 {
     constexpr int G = group_size(NT);
-    if (!Acc<NT>::kEach) {  // one group: accumulate straight into the per-lane partials
+    if constexpr (!Acc<NT>::kEach) {  // one group: accumulate straight into the per-lane partials
         XCodes<G> X;
         load_x_group<FMT, G>(a, xs, 0, NT, x, lane, X);
         compute_group<NT, G>(W, X, 0, reinterpret_cast<float(&)[G][8]>(acc.v));
-        return;
-    }
+    } else {
 #pragma unroll
-    for (int t0 = 0; t0 < NT; t0 += G) {
-        XCodes<G> X;
-        load_x_group<FMT, G>(a, xs, t0, NT, x, lane, X);
-        float part[G][8];
+        for (int t0 = 0; t0 < NT; t0 += G) {
+            XCodes<G> X;
+            load_x_group<FMT, G>(a, xs, t0, NT, x, lane, X);
+            float part[G][8];
 #pragma unroll
-        for (int j = 0; j < G; ++j)
+            for (int j = 0; j < G; ++j)
 #pragma unroll
-            for (int r = 0; r < 8; ++r) part[j][r] = 0.0f;
-        compute_group<NT, G>(W, X, t0, part);
+                for (int r = 0; r < 8; ++r) part[j][r] = 0.0f;
+            compute_group<NT, G>(W, X, t0, part);
 #pragma unroll
-        for (int j = 0; j < G; ++j)
-            if (t0 + j < NT) acc.s[t0 + j] += reduce8(part[j], lane);
+            for (int j = 0; j < G; ++j)
+                if (t0 + j < NT) acc.s[t0 + j] += reduce8(part[j], lane);
+        }
     }
 }
 
@@ -313,7 +313,7 @@ __device__ __forceinline__ void run_batch(const GemvLaunch &a, const GemvPart &P
     for (int k = 0; k < (Acc<NT>::kEach ? NT : 1); ++k) acc.s[k] = 0.0f;
 
     int done = 0;  // tiles flushed so far
-    if (!kTwoBuffers<NT>) {  // one buffer: the next chunk's loads follow its compute
+    if constexpr (!kTwoBuffers<NT>) {  // one buffer: the next chunk's loads follow its compute
         for (int u = 0; u < n_units; ++u) {
             compute<FMT, NT>(a, xs, xa, lane, A, acc);
             const int t = xa.t;
@@ -328,31 +328,31 @@ __device__ __forceinline__ void run_batch(const GemvLaunch &a, const GemvPart &P
                 ++done;
             }
         }
-        return;
-    }
-    for (int u = 0; u < n_units; u += 2) {
-        const bool has_b = u + 1 < n_units;
-        if (has_b) {
-            xb = unit_at(next);
-            load_w(xb, lane, B);
-            advance(next);
-        }
-        compute<FMT, NT>(a, xs, xa, lane, A, acc);
-        if (xa.c == c_hi - 1) {
-            flush_tile<NT>(a, P, xa.t, xa.t < P.ntiles, done, acc, lane);
-            ++done;
-        }
-        if (!has_b) break;
-        const bool has_a = u + 2 < n_units;
-        if (has_a) {
-            xa = unit_at(next);
-            load_w(xa, lane, A);
-            advance(next);
-        }
-        compute<FMT, NT>(a, xs, xb, lane, B, acc);
-        if (xb.c == c_hi - 1) {
-            flush_tile<NT>(a, P, xb.t, xb.t < P.ntiles, done, acc, lane);
-            ++done;
+    } else {
+        for (int u = 0; u < n_units; u += 2) {
+            const bool has_b = u + 1 < n_units;
+            if (has_b) {
+                xb = unit_at(next);
+                load_w(xb, lane, B);
+                advance(next);
+            }
+            compute<FMT, NT>(a, xs, xa, lane, A, acc);
+            if (xa.c == c_hi - 1) {
+                flush_tile<NT>(a, P, xa.t, xa.t < P.ntiles, done, acc, lane);
+                ++done;
+            }
+            if (!has_b) break;
+            const bool has_a = u + 2 < n_units;
+            if (has_a) {
+                xa = unit_at(next);
+                load_w(xa, lane, A);
+                advance(next);
+            }
+            compute<FMT, NT>(a, xs, xb, lane, B, acc);
+            if (xb.c == c_hi - 1) {
+                flush_tile<NT>(a, P, xb.t, xb.t < P.ntiles, done, acc, lane);
+                ++done;
+            }
         }
     }
 }

@@ -50,6 +50,22 @@ struct GemvLaunch {
 
 cudaError_t launch_gemv(const GemvLaunch &a, cudaStream_t st);
 cudaError_t launch_subdots(const GemvLaunch &a, cudaStream_t st);
+// Gate||up GEMV with the SwiGLU -> q8 epilogue (gemv_gateup.cu): g.part[0]
+// is gate, g.part[1] is up (same rows and format), g.q8 the input plane.
+// Rows come in q8 blocks of 32 (rows % 32 == 0); a CTA of wpb warps (1..8)
+// takes whole blocks, grid-stride over nblk blocks.
+struct GateUpLaunch {
+    GemvLaunch g;
+    float *act;                   // rows outputs: silu(gate) * up
+    uint8_t *q8o;                 // act's q8 plane (rows values)
+    unsigned o_d_off, o_sum_off;  // its fp16-scale and sum sections
+    int nblk;                     // rows / 32
+    int wpb;                      // warps per CTA
+};
+cudaError_t launch_gateup(const GateUpLaunch &L, int ctas, cudaStream_t st);
+int gateup_ctas_per_sm(int warps_per_cta, size_t smem);
+bool gateup_opt_in(size_t max_plane);  // accept a staged plane of max_plane bytes
+
 // Small-batch GEMV (gemv_batch.cu), 1 <= a.nt <= kMaxTokens, one part whose
 // y holds nt x rows outputs, token-major.  Its plan reads differently: each
 // CTA holds `splits` warps for each of kBatchMaxCtaSplits / splits tiles (a

@@ -112,6 +112,11 @@ WORKLOADS = {
                                         ("ffn_down", "q6k", HIDDEN_14B, INTER_14B, "rms")]),
     # the 152064 x 5120 q6_K output head, fed by rms_norm -> q8
     "lm_head_14b": Workload("lm_head_14b", [("output", "q6k", VOCAB, HIDDEN_14B, "rms")]),
+    # the FFN half of a Qwen2.5-14B layer: rms_norm -> q8 -> gate, up (q4_K)
+    # -> SwiGLU -> q8 -> down (q6_K)
+    "ffn_14b": Workload("ffn_14b", [("ffn_gate", "q4k", INTER_14B, HIDDEN_14B, "rms"),
+                                    ("ffn_up", "q4k", INTER_14B, HIDDEN_14B, "rms"),
+                                    ("ffn_down", "q6k", HIDDEN_14B, INTER_14B, "swiglu")]),
     # full 48-layer 14B decode weight sweep plus the head
     "sweep_14b": Workload("sweep_14b", _sweep_14b()),
 }

@@ -271,3 +271,35 @@ def test_batch_validation_rejects_before_launch(mq):
     assert L.mq_swiglu_quant_q8_batch(A, B, N, Y, 64, 2, N) == mq.MQ_ERR_NULL
     assert L.mq_rmsnorm_quant_q8_batch(A, B, ctypes.c_float(1e-6), Y, ctypes.c_void_p(0x40004), 64, 9,
                                        N) == mq.MQ_ERR_SHAPE
+
+
+# ------------------------------------------------------------------ gate||up + SwiGLU -> q8
+def test_gateup_plans(mq):
+    """GB300 model (152 SMs, 168 registers): the most warps per CTA whose
+    one-CTA-per-32-row-block grid fits one wave (12 warps per SM)."""
+    assert mq.mq_gemv_gateup_plan_for(13824, 152) == (4, 432)     # 14B: 432 CTAs x 4 warps
+    assert mq.mq_gemv_gateup_plan_for(18944, 152) == (3, 592)     # 7B: 592 CTAs x 3 warps
+    assert mq.mq_gemv_gateup_plan_for(32, 152) == (8, 1)
+    w, c = mq.mq_gemv_gateup_plan_for(152064, 152)                # more blocks than a wave holds
+    assert w == 4 and c == 152 * 3
+    for rows in (32, 4096, 13824, 18944, 27648, 65536):
+        w, c = mq.mq_gemv_gateup_plan_for(rows, 152)
+        assert 1 <= w <= 8 and 1 <= c <= rows // 32
+        assert c * w <= 152 * model_ctas(w) * w                   # one resident wave
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="fake device pointers are only passed where no GPU exists")
+def test_gateup_validation_rejects_before_launch(mq):
+    L = mq.lib()
+    G, U, Q = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30000)
+    A, O, N = ctypes.c_void_p(0x40000), ctypes.c_void_p(0x50000), ctypes.c_void_p(0)
+    assert L.mq_gemv_gateup_swiglu_q8(4, N, U, Q, 64, 1024, A, O, N) == mq.MQ_ERR_NULL
+    assert L.mq_gemv_gateup_swiglu_q8(5, G, U, Q, 64, 1024, A, O, N) == mq.MQ_ERR_SHAPE
+    assert L.mq_gemv_gateup_swiglu_q8(4, G, U, Q, 48, 1024, A, O, N) == mq.MQ_ERR_SHAPE
+    assert L.mq_gemv_gateup_swiglu_q8(4, G, U, Q, 64, 1000, A, O, N) == mq.MQ_ERR_SHAPE
+    assert L.mq_gemv_gateup_swiglu_q8(4, G, U, Q, 64, 1024, ctypes.c_void_p(0x40004), O, N) == \
+        mq.MQ_ERR_ALIGN
+    for w, c in ((0, 1), (9, 1), (4, 0), (4, 3)):
+        assert L.mq_gemv_gateup_swiglu_q8_plan(4, G, U, Q, 64, 1024, A, O, w, c, N) == \
+            mq.MQ_ERR_COVERAGE
