@@ -29,6 +29,7 @@ _lib = None
 
 Q6K_BYTES = 210
 Q4K_BYTES = 144
+Q5K_BYTES = 176
 QK = 256
 
 
@@ -53,16 +54,19 @@ def _bind(L):
     L.mqo_quantize_q8.argtypes = [P, I, P, P, P]
     L.mqo_dequant_q6k.argtypes = [P, ctypes.c_long, P]
     L.mqo_dequant_q4k.argtypes = [P, ctypes.c_long, P]
+    L.mqo_dequant_q5k.argtypes = [P, ctypes.c_long, P]
     L.mqo_q4k_scale_min.argtypes = [P, I, P, P]
     L.mqo_subdots_q6k.argtypes = [P, P, I, I, P]
     L.mqo_subdots_q4k.argtypes = [P, P, I, I, P]
+    L.mqo_subdots_q5k.argtypes = [P, P, I, I, P]
     L.mqo_gemv_q6k.argtypes = [P, P, P, I, I, I, P, P]
     L.mqo_gemv_q4k.argtypes = [P, P, P, I, I, I, P, P]
+    L.mqo_gemv_q5k.argtypes = [P, P, P, I, I, I, P, P]
     L.mqo_rmsnorm.argtypes = [P, P, ctypes.c_float, I, P]
     L.mqo_swiglu.argtypes = [P, P, I, P]
-    for f in ("mqo_quantize_q8", "mqo_dequant_q6k", "mqo_dequant_q4k", "mqo_q4k_scale_min",
-              "mqo_subdots_q6k", "mqo_subdots_q4k", "mqo_gemv_q6k", "mqo_gemv_q4k",
-              "mqo_rmsnorm", "mqo_swiglu"):
+    for f in ("mqo_quantize_q8", "mqo_dequant_q6k", "mqo_dequant_q4k", "mqo_dequant_q5k",
+              "mqo_q4k_scale_min", "mqo_subdots_q6k", "mqo_subdots_q4k", "mqo_subdots_q5k",
+              "mqo_gemv_q6k", "mqo_gemv_q4k", "mqo_gemv_q5k", "mqo_rmsnorm", "mqo_swiglu"):
         getattr(L, f).restype = None
     return L
 
@@ -150,6 +154,15 @@ def dequant_q4k(blocks: np.ndarray) -> np.ndarray:
     return w
 
 
+def dequant_q5k(blocks: np.ndarray) -> np.ndarray:
+    """q5_K blocks (GGUF order, 176 B each) -> fp64 weights."""
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(-1)
+    nblk = blocks.size // Q5K_BYTES
+    w = np.zeros(nblk * QK, np.float64)
+    lib().mqo_dequant_q5k(_p(blocks), nblk, _p(w))
+    return w
+
+
 def q4k_scale_min(block: np.ndarray, k: int):
     block = np.ascontiguousarray(block, dtype=np.uint8).reshape(-1)
     sc = ctypes.c_int()
@@ -159,15 +172,20 @@ def q4k_scale_min(block: np.ndarray, k: int):
 
 
 def subdots(fmt: str, W: np.ndarray, q8: np.ndarray, rows: int, cols: int) -> np.ndarray:
-    """Integer sub-block dots: q6_K rows x nb x 16, q4_K rows x nb x 8 (int32)."""
+    """Integer sub-block dots: q6_K rows x nb x 16, q4_K / q5_K rows x nb x 8 (int32)."""
     W = np.ascontiguousarray(W, dtype=np.uint8)
     q8 = np.ascontiguousarray(q8, dtype=np.int8)
     nb = cols // QK
     per = 16 if fmt == "q6k" else 8
     out = np.zeros((rows, nb, per), np.int32)
-    fn = lib().mqo_subdots_q6k if fmt == "q6k" else lib().mqo_subdots_q4k
-    fn(_p(W), _p(q8), rows, cols, _p(out))
+    getattr(lib(), "mqo_subdots_" + _fmt(fmt))(_p(W), _p(q8), rows, cols, _p(out))
     return out
+
+
+def _fmt(fmt: str) -> str:
+    if fmt not in ("q6k", "q4k", "q5k"):
+        raise ValueError(f"unknown format {fmt!r}")
+    return fmt
 
 
 def gemv(fmt: str, W: np.ndarray, d8: np.ndarray, q8: np.ndarray, rows: int, cols: int,
@@ -185,7 +203,7 @@ def gemv(fmt: str, W: np.ndarray, d8: np.ndarray, q8: np.ndarray, rows: int, col
     r0, r1 = (0, rows) if row_range is None else row_range
     y = np.zeros(rows, np.float64)
     a = np.zeros(rows, np.float64)
-    fn = lib().mqo_gemv_q6k if fmt == "q6k" else lib().mqo_gemv_q4k
+    fn = getattr(lib(), "mqo_gemv_" + _fmt(fmt))
     if threads <= 1 or r1 - r0 < 2 * threads:
         fn(_p(W), _p(d8), _p(q8), r0, r1, cols, _p(y), _p(a))
     else:

@@ -26,6 +26,9 @@
  * block format is not on the pages; it follows the GGUF q4_K field list
  * (fp16 d, fp16 dmin, 12 bytes of packed 6-bit scales/mins, 128 bytes of
  * nibbles) and is pinned by hand-built blocks with closed-form values.
+ * q5_K is only named on the pages (a sibling MMVQ class, [D3-5] §4); its
+ * block is GGUF q5_K: the q4_K fields plus 32 bytes holding each weight's
+ * fifth bit, pinned the same way.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (no fast-math, so
  * that IEEE division, rintf and the f16 rounding below are the ones C defines).
@@ -37,6 +40,7 @@
 #define QK 256          /* weights per k-quant super-block                   */
 #define Q6K_BYTES 210   /* [D4-4] §1: ql 128 + qh 64 + sc 16 + d 2            */
 #define Q4K_BYTES 144   /* GGUF q4_K: d 2 + dmin 2 + scales 12 + qs 128       */
+#define Q5K_BYTES 176   /* GGUF q5_K: d 2 + dmin 2 + scales 12 + qh 32 + qs 128 */
 #define Q8_BLOCK 32     /* [D3-5] §3.2: q8 activation blocks of 32 values     */
 
 /* ------------------------------------------------------------------------ */
@@ -206,12 +210,42 @@ void mqo_dequant_q4k(const uint8_t *blocks, long nblocks, double *w)
 }
 
 /* ------------------------------------------------------------------------ */
+/* q5_K element decode (GGUF q5_K; named but not printed on the pages).      */
+/* Block: d (fp16) @0, dmin (fp16) @2, scales[12] @4 (packed exactly as in   */
+/* q4_K), qh[32] @16, qs[128] @48.  Element e = 32k + l of sub-block k takes */
+/* its low 4 bits from qs as q4_K does (low nibble of qs[32*(k/2) + l] for k */
+/* even, high nibble for k odd) and its fifth bit from bit k of qh[l]:       */
+/*   q_e = nibble + 16 * ((qh[l] >> k) & 1),  0 <= q_e <= 31,                */
+/*   w_e = f16(d) * sc_k * q_e - f16(dmin) * m_k.                            */
+/* ------------------------------------------------------------------------ */
+static int q5k_q(const uint8_t *blk, int e)
+{
+    const int k = e >> 5, l = e & 31;
+    const int byte = blk[48 + 32 * (k >> 1) + l];
+    const int lo = (k & 1) ? (byte >> 4) : (byte & 0x0f);
+    return lo + 16 * ((blk[16 + l] >> k) & 1);
+}
+
+void mqo_dequant_q5k(const uint8_t *blocks, long nblocks, double *w)
+{
+    for (long b = 0; b < nblocks; ++b) {
+        const uint8_t *blk = blocks + (size_t)b * Q5K_BYTES;
+        const double d = q4k_half(blk, 0), dmin = q4k_half(blk, 2);
+        for (int e = 0; e < QK; ++e) {
+            int sc, m;
+            mqo_q4k_scale_min(blk, e >> 5, &sc, &m);
+            w[(size_t)b * QK + e] = d * (double)sc * (double)q5k_q(blk, e) - dmin * (double)m;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Integer sub-block dots (the bit-exact intermediate).                     */
 /*   q6_K: isum_s = sum over the 16 weights of sub-block s of (q-32)*q8      */
 /*         ([D4-2] §3.2 Excerpt C: one dp4a tree per 16-weight sub-block).   */
-/*   q4_K: isum_k = sum over the 32 weights of sub-block k of q*q8.          */
+/*   q4_K, q5_K: isum_k = sum over the 32 weights of sub-block k of q*q8.    */
 /* W is GGUF-ordered, rows x (cols/256) blocks; q8 holds cols int8 values.   */
-/* Output: rows x nb x 16 (q6_K) or rows x nb x 8 (q4_K) int32.              */
+/* Output: rows x nb x 16 (q6_K) or rows x nb x 8 (q4_K, q5_K) int32.        */
 /* ------------------------------------------------------------------------ */
 void mqo_subdots_q6k(const uint8_t *W, const int8_t *q8, int rows, int cols, int32_t *isums)
 {
@@ -243,11 +277,26 @@ void mqo_subdots_q4k(const uint8_t *W, const int8_t *q8, int rows, int cols, int
         }
 }
 
+void mqo_subdots_q5k(const uint8_t *W, const int8_t *q8, int rows, int cols, int32_t *isums)
+{
+    const int nb = cols / QK;
+    for (int r = 0; r < rows; ++r)
+        for (int b = 0; b < nb; ++b) {
+            const uint8_t *blk = W + ((size_t)r * nb + b) * Q5K_BYTES;
+            for (int k = 0; k < 8; ++k) {
+                int32_t acc = 0;
+                for (int e = 32 * k; e < 32 * k + 32; ++e)
+                    acc += q5k_q(blk, e) * (int32_t)q8[(size_t)b * QK + e];
+                isums[((size_t)r * nb + b) * 8 + k] = acc;
+            }
+        }
+}
+
 /* ------------------------------------------------------------------------ */
 /* GEMV y = W x_hat, x_hat_i = f16(d8_{i/32}) * q8_i.                        */
 /* q6_K ([D4-2] §3.2 Excerpt C, the per-unit accumulation statement):        */
 /*   y_r = sum_b sum_s f16(d_b) * sc_s * f16(d8_{u(s)}) * isum_s             */
-/* q4_K (the GGUF q4_K decode multiplied out against x_hat):                 */
+/* q4_K, q5_K (the GGUF decode multiplied out against x_hat):               */
 /*   y_r = sum_b sum_k f16(d8_k) * (f16(d)*sc_k*isum_k - f16(dmin)*m_k*qsum_k)*/
 /*   with qsum_k = sum of the q8 values of block k.                          */
 /* Accumulated in fp64 in ascending (b, s); absum receives sum |term| per    */
@@ -294,6 +343,36 @@ void mqo_gemv_q4k(const uint8_t *W, const uint16_t *d8, const int8_t *q8,
                 for (int e = 32 * k; e < 32 * k + 32; ++e) {
                     const int32_t xv = q8[(size_t)b * QK + e];
                     isum += q4k_q(blk, e) * xv;
+                    qsum += xv;
+                }
+                const double d8v = (double)mqo_f16_to_f32(d8[(size_t)b * 8 + k]);
+                const double t1 = d8v * d * (double)sc * (double)isum;
+                const double t2 = d8v * dmin * (double)m * (double)qsum;
+                acc += t1 - t2;
+                aacc += fabs(t1) + fabs(t2);
+            }
+        }
+        y[r] = acc;
+        if (absum) absum[r] = aacc;
+    }
+}
+
+void mqo_gemv_q5k(const uint8_t *W, const uint16_t *d8, const int8_t *q8,
+                  int r0, int r1, int cols, double *y, double *absum)
+{
+    const int nb = cols / QK;
+    for (int r = r0; r < r1; ++r) {
+        double acc = 0.0, aacc = 0.0;
+        for (int b = 0; b < nb; ++b) {
+            const uint8_t *blk = W + ((size_t)r * nb + b) * Q5K_BYTES;
+            const double d = q4k_half(blk, 0), dmin = q4k_half(blk, 2);
+            for (int k = 0; k < 8; ++k) {
+                int sc, m;
+                mqo_q4k_scale_min(blk, k, &sc, &m);
+                int32_t isum = 0, qsum = 0;
+                for (int e = 32 * k; e < 32 * k + 32; ++e) {
+                    const int32_t xv = q8[(size_t)b * QK + e];
+                    isum += q5k_q(blk, e) * xv;
                     qsum += xv;
                 }
                 const double d8v = (double)mqo_f16_to_f32(d8[(size_t)b * 8 + k]);

@@ -23,6 +23,7 @@ import numpy as np
 
 Q6K_BYTES = 210
 Q4K_BYTES = 144
+Q5K_BYTES = 176
 QK = 256
 
 
@@ -63,8 +64,25 @@ def q4k_blocks(g: np.random.Generator, rows: int, cols: int) -> np.ndarray:
     return out.reshape(rows, -1)
 
 
+def q5k_blocks(g: np.random.Generator, rows: int, cols: int) -> np.ndarray:
+    """GGUF q5_K rows: (rows, cols/256*176) uint8, blocks
+    [d 2|dmin 2|scales 12|qh 32|qs 128]; d, dmin uniform in [1e-4, 1e-3],
+    every other byte uniform."""
+    assert cols % QK == 0
+    nblk = rows * (cols // QK)
+    out = np.empty((nblk, Q5K_BYTES), np.uint8)
+    d = _f16_bits(g.uniform(1e-4, 1e-3, size=nblk))
+    dm = _f16_bits(g.uniform(1e-4, 1e-3, size=nblk))
+    out[:, 0] = d & 0xFF
+    out[:, 1] = d >> 8
+    out[:, 2] = dm & 0xFF
+    out[:, 3] = dm >> 8
+    out[:, 4:] = g.integers(0, 256, size=(nblk, Q5K_BYTES - 4), dtype=np.uint8)
+    return out.reshape(rows, -1)
+
+
 def blocks(fmt: str, g: np.random.Generator, rows: int, cols: int) -> np.ndarray:
-    return q6k_blocks(g, rows, cols) if fmt == "q6k" else q4k_blocks(g, rows, cols)
+    return {"q6k": q6k_blocks, "q4k": q4k_blocks, "q5k": q5k_blocks}[fmt](g, rows, cols)
 
 
 def normal(g: np.random.Generator, n: int, mean: float = 0.0, std: float = 1.0) -> np.ndarray:

@@ -35,6 +35,12 @@ MUTANTS = {
                              "*m = (s[k + 4] & 15) | ((s[k] >> 6) << 4);"),
     "q4k nibble order": ("(k & 1) ? (byte >> 4) : (byte & 0x0f)", "(k & 1) ? (byte & 0x0f) : (byte >> 4)"),
     "q4k dropped min term": ("acc += t1 - t2;", "acc += t1;"),
+    "q5k fifth-bit index": ("16 * ((blk[16 + l] >> k) & 1)", "16 * ((blk[16 + l] >> (k ^ 1)) & 1)"),
+    "q5k fifth-bit weight": ("16 * ((blk[16 + l] >> k) & 1)", "32 * ((blk[16 + l] >> k) & 1)"),
+    "q5k qh offset": ("16 * ((blk[16 + l] >> k) & 1)", "16 * ((blk[17 + (l & 15)] >> k) & 1)"),
+    "q5k qs offset": ("blk[48 + 32 * (k >> 1) + l]", "blk[16 + 32 * (k >> 1) + l]"),
+    "q5k gemv min sign": ("isum += q5k_q(blk, e) * xv;\n                    qsum += xv;",
+                          "isum += q5k_q(blk, e) * xv;\n                    qsum -= xv;"),
     "rms eps outside root": ("sqrt(ss / (double)n + (double)eps)", "(sqrt(ss / (double)n) + (double)eps)"),
     "rms sum not mean": ("sqrt(ss / (double)n + (double)eps)", "sqrt(ss + (double)eps)"),
     "swiglu sign": ("exp(-gv)", "exp(gv)"),

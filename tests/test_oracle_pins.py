@@ -88,6 +88,40 @@ def q4k_dequant_alt(blocks, orc):
     return out.reshape(-1)
 
 
+def q5k_block(d_bits, dmin_bits, sc, m, qh, qs):
+    blk = np.zeros(176, np.uint8)
+    blk[0], blk[1] = d_bits & 0xFF, d_bits >> 8
+    blk[2], blk[3] = dmin_bits & 0xFF, dmin_bits >> 8
+    blk[4:16] = q4k_pack_scales(sc, m)
+    blk[16:48] = qh
+    blk[48:] = qs
+    return blk
+
+
+def q5k_dequant_alt(blocks, orc):
+    """GGUF q5_K decode written per 64-weight group j with two moving bit
+    masks u1 = 1 << 2j, u2 = 2 << 2j: weight 64j + l (l < 32) is the low
+    nibble of qs[32j + l] plus 16 if qh[l] & u1, weight 64j + 32 + l the high
+    nibble plus 16 if qh[l] & u2; scales as q4_K."""
+    blocks = blocks.reshape(-1, 176)
+    out = np.zeros((blocks.shape[0], 256))
+    for i, b in enumerate(blocks):
+        d = float(np.uint16(int(b[0]) | (int(b[1]) << 8)).view(np.float16))
+        dmin = float(np.uint16(int(b[2]) | (int(b[3]) << 8)).view(np.float16))
+        qh = b[16:48].astype(np.int64)
+        u1, u2 = 1, 2
+        for j in range(4):
+            q = b[48 + 32 * j:48 + 32 * j + 32].astype(np.int64)
+            lo = (q & 15) + np.where(qh & u1, 16, 0)
+            hi = (q >> 4) + np.where(qh & u2, 16, 0)
+            for hsel, qv in ((0, lo), (1, hi)):
+                sc, m = orc.q4k_scale_min(b, 2 * j + hsel)
+                out[i, 64 * j + 32 * hsel:64 * j + 32 * hsel + 32] = d * sc * qv - dmin * m
+            u1 <<= 2
+            u2 <<= 2
+    return out.reshape(-1)
+
+
 def xhat(orc, x):
     d, q, _ = orc.quantize_q8(x)
     dd = np.array([orc.f16_to_f32(h) for h in d])
@@ -299,6 +333,67 @@ def test_q4k_subdots_and_gemv_brute(orc):
     nib = orc.dequant_q4k(Wn).astype(np.int64).reshape(rows, cols // 256, 8, 32)
     got = orc.subdots("q4k", W, q8, rows, cols)
     want = (nib * q8.astype(np.int64).reshape(1, cols // 256, 8, 32)).sum(-1)
+    assert np.array_equal(got, want)
+
+
+# ---------------------------------------------------------------- q5_K
+def test_q5k_without_fifth_bits_is_q4k(orc):
+    """A q5_K block whose qh bytes are zero decodes like the q4_K block with
+    the same d, dmin, scales and nibbles (whose decode is pinned above)."""
+    g = synth.rng("pin", "q5k-q4k")
+    W5 = synth.q5k_blocks(g, 2, 1024).reshape(-1, 176).copy()
+    W5[:, 16:48] = 0
+    W4 = np.concatenate([W5[:, :16], W5[:, 48:]], axis=1)
+    assert np.array_equal(orc.dequant_q5k(W5), orc.dequant_q4k(W4))
+
+
+def test_q5k_closed_forms(orc):
+    qs = (np.arange(128) * 59 % 256).astype(np.uint8)
+    nib = np.zeros(256)
+    for j in range(4):
+        nib[64 * j:64 * j + 32] = qs[32 * j:32 * j + 32] & 15
+        nib[64 * j + 32:64 * j + 64] = qs[32 * j:32 * j + 32] >> 4
+    one, zero = np.ones(8, int), np.zeros(8, int)
+    # every fifth bit set: d = 1, dmin = 0, sc = 1 gives nibble + 16
+    w = orc.dequant_q5k(q5k_block(F16_ONE, 0, one, zero, np.full(32, 255, np.uint8), qs))
+    assert np.array_equal(w, nib + 16)
+    # one fifth bit at a time: bit k of qh[l] lifts weight 32k + l alone
+    for k in range(8):
+        for l in (0, 13, 31):
+            qh = np.zeros(32, np.uint8)
+            qh[l] = 1 << k
+            w = orc.dequant_q5k(q5k_block(F16_ONE, 0, one, zero, qh, qs))
+            want = nib.copy()
+            want[32 * k + l] += 16
+            assert np.array_equal(w, want), (k, l)
+    # d = 2, dmin = 0.5, sc = 3, m = 4, all fifth bits: w = 6 (q + 16) - 2
+    w = orc.dequant_q5k(q5k_block(0x4000, 0x3800, np.full(8, 3), np.full(8, 4),
+                                  np.full(32, 255, np.uint8), qs))
+    assert np.array_equal(w, 6 * (nib + 16) - 2)
+
+
+def test_q5k_matches_second_formulation(orc):
+    g = synth.rng("pin", "q5k-alt")
+    W = synth.q5k_blocks(g, 3, 768)
+    assert np.array_equal(orc.dequant_q5k(W), q5k_dequant_alt(W, orc))
+
+
+def test_q5k_subdots_and_gemv_brute(orc):
+    g = synth.rng("pin", "gemv-q5k")
+    rows, cols = 6, 1280
+    W = synth.q5k_blocks(g, rows, cols)
+    d8, q8, xh = xhat(orc, synth.normal(g, cols))
+    y, a = orc.gemv("q5k", W, d8, q8, rows, cols)
+    ref = orc.dequant_q5k(W).reshape(rows, cols) @ xh
+    assert np.all(np.abs(y - ref) <= 1e-12 * a)
+    # sub-dots against codes recovered from a d = 1, dmin = 0, sc = 1 copy
+    Wn = W.reshape(-1, 176).copy()
+    Wn[:, 0], Wn[:, 1], Wn[:, 2], Wn[:, 3] = F16_ONE & 0xFF, F16_ONE >> 8, 0, 0
+    Wn[:, 4:16] = q4k_pack_scales(np.ones(8, int), np.zeros(8, int))
+    codes = orc.dequant_q5k(Wn).astype(np.int64).reshape(rows, cols // 256, 8, 32)
+    assert codes.min() >= 0 and codes.max() <= 31
+    got = orc.subdots("q5k", W, q8, rows, cols)
+    want = (codes * q8.astype(np.int64).reshape(1, cols // 256, 8, 32)).sum(-1)
     assert np.array_equal(got, want)
 
 
