@@ -47,7 +47,7 @@ typedef enum {
                               cover it twice; nothing was launched ([D4-2] §6
                               lesson 1: a gate must bound both sides)         */
     MQ_ERR_WORKSPACE = 5,  /* split-K needs a larger workspace               */
-    MQ_ERR_CUDA = 6        /* the CUDA launch failed                          */
+    MQ_ERR_CUDA = 6        /* a CUDA call failed (mq_last_error says which)   */
 } mq_status;
 
 /* Static message for a status code. */
@@ -55,6 +55,11 @@ const char *mq_strerror(int status);
 
 /* Library version string. */
 const char *mq_version(void);
+
+/* What the last MQ_ERR_CUDA on the calling thread came from: the library
+ * step and CUDA's error text (empty before any).  The buffer is the
+ * thread's own and is overwritten by its next failure. */
+const char *mq_last_error(void);
 
 /* ------------------------------------------------------------------------
  * Weight repack (host, once at load).  [D4-4] §2-§3.1: the GGUF q6_K block
@@ -64,8 +69,10 @@ const char *mq_version(void);
  * tile-chunk as planes in the order the kernel's lanes read them; it is a
  * lossless permutation of the block's bits (exactly rows*cols/256 * 210 B of
  * content; rows are padded to a multiple of 8 with zero rows, which decode to
- * zero).  q4_K (144 B: d | dmin | scales 12 | qs 128, the GGUF q4_K block) is
- * treated the same way.  The repacked layout is private to this library.
+ * zero).  q4_K (144 B: d | dmin | scales 12 | qs 128, the GGUF q4_K block)
+ * and q5_K (176 B: d | dmin | scales 12 | qh 32 | qs 128, the GGUF q5_K
+ * block; the pages only name it, [D3-5] §4) are treated the same way.  The
+ * repacked layout is private to this library.
  *
  * mq_repacked_bytes_*: bytes of the repacked matrix (0 on a bad shape).
  * mq_repack_*:   gguf (host, rows x cols/256 blocks, row-major, GGUF order)
@@ -76,10 +83,13 @@ const char *mq_version(void);
  * ------------------------------------------------------------------------ */
 size_t mq_repacked_bytes_q6k(int rows, int cols);
 size_t mq_repacked_bytes_q4k(int rows, int cols);
+size_t mq_repacked_bytes_q5k(int rows, int cols);
 int mq_repack_q6k(const void *gguf, void *dst, int rows, int cols);
 int mq_repack_q4k(const void *gguf, void *dst, int rows, int cols);
+int mq_repack_q5k(const void *gguf, void *dst, int rows, int cols);
 int mq_unrepack_q6k(const void *packed, void *gguf, int rows, int cols);
 int mq_unrepack_q4k(const void *packed, void *gguf, int rows, int cols);
+int mq_unrepack_q5k(const void *packed, void *gguf, int rows, int cols);
 
 /* ------------------------------------------------------------------------
  * The q8 activation plane ([D3-5] §3.2, the pad40 block's fields): for each
@@ -127,6 +137,7 @@ int mq_swiglu_quant_q8(const float *g, const float *u, float *y, void *q8, int n
  *   q4_K: y_r = sum over 32-weight sub-blocks k of
  *        f16(d8_k) * (f16(d) * sc_k * isum_k - f16(dmin) * m_k * qsum_k),
  *        isum_k = sum q * q8, qsum_k = the q8 block's sum.
+ *   q5_K: as q4_K with 5-bit codes q = nibble + 16 * fifth bit (0..31).
  * Wp: repacked weights (device, mq_repack_* output).  q8: plane of cols
  * values (device).  y: rows f32 (device).  The f32 combine order is fixed
  * (ascending chunks within a work item, a fixed butterfly across lanes,
@@ -159,8 +170,8 @@ int mq_swiglu_quant_q8(const float *g, const float *u, float *y, void *q8, int n
  *   device memory, zero-filled before its first use; every completed call
  *   leaves it zero-filled again.  ws may be NULL when 0 bytes are needed.
  * mq_gemv_workspace_bytes_for: the same for an explicit plan (0 if invalid).
- * mq_gemv_plan: the default plan for format 6 (q6_K) or 4 (q4_K) on the
- *   current device (from the kernel's measured occupancy).
+ * mq_gemv_plan: the default plan for format 6 (q6_K), 4 (q4_K) or 5 (q5_K)
+ *   on the current device (from the kernel's measured occupancy).
  * mq_gemv_plan_for: the default plan for a device with `sms` SMs and a
  *   kernel using regs_per_thread registers (64K registers per SM).  Host only.
  * mq_gemv_*_q8_plan: the GEMV with an explicit plan.
@@ -182,6 +193,11 @@ int mq_gemv_q6k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int 
                         int chunks_per_split, int tiles_per_item, void *ws, size_t ws_bytes,
                         void *stream);
 int mq_gemv_q4k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int cols, int splits,
+                        int chunks_per_split, int tiles_per_item, void *ws, size_t ws_bytes,
+                        void *stream);
+int mq_gemv_q5k_q8(const void *Wp, const void *q8, float *y, int rows, int cols, void *ws,
+                   size_t ws_bytes, void *stream);
+int mq_gemv_q5k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int cols, int splits,
                         int chunks_per_split, int tiles_per_item, void *ws, size_t ws_bytes,
                         void *stream);
 
@@ -222,12 +238,12 @@ int mq_gemv_q6k_q8_noalloc(const void *Wp, const void *q8, float *y, int rows, i
  *   mq_gemv_group_workspace_bytes: workspace for the default plan
  *     (splits == 0) or an explicit one; the Wp / y fields may be NULL here.
  * Errors: as mq_gemv_q6k_q8; MQ_ERR_SHAPE also for nparts outside
- *         1..MQ_MAX_GROUP or a format other than 6 / 4.
+ *         1..MQ_MAX_GROUP or a format other than 6 / 4 / 5.
  * ------------------------------------------------------------------------ */
 #define MQ_MAX_GROUP 8
 
 typedef struct {
-    int fmt;            /* 6 = q6_K, 4 = q4_K                         */
+    int fmt;            /* 6 = q6_K, 4 = q4_K, 5 = q5_K               */
     int rows;           /* rows of this matrix (>= 1)                  */
     const void *Wp;     /* its repacked weights (device)               */
     float *y;           /* its rows f32 outputs (device)               */
@@ -285,9 +301,13 @@ int mq_gemv_q6k_q8_batch(const void *Wp, const void *q8, int nt, float *y, int r
                          void *stream);
 int mq_gemv_q4k_q8_batch(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
                          void *stream);
+int mq_gemv_q5k_q8_batch(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
+                         void *stream);
 int mq_gemv_q6k_q8_batch_plan(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
                               int splits, int chunks_per_split, int tiles_per_item, void *stream);
 int mq_gemv_q4k_q8_batch_plan(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
+                              int splits, int chunks_per_split, int tiles_per_item, void *stream);
+int mq_gemv_q5k_q8_batch_plan(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
                               int splits, int chunks_per_split, int tiles_per_item, void *stream);
 
 /* Producers over nt rows (1..MQ_MAX_TOKENS) of n values each: x, g, u and y
@@ -313,7 +333,7 @@ int mq_swiglu_quant_q8_batch(const float *g, const float *u, float *y, void *q8,
  * produce in three launches, bit for bit.  This is the concatenated
  * gate||up launch with a SwiGLU epilogue that [D4-4] §2 and §5 closed on
  * GB10 for running 1.5 waves; here the grid is one resident wave.
- *   fmt: 6 (q6_K) or 4 (q4_K), for both matrices.  Wg, Wu: repacked
+ *   fmt: 6 (q6_K), 4 (q4_K) or 5 (q5_K), for both matrices.  Wg, Wu: repacked
  *   weights, rows x cols each (device).  q8: plane of cols values (device).
  *   act: rows f32 (device).  q8_out: mq_q8_bytes(rows) bytes (device).
  *   rows must be a multiple of 32 (q8 blocks of act are whole).
@@ -358,12 +378,15 @@ int mq_set_pdl(int enable);
  * Integer sub-block dots (device), for bit-exact testing of the GEMV's
  * integer path: the same kernel and lane mapping as the GEMV, writing
  * isums[r][b][s] (int32) instead of accumulating: 16 per block (q6_K,
- * isum_s = sum (q - 32) * q8) or 8 per block (q4_K, isum_k = sum q * q8).
+ * isum_s = sum (q - 32) * q8) or 8 per block (q4_K and q5_K,
+ * isum_k = sum q * q8).
  * isums: rows * cols/256 * {16, 8} int32 (device).
  * ------------------------------------------------------------------------ */
 int mq_gemv_q6k_q8_subdots(const void *Wp, const void *q8, int32_t *isums, int rows, int cols,
                            void *stream);
 int mq_gemv_q4k_q8_subdots(const void *Wp, const void *q8, int32_t *isums, int rows, int cols,
+                           void *stream);
+int mq_gemv_q5k_q8_subdots(const void *Wp, const void *q8, int32_t *isums, int rows, int cols,
                            void *stream);
 
 /* Number of streaming multiprocessors of the current device (0 on error);

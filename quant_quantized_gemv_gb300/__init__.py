@@ -27,7 +27,7 @@ MQ_OK, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_NULL, MQ_ERR_COVERAGE, MQ_ERR_WORKSPAC
 
 # every symbol include/mq.h declares
 EXPORTS = [
-    "mq_strerror", "mq_version", "mq_repacked_bytes_q6k", "mq_repacked_bytes_q4k",
+    "mq_strerror", "mq_version", "mq_last_error", "mq_repacked_bytes_q6k", "mq_repacked_bytes_q4k",
     "mq_repack_q6k", "mq_repack_q4k", "mq_unrepack_q6k", "mq_unrepack_q4k", "mq_q8_bytes",
     "mq_q8_unpack_host", "mq_quantize_q8", "mq_rmsnorm_quant_q8", "mq_swiglu_quant_q8",
     "mq_gemv_workspace_bytes", "mq_gemv_plan", "mq_gemv_q6k_q8", "mq_gemv_q4k_q8",
@@ -39,7 +39,9 @@ EXPORTS = [
     "mq_quantize_q8_batch", "mq_rmsnorm_quant_q8_batch", "mq_swiglu_quant_q8_batch",
     "mq_gemv_batch_plan", "mq_gemv_batch_plan_for", "mq_gemv_q6k_q8_batch", "mq_gemv_q4k_q8_batch", "mq_gemv_q6k_q8_batch_plan",
     "mq_gemv_q4k_q8_batch_plan", "mq_gemv_gateup_swiglu_q8", "mq_gemv_gateup_swiglu_q8_plan",
-    "mq_gemv_gateup_plan_for",
+    "mq_gemv_gateup_plan_for", "mq_repacked_bytes_q5k", "mq_repack_q5k", "mq_unrepack_q5k",
+    "mq_gemv_q5k_q8", "mq_gemv_q5k_q8_plan", "mq_gemv_q5k_q8_subdots", "mq_gemv_q5k_q8_batch",
+    "mq_gemv_q5k_q8_batch_plan",
 ]
 
 
@@ -56,7 +58,10 @@ MQ_MAX_TOKENS = 8
 class MQError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {lib().mq_strerror(status).decode()} (status {status})")
+        msg = f"{where}: {lib().mq_strerror(status).decode()} (status {status})"
+        if status == MQ_ERR_CUDA:
+            msg += f": {lib().mq_last_error().decode()}"
+        super().__init__(msg)
 
 
 def library_path() -> str:
@@ -76,6 +81,7 @@ def lib():
     sig = {
         "mq_strerror": ([I], ctypes.c_char_p),
         "mq_version": ([], ctypes.c_char_p),
+        "mq_last_error": ([], ctypes.c_char_p),
         "mq_repacked_bytes_q6k": ([I, I], S),
         "mq_repacked_bytes_q4k": ([I, I], S),
         "mq_repack_q6k": ([P, P, I, I], I),
@@ -116,6 +122,14 @@ def lib():
         "mq_gemv_gateup_swiglu_q8": ([I, P, P, P, I, I, P, P, P], I),
         "mq_gemv_gateup_swiglu_q8_plan": ([I, P, P, P, I, I, P, P, I, I, P], I),
         "mq_gemv_gateup_plan_for": ([I, I, I, P, P], I),
+        "mq_repacked_bytes_q5k": ([I, I], S),
+        "mq_repack_q5k": ([P, P, I, I], I),
+        "mq_unrepack_q5k": ([P, P, I, I], I),
+        "mq_gemv_q5k_q8": ([P, P, P, I, I, P, S, P], I),
+        "mq_gemv_q5k_q8_plan": ([P, P, P, I, I, I, I, I, P, S, P], I),
+        "mq_gemv_q5k_q8_subdots": ([P, P, P, I, I, P], I),
+        "mq_gemv_q5k_q8_batch": ([P, P, I, P, I, I, P], I),
+        "mq_gemv_q5k_q8_batch_plan": ([P, P, I, P, I, I, I, I, I, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -190,6 +204,38 @@ def mq_unrepack_q4k(packed: np.ndarray, rows: int, cols: int) -> np.ndarray:
     out = np.empty(rows * (cols // 256) * 144, np.uint8)
     _check(lib().mq_unrepack_q4k(_np_ptr(packed), _np_ptr(out), rows, cols), "mq_unrepack_q4k")
     return out.reshape(rows, -1)
+
+
+def mq_repacked_bytes_q5k(rows: int, cols: int) -> int:
+    return lib().mq_repacked_bytes_q5k(rows, cols)
+
+
+def mq_repack_q5k(gguf: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    """GGUF q5_K rows (host) -> repacked bytes (host numpy)."""
+    return _repack(lib().mq_repack_q5k, mq_repacked_bytes_q5k, gguf, rows, cols)
+
+
+def mq_unrepack_q5k(packed: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    out = np.empty(rows * (cols // 256) * 176, np.uint8)
+    _check(lib().mq_unrepack_q5k(_np_ptr(packed), _np_ptr(out), rows, cols), "mq_unrepack_q5k")
+    return out.reshape(rows, -1)
+
+
+FMT_CODES = {"q6k": 6, "q4k": 4, "q5k": 5}
+
+
+def fmt_code(fmt: str) -> int:
+    """The C ABI's format code of 'q6k', 'q4k' or 'q5k'."""
+    try:
+        return FMT_CODES[fmt]
+    except KeyError:
+        raise ValueError(f"unknown format {fmt!r}") from None
+
+
+def mq_repack(fmt: str, gguf: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    """GGUF rows of format fmt (host) -> repacked bytes (host numpy)."""
+    return {"q6k": mq_repack_q6k, "q4k": mq_repack_q4k, "q5k": mq_repack_q5k}[fmt](gguf, rows, cols)
 
 
 # ------------------------------------------------------------------ q8 plane
@@ -312,7 +358,7 @@ def _plan_out(fn, *args):
 
 def mq_gemv_plan(rows: int, cols: int, fmt: str = "q6k"):
     """Default (splits, chunks_per_split, tiles_per_item) on the current device."""
-    return _plan_out(lib().mq_gemv_plan, rows, cols, 6 if fmt == "q6k" else 4)
+    return _plan_out(lib().mq_gemv_plan, rows, cols, fmt_code(fmt))
 
 
 def mq_gemv_plan_for(rows: int, cols: int, sms: int, regs_per_thread: int = 168):
@@ -373,6 +419,17 @@ def mq_gemv_q4k_q8(Wp, q8, rows: int, cols: int, y=None, ws=None, stream=None, p
     return _gemv("mq_gemv_q4k_q8", Wp, q8, rows, cols, y, ws, stream, plan)
 
 
+def mq_gemv_q5k_q8(Wp, q8, rows: int, cols: int, y=None, ws=None, stream=None, plan=None):
+    """y = W x_hat for repacked q5_K weights Wp (device) and a q8 plane."""
+    return _gemv("mq_gemv_q5k_q8", Wp, q8, rows, cols, y, ws, stream, plan)
+
+
+def mq_gemv(fmt: str, Wp, q8, rows: int, cols: int, y=None, ws=None, stream=None, plan=None):
+    """The single-token GEMV of format fmt ('q6k', 'q4k', 'q5k')."""
+    return _gemv("mq_gemv_" + {6: "q6k", 4: "q4k", 5: "q5k"}[fmt_code(fmt)] + "_q8", Wp, q8, rows,
+                 cols, y, ws, stream, plan)
+
+
 # ------------------------------------------------------------------ small-batch GEMV
 def mq_gemv_batch_plan(rows: int, cols: int, nt: int):
     """Default plan of the nt-token GEMV on the current device."""
@@ -408,6 +465,11 @@ def mq_gemv_q4k_q8_batch(Wp, q8, nt: int, rows: int, cols: int, y=None, stream=N
     return _gemv_batch("mq_gemv_q4k_q8_batch", Wp, q8, nt, rows, cols, y, stream, plan)
 
 
+def mq_gemv_q5k_q8_batch(Wp, q8, nt: int, rows: int, cols: int, y=None, stream=None, plan=None):
+    """Y[nt, rows] = W x_hat_t for nt q8 planes (back to back), one pass over W."""
+    return _gemv_batch("mq_gemv_q5k_q8_batch", Wp, q8, nt, rows, cols, y, stream, plan)
+
+
 # ------------------------------------------------------------------ gate||up + SwiGLU -> q8
 def mq_gemv_gateup_swiglu_q8(fmt: str, Wg, Wu, q8, rows: int, cols: int, act=None, q8_out=None,
                              stream=None, plan=None):
@@ -417,7 +479,7 @@ def mq_gemv_gateup_swiglu_q8(fmt: str, Wg, Wu, q8, rows: int, cols: int, act=Non
     act = torch.empty(rows, dtype=torch.float32, device=Wg.device) if act is None else act
     q8_out = _q8_out(rows, act, q8_out)
     L = lib()
-    f = 6 if fmt == "q6k" else 4
+    f = fmt_code(fmt)
     if plan is None:
         st = L.mq_gemv_gateup_swiglu_q8(f, _dev(Wg), _dev(Wu), _dev(q8), rows, cols,
                                         _dev(act, torch.float32), _dev(q8_out), _stream(stream))
@@ -441,7 +503,7 @@ def _parts_array(parts, ys=None):
     """parts: [(fmt 'q6k'|'q4k', Wp tensor or None, rows)] -> ctypes array."""
     arr = (MQGemvPart * len(parts))()
     for i, (fmt, Wp, rows) in enumerate(parts):
-        arr[i].fmt = 6 if fmt == "q6k" else 4
+        arr[i].fmt = fmt_code(fmt)
         arr[i].rows = int(rows)
         arr[i].Wp = None if Wp is None else Wp.data_ptr()
         arr[i].y = None if ys is None else ys[i].data_ptr()
@@ -511,3 +573,7 @@ def mq_gemv_q6k_q8_subdots(Wp, q8, rows: int, cols: int, stream=None):
 
 def mq_gemv_q4k_q8_subdots(Wp, q8, rows: int, cols: int, stream=None):
     return _subdots("mq_gemv_q4k_q8_subdots", 8, Wp, q8, rows, cols, stream)
+
+
+def mq_gemv_q5k_q8_subdots(Wp, q8, rows: int, cols: int, stream=None):
+    return _subdots("mq_gemv_q5k_q8_subdots", 8, Wp, q8, rows, cols, stream)

@@ -2,6 +2,7 @@
 // plan and its coverage check, then the launch.  Nothing here allocates.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <string.h>
 
 #include <atomic>
@@ -10,6 +11,19 @@
 #include "kernels.h"
 #include "layout.h"
 #include "mq.h"
+
+namespace mq {
+
+thread_local char g_last_error[256];
+
+int cuda_fail(const char *where, cudaError_t e)
+{
+    snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", where, cudaGetErrorString(e),
+             cudaGetErrorName(e));
+    return MQ_ERR_CUDA;
+}
+
+}  // namespace mq
 
 namespace {
 
@@ -23,7 +37,7 @@ std::atomic<int> g_sms[kMaxDevices];
 std::atomic<int> g_ctas[kMaxDevices][kMaxCtaSplits + 1];
 std::atomic<int> g_pdl{0};
 // resident small-batch CTAs per SM (register limit): [device][nt][warps per CTA]
-std::atomic<int> g_batch_ctas[kMaxDevices][kMaxTokens + 1][kBatchMaxCtaSplits + 1];
+std::atomic<int> g_batch_ctas[kMaxDevices][kMaxTokens + 1][7][kBatchMaxCtaSplits + 1];  // [..][fmt]
 // resident gate||up CTAs per SM (register limit): [device][warps per CTA]
 constexpr int kGateUpMaxWarps = 8;
 std::atomic<int> g_gateup_ctas[kMaxDevices][kGateUpMaxWarps + 1];
@@ -40,7 +54,12 @@ bool vec_shape_ok(int n) { return n > 0 && n % 32 == 0; }
 int current_device()
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        cuda_fail("cudaGetDevice", e);
+        return -1;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return -1;
     return dev;
 }
 
@@ -78,11 +97,15 @@ bool device_limits(DeviceLimits *out)
         std::lock_guard<std::mutex> lock(g_limits_mutex);
         if (!g_limits_ok[dev].load(std::memory_order_relaxed)) {
             DeviceLimits l;
-            if (cudaDeviceGetAttribute(&l.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
-                                       dev) != cudaSuccess ||
-                cudaDeviceGetAttribute(&l.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock,
-                                       dev) != cudaSuccess)
+            cudaError_t e = cudaDeviceGetAttribute(&l.smem_per_sm,
+                                                   cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+            if (e == cudaSuccess)
+                e = cudaDeviceGetAttribute(&l.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock,
+                                           dev);
+            if (e != cudaSuccess) {
+                cuda_fail("shared-memory attributes", e);
                 return false;
+            }
             l.max_plane = gemv_max_plane_bytes();  // also opts the kernels in
             l.max_batch_planes = gemv_batch_max_smem();
             if (l.max_plane == 0 || l.max_batch_planes == 0 || !gateup_opt_in(l.max_plane))
@@ -120,7 +143,7 @@ bool device_occupancy(Occupancy *o, size_t plane)
 }
 
 // The small-batch kernel for nt tokens: every CTA stages all nt planes.
-bool batch_occupancy(Occupancy *o, int nt, size_t planes)
+bool batch_occupancy(Occupancy *o, int nt, int fmt, size_t planes)
 {
     const int dev = current_device();
     DeviceLimits lim;
@@ -128,10 +151,10 @@ bool batch_occupancy(Occupancy *o, int nt, size_t planes)
     const long long per_cta = (long long)planes + kBatchStaticSmem + lim.smem_reserved;
     const int by_smem = (int)(lim.smem_per_sm / per_cta);
     for (int w = 1; w <= kBatchMaxCtaSplits; ++w) {
-        std::atomic<int> &slot = g_batch_ctas[dev][nt][w];
+        std::atomic<int> &slot = g_batch_ctas[dev][nt][fmt][w];
         int v = slot.load(std::memory_order_relaxed);
         if (v <= 0) {
-            v = gemv_batch_ctas_per_sm(nt, w, 0);
+            v = gemv_batch_ctas_per_sm(nt, fmt, w, 0);
             if (v <= 0) return false;
             slot.store(v, std::memory_order_relaxed);
         }
@@ -287,7 +310,7 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
     long long total_tiles = 0;
     for (int p = 0; p < nparts; ++p) {
         const Part &x = parts[p];
-        if (x.fmt != 6 && x.fmt != 4) return MQ_ERR_SHAPE;
+        if (block_bytes(x.fmt) == 0) return MQ_ERR_SHAPE;
         if ((!x.Wp || !x.y) && !sizes_only) return MQ_ERR_NULL;
         if (!gemv_shape_ok(x.rows, cols)) return MQ_ERR_SHAPE;
         if (!aligned16(x.Wp) || !aligned16(x.y)) return MQ_ERR_ALIGN;
@@ -317,7 +340,7 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
             if (!device_occupancy(&o, plane)) return MQ_ERR_CUDA;
             pl = plan_for((int)total_tiles, nchunks, device_sms(), o);
         } else {
-            if (!batch_occupancy(&o, nt, (size_t)nt * plane)) return MQ_ERR_CUDA;
+            if (!batch_occupancy(&o, nt, parts[0].fmt, (size_t)nt * plane)) return MQ_ERR_CUDA;
             pl = batch_plan_for((int)total_tiles, nchunks, device_sms(), o);
         }
     }
@@ -326,7 +349,7 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
     long long items = 0, tiles = 0;
     for (int p = 0; p < nparts; ++p) {
         const Part &x = parts[p];
-        const Geom g = make_geom(x.rows, cols, x.fmt == 6 ? kQ6kBytes : kQ4kBytes);
+        const Geom g = make_geom(x.rows, cols, block_bytes(x.fmt));
         GemvPart &gp = a->part[p];
         gp.W = (const uint8_t *)x.Wp;
         gp.y = x.y;
@@ -382,7 +405,7 @@ int gemv_group(const Part *parts, int nparts, const void *q8, int cols, const Pl
     }
     const cudaError_t e = nt > 0 ? launch_gemv_batch(a, (cudaStream_t)stream)
                                  : launch_gemv(a, (cudaStream_t)stream);
-    return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+    return e == cudaSuccess ? MQ_OK : cuda_fail(nt > 0 ? "small-batch GEMV launch" : "GEMV launch", e);
 }
 
 int gemv_common(int fmt, const void *Wp, const void *q8, float *y, int rows, int cols,
@@ -402,7 +425,7 @@ int batch_plan_of(int rows, int cols, int nt, Plan *p)
     DeviceLimits lim;
     if (!device_limits(&lim)) return MQ_ERR_CUDA;
     if ((size_t)nt * plane > lim.max_batch_planes) return MQ_ERR_SHAPE;
-    if (!batch_occupancy(&o, nt, (size_t)nt * plane)) return MQ_ERR_CUDA;
+    if (!batch_occupancy(&o, nt, 6, (size_t)nt * plane)) return MQ_ERR_CUDA;
     *p = batch_plan_for(g.ntiles, g.nchunks, device_sms(), o);
     return MQ_OK;
 }
@@ -449,7 +472,7 @@ int gateup_common(int fmt, const void *Wg, const void *Wu, const void *q8, int r
                   float *act, void *q8o, const GateUpPlan *explicit_plan, void *stream)
 {
     if (!Wg || !Wu || !q8 || !act || !q8o) return MQ_ERR_NULL;
-    if (fmt != 6 && fmt != 4) return MQ_ERR_SHAPE;
+    if (block_bytes(fmt) == 0) return MQ_ERR_SHAPE;
     if (!gemv_shape_ok(rows, cols) || rows % 32 != 0) return MQ_ERR_SHAPE;
     if (!aligned16(act) || !aligned16(q8o)) return MQ_ERR_ALIGN;
     const int nblk = rows / 32;
@@ -485,7 +508,8 @@ int gateup_common(int fmt, const void *Wg, const void *Wu, const void *q8, int r
     L.o_sum_off = (unsigned)q8_sum_offset(rows);
     L.nblk = nblk;
     L.wpb = pl.wpb;
-    return launch_gateup(L, pl.ctas, (cudaStream_t)stream) == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+    const cudaError_t e = launch_gateup(L, pl.ctas, (cudaStream_t)stream);
+    return e == cudaSuccess ? MQ_OK : cuda_fail("gate||up launch", e);
 }
 
 int subdots_common(int fmt, const void *Wp, const void *q8, int32_t *isums, int rows, int cols,
@@ -494,7 +518,7 @@ int subdots_common(int fmt, const void *Wp, const void *q8, int32_t *isums, int 
     if (!Wp || !q8 || !isums) return MQ_ERR_NULL;
     if (!gemv_shape_ok(rows, cols)) return MQ_ERR_SHAPE;
     if (!aligned16(Wp) || !aligned16(q8) || !aligned16(isums)) return MQ_ERR_ALIGN;
-    const Geom g = make_geom(rows, cols, fmt == 6 ? kQ6kBytes : kQ4kBytes);
+    const Geom g = make_geom(rows, cols, block_bytes(fmt));
     const Plan pl{g.nchunks, 1, 1};  // one chunk per work item
     const Part part{fmt, rows, Wp, (float *)isums};
     GemvLaunch a;
@@ -503,7 +527,8 @@ int subdots_common(int fmt, const void *Wp, const void *q8, int32_t *isums, int 
     if (st != MQ_OK) return st;
     a.part[0].y = nullptr;
     a.isums = isums;
-    return launch_subdots(a, (cudaStream_t)stream) == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+    const cudaError_t e = launch_subdots(a, (cudaStream_t)stream);
+    return e == cudaSuccess ? MQ_OK : cuda_fail("sub-dot launch", e);
 }
 
 }  // namespace
@@ -519,12 +544,14 @@ const char *mq_strerror(int status)
     case MQ_ERR_NULL: return "required pointer is NULL";
     case MQ_ERR_COVERAGE: return "dispatch plan does not cover every chunk exactly once";
     case MQ_ERR_WORKSPACE: return "split-K workspace too small";
-    case MQ_ERR_CUDA: return "CUDA launch failed";
+    case MQ_ERR_CUDA: return "a CUDA call failed (mq_last_error names it)";
     default: return "unknown status";
     }
 }
 
 const char *mq_version(void) { return "mq 0.1 sm_103a"; }
+
+const char *mq_last_error(void) { return g_last_error; }
 
 int mq_device_sms(void) { return device_sms(); }
 
@@ -549,7 +576,7 @@ int mq_quantize_q8(const float *x, void *q8, int n, void *stream)
     const cudaError_t e = launch_quantize_q8(x, (uint8_t *)q8, n, 1, 0, (unsigned)q8_d_offset(n),
                                              (unsigned)q8_sum_offset(n), g_pdl.load(std::memory_order_relaxed),
                                              (cudaStream_t)stream);
-    return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+    return e == cudaSuccess ? MQ_OK : cuda_fail("producer launch", e);
 }
 
 int mq_rmsnorm_quant_q8(const float *x, const float *gain, float eps, float *y, void *q8, int n,
@@ -562,7 +589,7 @@ int mq_rmsnorm_quant_q8(const float *x, const float *gain, float eps, float *y, 
                                                   (unsigned)q8_d_offset(n),
                                                   (unsigned)q8_sum_offset(n), g_pdl.load(std::memory_order_relaxed),
                                              (cudaStream_t)stream);
-    return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+    return e == cudaSuccess ? MQ_OK : cuda_fail("producer launch", e);
 }
 
 int mq_swiglu_quant_q8(const float *g, const float *u, float *y, void *q8, int n, void *stream)
@@ -574,7 +601,7 @@ int mq_swiglu_quant_q8(const float *g, const float *u, float *y, void *q8, int n
                                                  (unsigned)q8_d_offset(n),
                                                  (unsigned)q8_sum_offset(n), g_pdl.load(std::memory_order_relaxed),
                                              (cudaStream_t)stream);
-    return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+    return e == cudaSuccess ? MQ_OK : cuda_fail("producer launch", e);
 }
 
 int mq_check_coverage(int nchunks, int splits, int chunks_per_split)
@@ -599,7 +626,7 @@ int mq_gemv_plan(int rows, int cols, int fmt, int *splits, int *chunks_per_split
                  int *tiles_per_item)
 {
     if (!splits || !chunks_per_split || !tiles_per_item) return MQ_ERR_NULL;
-    if (fmt != 6 && fmt != 4) return MQ_ERR_SHAPE;
+    if (block_bytes(fmt) == 0) return MQ_ERR_SHAPE;
     if (!gemv_shape_ok(rows, cols)) return MQ_ERR_SHAPE;
     Occupancy o;
     if (!device_occupancy(&o, q8_plane_bytes(cols))) return MQ_ERR_CUDA;
@@ -668,7 +695,7 @@ int mq_quantize_q8_batch(const float *x, void *q8, int n, int nt, void *stream)
     const cudaError_t e = launch_quantize_q8(x, (uint8_t *)q8, n, nt, (unsigned)q8_plane_bytes(n),
                                              (unsigned)q8_d_offset(n), (unsigned)q8_sum_offset(n),
                                              g_pdl.load(std::memory_order_relaxed), (cudaStream_t)stream);
-    return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+    return e == cudaSuccess ? MQ_OK : cuda_fail("producer launch", e);
 }
 
 int mq_rmsnorm_quant_q8_batch(const float *x, const float *gain, float eps, float *y, void *q8,
@@ -680,7 +707,7 @@ int mq_rmsnorm_quant_q8_batch(const float *x, const float *gain, float eps, floa
     const cudaError_t e = launch_rmsnorm_quant_q8(
         x, gain, eps, y, (uint8_t *)q8, n, nt, (unsigned)q8_plane_bytes(n), (unsigned)q8_d_offset(n),
         (unsigned)q8_sum_offset(n), g_pdl.load(std::memory_order_relaxed), (cudaStream_t)stream);
-    return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+    return e == cudaSuccess ? MQ_OK : cuda_fail("producer launch", e);
 }
 
 int mq_swiglu_quant_q8_batch(const float *g, const float *u, float *y, void *q8, int n, int nt,
@@ -692,7 +719,7 @@ int mq_swiglu_quant_q8_batch(const float *g, const float *u, float *y, void *q8,
     const cudaError_t e = launch_swiglu_quant_q8(
         g, u, y, (uint8_t *)q8, n, nt, (unsigned)q8_plane_bytes(n), (unsigned)q8_d_offset(n),
         (unsigned)q8_sum_offset(n), g_pdl.load(std::memory_order_relaxed), (cudaStream_t)stream);
-    return e == cudaSuccess ? MQ_OK : MQ_ERR_CUDA;
+    return e == cudaSuccess ? MQ_OK : cuda_fail("producer launch", e);
 }
 
 int mq_gemv_batch_plan(int rows, int cols, int nt, int *splits, int *chunks_per_split,
@@ -740,6 +767,21 @@ int mq_gemv_q4k_q8_batch(const void *Wp, const void *q8, int nt, float *y, int r
 {
     if (nt < 1) return MQ_ERR_SHAPE;
     return gemv_common(4, Wp, q8, y, rows, cols, nullptr, nullptr, 0, stream, nt);
+}
+
+int mq_gemv_q5k_q8_batch(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
+                         void *stream)
+{
+    if (nt < 1) return MQ_ERR_SHAPE;
+    return gemv_common(5, Wp, q8, y, rows, cols, nullptr, nullptr, 0, stream, nt);
+}
+
+int mq_gemv_q5k_q8_batch_plan(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
+                              int splits, int chunks_per_split, int tiles_per_item, void *stream)
+{
+    if (nt < 1) return MQ_ERR_SHAPE;
+    const Plan p{splits, chunks_per_split, tiles_per_item};
+    return gemv_common(5, Wp, q8, y, rows, cols, &p, nullptr, 0, stream, nt);
 }
 
 int mq_gemv_q6k_q8_batch_plan(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
@@ -816,6 +858,27 @@ int mq_gemv_q4k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int 
     if (splits < 1) return MQ_ERR_COVERAGE;
     const Plan p{splits, chunks_per_split, tiles_per_item};
     return gemv_common(4, Wp, q8, y, rows, cols, &p, ws, ws_bytes, stream);
+}
+
+int mq_gemv_q5k_q8(const void *Wp, const void *q8, float *y, int rows, int cols, void *ws,
+                   size_t ws_bytes, void *stream)
+{
+    return gemv_common(5, Wp, q8, y, rows, cols, nullptr, ws, ws_bytes, stream);
+}
+
+int mq_gemv_q5k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int cols, int splits,
+                        int chunks_per_split, int tiles_per_item, void *ws, size_t ws_bytes,
+                        void *stream)
+{
+    if (splits < 1) return MQ_ERR_COVERAGE;
+    const Plan p{splits, chunks_per_split, tiles_per_item};
+    return gemv_common(5, Wp, q8, y, rows, cols, &p, ws, ws_bytes, stream);
+}
+
+int mq_gemv_q5k_q8_subdots(const void *Wp, const void *q8, int32_t *isums, int rows, int cols,
+                           void *stream)
+{
+    return subdots_common(5, Wp, q8, isums, rows, cols, stream);
 }
 
 int mq_gemv_q6k_q8_subdots(const void *Wp, const void *q8, int32_t *isums, int rows, int cols,

@@ -151,8 +151,8 @@ template <int FMT, bool SUBDOTS>
 __device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P, uint8_t *smem,
                                           int item, int u0, int u1, int lane)
 {
-    using Regs = typename std::conditional<FMT == 6, Q6kRegs, Q4kRegs>::type;
-    constexpr int kChunkBytes = (FMT == 6 ? kQ6kChunkPerBlock : kQ4kChunkPerBlock) * kChunkBlocks;
+    using Regs = typename Fmt<FMT>::Regs;
+    constexpr int kChunkBytes = Fmt<FMT>::kChunkBytes;
     const int nch = a.nchunks;
     Regs A, B;
     int t = u0 / nch, c = u0 - t * nch;  // position of the next chunk to load
@@ -225,6 +225,8 @@ __global__ void __launch_bounds__(32 * kMaxCtaSplits, 1)
     }
     if (P.fmt == 6)
         run_range<6, SUBDOTS>(a, P, xs, item, u0, u1, lane);
+    else if (P.fmt == 5)
+        run_range<5, SUBDOTS>(a, P, xs, item, u0, u1, lane);
     else
         run_range<4, SUBDOTS>(a, P, xs, item, u0, u1, lane);
 }
@@ -248,21 +250,24 @@ int gemv_ctas_per_sm(int warps_per_cta, size_t smem)
     int blocks = 0;
     const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         &blocks, gemv_kernel<false>, 32 * warps_per_cta, smem);
+    if (e != cudaSuccess) cuda_fail("GEMV occupancy", e);
     return e == cudaSuccess ? blocks : 0;
 }
 
 size_t gemv_max_plane_bytes()
 {
     int dev = 0, optin = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-        return 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     const int limit = optin - 1024;  // room for the kernel's static shared memory
-    if (cudaFuncSetAttribute(gemv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(gemv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) !=
-            cudaSuccess)
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+    if (e != cudaSuccess) {
+        cuda_fail("GEMV shared-memory opt-in", e);
         return 0;
+    }
     return (size_t)limit & ~(size_t)15;
 }
 

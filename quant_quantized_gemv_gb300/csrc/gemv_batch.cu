@@ -124,20 +124,17 @@ __device__ __forceinline__ void compute_group(const Q6kW &W, const XCodes<G> &X,
     }
 }
 
-// q4_K: the unit is one 32-weight sub-block; term = d*sc*isum - dmin*m*qsum.
-template <int NT, int G>
-__device__ __forceinline__ void compute_group(const Q4kW &W, const XCodes<G> &X, int t0,
+// q4_K / q5_K: the unit is one 32-weight sub-block; term = d*sc*isum -
+// dmin*m*qsum.
+template <int NT, int G, class Q4like>
+__device__ __forceinline__ void compute_group(const Q4like &W, const XCodes<G> &X, int t0,
                                               float (&out)[G][8])
 {
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
         uint32_t lo[4], hi[4];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const uint32_t w = word(W.qs[r], m);
-            lo[m] = w & kLo4;
-            hi[m] = (w >> 4) & kLo4;
-        }
+        for (int m = 0; m < 4; ++m) codes(W, r, m, lo[m], hi[m]);
         int sc, mn;
         float d, dmin;
         q4k_scales(W, r, sc, mn, d, dmin);
@@ -158,9 +155,7 @@ __device__ __forceinline__ void compute_group(const Q4kW &W, const XCodes<G> &X,
 
 template <int FMT, int NT>
 __device__ __forceinline__ void compute(const GemvLaunch &a, const uint8_t *xs, const Unit &x,
-                                        int lane,
-                                        const typename std::conditional<FMT == 6, Q6kW, Q4kW>::type &W,
-                                        Acc<NT> &acc)
+                                        int lane, const typename Fmt<FMT>::W &W, Acc<NT> &acc)
 {
     constexpr int G = group_size(NT);
     if constexpr (!Acc<NT>::kEach) {  // one group: accumulate straight into the per-lane partials
@@ -278,8 +273,8 @@ constexpr bool kTwoBuffers = NT == 1;
 template <int FMT, int NT>
 __device__ __forceinline__ void run_batch(const GemvLaunch &a, const GemvPart &P, uint8_t *xs, int lane)
 {
-    using W = typename std::conditional<FMT == 6, Q6kW, Q4kW>::type;
-    constexpr int kChunkBytes = (FMT == 6 ? kQ6kChunkPerBlock : kQ4kChunkPerBlock) * kChunkBlocks;
+    using W = typename Fmt<FMT>::W;
+    constexpr int kChunkBytes = Fmt<FMT>::kChunkBytes;
     const int S = a.splits, G = kBatchMaxCtaSplits / S;
     const int w = threadIdx.x >> 5, sp = w % S, o = w / S;
     const int c_lo = sp * a.cps, c_hi = min(c_lo + a.cps, a.nchunks);
@@ -357,41 +352,37 @@ __device__ __forceinline__ void run_batch(const GemvLaunch &a, const GemvPart &P
     }
 }
 
-template <int NT>
+// One kernel per (tokens, format): each gets its own register allocation.
+template <int NT, int FMT>
 __global__ void __launch_bounds__(32 * kBatchMaxCtaSplits, 1)
     gemv_batch_kernel(const __grid_constant__ GemvLaunch a)
 {
     extern __shared__ __align__(16) uint8_t xs[];  // the nt q8 planes
     const int lane = threadIdx.x & 31;
     griddep_launch_dependents();
-    const GemvPart &P = a.part[0];
-    if (P.fmt == 6)
-        run_batch<6, NT>(a, P, xs, lane);
-    else
-        run_batch<4, NT>(a, P, xs, lane);
-}
-
-template <int NT>
-cudaError_t launch_nt(const GemvLaunch &a, cudaStream_t st)
-{
-    const int warps = gemv_batch_cta_warps(a.splits);
-    return launch_maybe_pdl(gemv_batch_kernel<NT>, dim3((unsigned)a.n_items), dim3(32 * warps),
-                            (size_t)a.nt * a.q8_bytes, a.pdl, st, a);
+    run_batch<FMT, NT>(a, a.part[0], xs, lane);
 }
 
 using KernelFn = void (*)(GemvLaunch);
 
-KernelFn kernel_for(int nt)
+template <int NT>
+KernelFn kernel_of_fmt(int fmt)
+{
+    return fmt == 6 ? gemv_batch_kernel<NT, 6> : fmt == 5 ? gemv_batch_kernel<NT, 5>
+         : fmt == 4 ? gemv_batch_kernel<NT, 4> : nullptr;
+}
+
+KernelFn kernel_for(int nt, int fmt)
 {
     switch (nt) {
-    case 1: return gemv_batch_kernel<1>;
-    case 2: return gemv_batch_kernel<2>;
-    case 3: return gemv_batch_kernel<3>;
-    case 4: return gemv_batch_kernel<4>;
-    case 5: return gemv_batch_kernel<5>;
-    case 6: return gemv_batch_kernel<6>;
-    case 7: return gemv_batch_kernel<7>;
-    case 8: return gemv_batch_kernel<8>;
+    case 1: return kernel_of_fmt<1>(fmt);
+    case 2: return kernel_of_fmt<2>(fmt);
+    case 3: return kernel_of_fmt<3>(fmt);
+    case 4: return kernel_of_fmt<4>(fmt);
+    case 5: return kernel_of_fmt<5>(fmt);
+    case 6: return kernel_of_fmt<6>(fmt);
+    case 7: return kernel_of_fmt<7>(fmt);
+    case 8: return kernel_of_fmt<8>(fmt);
     default: return nullptr;
     }
 }
@@ -400,40 +391,39 @@ KernelFn kernel_for(int nt)
 
 cudaError_t launch_gemv_batch(const GemvLaunch &a, cudaStream_t st)
 {
-    switch (a.nt) {
-    case 1: return launch_nt<1>(a, st);
-    case 2: return launch_nt<2>(a, st);
-    case 3: return launch_nt<3>(a, st);
-    case 4: return launch_nt<4>(a, st);
-    case 5: return launch_nt<5>(a, st);
-    case 6: return launch_nt<6>(a, st);
-    case 7: return launch_nt<7>(a, st);
-    case 8: return launch_nt<8>(a, st);
-    default: return cudaErrorInvalidValue;
-    }
+    const KernelFn k = kernel_for(a.nt, a.part[0].fmt);
+    if (!k) return cudaErrorInvalidValue;
+    const int warps = gemv_batch_cta_warps(a.splits);
+    return launch_maybe_pdl(k, dim3((unsigned)a.n_items), dim3(32 * warps),
+                            (size_t)a.nt * a.q8_bytes, a.pdl, st, a);
 }
 
-int gemv_batch_ctas_per_sm(int nt, int warps_per_cta, size_t smem)
+int gemv_batch_ctas_per_sm(int nt, int fmt, int warps_per_cta, size_t smem)
 {
-    const KernelFn k = kernel_for(nt);
+    const KernelFn k = kernel_for(nt, fmt);
     int blocks = 0;
     if (!k) return 0;
     const cudaError_t e =
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k, 32 * warps_per_cta, smem);
+    if (e != cudaSuccess) cuda_fail("small-batch GEMV occupancy", e);
     return e == cudaSuccess ? blocks : 0;
 }
 
 size_t gemv_batch_max_smem()
 {
     int dev = 0, optin = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-        return 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     const int limit = optin - 8192;  // room for the split-exchange buffers
-    for (int nt = 1; nt <= kMaxTokens; ++nt)
-        if (cudaFuncSetAttribute(kernel_for(nt), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 limit) != cudaSuccess)
-            return 0;
+    for (int nt = 1; nt <= kMaxTokens && e == cudaSuccess; ++nt)
+        for (int fmt : {6, 4, 5})
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(kernel_for(nt, fmt), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         limit);
+    if (e != cudaSuccess) {
+        cuda_fail("small-batch GEMV shared-memory opt-in", e);
+        return 0;
+    }
     return (size_t)limit & ~(size_t)15;
 }
 

@@ -133,17 +133,19 @@ struct Q4kW {
     uint32_t s0, s1, s2;         // 6-bit scales and mins of 8 rows, packed
 };
 
-__device__ __forceinline__ void load_w(const Unit &x, int lane, Q4kW &R)
+// The QS, SM and DM planes (q4_K, and q5_K at other SM / DM offsets).
+template <int SM, int DM>
+__device__ __forceinline__ void load_w_q4like(const Unit &x, int lane, Q4kW &R)
 {
     const int nu = 8 * x.cb, cb = x.cb;
     if (x.active) {
 #pragma unroll
         for (int r = 0; r < 8; ++r) R.qs[r] = ld_stream16(x.seg + ((size_t)r * nu + lane) * 16);
-        const uint8_t *smp = x.seg + (size_t)kQ4kSM * cb + (size_t)lane * 4;
+        const uint8_t *smp = x.seg + (size_t)SM * cb + (size_t)lane * 4;
         R.s0 = ld_stream4(smp);
         R.s1 = ld_stream4(smp + (size_t)nu * 4);
         R.s2 = ld_stream4(smp + (size_t)nu * 8);
-        const uint8_t *dmp = x.seg + (size_t)kQ4kDM * cb + (size_t)(lane >> 3) * 32;
+        const uint8_t *dmp = x.seg + (size_t)DM * cb + (size_t)(lane >> 3) * 32;
         R.dm0 = ld_stream16(dmp);
         R.dm1 = ld_stream16(dmp + 16);
     } else {
@@ -152,6 +154,20 @@ __device__ __forceinline__ void load_w(const Unit &x, int lane, Q4kW &R)
         R.s0 = R.s1 = R.s2 = 0;
         R.dm0 = R.dm1 = make_uint4(0, 0, 0, 0);
     }
+}
+
+__device__ __forceinline__ void load_w(const Unit &x, int lane, Q4kW &R)
+{
+    load_w_q4like<kQ4kSM, kQ4kDM>(x, lane, R);
+}
+
+// Row r's codes for words m of the unit: weights 4m..4m+3 (lo, against the
+// activation codes xa) and 16+4m..16+4m+3 (hi, against xb), one per byte.
+__device__ __forceinline__ void codes(const Q4kW &R, int r, int m, uint32_t &lo, uint32_t &hi)
+{
+    const uint32_t w = word(R.qs[r], m);
+    lo = w & kLo4;
+    hi = (w >> 4) & kLo4;
 }
 
 // Row r's 6-bit scale and min and fp16 d, dmin.
@@ -164,6 +180,32 @@ __device__ __forceinline__ void q4k_scales(const Q4kW &R, int r, int &sc, int &m
     const uint32_t dmw = word(r < 4 ? R.dm0 : R.dm1, r & 3);
     d = half_lo(dmw);
     dmin = half_hi(dmw);
+}
+
+// ---- q5_K: q4_K's fields plus each code's fifth bit -------------------------
+struct Q5kW : Q4kW {
+    uint4 qh[2];  // fifth-bit words H of rows 0..3 and 4..7
+};
+
+__device__ __forceinline__ void load_w(const Unit &x, int lane, Q5kW &R)
+{
+    load_w_q4like<kQ5kSM, kQ5kDM>(x, lane, R);
+    if (x.active) {
+        const uint8_t *hp = x.seg + (size_t)kQ5kQH * x.cb + (size_t)lane * 32;
+        R.qh[0] = ld_stream16(hp);
+        R.qh[1] = ld_stream16(hp + 16);
+    } else {
+        R.qh[0] = R.qh[1] = make_uint4(0, 0, 0, 0);
+    }
+}
+
+// As for q4_K, with bit 4 of every byte taken from the fifth-bit word.
+__device__ __forceinline__ void codes(const Q5kW &R, int r, int m, uint32_t &lo, uint32_t &hi)
+{
+    const uint32_t H = word(R.qh[r >> 2], r & 3);
+    const uint32_t w = word(R.qs[r], m);
+    lo = (w & kLo4) | (((H >> m) & 0x01010101u) << 4);
+    hi = ((w >> 4) & kLo4) | (((H >> (m + 4)) & 0x01010101u) << 4);
 }
 
 // ---- single-token activation codes and chunk compute ------------------------
@@ -235,15 +277,17 @@ __device__ __forceinline__ void compute(const GemvLaunch &a, const GemvPart &P, 
     }
 }
 
-// ---- q4_K ------------------------------------------------------------------
-struct Q4kRegs : Q4kW {
+// ---- q4_K and q5_K -----------------------------------------------------------
+struct XSum {                    // the unit's activation codes, scale and code sum
     uint4 xa, xb;
     unsigned short dh;
     int qsum;
 };
+struct Q4kRegs : Q4kW, XSum {};
+struct Q5kRegs : Q5kW, XSum {};
 
 __device__ __forceinline__ void load_x(const GemvLaunch &a, const uint8_t *xs, const Unit &x,
-                                       int lane, Q4kRegs &R)
+                                       int lane, XSum &R)
 {
     if (x.active) {
         const int U = 32 * x.c + lane;
@@ -267,9 +311,12 @@ __device__ __forceinline__ void load_x(const GemvLaunch &a, const uint8_t *xs, c
     }
 }
 
-template <bool SUBDOTS>
-__device__ __forceinline__ void compute(const GemvLaunch &a, const GemvPart &P, const Q4kRegs &R,
-                                        const Unit &x, int lane, float (&acc)[8])
+// q4_K / q5_K: the unit is one 32-weight sub-block; term = d*sc*isum -
+// dmin*m*qsum (qsum = the q8 block's code sum).
+template <bool SUBDOTS, class Regs>
+__device__ __forceinline__ void compute_q4like(const GemvLaunch &a, const GemvPart &P,
+                                               const Regs &R, const Unit &x, int lane,
+                                               float (&acc)[8])
 {
     const float d8 = __half2float(__ushort_as_half(R.dh));
 #pragma unroll
@@ -277,9 +324,10 @@ __device__ __forceinline__ void compute(const GemvLaunch &a, const GemvPart &P, 
         int dot = 0;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            const uint32_t w = word(R.qs[r], m);
-            dot = __dp4a((int)(w & kLo4), (int)word(R.xa, m), dot);
-            dot = __dp4a((int)((w >> 4) & kLo4), (int)word(R.xb, m), dot);
+            uint32_t lo, hi;
+            codes(R, r, m, lo, hi);
+            dot = __dp4a((int)lo, (int)word(R.xa, m), dot);
+            dot = __dp4a((int)hi, (int)word(R.xb, m), dot);
         }
         if (SUBDOTS) {
             const int row = x.t * kTileRows + r;
@@ -296,6 +344,43 @@ __device__ __forceinline__ void compute(const GemvLaunch &a, const GemvPart &P, 
         }
     }
 }
+
+template <bool SUBDOTS>
+__device__ __forceinline__ void compute(const GemvLaunch &a, const GemvPart &P, const Q4kRegs &R,
+                                        const Unit &x, int lane, float (&acc)[8])
+{
+    compute_q4like<SUBDOTS>(a, P, R, x, lane, acc);
+}
+
+template <bool SUBDOTS>
+__device__ __forceinline__ void compute(const GemvLaunch &a, const GemvPart &P, const Q5kRegs &R,
+                                        const Unit &x, int lane, float (&acc)[8])
+{
+    compute_q4like<SUBDOTS>(a, P, R, x, lane, acc);
+}
+
+// Per format code (6, 4, 5): the register set of one chunk and the bytes of
+// a full chunk.
+template <int FMT>
+struct Fmt;
+template <>
+struct Fmt<6> {
+    using Regs = Q6kRegs;
+    using W = Q6kW;
+    static constexpr int kChunkBytes = kQ6kChunkPerBlock * kChunkBlocks;
+};
+template <>
+struct Fmt<4> {
+    using Regs = Q4kRegs;
+    using W = Q4kW;
+    static constexpr int kChunkBytes = kQ4kChunkPerBlock * kChunkBlocks;
+};
+template <>
+struct Fmt<5> {
+    using Regs = Q5kRegs;
+    using W = Q5kW;
+    static constexpr int kChunkBytes = kQ5kChunkPerBlock * kChunkBlocks;
+};
 
 // Reduce acc[0..7] over the 32 lanes; returns the sum of row (lane >> 2) in
 // every lane (the 4 lanes of a group hold the same value).

@@ -68,12 +68,14 @@ __device__ __forceinline__ void quantize_block(float v, const GateUpLaunch &L, i
     }
 }
 
+// sums: [block parity][tile of the block][row] row sums, in the kernel's
+// shared memory (one array for every format instance of this function).
 template <int FMT>
-__device__ __forceinline__ void run_gateup(const GateUpLaunch &L, uint8_t *xs, int lane)
+__device__ __forceinline__ void run_gateup(const GateUpLaunch &L, uint8_t *xs, float (*sums)[8][8],
+                                           int lane)
 {
-    using Regs = typename std::conditional<FMT == 6, Q6kRegs, Q4kRegs>::type;
-    constexpr int kChunkBytes = (FMT == 6 ? kQ6kChunkPerBlock : kQ4kChunkPerBlock) * kChunkBlocks;
-    __shared__ float sums[2][8][8];  // [block parity][tile of the block][row]
+    using Regs = typename Fmt<FMT>::Regs;
+    constexpr int kChunkBytes = Fmt<FMT>::kChunkBytes;
     const GemvLaunch &a = L.g;
     const int W = blockDim.x >> 5, w = threadIdx.x >> 5;
     const int nch = a.nchunks;
@@ -158,12 +160,15 @@ __global__ void __launch_bounds__(32 * kMaxCtaSplits, 1)
     gateup_kernel(const __grid_constant__ GateUpLaunch L)
 {
     extern __shared__ __align__(16) uint8_t xs[];  // the q8 plane
+    __shared__ float sums[2][8][8];
     griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     if (L.g.part[0].fmt == 6)
-        run_gateup<6>(L, xs, lane);
+        run_gateup<6>(L, xs, sums, lane);
+    else if (L.g.part[0].fmt == 5)
+        run_gateup<5>(L, xs, sums, lane);
     else
-        run_gateup<4>(L, xs, lane);
+        run_gateup<4>(L, xs, sums, lane);
 }
 
 }  // namespace
@@ -179,13 +184,16 @@ int gateup_ctas_per_sm(int warps_per_cta, size_t smem)
     int blocks = 0;
     const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         &blocks, gateup_kernel, 32 * warps_per_cta, smem);
+    if (e != cudaSuccess) cuda_fail("gate||up occupancy", e);
     return e == cudaSuccess ? blocks : 0;
 }
 
 bool gateup_opt_in(size_t max_plane)
 {
-    return cudaFuncSetAttribute(gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)max_plane) == cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(
+        gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_plane);
+    if (e != cudaSuccess) cuda_fail("gate||up shared-memory opt-in", e);
+    return e == cudaSuccess;
 }
 
 }  // namespace mq

@@ -92,9 +92,10 @@ inline int gemv_batch_cta_warps(int splits)
     return splits * (kBatchMaxCtaSplits / splits);
 }
 
-// Resident CTAs per SM of the small-batch kernel for nt tokens (0 on error),
-// and the largest dynamic shared memory (all nt planes) it accepts.
-int gemv_batch_ctas_per_sm(int nt, int warps_per_cta, size_t smem);
+// Resident CTAs per SM of the small-batch kernel for nt tokens of format
+// fmt (0 on error), and the largest dynamic shared memory (all nt planes)
+// the small-batch kernels accept.
+int gemv_batch_ctas_per_sm(int nt, int fmt, int warps_per_cta, size_t smem);
 size_t gemv_batch_max_smem();
 
 // Resident CTAs per SM of the GEMV kernel with `warps_per_cta` warps and
@@ -116,6 +117,10 @@ cudaError_t launch_rmsnorm_quant_q8(const float *x, const float *gain, float eps
 cudaError_t launch_swiglu_quant_q8(const float *g, const float *u, float *y, uint8_t *q8, int n,
                                    int rows, unsigned stride, unsigned d_off, unsigned sum_off,
                                    int pdl, cudaStream_t st);
+
+// Record the library's last CUDA failure on this thread (`where` and the CUDA
+// error, readable with mq_last_error); returns MQ_ERR_CUDA.
+int cuda_fail(const char *where, cudaError_t e);
 
 // Launch `kernel` on `st`, with programmatic stream serialization when pdl
 // is set (the kernel then may start before its predecessor in the stream

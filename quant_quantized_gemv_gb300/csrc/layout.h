@@ -1,5 +1,5 @@
 // layout.h -- the repacked weight layout and the q8 plane layout, shared by
-// the host repack (repack.cpp) and the GEMV kernels (gemv.cu).  Internal to
+// the host repack (repack.cpp) and the GEMV kernels.  Internal to
 // the library; callers see only sizes (include/mq.h).
 //
 // Why a new layout.  The minfer pages (page "76 · D4-4 — dpl dense
@@ -36,9 +36,17 @@
 //                 word1 bits 4r.. = m_r & 15, word2 bits 4r,4r+1 = sc_r >> 4
 //                 and bits 4r+2,4r+3 = m_r >> 4   (r = row within the tile)
 //   DM  @1120*cb  [block cb][row 8][d fp16, dmin fp16]
+// q5_K chunk (1408*cb bytes): q4_K's planes plus the fifth bits
+//   QS  @0        as q4_K (low 4 bits of each code)
+//   QH  @1024*cb  [unit nu][row 8][4 B]  word H of (unit, row): bit
+//                 8b + 4h + m = fifth bit of weight 16h + 4m + b, so that
+//                 ((H >> m) & 0x01010101) << 4 lines up with the low-nibble
+//                 word m and ((H >> (m+4)) & 0x01010101) << 4 with the high
+//   SM  @1280*cb  as q4_K
+//   DM  @1376*cb  as q4_K
 // Every plane offset and every per-lane load address is 16-byte aligned for
-// QL/QH/QS/D/DM and 4-byte aligned for SM, because 8 rows x 210 B and
-// 8 rows x 144 B are both multiples of 16.
+// QL/QH/QS/D/DM and 4-byte aligned for SM, because 8 rows x 210 B,
+// 8 rows x 144 B and 8 rows x 176 B are all multiples of 16.
 #pragma once
 #include <stddef.h>
 #include <stdint.h>
@@ -50,11 +58,21 @@ constexpr int kTileRows = 8;       // rows per tile
 constexpr int kChunkBlocks = 4;    // super-blocks per chunk (32 units)
 constexpr int kQ6kBytes = 210;
 constexpr int kQ4kBytes = 144;
+constexpr int kQ5kBytes = 176;
 
 // q6_K chunk plane offsets, per block of the chunk (multiply by cb)
 constexpr int kQ6kQH = 1024, kQ6kSC = 1536, kQ6kD = 1664, kQ6kChunkPerBlock = 1680;
 // q4_K chunk plane offsets, per block of the chunk (multiply by cb)
 constexpr int kQ4kSM = 1024, kQ4kDM = 1120, kQ4kChunkPerBlock = 1152;
+// q5_K chunk plane offsets, per block of the chunk (multiply by cb)
+constexpr int kQ5kQH = 1024, kQ5kSM = 1280, kQ5kDM = 1376, kQ5kChunkPerBlock = 1408;
+
+// Bytes of one super-block (= per block of a chunk / 8 rows) by format code
+// (6 = q6_K, 4 = q4_K, 5 = q5_K); 0 for an unknown code.
+constexpr int block_bytes(int fmt)
+{
+    return fmt == 6 ? kQ6kBytes : fmt == 4 ? kQ4kBytes : fmt == 5 ? kQ5kBytes : 0;
+}
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 

@@ -44,11 +44,15 @@ void *g_scratch_addr[kMaxDev];  // device address of the array, per device
 int scratch_address(void **out)
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return MQ_ERR_CUDA;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+    if (dev < 0 || dev >= kMaxDev) return MQ_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     if (!g_scratch_addr[dev]) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MQ_ERR_CUDA;
+        const cudaError_t e2 = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e2 != cudaSuccess) return cuda_fail("cudaGetSymbolAddress(scratch)", e2);
+        if (!p) return MQ_ERR_CUDA;
         g_scratch_addr[dev] = p;
     }
     *out = g_scratch_addr[dev];
@@ -77,7 +81,8 @@ extern "C" int mq_gemv_q6k_q8_noalloc(const void *Wp, const void *q8, float *y, 
     // The counters must start at zero; a finished call leaves them at zero,
     // but clear them anyway so that an interrupted earlier call cannot leak.
     const size_t counter_bytes = round16((size_t)ceil_div(rows, kTileRows) * 4);
-    if (cudaMemsetAsync(ws, 0, counter_bytes, (cudaStream_t)stream) != cudaSuccess) return MQ_ERR_CUDA;
+    const cudaError_t e = cudaMemsetAsync(ws, 0, counter_bytes, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail("clearing the scratch counters", e);
     return mq_gemv_q6k_q8_plan(Wp, q8, y, rows, cols, splits, cps, tpi, ws, kNoAllocScratchBytes,
                                stream);
 }

@@ -1,4 +1,4 @@
-// repack.cpp -- host repack of GGUF q6_K / q4_K rows into the tile/chunk/plane
+// repack.cpp -- host repack of GGUF q6_K / q4_K / q5_K rows into the tile/chunk/plane
 // layout of layout.h, and its exact inverse.  Runs once per weight at load
 // (page "76 · D4-4 — dpl dense split-plane q6_K decode MMVQ", §3.1: the plane
 // is built once at registration, so decode pays nothing for it).
@@ -36,6 +36,8 @@ inline void q6k_put(uint8_t *blk, int p, int l, int lo, int hi)
 }
 
 // ---- q4_K source decode (GGUF block: d 2 | dmin 2 | scales 12 | qs 128) ---
+// Weight l of sub-block k is the low (k even) or high (k odd) nibble of
+// qs[32 * (k/2) + l]; the 6-bit scale and min of k are packed in 12 bytes.
 inline void q4k_get_sm(const uint8_t *s, int k, int *sc, int *m)
 {
     if (k < 4) {
@@ -57,10 +59,60 @@ inline void q4k_put_sm(uint8_t *s, int k, int sc, int m)
         s[k] |= (uint8_t)((m >> 4) << 6);
     }
 }
-inline int q4k_nib(const uint8_t *blk, int k, int l)
+// ---- q5_K source decode (GGUF block: d 2 | dmin 2 | scales 12 | qh 32 | qs 128)
+// Weight l of sub-block k: low 4 bits as q4_K (nibbles from qs @48), fifth
+// bit = bit k of qh[l].
+inline int q5k_bit(const uint8_t *blk, int k, int l) { return (blk[16 + l] >> k) & 1; }
+
+// Bit position, in the fifth-bit word H of a unit and row, of weight l
+// (= 16h + 4m + b) of the unit: 8b + 4h + m (layout.h).
+inline int q5k_hpos(int l) { return 8 * (l & 3) + 4 * (l >> 4) + ((l >> 2) & 3); }
+
+// The QS / SM / DM planes of a q4_K or q5_K unit (SM, DM: plane offsets).
+void put_q4like(uint8_t *out, size_t seg, int cb, int r, int i, const uint8_t *blk, int sm_off,
+                int dm_off, int nib_off)
 {
-    const uint8_t b = blk[16 + 32 * (k >> 1) + l];
-    return (k & 1) ? (b >> 4) : (b & 15);
+    const int nu = 8 * cb, k = i & 7;
+    uint8_t *qs = out + seg + ((size_t)r * nu + i) * 16;
+    for (int t = 0; t < 16; ++t) {
+        const uint8_t lo = blk[nib_off + 32 * (k >> 1) + t], hi = blk[nib_off + 32 * (k >> 1) + 16 + t];
+        qs[t] = (uint8_t)(((k & 1) ? lo >> 4 : lo & 15) | (((k & 1) ? hi >> 4 : hi & 15) << 4));
+    }
+    int sc, m;
+    q4k_get_sm(blk + 4, k, &sc, &m);
+    uint32_t w[3];
+    uint8_t *smp = out + seg + (size_t)sm_off * cb;
+    for (int j = 0; j < 3; ++j) memcpy(&w[j], smp + ((size_t)j * nu + i) * 4, 4);
+    w[0] |= (uint32_t)(sc & 15) << (4 * r);
+    w[1] |= (uint32_t)(m & 15) << (4 * r);
+    w[2] |= (uint32_t)((sc >> 4) | ((m >> 4) << 2)) << (4 * r);
+    for (int j = 0; j < 3; ++j) memcpy(smp + ((size_t)j * nu + i) * 4, &w[j], 4);
+    if (k == 0) {
+        uint8_t *dm = out + seg + (size_t)dm_off * cb + (size_t)(i >> 3) * 32 + r * 4;
+        memcpy(dm, blk, 4);
+    }
+}
+
+void get_q4like(const uint8_t *in, size_t seg, int cb, int r, int i, uint8_t *blk, int sm_off,
+                int dm_off, int nib_off)
+{
+    const int nu = 8 * cb, k = i & 7;
+    const uint8_t *qs = in + seg + ((size_t)r * nu + i) * 16;
+    for (int l = 0; l < 32; ++l) {
+        const int v = l < 16 ? (qs[l] & 15) : (qs[l - 16] >> 4);
+        blk[nib_off + 32 * (k >> 1) + l] |= (uint8_t)((k & 1) ? v << 4 : v);
+    }
+    uint32_t w[3];
+    const uint8_t *smp = in + seg + (size_t)sm_off * cb;
+    for (int j = 0; j < 3; ++j) memcpy(&w[j], smp + ((size_t)j * nu + i) * 4, 4);
+    const int hi = (w[2] >> (4 * r)) & 15;
+    const int sc = (int)((w[0] >> (4 * r)) & 15) | ((hi & 3) << 4);
+    const int m = (int)((w[1] >> (4 * r)) & 15) | ((hi >> 2) << 4);
+    q4k_put_sm(blk + 4, k, sc, m);
+    if (k == 0) {
+        const uint8_t *dm = in + seg + (size_t)dm_off * cb + (size_t)(i >> 3) * 32 + r * 4;
+        memcpy(blk, dm, 4);
+    }
 }
 
 bool shape_ok(int rows, int cols)
@@ -180,23 +232,7 @@ int mq_repack_q4k(const void *gguf, void *dst, int rows, int cols)
     memset(out, 0, (size_t)g.ntiles * g.tile_bytes);
     for_each_unit(g, kQ4kBytes, [&](size_t seg, int cb, int r, int row, int b, int i) {
         const uint8_t *blk = src + ((size_t)row * g.nb + b) * kQ4kBytes;
-        const int nu = 8 * cb, k = i & 7;
-        uint8_t *qs = out + seg + ((size_t)r * nu + i) * 16;
-        for (int t = 0; t < 16; ++t)
-            qs[t] = (uint8_t)(q4k_nib(blk, k, t) | (q4k_nib(blk, k, 16 + t) << 4));
-        int sc, m;
-        q4k_get_sm(blk + 4, k, &sc, &m);
-        uint32_t w[3];
-        uint8_t *smp = out + seg + (size_t)kQ4kSM * cb;
-        for (int j = 0; j < 3; ++j) memcpy(&w[j], smp + ((size_t)j * nu + i) * 4, 4);
-        w[0] |= (uint32_t)(sc & 15) << (4 * r);
-        w[1] |= (uint32_t)(m & 15) << (4 * r);
-        w[2] |= (uint32_t)((sc >> 4) | ((m >> 4) << 2)) << (4 * r);
-        for (int j = 0; j < 3; ++j) memcpy(smp + ((size_t)j * nu + i) * 4, &w[j], 4);
-        if (k == 0) {
-            uint8_t *dm = out + seg + (size_t)kQ4kDM * cb + (size_t)(i >> 3) * 32 + r * 4;
-            memcpy(dm, blk, 4);
-        }
+        put_q4like(out, seg, cb, r, i, blk, kQ4kSM, kQ4kDM, 16);
     });
     return MQ_OK;
 }
@@ -211,23 +247,52 @@ int mq_unrepack_q4k(const void *packed, void *gguf, int rows, int cols)
     memset(dst, 0, (size_t)rows * g.nb * kQ4kBytes);
     for_each_unit(g, kQ4kBytes, [&](size_t seg, int cb, int r, int row, int b, int i) {
         uint8_t *blk = dst + ((size_t)row * g.nb + b) * kQ4kBytes;
-        const int nu = 8 * cb, k = i & 7;
-        const uint8_t *qs = in + seg + ((size_t)r * nu + i) * 16;
-        for (int l = 0; l < 32; ++l) {
-            const int v = l < 16 ? (qs[l] & 15) : (qs[l - 16] >> 4);
-            blk[16 + 32 * (k >> 1) + l] |= (uint8_t)((k & 1) ? v << 4 : v);
-        }
-        uint32_t w[3];
-        const uint8_t *smp = in + seg + (size_t)kQ4kSM * cb;
-        for (int j = 0; j < 3; ++j) memcpy(&w[j], smp + ((size_t)j * nu + i) * 4, 4);
-        const int hi = (w[2] >> (4 * r)) & 15;
-        const int sc = (int)((w[0] >> (4 * r)) & 15) | ((hi & 3) << 4);
-        const int m = (int)((w[1] >> (4 * r)) & 15) | ((hi >> 2) << 4);
-        q4k_put_sm(blk + 4, k, sc, m);
-        if (k == 0) {
-            const uint8_t *dm = in + seg + (size_t)kQ4kDM * cb + (size_t)(i >> 3) * 32 + r * 4;
-            memcpy(blk, dm, 4);
-        }
+        get_q4like(in, seg, cb, r, i, blk, kQ4kSM, kQ4kDM, 16);
+    });
+    return MQ_OK;
+}
+
+size_t mq_repacked_bytes_q5k(int rows, int cols)
+{
+    if (!shape_ok(rows, cols)) return 0;
+    const Geom g = make_geom(rows, cols, kQ5kBytes);
+    return (size_t)g.ntiles * g.tile_bytes;
+}
+
+int mq_repack_q5k(const void *gguf, void *dst, int rows, int cols)
+{
+    if (!gguf || !dst) return MQ_ERR_NULL;
+    if (!shape_ok(rows, cols)) return MQ_ERR_SHAPE;
+    const Geom g = make_geom(rows, cols, kQ5kBytes);
+    const uint8_t *src = (const uint8_t *)gguf;
+    uint8_t *out = (uint8_t *)dst;
+    memset(out, 0, (size_t)g.ntiles * g.tile_bytes);
+    for_each_unit(g, kQ5kBytes, [&](size_t seg, int cb, int r, int row, int b, int i) {
+        const uint8_t *blk = src + ((size_t)row * g.nb + b) * kQ5kBytes;
+        put_q4like(out, seg, cb, r, i, blk, kQ5kSM, kQ5kDM, 48);
+        const int k = i & 7;
+        uint32_t H = 0;
+        for (int l = 0; l < 32; ++l) H |= (uint32_t)q5k_bit(blk, k, l) << q5k_hpos(l);
+        memcpy(out + seg + (size_t)kQ5kQH * cb + ((size_t)i * 8 + r) * 4, &H, 4);
+    });
+    return MQ_OK;
+}
+
+int mq_unrepack_q5k(const void *packed, void *gguf, int rows, int cols)
+{
+    if (!gguf || !packed) return MQ_ERR_NULL;
+    if (!shape_ok(rows, cols)) return MQ_ERR_SHAPE;
+    const Geom g = make_geom(rows, cols, kQ5kBytes);
+    const uint8_t *in = (const uint8_t *)packed;
+    uint8_t *dst = (uint8_t *)gguf;
+    memset(dst, 0, (size_t)rows * g.nb * kQ5kBytes);
+    for_each_unit(g, kQ5kBytes, [&](size_t seg, int cb, int r, int row, int b, int i) {
+        uint8_t *blk = dst + ((size_t)row * g.nb + b) * kQ5kBytes;
+        get_q4like(in, seg, cb, r, i, blk, kQ5kSM, kQ5kDM, 48);
+        const int k = i & 7;
+        uint32_t H;
+        memcpy(&H, in + seg + (size_t)kQ5kQH * cb + ((size_t)i * 8 + r) * 4, 4);
+        for (int l = 0; l < 32; ++l) blk[16 + l] |= (uint8_t)(((H >> q5k_hpos(l)) & 1) << k);
     });
     return MQ_OK;
 }

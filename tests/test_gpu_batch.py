@@ -66,14 +66,13 @@ def assert_close(y, yref, absum):
 def make(mq, fmt, rows, cols, nt, seed):
     g = synth.rng("batch", fmt, rows, cols, nt, seed)
     W = synth.blocks(fmt, g, rows, cols)
-    rep = mq.mq_repack_q6k if fmt == "q6k" else mq.mq_repack_q4k
-    Wp = dev(rep(W, rows, cols))
+    Wp = dev(mq.mq_repack(fmt, W, rows, cols))
     x = np.stack([synth.normal(g, cols) for _ in range(nt)]).astype(np.float32)
     return W, Wp, x
 
 
 def batch_fn(mq, fmt):
-    return mq.mq_gemv_q6k_q8_batch if fmt == "q6k" else mq.mq_gemv_q4k_q8_batch
+    return getattr(mq, f"mq_gemv_{fmt}_q8_batch")
 
 
 # ------------------------------------------------------------------ producers
@@ -142,7 +141,7 @@ def test_batch_producer_row_equals_single_row_call(mq):
 SHAPES = [(37, 4608), (64, 18944), (9, 1280), (8, 256), (200, 5120)]
 
 
-@pytest.mark.parametrize("fmt", ["q6k", "q4k"])
+@pytest.mark.parametrize("fmt", ["q6k", "q4k", "q5k"])
 @pytest.mark.parametrize("nt", [1, 2, 3, 4, 5, 8])
 @pytest.mark.parametrize("rows,cols", SHAPES)
 def test_batch_gemv_matches_oracle_per_token(mq, orc, fmt, nt, rows, cols):
@@ -169,7 +168,7 @@ def valid_plans(nchunks, ntiles):
     return out
 
 
-@pytest.mark.parametrize("fmt", ["q6k", "q4k"])
+@pytest.mark.parametrize("fmt", ["q6k", "q4k", "q5k"])
 @pytest.mark.parametrize("nt", [1, 2, 6])
 def test_batch_every_plan_agrees_and_is_deterministic(mq, orc, fmt, nt):
     rows, cols = 61, 7936                         # 8 tiles (ragged), 8 chunks (last: 3 blocks)
@@ -204,7 +203,7 @@ def test_batch_bad_plans_refused(mq):
     assert torch.all(y == 7.0)                    # nothing ran
 
 
-@pytest.mark.parametrize("fmt", ["q6k", "q4k"])
+@pytest.mark.parametrize("fmt", ["q6k", "q4k", "q5k"])
 def test_batch_of_one_needs_no_workspace(mq, orc, fmt):
     """One token through the batch entry point: long rows and few tiles (the
     single-token GEMV would take a workspace plan here), no workspace given."""
@@ -230,7 +229,8 @@ FULL = [("ffn_down_7b", "q6k", 3584, 18944, "swiglu", 4),
         ("ffn_down_7b", "q6k", 3584, 18944, "swiglu", 8),
         ("attn_v_14b", "q6k", 1024, 5120, "rms", 8),
         ("ffn_gate_14b", "q4k", 13824, 5120, "rms", 8),
-        ("lm_head_14b", "q6k", 152064, 5120, "rms", 2)]
+        ("lm_head_14b", "q6k", 152064, 5120, "rms", 2),
+        ("ffn_down_14b_q5k", "q5k", 5120, 13824, "swiglu", 4)]
 
 
 @pytest.mark.parametrize("name,fmt,rows,cols,producer,nt", FULL)
@@ -239,8 +239,7 @@ def test_batch_full_size_every_row(mq, orc, name, fmt, rows, cols, producer, nt)
     producers: every row of every token against the oracle; two runs equal."""
     g = synth.rng("batch-full", name, nt)
     W = synth.blocks(fmt, g, rows, cols)
-    rep = mq.mq_repack_q6k if fmt == "q6k" else mq.mq_repack_q4k
-    Wp = dev(rep(W, rows, cols))
+    Wp = dev(mq.mq_repack(fmt, W, rows, cols))
     if producer == "swiglu":
         gv = np.stack([synth.normal(g, cols) for _ in range(nt)]).astype(np.float32)
         uv = np.stack([synth.normal(g, cols) for _ in range(nt)]).astype(np.float32)

@@ -44,10 +44,9 @@ def setup(mq, fmt, rows, cols, seed):
     g = synth.rng("gateup", fmt, rows, cols, seed)
     Wg = synth.blocks(fmt, g, rows, cols)
     Wu = synth.blocks(fmt, g, rows, cols)
-    rep = mq.mq_repack_q6k if fmt == "q6k" else mq.mq_repack_q4k
     x, gain = synth.normal(g, cols), synth.normal(g, cols, 1.0, 0.1)
     _, plane = mq.mq_rmsnorm_quant_q8(dev(x), dev(gain), 1e-6)
-    return Wg, Wu, dev(rep(Wg, rows, cols)), dev(rep(Wu, rows, cols)), plane
+    return Wg, Wu, dev(mq.mq_repack(fmt, Wg, rows, cols)), dev(mq.mq_repack(fmt, Wu, rows, cols)), plane
 
 
 def fields(mq, plane, n):
@@ -62,14 +61,13 @@ def same_plane(mq, a, b, n):
 
 def unfused(mq, fmt, Wgp, Wup, plane, rows, cols):
     nch = -(-(cols // 256) // 4)
-    gemv = mq.mq_gemv_q6k_q8 if fmt == "q6k" else mq.mq_gemv_q4k_q8
-    yg = gemv(Wgp, plane, rows, cols, plan=(1, nch, 1))
-    yu = gemv(Wup, plane, rows, cols, plan=(1, nch, 1))
+    yg = mq.mq_gemv(fmt, Wgp, plane, rows, cols, plan=(1, nch, 1))
+    yu = mq.mq_gemv(fmt, Wup, plane, rows, cols, plan=(1, nch, 1))
     return mq.mq_swiglu_quant_q8(yg, yu)
 
 
 SHAPES = [("q4k", 13824, 5120), ("q4k", 18944, 3584), ("q6k", 256, 18944), ("q4k", 32, 1280),
-          ("q6k", 96, 4608)]
+          ("q6k", 96, 4608), ("q5k", 13824, 5120), ("q5k", 64, 2304)]
 
 
 @pytest.mark.parametrize("fmt,rows,cols", SHAPES)
@@ -81,7 +79,7 @@ def test_fused_equals_three_launches_bitwise(mq, fmt, rows, cols):
     assert same_plane(mq, q8, q82, rows)
 
 
-@pytest.mark.parametrize("fmt", ["q4k", "q6k"])
+@pytest.mark.parametrize("fmt", ["q4k", "q6k", "q5k"])
 def test_every_plan_gives_the_same_bits(mq, fmt):
     rows, cols = 320, 2304                        # 10 blocks of 32 rows; 9 super-blocks: 3 chunks
     Wg, Wu, Wgp, Wup, plane = setup(mq, fmt, rows, cols, 1)
@@ -94,7 +92,7 @@ def test_every_plan_gives_the_same_bits(mq, fmt):
             assert same_plane(mq, q8, ref_q8, rows), (w, ctas)
 
 
-@pytest.mark.parametrize("fmt,rows,cols", [("q4k", 13824, 5120), ("q6k", 96, 4608)])
+@pytest.mark.parametrize("fmt,rows,cols", [("q4k", 13824, 5120), ("q6k", 96, 4608), ("q5k", 320, 2304)])
 def test_fused_against_the_oracle_chain(mq, orc, fmt, rows, cols):
     Wg, Wu, Wgp, Wup, plane = setup(mq, fmt, rows, cols, 2)
     act, q8 = mq.mq_gemv_gateup_swiglu_q8(fmt, Wgp, Wup, plane, rows, cols)

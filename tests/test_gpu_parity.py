@@ -43,8 +43,7 @@ def host(t):
 
 
 def repack_dev(mq, fmt, W, rows, cols):
-    rep = mq.mq_repack_q6k if fmt == "q6k" else mq.mq_repack_q4k
-    return dev(rep(W, rows, cols))
+    return dev(mq.mq_repack(fmt, W, rows, cols))
 
 
 def q8_fields(mq, plane, n):
@@ -54,8 +53,7 @@ def q8_fields(mq, plane, n):
 def gemv(mq, fmt, Wp, q8, rows, cols, plan=None, ws=None):
     if ws is None:
         ws = mq.mq_gemv_workspace(rows, cols, plan=plan)
-    fn = mq.mq_gemv_q6k_q8 if fmt == "q6k" else mq.mq_gemv_q4k_q8
-    return fn(Wp, q8, rows, cols, ws=ws, plan=plan)
+    return mq.mq_gemv(fmt, Wp, q8, rows, cols, ws=ws, plan=plan)
 
 
 def assert_gemv_close(y, yref, absum):
@@ -143,7 +141,7 @@ def test_rmsnorm_one_scale_for_the_whole_row(mq, orc):
 
 
 # ------------------------------------------------------------------ integer path
-@pytest.mark.parametrize("fmt", ["q6k", "q4k"])
+@pytest.mark.parametrize("fmt", ["q6k", "q4k", "q5k"])
 @pytest.mark.parametrize("rows,cols", [(16, 2048), (13, 1280), (9, 18944), (1, 256)])
 def test_subdots_bit_exact(mq, orc, fmt, rows, cols):
     g = synth.rng("subdots", fmt, rows, cols)
@@ -151,7 +149,7 @@ def test_subdots_bit_exact(mq, orc, fmt, rows, cols):
     x = special_activation(cols, "subdots")
     Wp = repack_dev(mq, fmt, W, rows, cols)
     plane = mq.mq_quantize_q8(dev(x))
-    fn = mq.mq_gemv_q6k_q8_subdots if fmt == "q6k" else mq.mq_gemv_q4k_q8_subdots
+    fn = getattr(mq, f"mq_gemv_{fmt}_q8_subdots")
     got = host(fn(Wp, plane, rows, cols))
     _, q0, _ = orc.quantize_q8(x)
     want = orc.subdots(fmt, W, q0, rows, cols)
@@ -162,7 +160,7 @@ def test_subdots_bit_exact(mq, orc, fmt, rows, cols):
 SHAPES = [(512, 2048), (13, 1280), (1, 256), (37, 4608), (64, 18944), (8, 32768), (200, 5120)]
 
 
-@pytest.mark.parametrize("fmt", ["q6k", "q4k"])
+@pytest.mark.parametrize("fmt", ["q6k", "q4k", "q5k"])
 @pytest.mark.parametrize("rows,cols", SHAPES)
 def test_gemv_matches_oracle(mq, orc, fmt, rows, cols):
     g = synth.rng("gemv", fmt, rows, cols)
@@ -186,7 +184,7 @@ def all_plans(ntiles, nch):
     return plans
 
 
-@pytest.mark.parametrize("fmt", ["q6k", "q4k"])
+@pytest.mark.parametrize("fmt", ["q6k", "q4k", "q5k"])
 def test_every_plan_agrees_and_is_deterministic(mq, orc, fmt):
     """Every valid plan of a 5-tile x 19-chunk matrix (every split count,
     every tiles-per-item) against the oracle, twice, bitwise repeatable."""
@@ -264,7 +262,10 @@ FULL = [("ffn_down_7b", "q6k", 3584, 18944, "swiglu"),
         ("attn_q_14b", "q4k", 5120, 5120, "rms"),
         ("attn_k_14b", "q4k", 1024, 5120, "rms"),
         ("ffn_gate_14b", "q4k", 13824, 5120, "rms"),
-        ("lm_head_14b", "q6k", 152064, 5120, "rms")]
+        ("lm_head_14b", "q6k", 152064, 5120, "rms"),
+        # q5_K at the 14B ffn_down and gate shapes (the class of q5_K_M files)
+        ("ffn_down_14b_q5k", "q5k", 5120, 13824, "swiglu"),
+        ("ffn_gate_14b_q5k", "q5k", 13824, 5120, "rms")]
 
 
 @pytest.mark.parametrize("name,fmt,rows,cols,producer", FULL)
@@ -300,6 +301,8 @@ GROUPS = [
     (4608, [("q4k", 40), ("q4k", 13), ("q6k", 24)]),
     # a gate/up pair and a third part with long rows (19 chunks: > 12 splits possible)
     (18944, [("q4k", 16), ("q4k", 16), ("q6k", 9)]),
+    # all three formats in one launch
+    (5120, [("q5k", 24), ("q6k", 8), ("q4k", 17), ("q5k", 3)]),
 ]
 
 

@@ -38,15 +38,14 @@ def test_library_exports_every_declared_symbol(mq):
     assert sorted(mq.EXPORTS) == names
 
 
-@pytest.mark.parametrize("fmt", ["q6k", "q4k"])
+@pytest.mark.parametrize("fmt", ["q6k", "q4k", "q5k"])
 @pytest.mark.parametrize("rows,cols", [(1, 256), (7, 512), (8, 1024), (13, 1280), (24, 4608), (9, 18944)])
 def test_repack_round_trip_and_size(mq, fmt, rows, cols):
     g = synth.rng("host", "repack", fmt, rows, cols)
     W = synth.blocks(fmt, g, rows, cols)
-    bb = 210 if fmt == "q6k" else 144
-    rep = mq.mq_repack_q6k if fmt == "q6k" else mq.mq_repack_q4k
-    unrep = mq.mq_unrepack_q6k if fmt == "q6k" else mq.mq_unrepack_q4k
-    P = rep(W, rows, cols)
+    bb = {"q6k": 210, "q4k": 144, "q5k": 176}[fmt]
+    unrep = getattr(mq, f"mq_unrepack_{fmt}")
+    P = mq.mq_repack(fmt, W, rows, cols)
     nb = cols // 256
     tiles = -(-rows // 8)
     assert P.size == tiles * 8 * nb * bb                  # zero padding beyond whole tiles
@@ -57,17 +56,18 @@ def test_repack_round_trip_and_size(mq, fmt, rows, cols):
         assert P.size == W.size                            # exactly the content bytes
 
 
-def test_repack_differs_only_by_bit_permutation(mq):
+@pytest.mark.parametrize("fmt,bb", [("q6k", 210), ("q4k", 144), ("q5k", 176)])
+def test_repack_differs_only_by_bit_permutation(mq, fmt, bb):
     """Flipping one source bit flips exactly one repacked bit, and distinct
     source bits map to distinct repacked bits (an injective bit map)."""
     rows, cols = 8, 1024
-    W = np.zeros((rows, cols // 256 * 210), np.uint8)
+    W = np.zeros((rows, cols // 256 * bb), np.uint8)
     seen = set()
-    rng = synth.rng("host", "bits")
+    rng = synth.rng("host", "bits", fmt)
     for pos in rng.choice(W.size * 8, 400, replace=False):
         Wb = W.copy().reshape(-1)
         Wb[pos // 8] = 1 << (pos % 8)
-        P = mq.mq_repack_q6k(Wb.reshape(rows, -1), rows, cols)
+        P = mq.mq_repack(fmt, Wb.reshape(rows, -1), rows, cols)
         on = np.flatnonzero(np.unpackbits(P))
         assert on.size == 1
         assert on[0] not in seen
@@ -201,7 +201,11 @@ def test_group_workspace_and_validation(mq):
     assert mq.mq_gemv_group_workspace_bytes(qkv, 16384, (16, 1, 1)) == 896 * 4 + 896 * 16 * 8 * 4
     assert mq.mq_gemv_group_workspace_bytes(qkv, 16384, (1, 16, 3)) == 0     # whole tiles
     assert mq.mq_gemv_group_workspace_bytes(qkv, 16384, (2, 7, 1)) == 0      # invalid plan
-    assert mq.mq_gemv_group_workspace_bytes([("q5k", None, 8)], 1024, (1, 1, 1)) == 0
+    with pytest.raises(ValueError):
+        mq.mq_gemv_group_workspace_bytes([("q3k", None, 8)], 1024, (1, 1, 1))
+    arr = (mq.MQGemvPart * 1)()
+    arr[0].fmt, arr[0].rows = 7, 8                  # no such format: no plan, no bytes
+    assert mq.lib().mq_gemv_group_workspace_bytes(arr, 1, 1024, 16, 1, 1) == 0
     assert mq.mq_gemv_group_workspace_bytes(qkv * 3, 1024, (1, 1, 1)) == 0   # 9 parts > MQ_MAX_GROUP
     assert mq.MQ_MAX_GROUP == 8
 
@@ -219,7 +223,7 @@ def test_group_validation_rejects_before_launch(mq):
     assert L.mq_gemv_group_q8(arr, 9, Q, 5120, N, 0, N) == mq.MQ_ERR_SHAPE
     assert L.mq_gemv_group_q8(arr, 3, N, 5120, N, 0, N) == mq.MQ_ERR_NULL
     assert L.mq_gemv_group_q8_plan(arr, 3, Q, 5120, 3, 1, 1, N, 0, N) == mq.MQ_ERR_COVERAGE
-    arr[2].fmt = 5
+    arr[2].fmt = 7                                   # no such format
     assert L.mq_gemv_group_q8(arr, 3, Q, 5120, N, 0, N) == mq.MQ_ERR_SHAPE
     arr[2].fmt = 6
     arr[1].y = 0x100008
@@ -295,7 +299,7 @@ def test_gateup_validation_rejects_before_launch(mq):
     G, U, Q = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30000)
     A, O, N = ctypes.c_void_p(0x40000), ctypes.c_void_p(0x50000), ctypes.c_void_p(0)
     assert L.mq_gemv_gateup_swiglu_q8(4, N, U, Q, 64, 1024, A, O, N) == mq.MQ_ERR_NULL
-    assert L.mq_gemv_gateup_swiglu_q8(5, G, U, Q, 64, 1024, A, O, N) == mq.MQ_ERR_SHAPE
+    assert L.mq_gemv_gateup_swiglu_q8(7, G, U, Q, 64, 1024, A, O, N) == mq.MQ_ERR_SHAPE
     assert L.mq_gemv_gateup_swiglu_q8(4, G, U, Q, 48, 1024, A, O, N) == mq.MQ_ERR_SHAPE
     assert L.mq_gemv_gateup_swiglu_q8(4, G, U, Q, 64, 1000, A, O, N) == mq.MQ_ERR_SHAPE
     assert L.mq_gemv_gateup_swiglu_q8(4, G, U, Q, 64, 1024, ctypes.c_void_p(0x40004), O, N) == \
@@ -303,3 +307,19 @@ def test_gateup_validation_rejects_before_launch(mq):
     for w, c in ((0, 1), (9, 1), (4, 0), (4, 3)):
         assert L.mq_gemv_gateup_swiglu_q8_plan(4, G, U, Q, 64, 1024, A, O, w, c, N) == \
             mq.MQ_ERR_COVERAGE
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="needs a machine without a usable GPU")
+def test_cuda_failure_names_its_call(mq):
+    """Without a device, a valid call fails in its first device query with
+    MQ_ERR_CUDA, and mq_last_error names the query and CUDA's reason."""
+    L = mq.lib()
+    A, B, Y = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30000)
+    N = ctypes.c_void_p(0)
+    assert L.mq_gemv_q6k_q8(A, B, Y, 8, 1024, N, 0, N) == mq.MQ_ERR_CUDA
+    msg = L.mq_last_error().decode()
+    assert msg and ":" in msg
+    with pytest.raises(mq.MQError) as e:
+        mq._check(mq.MQ_ERR_CUDA, "probe")
+    assert msg in str(e.value)
