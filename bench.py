@@ -372,6 +372,13 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     mq.mq_set_pdl(False)
     n_kt = max(wl.n_copies, 16) if wl.n_gemv < 8 else 2
     kt_graph = capture(lambda: [wl.run_gemvs(i) for i in range(n_kt)], stream)
+    # ---- the single-launch read floor of the same weight bytes (one-GEMV
+    # workloads): a plain read of each step's weight copy, back to back
+    floor_graph = None
+    if wl.n_gemv == 1 and args.tokens == 1:
+        wcopies = wl.ops[-1][3][0][1]
+        floor_graph = capture(lambda: [mq.mq_read_floor(wcopies[i % wl.n_copies]) for i in range(n_kt)],
+                              stream)
     mq.mq_set_pdl(args.pdl)
     torch.cuda.synchronize()
 
@@ -433,6 +440,21 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
         e1.synchronize()
         kt.append(e0.elapsed_time(e1) / n_kt)
     gemv_step_ms = float(np.median(kt))
+    floor_ms = None
+    if floor_graph is not None:
+        with torch.cuda.stream(stream):
+            floor_graph.replay()
+        torch.cuda.synchronize()
+        ft = []
+        for rep in range(5):
+            e0, e1 = make_event(), make_event()
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                floor_graph.replay()
+                e1.record(stream)
+            e1.synchronize()
+            ft.append(e0.elapsed_time(e1) / n_kt)
+        floor_ms = float(np.median(ft))
 
     # ---- e2e: the public API, pinned host inputs in, result out, every step
     out_host = torch.empty(wl.output.shape, dtype=torch.float32).pin_memory()
@@ -497,6 +519,12 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
                         "gemv_us_per_step": round(gemv_step_ms * 1e3, 3),
                         "how": f"GEMV launches of {n_kt} steps back to back in one CUDA graph "
                                f"(PDL off, rotated copies), CUDA events around 5 replays, median"}
+    if floor_ms is not None:
+        # a plain one-launch read of the same weight copies (mq_read_floor),
+        # timed the same way: what any single launch of these bytes costs here
+        line["roofline"]["read_floor_us"] = round(floor_ms * 1e3, 3)
+        line["roofline"]["read_floor_gbs"] = round(wl.weight_bytes / (floor_ms * 1e-3) / 1e9, 1)
+        line["roofline"]["frac_of_read_floor"] = round(floor_ms / gemv_step_ms, 4)
     line["kernel_us"] = {"gemv_per_step_isolated": round(gemv_step_ms * 1e3, 3),
                          "step": round(ms_per_step * 1e3, 3)}
     line["e2e"] = {"value": round(wl.weight_bytes / (e2e_ms * 1e-3) / 1e9 * ws_, 2), "unit": "GB/s",

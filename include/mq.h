@@ -389,6 +389,14 @@ int mq_gemv_q4k_q8_subdots(const void *Wp, const void *q8, int32_t *isums, int r
 int mq_gemv_q5k_q8_subdots(const void *Wp, const void *q8, int32_t *isums, int rows, int cols,
                            void *stream);
 
+/* Measurement aid: read `bytes` (a multiple of 16) at src (device, 16-byte
+ * aligned) once, in one launch, and do nothing with them.  Its time is the
+ * floor for any single launch that streams that many bytes on this GPU,
+ * ramp and tail included, so a GEMV's time can be judged against it as well
+ * as against the sustained copy peak.  Errors: MQ_ERR_NULL, MQ_ERR_SHAPE,
+ * MQ_ERR_ALIGN, MQ_ERR_CUDA. */
+int mq_read_floor(const void *src, size_t bytes, void *stream);
+
 /* Number of streaming multiprocessors of the current device (0 on error);
  * the dispatch plan sizes its grid from it. */
 int mq_device_sms(void);

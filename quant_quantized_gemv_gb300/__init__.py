@@ -41,7 +41,7 @@ EXPORTS = [
     "mq_gemv_q4k_q8_batch_plan", "mq_gemv_gateup_swiglu_q8", "mq_gemv_gateup_swiglu_q8_plan",
     "mq_gemv_gateup_plan_for", "mq_repacked_bytes_q5k", "mq_repack_q5k", "mq_unrepack_q5k",
     "mq_gemv_q5k_q8", "mq_gemv_q5k_q8_plan", "mq_gemv_q5k_q8_subdots", "mq_gemv_q5k_q8_batch",
-    "mq_gemv_q5k_q8_batch_plan",
+    "mq_gemv_q5k_q8_batch_plan", "mq_read_floor",
 ]
 
 
@@ -130,6 +130,7 @@ def lib():
         "mq_gemv_q5k_q8_subdots": ([P, P, P, I, I, P], I),
         "mq_gemv_q5k_q8_batch": ([P, P, I, P, I, I, P], I),
         "mq_gemv_q5k_q8_batch_plan": ([P, P, I, P, I, I, I, I, I, P], I),
+        "mq_read_floor": ([P, S, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -369,6 +370,12 @@ def mq_gemv_plan_for(rows: int, cols: int, sms: int, regs_per_thread: int = 168)
 def mq_set_pdl(enable: bool) -> bool:
     """Programmatic dependent launch for every later launch (process-wide)."""
     return bool(lib().mq_set_pdl(1 if enable else 0))
+
+
+def mq_read_floor(buf, nbytes: int = None, stream=None):
+    """One plain read of nbytes (default: all) of a device tensor: the single-launch floor."""
+    nb = buf.numel() * buf.element_size() if nbytes is None else int(nbytes)
+    _check(lib().mq_read_floor(_dev(buf), nb, _stream(stream)), "mq_read_floor")
 
 
 def mq_device_sms() -> int:

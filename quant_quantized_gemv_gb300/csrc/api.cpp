@@ -40,7 +40,7 @@ std::atomic<int> g_pdl{0};
 std::atomic<int> g_batch_ctas[kMaxDevices][kMaxTokens + 1][7][kBatchMaxCtaSplits + 1];  // [..][fmt]
 // resident gate||up CTAs per SM (register limit): [device][warps per CTA]
 constexpr int kGateUpMaxWarps = 8;
-std::atomic<int> g_gateup_ctas[kMaxDevices][kGateUpMaxWarps + 1];
+std::atomic<int> g_gateup_ctas[kMaxDevices][7][kGateUpMaxWarps + 1];  // [device][fmt][warps]
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -451,15 +451,15 @@ GateUpPlan gateup_plan_for(int nblk, int sms, CtasOf ctas_of)
     return GateUpPlan{4, (int)(nblk < resident ? nblk : resident)};
 }
 
-int gateup_device_ctas(int w, size_t plane)
+int gateup_device_ctas(int fmt, int w, size_t plane)
 {
     const int dev = current_device();
     DeviceLimits lim;
     if (dev < 0 || !device_limits(&lim)) return 0;
-    std::atomic<int> &slot = g_gateup_ctas[dev][w];
+    std::atomic<int> &slot = g_gateup_ctas[dev][fmt][w];
     int v = slot.load(std::memory_order_relaxed);
     if (v <= 0) {
-        v = gateup_ctas_per_sm(w, 0);
+        v = gateup_ctas_per_sm(fmt, w, 0);
         if (v <= 0) return 0;
         slot.store(v, std::memory_order_relaxed);
     }
@@ -496,7 +496,7 @@ int gateup_common(int fmt, const void *Wg, const void *Wu, const void *q8, int r
         bool ok = true;
         const size_t plane = q8_plane_bytes(cols);
         pl = gateup_plan_for(nblk, device_sms(), [&](int w) {
-            const int c = gateup_device_ctas(w, plane);
+            const int c = gateup_device_ctas(fmt, w, plane);
             if (c <= 0) ok = false;
             return c;
         });
@@ -823,6 +823,17 @@ int mq_gemv_gateup_plan_for(int rows, int sms, int regs_per_thread, int *warps_p
     *warps_per_cta = p.wpb;
     *ctas = p.ctas;
     return MQ_OK;
+}
+
+int mq_read_floor(const void *src, size_t bytes, void *stream)
+{
+    if (!src) return MQ_ERR_NULL;
+    if (bytes == 0 || bytes % 16 != 0) return MQ_ERR_SHAPE;
+    if (!aligned16(src)) return MQ_ERR_ALIGN;
+    const int sms = device_sms();
+    if (sms <= 0) return MQ_ERR_CUDA;
+    const cudaError_t e = launch_read_floor(src, bytes, nullptr, sms, (cudaStream_t)stream);
+    return e == cudaSuccess ? MQ_OK : cuda_fail("read-floor launch", e);
 }
 
 int mq_set_pdl(int enable)

@@ -68,12 +68,10 @@ __device__ __forceinline__ void quantize_block(float v, const GateUpLaunch &L, i
     }
 }
 
-// sums: [block parity][tile of the block][row] row sums, in the kernel's
-// shared memory (one array for every format instance of this function).
 template <int FMT>
-__device__ __forceinline__ void run_gateup(const GateUpLaunch &L, uint8_t *xs, float (*sums)[8][8],
-                                           int lane)
+__device__ __forceinline__ void run_gateup(const GateUpLaunch &L, uint8_t *xs, int lane)
 {
+    __shared__ float sums[2][8][8];  // [block parity][tile of the block][row]
     using Regs = typename Fmt<FMT>::Regs;
     constexpr int kChunkBytes = Fmt<FMT>::kChunkBytes;
     const GemvLaunch &a = L.g;
@@ -156,42 +154,48 @@ __device__ __forceinline__ void run_gateup(const GateUpLaunch &L, uint8_t *xs, f
     }
 }
 
+// One kernel per format (a kernel carrying the other formats' code is
+// slower in a PDL decode chain; see gemv.cu).
+template <int FMT>
 __global__ void __launch_bounds__(32 * kMaxCtaSplits, 1)
     gateup_kernel(const __grid_constant__ GateUpLaunch L)
 {
     extern __shared__ __align__(16) uint8_t xs[];  // the q8 plane
-    __shared__ float sums[2][8][8];
     griddep_launch_dependents();
-    const int lane = threadIdx.x & 31;
-    if (L.g.part[0].fmt == 6)
-        run_gateup<6>(L, xs, sums, lane);
-    else if (L.g.part[0].fmt == 5)
-        run_gateup<5>(L, xs, sums, lane);
-    else
-        run_gateup<4>(L, xs, sums, lane);
+    run_gateup<FMT>(L, xs, threadIdx.x & 31);
+}
+
+using KernelFn = void (*)(GateUpLaunch);
+
+KernelFn gateup_kernel_for(int fmt)
+{
+    return fmt == 6 ? gateup_kernel<6> : fmt == 5 ? gateup_kernel<5> : gateup_kernel<4>;
 }
 
 }  // namespace
 
 cudaError_t launch_gateup(const GateUpLaunch &L, int ctas, cudaStream_t st)
 {
-    return launch_maybe_pdl(gateup_kernel, dim3((unsigned)ctas), dim3(32 * L.wpb),
-                            (size_t)L.g.q8_bytes, L.g.pdl, st, L);
+    return launch_maybe_pdl(gateup_kernel_for(L.g.part[0].fmt), dim3((unsigned)ctas),
+                            dim3(32 * L.wpb), (size_t)L.g.q8_bytes, L.g.pdl, st, L);
 }
 
-int gateup_ctas_per_sm(int warps_per_cta, size_t smem)
+int gateup_ctas_per_sm(int fmt, int warps_per_cta, size_t smem)
 {
     int blocks = 0;
     const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &blocks, gateup_kernel, 32 * warps_per_cta, smem);
+        &blocks, gateup_kernel_for(fmt), 32 * warps_per_cta, smem);
     if (e != cudaSuccess) cuda_fail("gate||up occupancy", e);
     return e == cudaSuccess ? blocks : 0;
 }
 
 bool gateup_opt_in(size_t max_plane)
 {
-    const cudaError_t e = cudaFuncSetAttribute(
-        gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_plane);
+    cudaError_t e = cudaSuccess;
+    for (int fmt : {6, 4, 5})
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gateup_kernel_for(fmt), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)max_plane);
     if (e != cudaSuccess) cuda_fail("gate||up shared-memory opt-in", e);
     return e == cudaSuccess;
 }

@@ -63,7 +63,7 @@ struct GateUpLaunch {
     int wpb;                      // warps per CTA
 };
 cudaError_t launch_gateup(const GateUpLaunch &L, int ctas, cudaStream_t st);
-int gateup_ctas_per_sm(int warps_per_cta, size_t smem);
+int gateup_ctas_per_sm(int fmt, int warps_per_cta, size_t smem);
 bool gateup_opt_in(size_t max_plane);  // accept a staged plane of max_plane bytes
 
 // Small-batch GEMV (gemv_batch.cu), 1 <= a.nt <= kMaxTokens, one part whose
@@ -117,6 +117,10 @@ cudaError_t launch_rmsnorm_quant_q8(const float *x, const float *gain, float eps
 cudaError_t launch_swiglu_quant_q8(const float *g, const float *u, float *y, uint8_t *q8, int n,
                                    int rows, unsigned stride, unsigned d_off, unsigned sum_off,
                                    int pdl, cudaStream_t st);
+
+// A plain one-launch read of `bytes` (multiple of 16) from src: the floor for
+// any kernel that streams those bytes once (readfloor.cu).  sink may be null.
+cudaError_t launch_read_floor(const void *src, size_t bytes, unsigned *sink, int sms, cudaStream_t st);
 
 // Record the library's last CUDA failure on this thread (`where` and the CUDA
 // error, readable with mq_last_error); returns MQ_ERR_CUDA.

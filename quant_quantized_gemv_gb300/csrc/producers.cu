@@ -68,30 +68,23 @@ __device__ __forceinline__ void quantize4(float4 v, bool valid, long long gid, u
 }
 
 // Rows of n values (n4 = n / 4 lane groups each) are quantized into planes
-// `stride` bytes apart.  n4 is a multiple of 8, so no 8-lane block straddles
-// two rows; lanes past the last row only join the shuffles.
-struct RowSplit {
-    long long row, w;  // row of this lane group and its index within the row
-};
-__device__ __forceinline__ RowSplit row_split(long long gid, int n4)
-{
-    const long long row = gid / n4;
-    return RowSplit{row, gid - row * n4};
-}
-
+// `stride` bytes apart: blockIdx.y is the row, blockIdx.x * blockDim.x +
+// threadIdx.x the lane group within it.  n4 is a multiple of 8, so every
+// 8-lane block lies in one row; lanes past the row's end only join the
+// shuffles.
 __global__ void __launch_bounds__(256) quantize_q8_kernel(const float *__restrict__ x,
                                                           uint8_t *__restrict__ q8, int n4,
-                                                          int rows, unsigned stride,
-                                                          unsigned d_off, unsigned sum_off)
+                                                          unsigned stride, unsigned d_off,
+                                                          unsigned sum_off)
 {
     griddep_launch_dependents();
     griddep_wait();  // x may come from the preceding kernel
-    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const bool valid = gid < (long long)n4 * rows;
-    const RowSplit rs = row_split(gid, n4);
-    const float4 v = valid ? __ldcg(reinterpret_cast<const float4 *>(x) + gid)
+    const size_t row = blockIdx.y;
+    const int gid = blockIdx.x * blockDim.x + threadIdx.x;
+    const bool valid = gid < n4;
+    const float4 v = valid ? __ldcg(reinterpret_cast<const float4 *>(x) + row * n4 + gid)
                            : make_float4(0.f, 0.f, 0.f, 0.f);
-    quantize4(v, valid, rs.w, q8 + rs.row * stride, d_off, sum_off);
+    quantize4(v, valid, gid, q8 + row * stride, d_off, sum_off);
 }
 
 // y = (g / (1 + exp(-g))) * u, the swiglu body of the D3-5 page §3.2, over
@@ -99,25 +92,26 @@ __global__ void __launch_bounds__(256) quantize_q8_kernel(const float *__restric
 // writing them).
 __global__ void __launch_bounds__(256) swiglu_quant_q8_kernel(const float *g, const float *u,
                                                               float *y, uint8_t *__restrict__ q8,
-                                                              int n4, int rows, unsigned stride,
+                                                              int n4, unsigned stride,
                                                               unsigned d_off, unsigned sum_off)
 {
     griddep_launch_dependents();
     griddep_wait();  // g and u may come from the preceding kernels
-    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const bool valid = gid < (long long)n4 * rows;
-    const RowSplit rs = row_split(gid, n4);
+    const size_t row = blockIdx.y;
+    const int gid = blockIdx.x * blockDim.x + threadIdx.x;
+    const bool valid = gid < n4;
+    const size_t at = row * n4 + gid;  // float4 index in the nt x n arrays
     float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
     if (valid) {
-        const float4 gv = __ldcg(reinterpret_cast<const float4 *>(g) + gid);
-        const float4 uv = __ldcg(reinterpret_cast<const float4 *>(u) + gid);
+        const float4 gv = __ldcg(reinterpret_cast<const float4 *>(g) + at);
+        const float4 uv = __ldcg(reinterpret_cast<const float4 *>(u) + at);
         out.x = (gv.x / (1.0f + expf(-gv.x))) * uv.x;
         out.y = (gv.y / (1.0f + expf(-gv.y))) * uv.y;
         out.z = (gv.z / (1.0f + expf(-gv.z))) * uv.z;
         out.w = (gv.w / (1.0f + expf(-gv.w))) * uv.w;
-        reinterpret_cast<float4 *>(y)[gid] = out;
+        reinterpret_cast<float4 *>(y)[at] = out;
     }
-    quantize4(out, valid, rs.w, q8 + rs.row * stride, d_off, sum_off);
+    quantize4(out, valid, gid, q8 + row * stride, d_off, sum_off);
 }
 
 // Each row (blockIdx.y) over a grid of CTAs with no inter-CTA communication: every CTA
@@ -196,8 +190,8 @@ cudaError_t launch_quantize_q8(const float *x, uint8_t *q8, int n, int rows, uns
                                unsigned d_off, unsigned sum_off, int pdl, cudaStream_t st)
 {
     const int n4 = n / 4;
-    return launch_maybe_pdl(quantize_q8_kernel, dim3(blocks_for((long long)n4 * rows, 256)), dim3(256),
-                            0, pdl, st, x, q8, n4, rows, stride, d_off, sum_off);
+    return launch_maybe_pdl(quantize_q8_kernel, dim3(blocks_for(n4, 256), (unsigned)rows), dim3(256),
+                            0, pdl, st, x, q8, n4, stride, d_off, sum_off);
 }
 
 cudaError_t launch_swiglu_quant_q8(const float *g, const float *u, float *y, uint8_t *q8, int n,
@@ -205,8 +199,8 @@ cudaError_t launch_swiglu_quant_q8(const float *g, const float *u, float *y, uin
                                    int pdl, cudaStream_t st)
 {
     const int n4 = n / 4;
-    return launch_maybe_pdl(swiglu_quant_q8_kernel, dim3(blocks_for((long long)n4 * rows, 256)),
-                            dim3(256), 0, pdl, st, g, u, y, q8, n4, rows, stride, d_off, sum_off);
+    return launch_maybe_pdl(swiglu_quant_q8_kernel, dim3(blocks_for(n4, 256), (unsigned)rows),
+                            dim3(256), 0, pdl, st, g, u, y, q8, n4, stride, d_off, sum_off);
 }
 
 cudaError_t launch_rmsnorm_quant_q8(const float *x, const float *gain, float eps, float *y,

@@ -341,3 +341,14 @@ def test_group_of_one_is_the_single_gemv(mq):
     (y2,) = mq.mq_gemv_group_q8([("q6k", Wp, rows)], plane, cols,
                                 ws=mq.mq_gemv_group_workspace([("q6k", Wp, rows)], cols))
     assert np.array_equal(y1, host(y2))
+
+
+def test_read_floor_runs(mq):
+    """The measurement aid reads a buffer without error (bench.py times it)."""
+    import torch
+    buf = torch.ones(1 << 20, dtype=torch.uint8, device="cuda")
+    mq.mq_read_floor(buf)
+    mq.mq_read_floor(buf, 4096)
+    torch.cuda.synchronize()
+    with pytest.raises(mq.MQError):
+        mq.mq_read_floor(buf, 4095)

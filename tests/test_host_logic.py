@@ -323,3 +323,14 @@ def test_cuda_failure_names_its_call(mq):
     with pytest.raises(mq.MQError) as e:
         mq._check(mq.MQ_ERR_CUDA, "probe")
     assert msg in str(e.value)
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="fake device pointers are only passed where no GPU exists")
+def test_read_floor_validation(mq):
+    L = mq.lib()
+    N = ctypes.c_void_p(0)
+    assert L.mq_read_floor(N, 1024, N) == mq.MQ_ERR_NULL
+    assert L.mq_read_floor(ctypes.c_void_p(0x10000), 1000, N) == mq.MQ_ERR_SHAPE
+    assert L.mq_read_floor(ctypes.c_void_p(0x10000), 0, N) == mq.MQ_ERR_SHAPE
+    assert L.mq_read_floor(ctypes.c_void_p(0x10008), 1024, N) == mq.MQ_ERR_ALIGN
