@@ -192,11 +192,12 @@ __device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P
 // of kGemvWarpsPerBlock independent warps; 2..kMaxCtaSplits splits use one
 // CTA per tile whose warps are its splits.  The part of a work item is found
 // with constant indices (the part table stays in parameter space).
-// FMTS: the one format (6, 4, 5) of every part of the launch, or 0 for a
-// group that mixes formats.  Launches of one format get a kernel compiled
-// for that format alone: carrying the other formats' code costs ~2.5 us
-// per launch in a PDL decode chain (measured), though not in isolation.
-template <bool SUBDOTS, int FMTS>
+// One kernel serves every format (the part's format picks the code path):
+// in a decode chain with programmatic dependent launch, switching between
+// kernel functions from one GEMV to the next costs more than the branch.
+// Measured on the 14B sweep: 2.39 ms with one kernel for all formats
+// against 2.49 ms with a kernel per format set (qkv, o, down alternating).
+template <bool SUBDOTS>
 __global__ void __launch_bounds__(32 * kMaxCtaSplits, 1)
     gemv_kernel(const __grid_constant__ GemvLaunch a)
 {
@@ -227,29 +228,12 @@ __global__ void __launch_bounds__(32 * kMaxCtaSplits, 1)
         u0 = li * a.tpi * nch;
         u1 = min(u0 + a.tpi * nch, P.ntiles * nch);
     }
-    if (FMTS == 6 || (FMTS == 0 && P.fmt == 6))
+    if (P.fmt == 6)
         run_range<6, SUBDOTS>(a, P, xs, item, u0, u1, lane);
-    else if (FMTS == 5 || (FMTS == 0 && P.fmt == 5))
+    else if (P.fmt == 5)
         run_range<5, SUBDOTS>(a, P, xs, item, u0, u1, lane);
     else
         run_range<4, SUBDOTS>(a, P, xs, item, u0, u1, lane);
-}
-
-using KernelFn = void (*)(GemvLaunch);
-
-// The kernel for a launch: its parts' common format, else the mixed one.
-template <bool SUBDOTS>
-KernelFn kernel_of(const GemvLaunch &a)
-{
-    int fmt = a.part[0].fmt;
-    for (int p = 1; p < a.nparts; ++p)
-        if (a.part[p].fmt != fmt) fmt = 0;
-    switch (fmt) {
-    case 6: return gemv_kernel<SUBDOTS, 6>;
-    case 4: return gemv_kernel<SUBDOTS, 4>;
-    case 5: return gemv_kernel<SUBDOTS, 5>;
-    default: return gemv_kernel<SUBDOTS, 0>;
-    }
 }
 
 template <bool SUBDOTS>
@@ -257,13 +241,12 @@ cudaError_t launch(const GemvLaunch &a, cudaStream_t st)
 {
     const int warps = gemv_cta_warps(a.splits, SUBDOTS);
     const long long blocks = (a.n_items + warps - 1) / warps;
-    return launch_maybe_pdl(kernel_of<SUBDOTS>(a), dim3((unsigned)blocks), dim3(32 * warps),
+    return launch_maybe_pdl(gemv_kernel<SUBDOTS>, dim3((unsigned)blocks), dim3(32 * warps),
                             a.splits == 1 ? (size_t)a.q8_bytes : 0, a.pdl, st, a);
 }
 
-const KernelFn kAllKernels[] = {gemv_kernel<false, 0>, gemv_kernel<false, 6>, gemv_kernel<false, 4>,
-                                gemv_kernel<false, 5>, gemv_kernel<true, 0>,  gemv_kernel<true, 6>,
-                                gemv_kernel<true, 4>,  gemv_kernel<true, 5>};
+using KernelFn = void (*)(GemvLaunch);
+const KernelFn kAllKernels[] = {gemv_kernel<false>, gemv_kernel<true>};
 
 }  // namespace
 
@@ -274,7 +257,7 @@ int gemv_ctas_per_sm(int warps_per_cta, size_t smem)
 {
     int blocks = 0;
     const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &blocks, gemv_kernel<false, 0>, 32 * warps_per_cta, smem);
+        &blocks, gemv_kernel<false>, 32 * warps_per_cta, smem);
     if (e != cudaSuccess) cuda_fail("GEMV occupancy", e);
     return e == cudaSuccess ? blocks : 0;
 }

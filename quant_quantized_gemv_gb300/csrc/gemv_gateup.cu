@@ -154,8 +154,9 @@ __device__ __forceinline__ void run_gateup(const GateUpLaunch &L, uint8_t *xs, i
     }
 }
 
-// One kernel per format (a kernel carrying the other formats' code is
-// slower in a PDL decode chain; see gemv.cu).
+// One kernel per format.  Unlike the single-token GEMV (gemv.cu), here the
+// per-format kernels measured faster in a PDL decode chain (rms -> gate||up
+// -> down: 30.5 us against 33.9 us with all three formats in one kernel).
 template <int FMT>
 __global__ void __launch_bounds__(32 * kMaxCtaSplits, 1)
     gateup_kernel(const __grid_constant__ GateUpLaunch L)
