@@ -62,11 +62,13 @@ def _bind(L):
     L.mqo_gemv_q6k.argtypes = [P, P, P, I, I, I, P, P]
     L.mqo_gemv_q4k.argtypes = [P, P, P, I, I, I, P, P]
     L.mqo_gemv_q5k.argtypes = [P, P, P, I, I, I, P, P]
+    L.mqo_gemv_q6k_f32.argtypes = [P, P, I, I, I, P, P]
     L.mqo_rmsnorm.argtypes = [P, P, ctypes.c_float, I, P]
     L.mqo_swiglu.argtypes = [P, P, I, P]
     for f in ("mqo_quantize_q8", "mqo_dequant_q6k", "mqo_dequant_q4k", "mqo_dequant_q5k",
               "mqo_q4k_scale_min", "mqo_subdots_q6k", "mqo_subdots_q4k", "mqo_subdots_q5k",
-              "mqo_gemv_q6k", "mqo_gemv_q4k", "mqo_gemv_q5k", "mqo_rmsnorm", "mqo_swiglu"):
+              "mqo_gemv_q6k", "mqo_gemv_q4k", "mqo_gemv_q5k", "mqo_gemv_q6k_f32", "mqo_rmsnorm",
+              "mqo_swiglu"):
         getattr(L, f).restype = None
     return L
 
@@ -211,6 +213,30 @@ def gemv(fmt: str, W: np.ndarray, d8: np.ndarray, q8: np.ndarray, rows: int, col
         with ThreadPoolExecutor(threads) as ex:
             list(ex.map(lambda i: fn(_p(W), _p(d8), _p(q8), int(edges[i]), int(edges[i + 1]),
                                      cols, _p(y), _p(a)), range(threads)))
+    return y[r0:r1], a[r0:r1]
+
+
+def gemv_q6k_f32(W: np.ndarray, x: np.ndarray, rows: int, cols: int, row_range=None,
+                 threads: int = 1):
+    """y = W x for q6_K weights and an f32 activation row, in fp64 (the
+    dequantize-and-FMA "padded f32" family of the D3 page, §2.3 and §3.3).
+
+    Returns (y, absum) over the requested row range, as gemv() does.
+    """
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert x.size == cols
+    r0, r1 = (0, rows) if row_range is None else row_range
+    y = np.zeros(rows, np.float64)
+    a = np.zeros(rows, np.float64)
+    fn = lib().mqo_gemv_q6k_f32
+    if threads <= 1 or r1 - r0 < 2 * threads:
+        fn(_p(W), _p(x), r0, r1, cols, _p(y), _p(a))
+    else:
+        edges = np.linspace(r0, r1, threads + 1).astype(int)
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(lambda i: fn(_p(W), _p(x), int(edges[i]), int(edges[i + 1]), cols,
+                                     _p(y), _p(a)), range(threads)))
     return y[r0:r1], a[r0:r1]
 
 

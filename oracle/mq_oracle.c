@@ -388,6 +388,35 @@ void mqo_gemv_q5k(const uint8_t *W, const uint16_t *d8, const int8_t *q8,
 }
 
 /* ------------------------------------------------------------------------ */
+/* The f32-activation q6_K GEMV ([D3] §2.3 and §3.3: the "padded f32"        */
+/* family, which dequantizes each block and multiplies it into the f32       */
+/* activation row directly, without a q8 producer):                          */
+/*   y_r = sum_b sum_e w_{r,b,e} * x_{256b+e},  w = f16(d) * sc_{e/16} * q_e */
+/* Every term is exact in fp64 (w has at most 11 + 7 + 6 significant bits,   */
+/* x at most 24), summed in ascending (b, e); absum receives sum |term|.     */
+/* ------------------------------------------------------------------------ */
+void mqo_gemv_q6k_f32(const uint8_t *W, const float *x, int r0, int r1, int cols,
+                      double *y, double *absum)
+{
+    const int nb = cols / QK;
+    for (int r = r0; r < r1; ++r) {
+        double acc = 0.0, aacc = 0.0;
+        for (int b = 0; b < nb; ++b) {
+            const uint8_t *blk = W + ((size_t)r * nb + b) * Q6K_BYTES;
+            const double d = q6k_d(blk);
+            for (int e = 0; e < QK; ++e) {
+                const double w = d * (double)q6k_scale(blk, e >> 4) * (double)q6k_q(blk, e);
+                const double term = w * (double)x[(size_t)b * QK + e];
+                acc += term;
+                aacc += fabs(term);
+            }
+        }
+        y[r] = acc;
+        if (absum) absum[r] = aacc;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Producers ([D3-5] §3.2).  The rms body is not printed on the pages; the   */
 /* plain reading is y_i = x_i / sqrt(mean(x^2) + eps) * gain_i.  SwiGLU is   */
 /* printed: y_i = (g_i / (1 + exp(-g_i))) * u_i.  Both in fp64.              */

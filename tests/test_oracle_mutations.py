@@ -23,6 +23,10 @@ MUTANTS = {
     "q6k gemv activation scale index": ("d8[(size_t)b * 8 + s / 2]", "d8[(size_t)b * 8 + s / 4]"),
     "q6k gemv activation index": ("q8[(size_t)b * QK + e];\n                const double d8v",
                                   "q8[(size_t)b * QK + (e ^ 1)];\n                const double d8v"),
+    "q6k f32 activation index": ("(double)x[(size_t)b * QK + e]", "(double)x[(size_t)b * QK + (e ^ 1)]"),
+    "q6k f32 scale index": ("const double w = d * (double)q6k_scale(blk, e >> 4)",
+                            "const double w = d * (double)q6k_scale(blk, e >> 5)"),
+    "q6k f32 dropped block scale": ("const double w = d * ", "const double w = 1.0 * "),
     "q8 rounding mode": ("int q = (int)rintf(p);", "int q = (int)roundf(p);"),
     "q8 scale divisor": ("const float d = am / 127.0f;", "const float d = am / 128.0f;"),
     "q8 dropped clamp+sum": ("        s += q;\n", ""),

@@ -285,6 +285,65 @@ def test_gemv_threaded_rows_equal_serial(orc):
     assert np.array_equal(y1, y4) and np.array_equal(a1, a4)
 
 
+# ---------------------------------------------------------------- q6_K x f32 GEMV
+def test_gemv_q6k_f32_brute_force(orc):
+    """Against the second q6_K decode (q6k_dequant_alt) and an fp64 matmul."""
+    g = synth.rng("pin", "gemv-q6k-f32")
+    rows, cols = 9, 1280
+    W = synth.q6k_blocks(g, rows, cols)
+    x = synth.normal(g, cols)
+    y, a = orc.gemv_q6k_f32(W, x, rows, cols)
+    w = q6k_dequant_alt(W).reshape(rows, cols)
+    ref = w @ x.astype(np.float64)
+    assert np.all(np.abs(y - ref) <= 1e-12 * a)
+    assert np.allclose(a, np.abs(w) @ np.abs(x.astype(np.float64)), rtol=1e-12, atol=0)
+
+
+def test_gemv_q6k_f32_one_hot_picks_each_weight(orc):
+    g = synth.rng("pin", "gemv-f32-onehot")
+    W = synth.q6k_blocks(g, 3, 512)
+    w = q6k_dequant_alt(W).reshape(3, 512)
+    for k in range(0, 512, 7):
+        x = np.zeros(512, np.float32)
+        x[k] = -2.5
+        y, _ = orc.gemv_q6k_f32(W, x, 3, 512)
+        assert np.array_equal(y, -2.5 * w[:, k])
+
+
+def test_gemv_q6k_f32_closed_form(orc):
+    """Every code 45 (q = 13), sub-block scales 1..16, d = 2^-3, x = 1 on
+    every element: y = 2^-3 * 13 * 16 * (1 + 2 + ... + 16) per block."""
+    ql = np.full(128, 0xDD, np.uint8)            # low and high nibbles 13
+    qh = np.zeros(64, np.uint8)
+    blk = q6k_block(ql, qh, np.arange(1, 17), d_bits=0x3000)   # fp16 0.125
+    nb = 3
+    W = np.tile(blk, nb)
+    y, a = orc.gemv_q6k_f32(W, np.ones(256 * nb, np.float32), 1, 256 * nb)
+    assert y[0] == 0.125 * (13 - 32) * 16 * 136 * nb and a[0] == abs(y[0])
+
+
+def test_gemv_q6k_f32_equals_q8_path_on_q8_values(orc):
+    """When x is exactly f16(d8) * q8 (representable in f32), the f32-activation
+    GEMV and the q8 GEMV compute the same real number."""
+    g = synth.rng("pin", "gemv-f32-q8")
+    rows, cols = 6, 2048
+    W = synth.q6k_blocks(g, rows, cols)
+    d8, q8, xh = xhat(orc, synth.normal(g, cols))
+    assert np.array_equal(xh.astype(np.float32).astype(np.float64), xh)
+    y1, a1 = orc.gemv_q6k_f32(W, xh.astype(np.float32), rows, cols)
+    y2, _ = orc.gemv("q6k", W, d8, q8, rows, cols)
+    assert np.all(np.abs(y1 - y2) <= 1e-12 * a1)
+
+
+def test_gemv_q6k_f32_threaded_rows_equal_serial(orc):
+    g = synth.rng("pin", "gemv-f32-thr")
+    W = synth.q6k_blocks(g, 29, 512)
+    x = synth.normal(g, 512)
+    y1, a1 = orc.gemv_q6k_f32(W, x, 29, 512)
+    y4, a4 = orc.gemv_q6k_f32(W, x, 29, 512, threads=4)
+    assert np.array_equal(y1, y4) and np.array_equal(a1, a4)
+
+
 # ---------------------------------------------------------------- q4_K
 def test_q4k_scale_min_unpack(orc):
     g = synth.rng("pin", "q4k-sm")
