@@ -49,6 +49,8 @@ DESCR = {
     "layer_14b": "Qwen2.5-14B attn_v q6_K 1024x5120 + ffn_down q6_K 5120x13824, each fed by "
                  "rms_norm->q8, batch 1",
     "lm_head_14b": "Qwen2.5-14B output head q6_K 152064x5120, rms_norm->q8, batch 1",
+    "attn_v_14b": "Qwen2.5-14B attn_v q6_K 1024x5120, rms_norm->q8, batch 1",
+    "q6k_2048x4864": "q6_K 2048x4864 GEMV, x -> standalone q8 quantize, batch 1",
     "ffn_14b": "Qwen2.5-14B FFN: rms_norm->q8 -> gate, up q4_K 13824x5120 -> SwiGLU->q8 -> "
                "down q6_K 5120x13824, batch 1",
     "sweep_14b": "Qwen2.5-14B decode weight sweep: 48 layers x {q,k,o,gate,up q4_K; v,down q6_K} "
@@ -145,34 +147,36 @@ def measured_peak_gbs():
         return 6800.0, "fallback"
 
 
-def gemv_source_hash() -> str:
+def gemv_source_hash(act: str = "q8") -> str:
     h = hashlib.sha256()
-    for f in ("gemv.cu", "gemv_common.cuh", "layout.h"):
+    for f in ("gemv_f32.cu" if act == "f32" else "gemv.cu", "gemv_common.cuh", "layout.h"):
         with open(os.path.join(ROOT, "quant_quantized_gemv_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, act: str = "q8"):
     """DRAM bytes per GEMV launch from the committed ncu summary of this
     workload, if it was taken on the current kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", f"gemv_{workload}.md")
+    p = os.path.join(ROOT, "profiles", f"gemv_{'f32_' if act == 'f32' else ''}{workload}.md")
     if not os.path.exists(p):
         return None
     txt = open(p).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
     h = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
-    if not m or not h or h.group(1) != gemv_source_hash():
+    if not m or not h or h.group(1) != gemv_source_hash(act):
         return None
     return float(m.group(1))
 
 
 # ---------------------------------------------------------------- workload on the device
 class DeviceWorkload:
-    """Ops of one decode step: producers writing q8 planes, GEMVs reading them."""
+    """Ops of one decode step: producers writing q8 planes, GEMVs reading them.
+    With acts == "f32" every GEMV is the q6_K x f32 GEMV reading its
+    producer's f32 output (or its raw input: no quantize op runs)."""
 
     def __init__(self, name: str, device, l2_bytes: int, group: bool = True, nt: int = 1,
-                 fuse: bool = True):
+                 fuse: bool = True, acts: str = "q8"):
         import torch
         import quant_quantized_gemv_gb300 as mq
         self.mq = mq
@@ -180,6 +184,11 @@ class DeviceWorkload:
         self.nt = nt                 # tokens per step (> 1: the small-batch kernels)
         group = group and nt == 1    # the small-batch GEMV takes one matrix per launch
         self.wl = synth.WORKLOADS[name]
+        self.f32 = acts == "f32"
+        if self.f32:
+            if nt != 1 or any(fmt != "q6k" for _, fmt, _, _, _ in self.wl.gemvs):
+                raise SystemExit("--act f32: the f32-activation GEMV is q6_K at one token")
+            group = fuse = False
         self.dev = device
         self.weight_bytes = self.wl.weight_bytes()
         self.n_copies = max(1, math.ceil(4 * l2_bytes / self.weight_bytes))
@@ -207,6 +216,7 @@ class DeviceWorkload:
                     x = self._input(act(cols))
                     gain = torch.from_numpy(synth.normal(g, cols, 1.0, 0.1)).to(device)
                     self.ops.append(("rms", x, gain, yp, plane, cols))
+                    xsrc = yp
                 elif producer == "swiglu":
                     if len(prev_outputs) >= 2 and prev_outputs[-1].numel() == nt * cols and \
                             prev_outputs[-2].numel() == nt * cols:
@@ -215,16 +225,21 @@ class DeviceWorkload:
                         gv = self._input(act(cols))
                         uv = self._input(act(cols))
                     self.ops.append(("swiglu", gv, uv, yp, plane, cols))
+                    xsrc = yp
                 else:
                     x = self._input(act(cols))
-                    self.ops.append(("quant", x, plane, cols))
+                    xsrc = x
+                    if not self.f32:
+                        self.ops.append(("quant", x, plane, cols))
             prev_kind, prev_cols = producer, cols
             W0 = base[(fmt, rows, cols)][1]
             copies = [W0.clone() for _ in range(self.n_copies)]
             y = torch.empty((nt, rows) if nt > 1 else rows, dtype=torch.float32, device=device)
             part = (fmt, copies, rows, y, gname)
             last = self.ops[-1] if self.ops else None
-            if group and last is not None and last[0] == "gemv" and last[1] is plane and \
+            if self.f32:
+                self.ops.append(["gemv32", xsrc, cols, [part], None])
+            elif group and last is not None and last[0] == "gemv" and last[1] is plane and \
                     len(last[3]) < mq.MQ_MAX_GROUP:
                 last[3].append(part)             # same q8 plane: one launch for the group
             else:
@@ -236,11 +251,12 @@ class DeviceWorkload:
             if o[0] == "gemv" and nt == 1:
                 o[4] = mq.mq_gemv_group_workspace(self._spec(o), o[2], device=device)
         self.output = self.ops[-1][3][-1][3]
-        gemv_ops = [o for o in self.ops if o[0] in ("gemv", "gateup")]
+        gemv_ops = [o for o in self.ops if o[0] in ("gemv", "gateup", "gemv32")]
         self.n_gemv = sum(len(o[3]) for o in gemv_ops)
         self.n_gemv_launches = len(gemv_ops)
         self.n_kernels = len(self.ops)
-        self.gemv_bytes = [self._part_alg_bytes(p[0], p[2], o[2], nt) for o in gemv_ops for p in o[3]]
+        self.gemv_bytes = [self._part_alg_bytes(p[0], p[2], o[2], nt, self.f32) for o in gemv_ops
+                           for p in o[3]]
 
     def _fuse_gateup(self):
         """A two-matrix GEMV launch (gate, up) whose outputs feed the next
@@ -268,9 +284,11 @@ class DeviceWorkload:
         return t
 
     @staticmethod
-    def _part_alg_bytes(fmt, rows, cols, nt=1) -> int:
+    def _part_alg_bytes(fmt, rows, cols, nt=1, f32=False) -> int:
         wb = rows * (cols // 256) * (210 if fmt == "q6k" else 144)
         act = (cols // 32) * (34 if fmt == "q6k" else 38)      # codes + fp16 d (+ int32 sum)
+        if f32:
+            act = 4 * cols                                      # the f32 row
         return wb + nt * (act + 4 * rows)
 
     @staticmethod
@@ -291,6 +309,11 @@ class DeviceWorkload:
         else:
             mq.mq_gemv_group_q8(self._spec(o, c), plane, cols, ys=[p[3] for p in parts], ws=ws)
 
+    def _launch32(self, o, c):
+        _, xsrc, cols, parts, _ = o
+        _, copies, rows, y, _ = parts[0]
+        self.mq.mq_gemv_q6k_f32(copies[c], xsrc, rows, cols, y=y)
+
     def _launch_gateup(self, o, c):
         _, plane, cols, parts, act, plane_out = o
         (fmt, cg, rows, _, _), (_, cu, _, _, _) = parts
@@ -302,6 +325,8 @@ class DeviceWorkload:
         for o in self.ops:
             if o[0] == "gemv":
                 self._launch(o, c)
+            elif o[0] == "gemv32":
+                self._launch32(o, c)
             elif o[0] == "gateup":
                 self._launch_gateup(o, c)
 
@@ -321,6 +346,8 @@ class DeviceWorkload:
                 (mq.mq_quantize_q8_batch if b else mq.mq_quantize_q8)(o[1], q8=o[2])
             elif kind == "gateup":
                 self._launch_gateup(o, c)
+            elif kind == "gemv32":
+                self._launch32(o, c)
             else:
                 self._launch(o, c)
 
@@ -353,7 +380,8 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     import quant_quantized_gemv_gb300 as mq
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
-    wl = DeviceWorkload(args.workload, dev, l2, group=args.group, nt=args.tokens, fuse=args.fuse)
+    wl = DeviceWorkload(args.workload, dev, l2, group=args.group, nt=args.tokens, fuse=args.fuse,
+                        acts=args.act)
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -508,8 +536,10 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws_,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "i8", "data": "synthetic",
+        "dtype": "f32" if wl.f32 else "i8", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {DESCR[args.workload]}",
+                   "activations": ("f32 row (q6_K x f32 GEMV, no quantize producer)" if wl.f32
+                                   else "q8 plane"),
                    "tokens_per_step": args.tokens,
                    "weight_content_bytes_per_step": wl.weight_bytes,
                    "gemvs_per_step": wl.n_gemv, "gemv_launches_per_step": wl.n_gemv_launches,
@@ -520,18 +550,20 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
                    "timing": f"CUDA graphs of {m} steps (+ single-step graphs for a remainder), "
                              f"CUDA events on the launching stream; PDL {'on' if args.pdl else 'off'}",
                    "parallelism": f"replicas{ws_}" if ws_ > 1 else "single GPU"},
-        "compute": "int8 x (6-bit|4-bit) dp4a dots, int32 sub-block sums, f32 scale combine",
+        "compute": ("6-bit codes x f32 FMA chains per sub-block, f32 scale combine" if wl.f32 else
+                    "int8 x (6-bit|4-bit) dp4a dots, int32 sub-block sums, f32 scale combine"),
         "pct_of_hbm_peak": round(100 * value / ws_ / peak, 2),
         "tokens_per_s": round(ws_ * args.tokens * args.steps / (max_ms * 1e-3), 1),
     }
     alg = float(sum(wl.gemv_bytes))
     achieved = alg / (gemv_step_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(args.workload) if wl.n_gemv == 1 and args.tokens == 1 else None
+    traffic = profiled_traffic(args.workload, args.act) if wl.n_gemv == 1 and args.tokens == 1 else None
     line["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                         "unit": "GB/s", "frac": round(achieved / peak, 4),
                         "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
                         "algorithmic_bytes_per_step": int(alg),
-                        "kernel": ("gemv_kernel (q6_K/q4_K x q8)" if args.tokens == 1 else
+                        "kernel": ("gemv_q6k_f32_kernel (q6_K x f32 row)" if wl.f32 else
+                                   "gemv_kernel (q6_K/q4_K x q8)" if args.tokens == 1 else
                                    f"gemv_batch_kernel<{args.tokens}> (q6_K/q4_K x {args.tokens} q8 rows)"),
                         "gemv_us_per_step": round(gemv_step_ms * 1e3, 3),
                         "how": f"GEMV launches of {n_kt} steps back to back in one CUDA graph "
@@ -559,7 +591,7 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     line["clocks_window"] = (f"{args.soak:.1f}s soak + timed steps + {args.soak:.1f}s soak of the same "
                              f"graphs ({(t_timed1 - t_win0):.2f}s to end of timed region)")
     if ws_ == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds, args.tokens)
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds, args.tokens, args.act)
     return line
 
 
@@ -589,7 +621,7 @@ def oracle_sample(workload: str, rows_cap: int, nt: int = 1):
     return items
 
 
-def oracle_step(items):
+def oracle_step(items, acts: str = "q8"):
     """One step: every token's producer and GEMV; returns the weight bytes
     (read once per step, as on the GPU)."""
     import oracle
@@ -602,19 +634,22 @@ def oracle_step(items):
                 x = oracle.swiglu(inp[0], inp[1]).astype(np.float32)
             else:
                 x = inp[0]
-            d, q, _ = oracle.quantize_q8(x)
-            oracle.gemv(fmt, W, d, q, r, cols)
+            if acts == "f32":
+                oracle.gemv_q6k_f32(W, x, r, cols)
+            else:
+                d, q, _ = oracle.quantize_q8(x)
+                oracle.gemv(fmt, W, d, q, r, cols)
         nbytes += W.nbytes
     return nbytes
 
 
-def cpu_baseline(workload: str, seconds: float, nt: int = 1) -> dict:
+def cpu_baseline(workload: str, seconds: float, nt: int = 1, acts: str = "q8") -> dict:
     items = oracle_sample(workload, 512, nt)
-    oracle_step(items)                                   # warm (page-in, build)
+    oracle_step(items, acts)                             # warm (page-in, build)
     done, t0 = 0, time.perf_counter()
     n = 0
     while True:
-        done += oracle_step(items)
+        done += oracle_step(items, acts)
         n += 1
         if time.perf_counter() - t0 >= seconds or n >= 10000:
             break
@@ -622,7 +657,8 @@ def cpu_baseline(workload: str, seconds: float, nt: int = 1) -> dict:
     rows = ", ".join(f"{fmt} {r}x{cols}" for fmt, r, cols, _, _, _ in items)
     return {"value": round(done / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{n} passes over the first <=512 rows of each distinct GEMV ({rows}) with "
-                      f"its producer, {nt} token(s) per pass, single-threaded C oracle, {dt:.1f} s"}
+                      f"its producer, {nt} token(s) per pass, {acts} activations, single-threaded C "
+                      f"oracle, {dt:.1f} s"}
 
 
 def bench_reference(args, ws_, rank) -> dict | None:
@@ -630,20 +666,21 @@ def bench_reference(args, ws_, rank) -> dict | None:
         return None
     items = oracle_sample(args.workload, 512, args.tokens)
     for _ in range(args.warmup):
-        oracle_step(items)
+        oracle_step(items, args.act)
     t0 = time.perf_counter()
     nbytes = 0
     for _ in range(args.steps):
-        nbytes += oracle_step(items)
+        nbytes += oracle_step(items, args.act)
     dt = time.perf_counter() - t0
     value = nbytes / dt / 1e9
     rows = ", ".join(f"{fmt} {r}x{cols}" for fmt, r, cols, _, _, _ in items)
     sample = (f"each step: the first <=512 rows of each distinct GEMV ({rows}) with its producer, "
-              f"{args.tokens} token(s)")
+              f"{args.tokens} token(s), {args.act} activations")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "i8", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32" if args.act == "f32" else "i8",
+            "data": "synthetic",
             "config": {"workload": f"{args.workload}: {DESCR[args.workload]}",
                        "tokens_per_step": args.tokens, "sample": sample},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
@@ -671,6 +708,9 @@ def main(argv=None):
                          "one gate||up launch with the SwiGLU -> q8 epilogue")
     ap.add_argument("--tokens", type=int, default=1, choices=range(1, 9), metavar="NT",
                     help="tokens per step (1..8); > 1 uses the small-batch producers and GEMV")
+    ap.add_argument("--act", default="q8", choices=["q8", "f32"],
+                    help="activation form the GEMVs read: the q8 plane (default) or, for q6_K "
+                         "workloads at one token, the f32 row through the q6_K x f32 GEMV")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

@@ -225,6 +225,32 @@ int mq_gemv_q6k_q8_noalloc(const void *Wp, const void *q8, float *y, int rows, i
                            void *stream);
 
 /* ------------------------------------------------------------------------
+ * q6_K GEMV against an f32 activation row (device): the dequantize-and-FMA
+ * family the pages keep beside the q8 MMVQ ([D3] §2.3 and §3.3, the
+ * "padded f32" kernels; on GB10 they won below od*id ~ 24M).  No q8
+ * producer is needed: x is read as is.
+ *   y_r = sum_e w_{r,e} x_e,   w = f16(d) * sc_{e/16} * (q_e - 32)
+ * computed in f32: a fused multiply-add chain over each 16-weight
+ * sub-block, then acc_r += (d * sc) * subsum, partial sums combined in the
+ * fixed order of the q8 GEMV (deterministic run to run).
+ *   Wp: repacked q6_K weights (device, mq_repack_q6k output; the same copy
+ *       serves the q8 GEMV).  x: cols f32 (device).  y: rows f32 (device).
+ *   Every CTA stages x in shared memory, so cols * 4 bytes must fit in one
+ *   CTA's opt-in shared memory less 1 KB (cols <= 57856 on GB300), else
+ *   MQ_ERR_SHAPE.
+ *   Plans are those of mq_gemv_q6k_q8 without workspace splits: splits must
+ *   be 1..12 (MQ_ERR_COVERAGE otherwise, with the same coverage checks);
+ *   mq_gemv_q6k_f32_plan_of returns the default plan on the current device.
+ * Errors: MQ_ERR_NULL, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_COVERAGE,
+ *         MQ_ERR_CUDA.
+ * ------------------------------------------------------------------------ */
+int mq_gemv_q6k_f32(const void *Wp, const float *x, float *y, int rows, int cols, void *stream);
+int mq_gemv_q6k_f32_plan(const void *Wp, const float *x, float *y, int rows, int cols, int splits,
+                         int chunks_per_split, int tiles_per_item, void *stream);
+int mq_gemv_q6k_f32_plan_of(int rows, int cols, int *splits, int *chunks_per_split,
+                            int *tiles_per_item);
+
+/* ------------------------------------------------------------------------
  * Grouped GEMV (device): up to MQ_MAX_GROUP matrices that read the same q8
  * plane (same cols) in ONE launch, e.g. the q, k, v projections of a layer
  * (q4_K, q4_K, q6_K) after one rms_norm->q8, or its gate and up (the

@@ -41,7 +41,8 @@ EXPORTS = [
     "mq_gemv_q4k_q8_batch_plan", "mq_gemv_gateup_swiglu_q8", "mq_gemv_gateup_swiglu_q8_plan",
     "mq_gemv_gateup_plan_for", "mq_repacked_bytes_q5k", "mq_repack_q5k", "mq_unrepack_q5k",
     "mq_gemv_q5k_q8", "mq_gemv_q5k_q8_plan", "mq_gemv_q5k_q8_subdots", "mq_gemv_q5k_q8_batch",
-    "mq_gemv_q5k_q8_batch_plan", "mq_read_floor",
+    "mq_gemv_q5k_q8_batch_plan", "mq_read_floor", "mq_gemv_q6k_f32", "mq_gemv_q6k_f32_plan",
+    "mq_gemv_q6k_f32_plan_of",
 ]
 
 
@@ -131,6 +132,9 @@ def lib():
         "mq_gemv_q5k_q8_batch": ([P, P, I, P, I, I, P], I),
         "mq_gemv_q5k_q8_batch_plan": ([P, P, I, P, I, I, I, I, I, P], I),
         "mq_read_floor": ([P, S, P], I),
+        "mq_gemv_q6k_f32": ([P, P, P, I, I, P], I),
+        "mq_gemv_q6k_f32_plan": ([P, P, P, I, I, I, I, I, P], I),
+        "mq_gemv_q6k_f32_plan_of": ([I, I, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -435,6 +439,27 @@ def mq_gemv(fmt: str, Wp, q8, rows: int, cols: int, y=None, ws=None, stream=None
     """The single-token GEMV of format fmt ('q6k', 'q4k', 'q5k')."""
     return _gemv("mq_gemv_" + {6: "q6k", 4: "q4k", 5: "q5k"}[fmt_code(fmt)] + "_q8", Wp, q8, rows,
                  cols, y, ws, stream, plan)
+
+
+# ------------------------------------------------------------------ f32 activations
+def mq_gemv_q6k_f32_plan_of(rows: int, cols: int):
+    """Default plan of the f32-activation q6_K GEMV on the current device."""
+    return _plan_out(lib().mq_gemv_q6k_f32_plan_of, rows, cols)
+
+
+def mq_gemv_q6k_f32(Wp, x, rows: int, cols: int, y=None, stream=None, plan=None):
+    """y = W x for repacked q6_K weights Wp and an f32 activation row x (device)."""
+    import torch
+    y = torch.empty(rows, dtype=torch.float32, device=Wp.device) if y is None else y
+    L = lib()
+    if plan is None:
+        st = L.mq_gemv_q6k_f32(_dev(Wp), _dev(x, torch.float32), _dev(y, torch.float32), rows, cols,
+                               _stream(stream))
+    else:
+        st = L.mq_gemv_q6k_f32_plan(_dev(Wp), _dev(x, torch.float32), _dev(y, torch.float32), rows,
+                                    cols, int(plan[0]), int(plan[1]), int(plan[2]), _stream(stream))
+    _check(st, "mq_gemv_q6k_f32")
+    return y
 
 
 # ------------------------------------------------------------------ small-batch GEMV

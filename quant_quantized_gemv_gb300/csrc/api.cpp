@@ -41,6 +41,8 @@ std::atomic<int> g_batch_ctas[kMaxDevices][kMaxTokens + 1][7][kBatchMaxCtaSplits
 // resident gate||up CTAs per SM (register limit): [device][warps per CTA]
 constexpr int kGateUpMaxWarps = 8;
 std::atomic<int> g_gateup_ctas[kMaxDevices][7][kGateUpMaxWarps + 1];  // [device][fmt][warps]
+// resident f32-activation GEMV CTAs per SM (register limit): [device][warps per CTA]
+std::atomic<int> g_f32_ctas[kMaxDevices][kMaxCtaSplits + 1];
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -84,6 +86,7 @@ struct DeviceLimits {
     int smem_per_sm, smem_reserved;  // shared memory per SM, reserved per CTA
     size_t max_plane;                // largest q8 plane the GEMV stages
     size_t max_batch_planes;         // largest nt planes the small-batch GEMV stages
+    size_t max_x_f32;                // largest f32 row the f32-activation GEMV stages
 };
 std::atomic<bool> g_limits_ok[kMaxDevices];
 DeviceLimits g_limits[kMaxDevices];
@@ -108,7 +111,9 @@ bool device_limits(DeviceLimits *out)
             }
             l.max_plane = gemv_max_plane_bytes();  // also opts the kernels in
             l.max_batch_planes = gemv_batch_max_smem();
-            if (l.max_plane == 0 || l.max_batch_planes == 0 || !gateup_opt_in(l.max_plane))
+            l.max_x_f32 = gemv_f32_max_x_bytes();
+            if (l.max_plane == 0 || l.max_batch_planes == 0 || l.max_x_f32 == 0 ||
+                !gateup_opt_in(l.max_plane))
                 return false;
             g_limits[dev] = l;
             g_limits_ok[dev].store(true, std::memory_order_release);
@@ -531,6 +536,105 @@ int subdots_common(int fmt, const void *Wp, const void *q8, int32_t *isums, int 
     return e == cudaSuccess ? MQ_OK : cuda_fail("sub-dot launch", e);
 }
 
+// ---- q6_K against an f32 activation row --------------------------------
+// CTAs per SM of the f32 kernel: its register limit and the shared memory
+// of a staged row of `xbytes` (every CTA stages it, split CTAs included).
+bool f32_occupancy(Occupancy *o, size_t xbytes)
+{
+    const int dev = current_device();
+    DeviceLimits lim;
+    if (dev < 0 || !device_limits(&lim)) return false;
+    const long long per_cta = (long long)xbytes + kGemvStaticSmem + lim.smem_reserved;
+    const int by_smem = (int)(lim.smem_per_sm / per_cta);
+    for (int w = 1; w <= kMaxCtaSplits; ++w) {
+        std::atomic<int> &slot = g_f32_ctas[dev][w];
+        int v = slot.load(std::memory_order_relaxed);
+        if (v <= 0) {
+            v = gemv_f32_ctas_per_sm(w, 0);
+            if (v <= 0) return false;
+            slot.store(v, std::memory_order_relaxed);
+        }
+        o->ctas[w] = v < by_smem ? v : by_smem;
+    }
+    o->ctas_tiles = o->ctas[kGemvWarpsPerBlock];
+    return o->ctas_tiles > 0;
+}
+
+// The q8 GEMV's plan with the split count capped at one CTA's warps.
+Plan f32_plan_for(int ntiles, int nchunks, int sms, const Occupancy &o)
+{
+    Plan p = plan_for(ntiles, nchunks, sms, o);
+    if (p.splits > kMaxCtaSplits) {
+        p.cps = ceil_div(nchunks, kMaxCtaSplits);
+        p.splits = ceil_div(nchunks, p.cps);
+        p.tpi = 1;
+    }
+    return p;
+}
+
+int f32_plan_of(int rows, int cols, Plan *p)
+{
+    if (!gemv_shape_ok(rows, cols)) return MQ_ERR_SHAPE;
+    DeviceLimits lim;
+    if (!device_limits(&lim)) return MQ_ERR_CUDA;
+    const size_t xbytes = (size_t)cols * 4;
+    if (xbytes > lim.max_x_f32) return MQ_ERR_SHAPE;
+    Occupancy o;
+    if (!f32_occupancy(&o, xbytes)) return MQ_ERR_CUDA;
+    const Geom g = make_geom(rows, cols, kQ6kBytes);
+    *p = f32_plan_for(g.ntiles, g.nchunks, device_sms(), o);
+    return MQ_OK;
+}
+
+int gemv_f32_common(const void *Wp, const float *x, float *y, int rows, int cols,
+                    const Plan *explicit_plan, void *stream)
+{
+    if (!Wp || !x || !y) return MQ_ERR_NULL;
+    if (!gemv_shape_ok(rows, cols)) return MQ_ERR_SHAPE;
+    if (!aligned16(Wp) || !aligned16(x) || !aligned16(y)) return MQ_ERR_ALIGN;
+    const Geom g = make_geom(rows, cols, kQ6kBytes);
+    if ((long long)g.ntiles * g.nchunks >= (1LL << 31)) return MQ_ERR_SHAPE;
+    if (explicit_plan) {  // refused before anything touches the device
+        if (explicit_plan->splits > kMaxCtaSplits) return MQ_ERR_COVERAGE;
+        const int cov = check_plan(g.nchunks, *explicit_plan);
+        if (cov != MQ_OK) return cov;
+    }
+    Plan pl;
+    if (explicit_plan) {
+        DeviceLimits lim;
+        if (!device_limits(&lim)) return MQ_ERR_CUDA;
+        if ((size_t)cols * 4 > lim.max_x_f32) return MQ_ERR_SHAPE;
+        pl = *explicit_plan;
+    } else {
+        const int st = f32_plan_of(rows, cols, &pl);
+        if (st != MQ_OK) return st;
+    }
+    GemvLaunch a;
+    memset(&a, 0, sizeof a);
+    GemvPart &gp = a.part[0];
+    gp.W = (const uint8_t *)Wp;
+    gp.y = y;
+    gp.rows = rows;
+    gp.ntiles = g.ntiles;
+    gp.fmt = 6;
+    gp.tile_bytes_div16 = (int)(g.tile_bytes / 16);
+    const long long items = plan_items(g.ntiles, pl);
+    if (items >= (1LL << 31)) return MQ_ERR_SHAPE;
+    a.nparts = 1;
+    a.q8 = (const uint8_t *)x;
+    a.nb = g.nb;
+    a.nchunks = g.nchunks;
+    a.splits = pl.splits;
+    a.cps = pl.cps;
+    a.tpi = pl.tpi;
+    a.n_items = (int)items;
+    a.q8_bytes = (unsigned)((size_t)cols * 4);
+    a.pdl = g_pdl.load(std::memory_order_relaxed);
+    a.nt = 1;
+    const cudaError_t e = launch_gemv_f32(a, (cudaStream_t)stream);
+    return e == cudaSuccess ? MQ_OK : cuda_fail("f32 GEMV launch", e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -902,6 +1006,32 @@ int mq_gemv_q4k_q8_subdots(const void *Wp, const void *q8, int32_t *isums, int r
                            void *stream)
 {
     return subdots_common(4, Wp, q8, isums, rows, cols, stream);
+}
+
+int mq_gemv_q6k_f32(const void *Wp, const float *x, float *y, int rows, int cols, void *stream)
+{
+    return gemv_f32_common(Wp, x, y, rows, cols, nullptr, stream);
+}
+
+int mq_gemv_q6k_f32_plan(const void *Wp, const float *x, float *y, int rows, int cols, int splits,
+                         int chunks_per_split, int tiles_per_item, void *stream)
+{
+    if (splits < 1) return MQ_ERR_COVERAGE;
+    const Plan p{splits, chunks_per_split, tiles_per_item};
+    return gemv_f32_common(Wp, x, y, rows, cols, &p, stream);
+}
+
+int mq_gemv_q6k_f32_plan_of(int rows, int cols, int *splits, int *chunks_per_split,
+                            int *tiles_per_item)
+{
+    if (!splits || !chunks_per_split || !tiles_per_item) return MQ_ERR_NULL;
+    Plan p;
+    const int st = f32_plan_of(rows, cols, &p);
+    if (st != MQ_OK) return st;
+    *splits = p.splits;
+    *chunks_per_split = p.cps;
+    *tiles_per_item = p.tpi;
+    return MQ_OK;
 }
 
 }  // extern "C"

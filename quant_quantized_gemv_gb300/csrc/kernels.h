@@ -72,6 +72,13 @@ bool gateup_opt_in(size_t max_plane);  // accept a staged plane of max_plane byt
 // group) and runs tpi consecutive groups; n_items is the number of CTAs.
 cudaError_t launch_gemv_batch(const GemvLaunch &a, cudaStream_t st);
 
+// q6_K GEMV against an f32 activation row (gemv_f32.cu): one part; q8 is
+// the row (cols floats) and q8_bytes its size; whole-tile plans or 2..12
+// splits per tile (no workspace).  Every CTA stages the row.
+cudaError_t launch_gemv_f32(const GemvLaunch &a, cudaStream_t st);
+int gemv_f32_ctas_per_sm(int warps_per_cta, size_t smem);
+size_t gemv_f32_max_x_bytes();  // largest row it stages; opts the kernel in
+
 constexpr int kGemvWarpsPerBlock = 4;   // CTA of independent warps
 constexpr int kMaxCtaSplits = 12;       // largest CTA whose warps are one tile's splits
 constexpr int kGemvStaticSmem = kMaxCtaSplits * 8 * 4;  // the split-combine buffer

@@ -128,6 +128,10 @@ WORKLOADS = {
     # Qwen2.5-14B attn_v and ffn_down, each fed by rms_norm -> q8
     "layer_14b": Workload("layer_14b", [("attn_v", "q6k", KV_14B, HIDDEN_14B, "rms"),
                                         ("ffn_down", "q6k", HIDDEN_14B, INTER_14B, "rms")]),
+    # the shapes of the pages' MMVQ-vs-f32 crossover (the D3 page, §2.3):
+    # 14B attn_v alone, and 2048 x 4864
+    "attn_v_14b": Workload("attn_v_14b", [("attn_v", "q6k", KV_14B, HIDDEN_14B, "rms")]),
+    "q6k_2048x4864": Workload("q6k_2048x4864", [("w", "q6k", 2048, 4864, "quantize")]),
     # the 152064 x 5120 q6_K output head, fed by rms_norm -> q8
     "lm_head_14b": Workload("lm_head_14b", [("output", "q6k", VOCAB, HIDDEN_14B, "rms")]),
     # the FFN half of a Qwen2.5-14B layer: rms_norm -> q8 -> gate, up (q4_K)

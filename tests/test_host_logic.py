@@ -334,3 +334,22 @@ def test_read_floor_validation(mq):
     assert L.mq_read_floor(ctypes.c_void_p(0x10000), 1000, N) == mq.MQ_ERR_SHAPE
     assert L.mq_read_floor(ctypes.c_void_p(0x10000), 0, N) == mq.MQ_ERR_SHAPE
     assert L.mq_read_floor(ctypes.c_void_p(0x10008), 1024, N) == mq.MQ_ERR_ALIGN
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="fake device pointers are only passed where no GPU exists")
+def test_f32_gemv_validation_rejects_before_launch(mq):
+    L = mq.lib()
+    A, X, Y = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30000)
+    N = ctypes.c_void_p(0)
+    assert L.mq_gemv_q6k_f32(N, X, Y, 8, 1024, N) == mq.MQ_ERR_NULL
+    assert L.mq_gemv_q6k_f32(A, N, Y, 8, 1024, N) == mq.MQ_ERR_NULL
+    assert L.mq_gemv_q6k_f32(A, X, Y, 8, 1000, N) == mq.MQ_ERR_SHAPE
+    assert L.mq_gemv_q6k_f32(A, ctypes.c_void_p(0x20004), Y, 8, 1024, N) == mq.MQ_ERR_ALIGN
+    # 64 x 18944: 19 chunks.  Dropped, empty, workspace-sized or zero plans never launch
+    for plan in [(5, 3, 1), (11, 2, 1), (1, 18, 1), (4, 5, 2), (19, 1, 1), (13, 2, 1), (0, 19, 1)]:
+        assert L.mq_gemv_q6k_f32_plan(A, X, Y, 64, 18944, *plan, N) == mq.MQ_ERR_COVERAGE, plan
+    s, c, t = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    assert L.mq_gemv_q6k_f32_plan_of(64, 18944, N, ctypes.byref(c), ctypes.byref(t)) == mq.MQ_ERR_NULL
+    assert L.mq_gemv_q6k_f32_plan_of(64, 1000, ctypes.byref(s), ctypes.byref(c),
+                                     ctypes.byref(t)) == mq.MQ_ERR_SHAPE
