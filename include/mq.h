@@ -209,9 +209,9 @@ int mq_gemv_q5k_q8_plan(const void *Wp, const void *q8, float *y, int rows, int 
  * device.  They cannot provide the split-K workspace of mq_gemv_q6k_q8.
  * This entry point computes the same y with the same kernel and default
  * plan; when that plan needs scratch (more than 12 splits per tile) it is
- * kept in a static device array inside the library (64 KiB per GPU, held
+ * kept in a static device array inside the library (128 KiB per GPU, held
  * until the process exits).  It allocates nothing.
- *   - Limit: if the default plan on this device needs more than 64 KiB of
+ *   - Limit: if the default plan on this device needs more than 128 KiB of
  *     scratch the call returns MQ_ERR_WORKSPACE and launches nothing.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call

@@ -366,7 +366,7 @@ def mq_gemv_plan(rows: int, cols: int, fmt: str = "q6k"):
     return _plan_out(lib().mq_gemv_plan, rows, cols, fmt_code(fmt))
 
 
-def mq_gemv_plan_for(rows: int, cols: int, sms: int, regs_per_thread: int = 168):
+def mq_gemv_plan_for(rows: int, cols: int, sms: int, regs_per_thread: int = 128):
     """Default plan for a device with `sms` SMs and a kernel of regs_per_thread registers."""
     return _plan_out(lib().mq_gemv_plan_for, rows, cols, sms, regs_per_thread)
 

@@ -14,8 +14,14 @@
 //     independent 16-byte loads per chunk, every warp-wide load instruction
 //     covers 512 contiguous bytes, and the weight loads bypass L1
 //     (ld.global.nc.L1::no_allocate) because each byte is used once.
-//   * Two register buffers per lane: chunk u+1 is in flight while chunk u is
-//     being computed, so a warp always has ~7 KB of loads outstanding.
+//   * One register buffer per lane and a 128-register cap, so 16 warps fit
+//     an SM: a warp issues chunk u+1's loads (~7 KB per warp) as soon as
+//     chunk u is computed, and the other warps of the SM hide the latency.
+//     Two buffers at 168 registers (12 warps per SM, each with a chunk in
+//     flight while it computes the other) measured slower on GB300: 14B
+//     decode sweep 2.383 against 2.298 ms per step, 5120 x 13824 13.7
+//     against 12.4 us, 3584 x 18944 12.38 against 11.71 us, the 152064 x
+//     5120 head equal (93.4 against 93.0 us).
 //   * One resident wave of warps: the host sizes the grid to the number of
 //     warps the SMs can hold.  A warp's work item is a contiguous run of
 //     chunk units: whole 8-row tiles when there are more tiles than warps,
@@ -146,7 +152,9 @@ __device__ __forceinline__ const uint8_t *stage_plane(const GemvLaunch &a, uint8
     return xs;
 }
 
-// Stream the part's units [u0, u1) with two register buffers.
+// Stream the part's units [u0, u1) through one register buffer: compute a
+// chunk, issue the next chunk's loads into the same registers, then finish
+// the tile if the chunk was its last.
 template <int FMT, bool SUBDOTS>
 __device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P, uint8_t *smem,
                                           int item, int u0, int u1, int lane)
@@ -154,9 +162,9 @@ __device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P
     using Regs = typename Fmt<FMT>::Regs;
     constexpr int kChunkBytes = Fmt<FMT>::kChunkBytes;
     const int nch = a.nchunks;
-    Regs A, B;
+    Regs A;
     int t = u0 / nch, c = u0 - t * nch;  // position of the next chunk to load
-    Unit xa = locate(a, P, t, c, lane, kChunkBytes), xb;
+    Unit xa = locate(a, P, t, c, lane, kChunkBytes);
     load_w(xa, lane, A);   // weights do not depend on the preceding kernel
     const uint8_t *xs = stage_plane(a, smem);  // the q8 plane, y and the workspace do
     load_x(a, xs, xa, lane, A);
@@ -165,26 +173,17 @@ __device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P
     float acc[8];
 #pragma unroll
     for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
-    for (int u = u0; u < u1; u += 2) {
-        const bool has_b = u + 1 < u1;
-        if (has_b) {
-            xb = locate(a, P, t, c, lane, kChunkBytes);
-            load_w(xb, lane, B);
-            load_x(a, xs, xb, lane, B);
-            if (++c == nch) { c = 0; ++t; }
-        }
+    for (int u = u0; u < u1; ++u) {
+        const int tcur = xa.t;
         compute<SUBDOTS>(a, P, A, xa, lane, acc);
-        if (!SUBDOTS && (!has_b || xb.t != xa.t)) flush_tile(a, P, xa.t, acc, item, u0, u1, lane);
-        if (!has_b) break;
-        const bool has_a = u + 2 < u1;
-        if (has_a) {
+        const bool more = u + 1 < u1;
+        if (more) {
             xa = locate(a, P, t, c, lane, kChunkBytes);
             load_w(xa, lane, A);
             load_x(a, xs, xa, lane, A);
             if (++c == nch) { c = 0; ++t; }
         }
-        compute<SUBDOTS>(a, P, B, xb, lane, acc);
-        if (!SUBDOTS && (!has_a || xa.t != xb.t)) flush_tile(a, P, xb.t, acc, item, u0, u1, lane);
+        if (!SUBDOTS && (!more || xa.t != tcur)) flush_tile(a, P, tcur, acc, item, u0, u1, lane);
     }
 }
 
@@ -198,7 +197,7 @@ __device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P
 // Measured on the 14B sweep: 2.39 ms with one kernel for all formats
 // against 2.49 ms with a kernel per format set (qkv, o, down alternating).
 template <bool SUBDOTS>
-__global__ void __launch_bounds__(32 * kMaxCtaSplits, 1)
+__global__ void __launch_bounds__(32 * kMaxCtaSplits) __maxnreg__(SUBDOTS ? 168 : kGemvMaxRegs)
     gemv_kernel(const __grid_constant__ GemvLaunch a)
 {
     extern __shared__ __align__(16) uint8_t xs[];  // the q8 plane, staged per CTA

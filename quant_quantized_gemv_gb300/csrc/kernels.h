@@ -80,6 +80,7 @@ int gemv_f32_ctas_per_sm(int warps_per_cta, size_t smem);
 size_t gemv_f32_max_x_bytes();  // largest row it stages; opts the kernel in
 
 constexpr int kGemvWarpsPerBlock = 4;   // CTA of independent warps
+constexpr int kGemvMaxRegs = 128;       // single-token GEMV registers per thread: 16 warps per SM
 constexpr int kMaxCtaSplits = 12;       // largest CTA whose warps are one tile's splits
 constexpr int kGemvStaticSmem = kMaxCtaSplits * 8 * 4;  // the split-combine buffer
 constexpr int kMaxTokens = 8;           // activation rows of the small-batch GEMV

@@ -27,10 +27,10 @@ namespace {
 
 using namespace mq;
 
-// Largest scratch a call may use.  With one resident wave of at most 1824
-// warps (152 SMs x 12 warps) a split plan needs at most 1824 x 32 B of
-// partials plus 4 B per tile of counters, about 62 KB.
-constexpr size_t kNoAllocScratchBytes = 64 * 1024;
+// Largest scratch a call may use.  With one resident wave of at most 2432
+// warps (152 SMs x 16 warps) a split plan needs at most 2432 x 32 B of
+// partials plus 4 B per tile of counters, about 80 KB.
+constexpr size_t kNoAllocScratchBytes = 128 * 1024;
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 

@@ -137,13 +137,18 @@ def test_plan_always_covers(mq, sms, regs):
 
 
 def test_plans_of_the_benchmark_shapes(mq):
-    """GB300: 152 SMs, 168 registers -> 3 four-warp CTAs (12 warps) per SM."""
-    assert mq.mq_gemv_plan_for(3584, 18944, 152, 168) == (4, 5, 1)     # 448 tiles x 4 splits
-    assert mq.mq_gemv_plan_for(152064, 5120, 152, 168) == (1, 5, 11)   # 11 whole tiles per warp
+    """GB300: 152 SMs, 128 registers -> 4 four-warp CTAs (16 warps) per SM."""
+    assert mq.mq_gemv_plan_for(3584, 18944, 152, 128) == (5, 4, 1)     # 448 tiles x 5 splits
+    assert mq.mq_gemv_plan_for(152064, 5120, 152, 128) == (1, 5, 8)    # 8 whole tiles per warp
+    assert mq.mq_gemv_plan_for(5120, 13824, 152, 128) == (3, 5, 1)
+    assert mq.mq_gemv_plan_for(5120, 5120, 152, 128) == (3, 2, 1)
+    assert mq.mq_gemv_plan_for(1024, 5120, 152, 128) == (5, 1, 1)
+    assert mq.mq_gemv_plan_for(13824, 5120, 152, 128) == (1, 5, 1)
+    assert mq.mq_gemv_plan_for(512, 18944, 152, 128) == (19, 1, 1)     # few tiles: workspace splits
+    # the same shapes at 168 registers (12 warps per SM)
+    assert mq.mq_gemv_plan_for(3584, 18944, 152, 168) == (4, 5, 1)
+    assert mq.mq_gemv_plan_for(152064, 5120, 152, 168) == (1, 5, 11)
     assert mq.mq_gemv_plan_for(5120, 13824, 152, 168) == (2, 7, 1)
-    assert mq.mq_gemv_plan_for(1024, 5120, 152, 168) == (5, 1, 1)
-    assert mq.mq_gemv_plan_for(13824, 5120, 152, 168) == (1, 5, 1)
-    assert mq.mq_gemv_plan_for(512, 18944, 152, 168) == (19, 1, 1)     # few tiles: workspace splits
 
 
 def test_workspace_sizes(mq):
