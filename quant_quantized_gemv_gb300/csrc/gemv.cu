@@ -197,7 +197,7 @@ __device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P
 // Measured on the 14B sweep: 2.39 ms with one kernel for all formats
 // against 2.49 ms with a kernel per format set (qkv, o, down alternating).
 template <bool SUBDOTS>
-__global__ void __launch_bounds__(32 * kMaxCtaSplits) __maxnreg__(SUBDOTS ? 168 : kGemvMaxRegs)
+__global__ void __maxnreg__(SUBDOTS ? 168 : kGemvMaxRegs)
     gemv_kernel(const __grid_constant__ GemvLaunch a)
 {
     extern __shared__ __align__(16) uint8_t xs[];  // the q8 plane, staged per CTA
