@@ -47,7 +47,9 @@ typedef enum {
                               cover it twice; nothing was launched ([D4-2] §6
                               lesson 1: a gate must bound both sides)         */
     MQ_ERR_WORKSPACE = 5,  /* split-K needs a larger workspace               */
-    MQ_ERR_CUDA = 6        /* a CUDA call failed (mq_last_error says which)   */
+    MQ_ERR_CUDA = 6,       /* a CUDA call failed (mq_last_error says which)   */
+    MQ_ERR_ACCESS = 7      /* a pointer the GPU cannot address (pageable host
+                              memory, or not an allocation CUDA knows)         */
 } mq_status;
 
 /* Static message for a status code. */
@@ -414,6 +416,24 @@ int mq_gemv_q4k_q8_subdots(const void *Wp, const void *q8, int32_t *isums, int r
                            void *stream);
 int mq_gemv_q5k_q8_subdots(const void *Wp, const void *q8, int32_t *isums, int rows, int cols,
                            void *stream);
+
+/* Copy for the ends of a decode step (no counterpart on the pages): moves
+ * `bytes` from src to dst with a kernel, so that the host-to-device copy of
+ * a step's input and the device-to-host copy of its result join the launch
+ * chain of the producers and GEMVs (programmatic dependent launch, graph
+ * capture) instead of handing the stream to a copy engine and back.
+ *   src, dst: device memory of the current device, or pinned host memory
+ *     (cudaHostAlloc / cudaMallocHost / cudaHostRegister) that the device
+ *     can address; the library looks each pointer up (cudaPointerGetAttributes)
+ *     and uses the device-side address of pinned host memory.  Pageable host
+ *     memory and unknown pointers give MQ_ERR_ACCESS and nothing runs.
+ *   bytes: a multiple of 16 (> 0); both pointers 16-byte aligned.
+ *   Ordering: the kernel waits for the preceding kernel in the stream
+ *   before it reads or writes, so it may follow a GEMV (its output) or
+ *   precede a producer (its input).  The host must not touch a pinned buffer
+ *   while a copy that uses it may run (synchronize first).
+ * Errors: MQ_ERR_NULL, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_ACCESS, MQ_ERR_CUDA. */
+int mq_copy(void *dst, const void *src, size_t bytes, void *stream);
 
 /* Measurement aid: read `bytes` (a multiple of 16) at src (device, 16-byte
  * aligned) once, in one launch, and do nothing with them.  Its time is the

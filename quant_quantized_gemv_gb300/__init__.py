@@ -23,7 +23,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 _SO = os.path.join(_PKG, "_build", "libmq.so")
 _lib = None
 
-MQ_OK, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_NULL, MQ_ERR_COVERAGE, MQ_ERR_WORKSPACE, MQ_ERR_CUDA = range(7)
+(MQ_OK, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_NULL, MQ_ERR_COVERAGE, MQ_ERR_WORKSPACE, MQ_ERR_CUDA,
+ MQ_ERR_ACCESS) = range(8)
 
 # every symbol include/mq.h declares
 EXPORTS = [
@@ -42,7 +43,7 @@ EXPORTS = [
     "mq_gemv_gateup_plan_for", "mq_repacked_bytes_q5k", "mq_repack_q5k", "mq_unrepack_q5k",
     "mq_gemv_q5k_q8", "mq_gemv_q5k_q8_plan", "mq_gemv_q5k_q8_subdots", "mq_gemv_q5k_q8_batch",
     "mq_gemv_q5k_q8_batch_plan", "mq_read_floor", "mq_gemv_q6k_f32", "mq_gemv_q6k_f32_plan",
-    "mq_gemv_q6k_f32_plan_of",
+    "mq_gemv_q6k_f32_plan_of", "mq_copy",
 ]
 
 
@@ -135,6 +136,7 @@ def lib():
         "mq_gemv_q6k_f32": ([P, P, P, I, I, P], I),
         "mq_gemv_q6k_f32_plan": ([P, P, P, I, I, I, I, I, P], I),
         "mq_gemv_q6k_f32_plan_of": ([I, I, P, P, P], I),
+        "mq_copy": ([P, P, S, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -380,6 +382,22 @@ def mq_read_floor(buf, nbytes: int = None, stream=None):
     """One plain read of nbytes (default: all) of a device tensor: the single-launch floor."""
     nb = buf.numel() * buf.element_size() if nbytes is None else int(nbytes)
     _check(lib().mq_read_floor(_dev(buf), nb, _stream(stream)), "mq_read_floor")
+
+
+def mq_copy(dst, src, nbytes: int = None, stream=None):
+    """Copy nbytes (default: all of src) from src to dst with a kernel; each
+    may be a CUDA tensor or a pinned CPU tensor."""
+    import torch
+    for t in (dst, src):
+        if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+            raise TypeError("expected contiguous tensors")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError("a CPU tensor must be pinned (the GPU reads it directly)")
+    nb = src.numel() * src.element_size() if nbytes is None else int(nbytes)
+    if nb > dst.numel() * dst.element_size():
+        raise ValueError("destination smaller than the copy")
+    _check(lib().mq_copy(ctypes.c_void_p(dst.data_ptr()), ctypes.c_void_p(src.data_ptr()), nb,
+                         _stream(stream)), "mq_copy")
 
 
 def mq_device_sms() -> int:

@@ -635,6 +635,35 @@ int gemv_f32_common(const void *Wp, const float *x, float *y, int rows, int cols
     return e == cudaSuccess ? MQ_OK : cuda_fail("f32 GEMV launch", e);
 }
 
+// The address a kernel on the current device uses for p: p itself for
+// device or managed memory, the mapped device address for pinned host
+// memory; MQ_ERR_ACCESS for pageable host memory or unknown pointers.
+int device_address(const void *p, void **out)
+{
+    cudaPointerAttributes at;
+    const cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error of a failed lookup
+        return MQ_ERR_ACCESS;
+    }
+    const int dev = current_device();
+    switch (at.type) {
+    case cudaMemoryTypeDevice:
+        if (at.device != dev) return MQ_ERR_ACCESS;
+        *out = const_cast<void *>(p);
+        return MQ_OK;
+    case cudaMemoryTypeManaged:
+        *out = const_cast<void *>(p);
+        return MQ_OK;
+    case cudaMemoryTypeHost:
+        if (!at.devicePointer) return MQ_ERR_ACCESS;
+        *out = at.devicePointer;
+        return MQ_OK;
+    default:
+        return MQ_ERR_ACCESS;
+    }
+}
+
 }  // namespace
 
 extern "C" {
@@ -649,6 +678,7 @@ const char *mq_strerror(int status)
     case MQ_ERR_COVERAGE: return "dispatch plan does not cover every chunk exactly once";
     case MQ_ERR_WORKSPACE: return "split-K workspace too small";
     case MQ_ERR_CUDA: return "a CUDA call failed (mq_last_error names it)";
+    case MQ_ERR_ACCESS: return "pointer not addressable by the GPU (pageable host memory?)";
     default: return "unknown status";
     }
 }
@@ -927,6 +957,22 @@ int mq_gemv_gateup_plan_for(int rows, int sms, int regs_per_thread, int *warps_p
     *warps_per_cta = p.wpb;
     *ctas = p.ctas;
     return MQ_OK;
+}
+
+int mq_copy(void *dst, const void *src, size_t bytes, void *stream)
+{
+    if (!dst || !src) return MQ_ERR_NULL;
+    if (bytes == 0 || bytes % 16 != 0) return MQ_ERR_SHAPE;
+    if (!aligned16(dst) || !aligned16(src)) return MQ_ERR_ALIGN;
+    void *d = nullptr;
+    const void *sp = nullptr;
+    int st = device_address(dst, &d);
+    if (st == MQ_OK) st = device_address(src, const_cast<void **>(&sp));
+    if (st != MQ_OK) return st;
+    if (!aligned16(d) || !aligned16(sp)) return MQ_ERR_ALIGN;
+    const cudaError_t e = launch_copy(d, sp, bytes, g_pdl.load(std::memory_order_relaxed),
+                                      (cudaStream_t)stream);
+    return e == cudaSuccess ? MQ_OK : cuda_fail("copy launch", e);
 }
 
 int mq_read_floor(const void *src, size_t bytes, void *stream)

@@ -130,6 +130,10 @@ cudaError_t launch_swiglu_quant_q8(const float *g, const float *u, float *y, uin
 // any kernel that streams those bytes once (readfloor.cu).  sink may be null.
 cudaError_t launch_read_floor(const void *src, size_t bytes, unsigned *sink, int sms, cudaStream_t st);
 
+// Copy `bytes` (multiple of 16) from src to dst, both device-addressable
+// (copy.cu), as a kernel that takes part in the launch chain.
+cudaError_t launch_copy(void *dst, const void *src, size_t bytes, int pdl, cudaStream_t st);
+
 // Record the library's last CUDA failure on this thread (`where` and the CUDA
 // error, readable with mq_last_error); returns MQ_ERR_CUDA.
 int cuda_fail(const char *where, cudaError_t e);

@@ -358,3 +358,18 @@ def test_f32_gemv_validation_rejects_before_launch(mq):
     assert L.mq_gemv_q6k_f32_plan_of(64, 18944, N, ctypes.byref(c), ctypes.byref(t)) == mq.MQ_ERR_NULL
     assert L.mq_gemv_q6k_f32_plan_of(64, 1000, ctypes.byref(s), ctypes.byref(c),
                                      ctypes.byref(t)) == mq.MQ_ERR_SHAPE
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="fake device pointers are only passed where no GPU exists")
+def test_copy_validation(mq):
+    L = mq.lib()
+    N = ctypes.c_void_p(0)
+    A, B = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000)
+    assert L.mq_copy(N, B, 1024, N) == mq.MQ_ERR_NULL
+    assert L.mq_copy(A, N, 1024, N) == mq.MQ_ERR_NULL
+    assert L.mq_copy(A, B, 1000, N) == mq.MQ_ERR_SHAPE
+    assert L.mq_copy(A, B, 0, N) == mq.MQ_ERR_SHAPE
+    assert L.mq_copy(A, ctypes.c_void_p(0x20008), 1024, N) == mq.MQ_ERR_ALIGN
+    assert L.mq_copy(A, B, 1024, N) == mq.MQ_ERR_ACCESS      # nothing CUDA knows
+    assert b"pageable" in L.mq_strerror(mq.MQ_ERR_ACCESS)
