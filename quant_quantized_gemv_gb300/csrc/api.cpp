@@ -37,7 +37,7 @@ std::atomic<int> g_sms[kMaxDevices];
 std::atomic<int> g_ctas[kMaxDevices][kMaxCtaSplits + 1];
 std::atomic<int> g_pdl{0};
 // resident small-batch CTAs per SM (register limit): [device][nt][warps per CTA]
-std::atomic<int> g_batch_ctas[kMaxDevices][kMaxTokens + 1][7][kBatchMaxCtaSplits + 1];  // [..][fmt]
+std::atomic<int> g_batch_ctas[kMaxDevices][kMaxTokens + 1][7][kBatchMaxCtaWarps + 1];  // [..][fmt]
 // resident gate||up CTAs per SM (register limit): [device][warps per CTA]
 constexpr int kGateUpMaxWarps = 8;
 std::atomic<int> g_gateup_ctas[kMaxDevices][7][kGateUpMaxWarps + 1];  // [device][fmt][warps]
@@ -78,7 +78,7 @@ int device_sms()
 
 // ctas[w], w = 1..kMaxCtaSplits: resident GEMV CTAs per SM with w warps each.
 struct Occupancy {
-    int ctas[kMaxCtaSplits + 1];  // CTAs with w warps, no dynamic shared memory
+    int ctas[kBatchMaxCtaWarps + 1];  // CTAs with w warps, no dynamic shared memory
     int ctas_tiles;               // 4-warp whole-tile CTAs holding the staged plane
 };
 
@@ -148,6 +148,7 @@ bool device_occupancy(Occupancy *o, size_t plane)
 }
 
 // The small-batch kernel for nt tokens: every CTA stages all nt planes.
+// CTA shapes up to the kernel's warp budget (batch_warp_budget).
 bool batch_occupancy(Occupancy *o, int nt, int fmt, size_t planes)
 {
     const int dev = current_device();
@@ -155,7 +156,8 @@ bool batch_occupancy(Occupancy *o, int nt, int fmt, size_t planes)
     if (dev < 0 || !device_limits(&lim)) return false;
     const long long per_cta = (long long)planes + kBatchStaticSmem + lim.smem_reserved;
     const int by_smem = (int)(lim.smem_per_sm / per_cta);
-    for (int w = 1; w <= kBatchMaxCtaSplits; ++w) {
+    const int budget = batch_warp_budget(nt, fmt);
+    for (int w = 1; w <= budget; ++w) {
         std::atomic<int> &slot = g_batch_ctas[dev][nt][fmt][w];
         int v = slot.load(std::memory_order_relaxed);
         if (v <= 0) {
@@ -165,9 +167,9 @@ bool batch_occupancy(Occupancy *o, int nt, int fmt, size_t planes)
         }
         o->ctas[w] = v < by_smem ? v : by_smem;
     }
-    for (int w = kBatchMaxCtaSplits + 1; w <= kMaxCtaSplits; ++w) o->ctas[w] = 0;
+    for (int w = budget + 1; w <= kBatchMaxCtaWarps; ++w) o->ctas[w] = 0;
     o->ctas_tiles = 0;  // unused by the small-batch plans
-    return o->ctas[kBatchMaxCtaSplits] > 0;
+    return o->ctas[budget] > 0;
 }
 
 // The same from a register count (host-only planning, tests): 64K registers
@@ -177,7 +179,7 @@ Occupancy model_occupancy(int regs_per_thread, size_t plane)
     Occupancy o;
     const int regs = ((regs_per_thread + 7) / 8) * 8;
     const int by_smem = (int)(233472 / ((long long)plane + kGemvStaticSmem + 1024));
-    for (int w = 1; w <= kMaxCtaSplits; ++w) {
+    for (int w = 1; w <= kBatchMaxCtaWarps; ++w) {
         int c = 65536 / (w * 32 * regs);
         if (c > 2048 / (32 * w)) c = 2048 / (32 * w);
         if (c > 32) c = 32;
@@ -222,11 +224,11 @@ Plan plan_for(int ntiles, int nchunks, int sms, const Occupancy &o)
 }
 
 // Small-batch plan: S splits per tile (1..12, none empty), CTAs of S warps
-// per tile x 12 / S tiles, each CTA running tpi tile groups.  Every CTA
+// per tile x budget / S tiles, each CTA running tpi tile groups.  Every CTA
 // stages all nt planes, so the resident CTAs per SM come from the
 // occupancy with that much shared memory.  Choose the S whose busiest warp
 // streams the fewest chunks, scaled up when the grid leaves SMs idle.
-Plan batch_plan_for(int ntiles, int nchunks, int sms, const Occupancy &o)
+Plan batch_plan_for(int ntiles, int nchunks, int sms, const Occupancy &o, int budget)
 {
     if (sms <= 0) sms = 1;
     Plan best{1, nchunks, 1};
@@ -234,7 +236,7 @@ Plan batch_plan_for(int ntiles, int nchunks, int sms, const Occupancy &o)
     for (int S = 1; S <= kBatchMaxCtaSplits && S <= nchunks; ++S) {
         const int cps = ceil_div(nchunks, S);
         if ((long long)(S - 1) * cps >= nchunks) continue;  // an empty split
-        const int G = kBatchMaxCtaSplits / S, W = S * G;
+        const int G = budget / S, W = S * G;
         const long long resident = (long long)sms * o.ctas[W];
         if (resident <= 0) continue;
         const long long groups = (ntiles + G - 1) / G;
@@ -250,9 +252,9 @@ Plan batch_plan_for(int ntiles, int nchunks, int sms, const Occupancy &o)
     return best;
 }
 
-long long batch_ctas(int ntiles, const Plan &p)
+long long batch_ctas(int ntiles, const Plan &p, int budget)
 {
-    const int G = kBatchMaxCtaSplits / p.splits;
+    const int G = budget / p.splits;
     const long long groups = (ntiles + G - 1) / G;
     return (groups + p.tpi - 1) / p.tpi;
 }
@@ -346,7 +348,8 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
             pl = plan_for((int)total_tiles, nchunks, device_sms(), o);
         } else {
             if (!batch_occupancy(&o, nt, parts[0].fmt, (size_t)nt * plane)) return MQ_ERR_CUDA;
-            pl = batch_plan_for((int)total_tiles, nchunks, device_sms(), o);
+            pl = batch_plan_for((int)total_tiles, nchunks, device_sms(), o,
+                                batch_warp_budget(nt, parts[0].fmt));
         }
     }
     const int cov = batch ? check_batch_plan(nchunks, pl) : check_plan(nchunks, pl);
@@ -364,7 +367,7 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
         gp.item0 = (int)items;
         gp.tile0 = (int)tiles;
         gp.tile_bytes_div16 = (int)(g.tile_bytes / 16);
-        items += batch ? batch_ctas(g.ntiles, pl) : plan_items(g.ntiles, pl);
+        items += batch ? batch_ctas(g.ntiles, pl, batch_warp_budget(nt, x.fmt)) : plan_items(g.ntiles, pl);
         tiles += g.ntiles;
     }
     if (items >= (1LL << 31)) return MQ_ERR_SHAPE;
@@ -431,7 +434,7 @@ int batch_plan_of(int rows, int cols, int nt, Plan *p)
     if (!device_limits(&lim)) return MQ_ERR_CUDA;
     if ((size_t)nt * plane > lim.max_batch_planes) return MQ_ERR_SHAPE;
     if (!batch_occupancy(&o, nt, 6, (size_t)nt * plane)) return MQ_ERR_CUDA;
-    *p = batch_plan_for(g.ntiles, g.nchunks, device_sms(), o);
+    *p = batch_plan_for(g.ntiles, g.nchunks, device_sms(), o, batch_warp_budget(nt, 6));
     return MQ_OK;
 }
 
@@ -880,9 +883,11 @@ int mq_gemv_batch_plan_for(int rows, int cols, int nt, int sms, int regs_per_thr
     const size_t planes = (size_t)nt * q8_plane_bytes(cols);
     Occupancy o = model_occupancy(regs_per_thread, 0);
     const int by_smem = (int)(233472 / ((long long)planes + kBatchStaticSmem + 1024));
-    for (int w = 1; w <= kMaxCtaSplits; ++w)
+    for (int w = 1; w <= kBatchMaxCtaWarps; ++w)
         if (o.ctas[w] > by_smem) o.ctas[w] = by_smem;
-    const Plan p = batch_plan_for(g.ntiles, g.nchunks, sms, o);
+    // the kernel's budget follows its register cap: 16 warps at 128, else 12
+    const int budget = regs_per_thread <= 128 ? kBatchMaxCtaWarps : 12;
+    const Plan p = batch_plan_for(g.ntiles, g.nchunks, sms, o, budget);
     *splits = p.splits;
     *chunks_per_split = p.cps;
     *tiles_per_item = p.tpi;

@@ -21,8 +21,9 @@
 //   * A weight row's codes are decoded once per token group and used for
 //     every token of the group: the decode, not the dp4a, dominates the ALU
 //     work of a chunk.
-//   * CTAs hold at most 12 warps of at most 168 registers: one CTA per SM
-//     stages the planes once for 12 warps.
+//   * One CTA per SM stages the planes once for all its warps: 16 warps at
+//     128 registers where the token count allows it without spilling (2
+//     tokens; 3 of q4_K / q5_K), else 12 warps at 168 registers.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -186,11 +187,12 @@ __device__ __forceinline__ void compute(const GemvLaunch &a, const uint8_t *xs, 
 // partials in ascending split order.  The exchange buffer alternates with the
 // tile iteration, so one barrier per tile suffices: a buffer is rewritten two
 // iterations later, after every warp has passed the barrier in between.
-template <int NT>
+template <int NT, int FMT>
 __device__ __forceinline__ void flush_tile(const GemvLaunch &a, const GemvPart &P, int t, bool valid,
                                            int iter, Acc<NT> &acc, int lane)
 {
-    __shared__ float xchg[2][kBatchMaxCtaSplits][NT][8];
+    constexpr int kWarps = batch_warp_budget(NT, FMT);
+    __shared__ float xchg[2][kWarps][NT][8];
     float v[NT];
 #pragma unroll
     for (int k = 0; k < NT; ++k) {
@@ -212,7 +214,7 @@ __device__ __forceinline__ void flush_tile(const GemvLaunch &a, const GemvPart &
         return;
     }
     const int w = threadIdx.x >> 5, sp = w % a.splits;
-    float(&buf)[kBatchMaxCtaSplits][NT][8] = xchg[iter & 1];
+    float(&buf)[kWarps][NT][8] = xchg[iter & 1];
 #pragma unroll
     for (int k = 0; k < NT; ++k) {
 #pragma unroll
@@ -249,7 +251,7 @@ __device__ __forceinline__ void stage_planes(const GemvLaunch &a, uint8_t *xs)
     asm volatile("bar.sync 1, %0;" ::"r"(blockDim.x) : "memory");
 }
 
-// Work decomposition.  A CTA has S * G warps (S = a.splits, G = 12 / S tiles
+// Work decomposition.  A CTA has S * G warps (S = a.splits, G = budget / S tiles
 // per group): warp w takes split w % S of tile w / S of each group.  The CTA
 // runs a.tpi consecutive groups, so the staged planes serve a.tpi * G tiles.
 // Split s covers chunks [s * cps, min((s + 1) * cps, nchunks)) of a row.  A
@@ -275,7 +277,7 @@ __device__ __forceinline__ void run_batch(const GemvLaunch &a, const GemvPart &P
 {
     using W = typename Fmt<FMT>::W;
     constexpr int kChunkBytes = Fmt<FMT>::kChunkBytes;
-    const int S = a.splits, G = kBatchMaxCtaSplits / S;
+    const int S = a.splits, G = batch_warp_budget(NT, FMT) / S;
     const int w = threadIdx.x >> 5, sp = w % S, o = w / S;
     const int c_lo = sp * a.cps, c_hi = min(c_lo + a.cps, a.nchunks);
     const int group0 = blockIdx.x * a.tpi;
@@ -319,7 +321,7 @@ __device__ __forceinline__ void run_batch(const GemvLaunch &a, const GemvPart &P
                 advance(next);
             }
             if (last) {
-                flush_tile<NT>(a, P, t, t < P.ntiles, done, acc, lane);
+                flush_tile<NT, FMT>(a, P, t, t < P.ntiles, done, acc, lane);
                 ++done;
             }
         }
@@ -333,7 +335,7 @@ __device__ __forceinline__ void run_batch(const GemvLaunch &a, const GemvPart &P
             }
             compute<FMT, NT>(a, xs, xa, lane, A, acc);
             if (xa.c == c_hi - 1) {
-                flush_tile<NT>(a, P, xa.t, xa.t < P.ntiles, done, acc, lane);
+                flush_tile<NT, FMT>(a, P, xa.t, xa.t < P.ntiles, done, acc, lane);
                 ++done;
             }
             if (!has_b) break;
@@ -345,7 +347,7 @@ __device__ __forceinline__ void run_batch(const GemvLaunch &a, const GemvPart &P
             }
             compute<FMT, NT>(a, xs, xb, lane, B, acc);
             if (xb.c == c_hi - 1) {
-                flush_tile<NT>(a, P, xb.t, xb.t < P.ntiles, done, acc, lane);
+                flush_tile<NT, FMT>(a, P, xb.t, xb.t < P.ntiles, done, acc, lane);
                 ++done;
             }
         }
@@ -354,7 +356,7 @@ __device__ __forceinline__ void run_batch(const GemvLaunch &a, const GemvPart &P
 
 // One kernel per (tokens, format): each gets its own register allocation.
 template <int NT, int FMT>
-__global__ void __launch_bounds__(32 * kBatchMaxCtaSplits, 1)
+__global__ void __maxnreg__(batch_small_regs(NT, FMT) ? 128 : 168)
     gemv_batch_kernel(const __grid_constant__ GemvLaunch a)
 {
     extern __shared__ __align__(16) uint8_t xs[];  // the nt q8 planes
@@ -393,7 +395,7 @@ cudaError_t launch_gemv_batch(const GemvLaunch &a, cudaStream_t st)
 {
     const KernelFn k = kernel_for(a.nt, a.part[0].fmt);
     if (!k) return cudaErrorInvalidValue;
-    const int warps = gemv_batch_cta_warps(a.splits);
+    const int warps = gemv_batch_cta_warps(a.splits, batch_warp_budget(a.nt, a.part[0].fmt));
     return launch_maybe_pdl(k, dim3((unsigned)a.n_items), dim3(32 * warps),
                             (size_t)a.nt * a.q8_bytes, a.pdl, st, a);
 }

@@ -68,7 +68,7 @@ bool gateup_opt_in(size_t max_plane);  // accept a staged plane of max_plane byt
 
 // Small-batch GEMV (gemv_batch.cu), 1 <= a.nt <= kMaxTokens, one part whose
 // y holds nt x rows outputs, token-major.  Its plan reads differently: each
-// CTA holds `splits` warps for each of kBatchMaxCtaSplits / splits tiles (a
+// CTA holds `splits` warps for each of batch_warp_budget / splits tiles (a
 // group) and runs tpi consecutive groups; n_items is the number of CTAs.
 cudaError_t launch_gemv_batch(const GemvLaunch &a, cudaStream_t st);
 
@@ -84,8 +84,22 @@ constexpr int kGemvMaxRegs = 128;       // single-token GEMV registers per threa
 constexpr int kMaxCtaSplits = 12;       // largest CTA whose warps are one tile's splits
 constexpr int kGemvStaticSmem = kMaxCtaSplits * 8 * 4;  // the split-combine buffer
 constexpr int kMaxTokens = 8;           // activation rows of the small-batch GEMV
-constexpr int kBatchMaxCtaSplits = 12;  // its CTAs hold at most 12 warps (168 registers each)
-constexpr int kBatchStaticSmem = 2 * kBatchMaxCtaSplits * kMaxTokens * 8 * 4;  // split exchange
+constexpr int kBatchMaxCtaSplits = 12;  // most splits of a tile (warps of one tile in a CTA)
+constexpr int kBatchMaxCtaWarps = 16;   // most warps of a CTA (a whole SM at 128 registers)
+constexpr int kBatchStaticSmem = 2 * kBatchMaxCtaSplits * kMaxTokens * 8 * 4;  // split exchange (max)
+
+// Register cap and warps per CTA of the small-batch kernel for nt tokens of
+// format fmt.  Where the kernel fits 128 registers without spilling (2
+// tokens; 3 tokens of q4_K / q5_K) a CTA holds 16 warps, the whole SM;
+// otherwise 168 registers and 12 warps.
+__host__ __device__ constexpr bool batch_small_regs(int nt, int fmt)
+{
+    return nt == 2 || (nt == 3 && fmt != 6);
+}
+__host__ __device__ constexpr int batch_warp_budget(int nt, int fmt)
+{
+    return batch_small_regs(nt, fmt) ? kBatchMaxCtaWarps : 12;
+}
 
 // Warps per CTA for a plan with `splits` splits.
 inline int gemv_cta_warps(int splits, bool subdots = false)
@@ -94,10 +108,10 @@ inline int gemv_cta_warps(int splits, bool subdots = false)
 }
 
 // Warps per CTA of the small-batch kernel: `splits` warps per tile times
-// kBatchMaxCtaSplits / splits tiles per group.
-inline int gemv_batch_cta_warps(int splits)
+// budget / splits tiles per group.
+inline int gemv_batch_cta_warps(int splits, int budget)
 {
-    return splits * (kBatchMaxCtaSplits / splits);
+    return splits * (budget / splits);
 }
 
 // Resident CTAs per SM of the small-batch kernel for nt tokens of format

@@ -260,6 +260,17 @@ def test_batch_plans_of_the_benchmark_shapes(mq):
         assert mq.mq_gemv_batch_plan_for(13824, 5120, nt, 152) == (1, 5, 1)
 
 
+def test_batch_plans_with_sixteen_warp_ctas(mq):
+    """At 128 registers a CTA holds 16 warps: 7B ffn_down takes 5 splits x 3
+    tiles (15 warps) per CTA."""
+    assert mq.mq_gemv_batch_plan_for(3584, 18944, 2, 152, 128) == (5, 4, 1)
+    for nt in (2, 3):
+        for rows, cols in [(152064, 5120), (5120, 13824), (1024, 5120), (61, 1280)]:
+            s, cps, tpi = mq.mq_gemv_batch_plan_for(rows, cols, nt, 152, 128)
+            nch = -(-(cols // 256) // 4)
+            assert 1 <= s <= 12 and mq.mq_check_coverage(nch, s, cps) == mq.MQ_OK
+
+
 @pytest.mark.skipif(__import__("torch").cuda.is_available(),
                     reason="fake device pointers are only passed where no GPU exists")
 def test_batch_validation_rejects_before_launch(mq):
