@@ -417,6 +417,17 @@ int mq_gemv_q4k_q8_subdots(const void *Wp, const void *q8, int32_t *isums, int r
 int mq_gemv_q5k_q8_subdots(const void *Wp, const void *q8, int32_t *isums, int rows, int cols,
                            void *stream);
 
+/* Repack on the device: the same bytes as mq_repack_q6k / _q4k / _q5k (host)
+ * for GGUF rows that are already in device memory, written by a kernel
+ * (the pages build the dense plane once at weight registration, [D4-4]
+ * §3.1; on the GPU a multi-GB weight set repacks at memory speed).
+ *   fmt: 6 (q6_K), 4 (q4_K) or 5 (q5_K).
+ *   gguf: device, rows x cols/256 GGUF blocks (2-byte aligned or better).
+ *   dst: device, mq_repacked_bytes_*(rows, cols) bytes, 16-byte aligned;
+ *        zero-filled, then written (padding rows stay zero), on `stream`.
+ * Errors: MQ_ERR_NULL, MQ_ERR_SHAPE (fmt or shape), MQ_ERR_ALIGN, MQ_ERR_CUDA. */
+int mq_repack_device(int fmt, const void *gguf, void *dst, int rows, int cols, void *stream);
+
 /* Copy for the ends of a decode step (no counterpart on the pages): moves
  * `bytes` from src to dst with a kernel, so that the host-to-device copy of
  * a step's input and the device-to-host copy of its result join the launch

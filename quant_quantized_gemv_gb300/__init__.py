@@ -43,7 +43,7 @@ EXPORTS = [
     "mq_gemv_gateup_plan_for", "mq_repacked_bytes_q5k", "mq_repack_q5k", "mq_unrepack_q5k",
     "mq_gemv_q5k_q8", "mq_gemv_q5k_q8_plan", "mq_gemv_q5k_q8_subdots", "mq_gemv_q5k_q8_batch",
     "mq_gemv_q5k_q8_batch_plan", "mq_read_floor", "mq_gemv_q6k_f32", "mq_gemv_q6k_f32_plan",
-    "mq_gemv_q6k_f32_plan_of", "mq_copy",
+    "mq_gemv_q6k_f32_plan_of", "mq_copy", "mq_repack_device",
 ]
 
 
@@ -137,6 +137,7 @@ def lib():
         "mq_gemv_q6k_f32_plan": ([P, P, P, I, I, I, I, I, P], I),
         "mq_gemv_q6k_f32_plan_of": ([I, I, P, P, P], I),
         "mq_copy": ([P, P, S, P], I),
+        "mq_repack_device": ([I, P, P, I, I, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -382,6 +383,23 @@ def mq_read_floor(buf, nbytes: int = None, stream=None):
     """One plain read of nbytes (default: all) of a device tensor: the single-launch floor."""
     nb = buf.numel() * buf.element_size() if nbytes is None else int(nbytes)
     _check(lib().mq_read_floor(_dev(buf), nb, _stream(stream)), "mq_read_floor")
+
+
+def mq_repack_device(fmt: str, gguf, rows: int, cols: int, out=None, stream=None):
+    """Repack GGUF rows already on the device (a uint8 CUDA tensor) into a
+    new (or the given) device buffer; the bytes equal mq_repack(fmt, ...)."""
+    import torch
+    code = fmt_code(fmt)
+    nbytes = {6: mq_repacked_bytes_q6k, 4: mq_repacked_bytes_q4k, 5: mq_repacked_bytes_q5k}[code](rows, cols)
+    if nbytes == 0:
+        raise MQError(MQ_ERR_SHAPE, "mq_repack_device")
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=gguf.device)
+    elif out.numel() * out.element_size() < nbytes:
+        raise ValueError("output smaller than the repacked size")
+    _check(lib().mq_repack_device(code, _dev(gguf), _dev(out), rows, cols, _stream(stream)),
+           "mq_repack_device")
+    return out
 
 
 def mq_copy(dst, src, nbytes: int = None, stream=None):

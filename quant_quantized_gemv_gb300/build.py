@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 SO = os.path.join(BUILD, "libmq.so")
 SOURCES = ["gemv.cu", "gemv_batch.cu", "gemv_gateup.cu", "gemv_f32.cu", "producers.cu", "noalloc.cu",
-           "readfloor.cu", "copy.cu", "api.cpp", "repack.cpp"]
+           "readfloor.cu", "copy.cu", "repack_device.cu", "api.cpp", "repack.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

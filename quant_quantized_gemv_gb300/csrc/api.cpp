@@ -964,6 +964,15 @@ int mq_gemv_gateup_plan_for(int rows, int sms, int regs_per_thread, int *warps_p
     return MQ_OK;
 }
 
+int mq_repack_device(int fmt, const void *gguf, void *dst, int rows, int cols, void *stream)
+{
+    if (!gguf || !dst) return MQ_ERR_NULL;
+    if (block_bytes(fmt) == 0 || !gemv_shape_ok(rows, cols)) return MQ_ERR_SHAPE;
+    if (!aligned16(dst) || ((uintptr_t)gguf & 1u) != 0) return MQ_ERR_ALIGN;
+    const cudaError_t e = launch_repack(fmt, gguf, dst, rows, cols, (cudaStream_t)stream);
+    return e == cudaSuccess ? MQ_OK : cuda_fail("device repack launch", e);
+}
+
 int mq_copy(void *dst, const void *src, size_t bytes, void *stream)
 {
     if (!dst || !src) return MQ_ERR_NULL;

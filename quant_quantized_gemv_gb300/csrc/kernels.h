@@ -144,6 +144,10 @@ cudaError_t launch_swiglu_quant_q8(const float *g, const float *u, float *y, uin
 // any kernel that streams those bytes once (readfloor.cu).  sink may be null.
 cudaError_t launch_read_floor(const void *src, size_t bytes, unsigned *sink, int sms, cudaStream_t st);
 
+// The host repack of repack.cpp on the device (repack_device.cu): zero-fills
+// dst, then writes every unit's planes (fmt 6, 4 or 5; shape already checked).
+cudaError_t launch_repack(int fmt, const void *src, void *dst, int rows, int cols, cudaStream_t st);
+
 // Copy `bytes` (multiple of 16) from src to dst, both device-addressable
 // (copy.cu), as a kernel that takes part in the launch chain.
 cudaError_t launch_copy(void *dst, const void *src, size_t bytes, int pdl, cudaStream_t st);

@@ -384,3 +384,18 @@ def test_copy_validation(mq):
     assert L.mq_copy(A, ctypes.c_void_p(0x20008), 1024, N) == mq.MQ_ERR_ALIGN
     assert L.mq_copy(A, B, 1024, N) == mq.MQ_ERR_ACCESS      # nothing CUDA knows
     assert b"pageable" in L.mq_strerror(mq.MQ_ERR_ACCESS)
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="fake device pointers are only passed where no GPU exists")
+def test_device_repack_validation(mq):
+    L = mq.lib()
+    N = ctypes.c_void_p(0)
+    A, B = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000)
+    assert L.mq_repack_device(6, N, B, 8, 256, N) == mq.MQ_ERR_NULL
+    assert L.mq_repack_device(6, A, N, 8, 256, N) == mq.MQ_ERR_NULL
+    assert L.mq_repack_device(3, A, B, 8, 256, N) == mq.MQ_ERR_SHAPE
+    assert L.mq_repack_device(4, A, B, 0, 256, N) == mq.MQ_ERR_SHAPE
+    assert L.mq_repack_device(5, A, B, 8, 300, N) == mq.MQ_ERR_SHAPE
+    assert L.mq_repack_device(6, A, ctypes.c_void_p(0x20004), 8, 256, N) == mq.MQ_ERR_ALIGN
+    assert L.mq_repack_device(6, ctypes.c_void_p(0x10001), B, 8, 256, N) == mq.MQ_ERR_ALIGN
