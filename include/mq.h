@@ -417,6 +417,20 @@ int mq_gemv_q4k_q8_subdots(const void *Wp, const void *q8, int32_t *isums, int r
 int mq_gemv_q5k_q8_subdots(const void *Wp, const void *q8, int32_t *isums, int rows, int cols,
                            void *stream);
 
+/* Device-side coverage check of a plan (test and debug aid): the grouped
+ * GEMV of mq_gemv_group_q8_plan (splits == 0: the default plan), same
+ * arguments and the same outputs, which also adds 1 to
+ * counts[global tile * nchunks + chunk] for every chunk unit a warp
+ * processes.  Global tiles number the parts' 8-row tiles in part order;
+ * nchunks = ceil(cols / 1024).  counts: device, 16-byte aligned, one uint32
+ * per unit, zero-filled by the caller.  The plan covers the work exactly
+ * once iff every count is 1 afterwards (the host check of the plan runs
+ * first, as for every GEMV).
+ * Errors: as mq_gemv_group_q8_plan. */
+int mq_gemv_group_q8_coverage(const mq_gemv_part *parts, int nparts, const void *q8, int cols,
+                              int splits, int chunks_per_split, int tiles_per_item, void *ws,
+                              size_t ws_bytes, unsigned *counts, void *stream);
+
 /* Repack on the device: the same bytes as mq_repack_q6k / _q4k / _q5k (host)
  * for GGUF rows that are already in device memory, written by a kernel
  * (the pages build the dense plane once at weight registration, [D4-4]

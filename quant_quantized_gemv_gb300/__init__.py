@@ -43,7 +43,7 @@ EXPORTS = [
     "mq_gemv_gateup_plan_for", "mq_repacked_bytes_q5k", "mq_repack_q5k", "mq_unrepack_q5k",
     "mq_gemv_q5k_q8", "mq_gemv_q5k_q8_plan", "mq_gemv_q5k_q8_subdots", "mq_gemv_q5k_q8_batch",
     "mq_gemv_q5k_q8_batch_plan", "mq_read_floor", "mq_gemv_q6k_f32", "mq_gemv_q6k_f32_plan",
-    "mq_gemv_q6k_f32_plan_of", "mq_copy", "mq_repack_device",
+    "mq_gemv_q6k_f32_plan_of", "mq_copy", "mq_repack_device", "mq_gemv_group_q8_coverage",
 ]
 
 
@@ -138,6 +138,7 @@ def lib():
         "mq_gemv_q6k_f32_plan_of": ([I, I, P, P, P], I),
         "mq_copy": ([P, P, S, P], I),
         "mq_repack_device": ([I, P, P, I, I, P], I),
+        "mq_gemv_group_q8_coverage": ([P, I, P, I, I, I, I, P, S, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -612,6 +613,29 @@ def mq_gemv_group_q8(parts, q8, cols: int, ys=None, ws=None, stream=None, plan=N
                                          int(plan[2]), wsp, wsb, _stream(stream))
     _check(st, "mq_gemv_group_q8")
     return ys
+
+
+def mq_gemv_group_q8_coverage(parts, q8, cols: int, ys=None, ws=None, stream=None, plan=None):
+    """The grouped GEMV that also counts, per (global tile, chunk) unit, how
+    often a warp processed it.  Returns (ys, counts) with counts a CUDA int32
+    tensor [total tiles, nchunks]; every count is 1 when the plan covers the
+    work exactly once."""
+    import torch
+    for _, Wp, _ in parts:
+        _dev(Wp)
+    if ys is None:
+        ys = [torch.empty(rows, dtype=torch.float32, device=q8.device) for _, _, rows in parts]
+    for y in ys:
+        _dev(y, torch.float32)
+    tiles = sum(-(-rows // 8) for _, _, rows in parts)
+    nch = -(-(cols // 256) // 4)
+    counts = torch.zeros((tiles, nch), dtype=torch.int32, device=q8.device)
+    arr = _parts_array(parts, ys)
+    wsp, wsb = _ws_args(ws)
+    s, c, t = (0, 0, 0) if plan is None else (int(plan[0]), int(plan[1]), int(plan[2]))
+    _check(lib().mq_gemv_group_q8_coverage(arr, len(parts), _dev(q8), cols, s, c, t, wsp, wsb,
+                                           _dev(counts), _stream(stream)), "mq_gemv_group_q8_coverage")
+    return ys, counts
 
 
 def mq_gemv_q6k_q8_noalloc(Wp, q8, rows: int, cols: int, y=None, stream=None):

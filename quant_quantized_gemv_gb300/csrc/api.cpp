@@ -390,7 +390,7 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
 }
 
 int gemv_group(const Part *parts, int nparts, const void *q8, int cols, const Plan *explicit_plan,
-               void *ws, size_t ws_bytes, void *stream, int nt = 0)
+               void *ws, size_t ws_bytes, void *stream, int nt = 0, unsigned *cover = nullptr)
 {
     GemvLaunch a;
     size_t need = 0;
@@ -411,8 +411,10 @@ int gemv_group(const Part *parts, int nparts, const void *q8, int cols, const Pl
         a.ws_cnt = (unsigned *)ws;
         a.ws_part = (float *)((uint8_t *)ws + round16((size_t)total_tiles * 4));
     }
+    a.cover = cover;
     const cudaError_t e = nt > 0 ? launch_gemv_batch(a, (cudaStream_t)stream)
-                                 : launch_gemv(a, (cudaStream_t)stream);
+                          : cover ? launch_cover(a, (cudaStream_t)stream)
+                                  : launch_gemv(a, (cudaStream_t)stream);
     return e == cudaSuccess ? MQ_OK : cuda_fail(nt > 0 ? "small-batch GEMV launch" : "GEMV launch", e);
 }
 
@@ -810,6 +812,19 @@ int mq_gemv_group_q8(const mq_gemv_part *parts, int nparts, const void *q8, int 
                      size_t ws_bytes, void *stream)
 {
     return mq_gemv_group_q8_plan(parts, nparts, q8, cols, 0, 0, 0, ws, ws_bytes, stream);
+}
+
+int mq_gemv_group_q8_coverage(const mq_gemv_part *parts, int nparts, const void *q8, int cols,
+                              int splits, int chunks_per_split, int tiles_per_item, void *ws,
+                              size_t ws_bytes, unsigned *counts, void *stream)
+{
+    if (!parts || !counts) return MQ_ERR_NULL;
+    if (nparts < 1 || nparts > kMaxParts) return MQ_ERR_SHAPE;
+    if (!aligned16(counts)) return MQ_ERR_ALIGN;
+    Part ps[kMaxParts];
+    for (int p = 0; p < nparts; ++p) ps[p] = Part{parts[p].fmt, parts[p].rows, parts[p].Wp, parts[p].y};
+    const Plan pl{splits, chunks_per_split, tiles_per_item};
+    return gemv_group(ps, nparts, q8, cols, splits > 0 ? &pl : nullptr, ws, ws_bytes, stream, 0, counts);
 }
 
 int mq_gemv_group_q8_plan(const mq_gemv_part *parts, int nparts, const void *q8, int cols,

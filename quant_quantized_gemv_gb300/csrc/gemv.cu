@@ -152,10 +152,15 @@ __device__ __forceinline__ const uint8_t *stage_plane(const GemvLaunch &a, uint8
     return xs;
 }
 
+// Kernel modes: the GEMV; its integer sub-dots; the GEMV that also counts,
+// per (tile, chunk) unit, how many times a warp processed it (a debug and
+// test aid that checks the work decomposition on the device).
+constexpr int kModeGemv = 0, kModeSubdots = 1, kModeCover = 2;
+
 // Stream the part's units [u0, u1) through one register buffer: compute a
 // chunk, issue the next chunk's loads into the same registers, then finish
 // the tile if the chunk was its last.
-template <int FMT, bool SUBDOTS>
+template <int FMT, int MODE>
 __device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P, uint8_t *smem,
                                           int item, int u0, int u1, int lane)
 {
@@ -175,6 +180,10 @@ __device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P
     for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
     for (int u = u0; u < u1; ++u) {
         const int tcur = xa.t;
+        constexpr bool SUBDOTS = MODE == kModeSubdots;
+        if constexpr (MODE == kModeCover) {
+            if (lane == 0) atomicAdd(a.cover + ((size_t)(P.tile0 + xa.t) * nch + xa.c), 1u);
+        }
         compute<SUBDOTS>(a, P, A, xa, lane, acc);
         const bool more = u + 1 < u1;
         if (more) {
@@ -196,8 +205,8 @@ __device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P
 // kernel functions from one GEMV to the next costs more than the branch.
 // Measured on the 14B sweep: 2.39 ms with one kernel for all formats
 // against 2.49 ms with a kernel per format set (qkv, o, down alternating).
-template <bool SUBDOTS>
-__global__ void __maxnreg__(SUBDOTS ? 168 : kGemvMaxRegs)
+template <int MODE>
+__global__ void __maxnreg__(MODE == kModeSubdots ? 168 : kGemvMaxRegs)
     gemv_kernel(const __grid_constant__ GemvLaunch a)
 {
     extern __shared__ __align__(16) uint8_t xs[];  // the q8 plane, staged per CTA
@@ -228,35 +237,36 @@ __global__ void __maxnreg__(SUBDOTS ? 168 : kGemvMaxRegs)
         u1 = min(u0 + a.tpi * nch, P.ntiles * nch);
     }
     if (P.fmt == 6)
-        run_range<6, SUBDOTS>(a, P, xs, item, u0, u1, lane);
+        run_range<6, MODE>(a, P, xs, item, u0, u1, lane);
     else if (P.fmt == 5)
-        run_range<5, SUBDOTS>(a, P, xs, item, u0, u1, lane);
+        run_range<5, MODE>(a, P, xs, item, u0, u1, lane);
     else
-        run_range<4, SUBDOTS>(a, P, xs, item, u0, u1, lane);
+        run_range<4, MODE>(a, P, xs, item, u0, u1, lane);
 }
 
-template <bool SUBDOTS>
+template <int MODE>
 cudaError_t launch(const GemvLaunch &a, cudaStream_t st)
 {
-    const int warps = gemv_cta_warps(a.splits, SUBDOTS);
+    const int warps = gemv_cta_warps(a.splits, MODE == kModeSubdots);
     const long long blocks = (a.n_items + warps - 1) / warps;
-    return launch_maybe_pdl(gemv_kernel<SUBDOTS>, dim3((unsigned)blocks), dim3(32 * warps),
+    return launch_maybe_pdl(gemv_kernel<MODE>, dim3((unsigned)blocks), dim3(32 * warps),
                             a.splits == 1 ? (size_t)a.q8_bytes : 0, a.pdl, st, a);
 }
 
 using KernelFn = void (*)(GemvLaunch);
-const KernelFn kAllKernels[] = {gemv_kernel<false>, gemv_kernel<true>};
+const KernelFn kAllKernels[] = {gemv_kernel<kModeGemv>, gemv_kernel<kModeSubdots>, gemv_kernel<kModeCover>};
 
 }  // namespace
 
-cudaError_t launch_gemv(const GemvLaunch &a, cudaStream_t st) { return launch<false>(a, st); }
-cudaError_t launch_subdots(const GemvLaunch &a, cudaStream_t st) { return launch<true>(a, st); }
+cudaError_t launch_gemv(const GemvLaunch &a, cudaStream_t st) { return launch<kModeGemv>(a, st); }
+cudaError_t launch_subdots(const GemvLaunch &a, cudaStream_t st) { return launch<kModeSubdots>(a, st); }
+cudaError_t launch_cover(const GemvLaunch &a, cudaStream_t st) { return launch<kModeCover>(a, st); }
 
 int gemv_ctas_per_sm(int warps_per_cta, size_t smem)
 {
     int blocks = 0;
     const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &blocks, gemv_kernel<false>, 32 * warps_per_cta, smem);
+        &blocks, gemv_kernel<kModeGemv>, 32 * warps_per_cta, smem);
     if (e != cudaSuccess) cuda_fail("GEMV occupancy", e);
     return e == cudaSuccess ? blocks : 0;
 }

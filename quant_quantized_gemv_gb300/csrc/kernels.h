@@ -46,10 +46,14 @@ struct GemvLaunch {
     int pdl;                // launch with programmatic stream serialization
     int nt;                 // activation rows (tokens) of the small-batch kernel
     unsigned q8_stride;     // bytes from one token's plane to the next (small batch)
+    unsigned *cover;        // coverage mode: a count per (global tile, chunk), else null
 };
 
 cudaError_t launch_gemv(const GemvLaunch &a, cudaStream_t st);
 cudaError_t launch_subdots(const GemvLaunch &a, cudaStream_t st);
+// The GEMV that also adds 1 to a.cover[global tile * nchunks + chunk] for
+// every unit a warp processes (a device-side check of the decomposition).
+cudaError_t launch_cover(const GemvLaunch &a, cudaStream_t st);
 // Gate||up GEMV with the SwiGLU -> q8 epilogue (gemv_gateup.cu): g.part[0]
 // is gate, g.part[1] is up (same rows and format), g.q8 the input plane.
 // Rows come in q8 blocks of 32 (rows % 32 == 0); a CTA of wpb warps (1..8)

@@ -399,3 +399,17 @@ def test_device_repack_validation(mq):
     assert L.mq_repack_device(5, A, B, 8, 300, N) == mq.MQ_ERR_SHAPE
     assert L.mq_repack_device(6, A, ctypes.c_void_p(0x20004), 8, 256, N) == mq.MQ_ERR_ALIGN
     assert L.mq_repack_device(6, ctypes.c_void_p(0x10001), B, 8, 256, N) == mq.MQ_ERR_ALIGN
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="fake device pointers are only passed where no GPU exists")
+def test_coverage_mode_validation(mq):
+    L = mq.lib()
+    N = ctypes.c_void_p(0)
+    Q, C = ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30000)
+    arr = (mq.MQGemvPart * 1)(mq.MQGemvPart(6, 64, 0x10000, 0x40000))
+    assert L.mq_gemv_group_q8_coverage(arr, 1, Q, 18944, 4, 5, 1, N, 0, N, N) == mq.MQ_ERR_NULL
+    assert L.mq_gemv_group_q8_coverage(arr, 1, Q, 18944, 4, 5, 1, N, 0, ctypes.c_void_p(0x30004), N) == \
+        mq.MQ_ERR_ALIGN
+    assert L.mq_gemv_group_q8_coverage(arr, 1, Q, 18944, 5, 3, 1, N, 0, C, N) == mq.MQ_ERR_COVERAGE
+    assert L.mq_gemv_group_q8_coverage(arr, 0, Q, 18944, 4, 5, 1, N, 0, C, N) == mq.MQ_ERR_SHAPE
