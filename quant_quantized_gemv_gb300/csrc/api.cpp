@@ -147,28 +147,54 @@ bool device_occupancy(Occupancy *o, size_t plane)
     return o->ctas_tiles > 0;
 }
 
-// The small-batch kernel for nt tokens: every CTA stages all nt planes.
-// CTA shapes up to the kernel's warp budget (batch_warp_budget).
-bool batch_occupancy(Occupancy *o, int nt, int fmt, size_t planes)
+// Resident CTAs per SM of the small-batch kernel for nt tokens of format fmt
+// with w warps (register limit, measured once per device and shape); 0
+// when such a CTA does not fit, -1 on a CUDA error.
+int batch_ctas_regs(int nt, int fmt, int w)
 {
     const int dev = current_device();
+    if (dev < 0) return -1;
+    std::atomic<int> &slot = g_batch_ctas[dev][nt][fmt][w];
+    int v = slot.load(std::memory_order_relaxed);
+    if (v == 0) {
+        v = gemv_batch_ctas_per_sm(nt, fmt, w, 0);
+        if (v < 0) return -1;
+        slot.store(v > 0 ? v : -2, std::memory_order_relaxed);  // -2: does not fit
+    }
+    return v > 0 ? v : (v == -2 ? 0 : v);
+}
+
+// Warps a CTA of the small-batch kernel holds on this device: the most (up
+// to the kernel's compile-time bound) for which one CTA fits an SM; 0 on
+// error.
+int batch_budget(int nt, int fmt)
+{
+    int best = 0;
+    for (int w = 1; w <= batch_warp_budget_max(nt, fmt); ++w) {
+        const int v = batch_ctas_regs(nt, fmt, w);
+        if (v < 0) return 0;
+        if (v == 0) break;
+        best = w;
+    }
+    return best;
+}
+
+// The small-batch kernel for nt tokens: every CTA stages all nt planes.
+// CTA shapes up to the device's warp budget (batch_budget).
+bool batch_occupancy(Occupancy *o, int nt, int fmt, size_t planes, int *budget_out)
+{
     DeviceLimits lim;
-    if (dev < 0 || !device_limits(&lim)) return false;
+    if (!device_limits(&lim)) return false;
     const long long per_cta = (long long)planes + kBatchStaticSmem + lim.smem_reserved;
     const int by_smem = (int)(lim.smem_per_sm / per_cta);
-    const int budget = batch_warp_budget(nt, fmt);
-    for (int w = 1; w <= budget; ++w) {
-        std::atomic<int> &slot = g_batch_ctas[dev][nt][fmt][w];
-        int v = slot.load(std::memory_order_relaxed);
-        if (v <= 0) {
-            v = gemv_batch_ctas_per_sm(nt, fmt, w, 0);
-            if (v <= 0) return false;
-            slot.store(v, std::memory_order_relaxed);
-        }
+    const int budget = batch_budget(nt, fmt);
+    if (budget < 1) return false;
+    for (int w = 1; w <= kBatchMaxCtaWarps; ++w) {
+        const int v = w <= budget ? batch_ctas_regs(nt, fmt, w) : 0;
         o->ctas[w] = v < by_smem ? v : by_smem;
     }
-    for (int w = budget + 1; w <= kBatchMaxCtaWarps; ++w) o->ctas[w] = 0;
     o->ctas_tiles = 0;  // unused by the small-batch plans
+    *budget_out = budget;
     return o->ctas[budget] > 0;
 }
 
@@ -331,12 +357,16 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
                               : check_plan(nchunks, *explicit_plan);
         if (cov != MQ_OK) return cov;
     }
+    // small batch: the warps one CTA holds (the device's, or the compile-time
+    // bound when only sizes are asked for: then nothing is launched)
+    int wpc = batch ? batch_warp_budget_max(nt, parts[0].fmt) : 0;
     if (!sizes_only) {
         DeviceLimits lim;
         if (!device_limits(&lim)) return MQ_ERR_CUDA;
         // the plane(s) must fit in shared memory
         if (!batch ? plane > lim.max_plane : (size_t)nt * plane > lim.max_batch_planes)
             return MQ_ERR_SHAPE;
+        if (batch && (wpc = batch_budget(nt, parts[0].fmt)) < 1) return MQ_ERR_CUDA;
     }
     Plan pl;
     if (explicit_plan) {
@@ -347,9 +377,8 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
             if (!device_occupancy(&o, plane)) return MQ_ERR_CUDA;
             pl = plan_for((int)total_tiles, nchunks, device_sms(), o);
         } else {
-            if (!batch_occupancy(&o, nt, parts[0].fmt, (size_t)nt * plane)) return MQ_ERR_CUDA;
-            pl = batch_plan_for((int)total_tiles, nchunks, device_sms(), o,
-                                batch_warp_budget(nt, parts[0].fmt));
+            if (!batch_occupancy(&o, nt, parts[0].fmt, (size_t)nt * plane, &wpc)) return MQ_ERR_CUDA;
+            pl = batch_plan_for((int)total_tiles, nchunks, device_sms(), o, wpc);
         }
     }
     const int cov = batch ? check_batch_plan(nchunks, pl) : check_plan(nchunks, pl);
@@ -367,7 +396,7 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
         gp.item0 = (int)items;
         gp.tile0 = (int)tiles;
         gp.tile_bytes_div16 = (int)(g.tile_bytes / 16);
-        items += batch ? batch_ctas(g.ntiles, pl, batch_warp_budget(nt, x.fmt)) : plan_items(g.ntiles, pl);
+        items += batch ? batch_ctas(g.ntiles, pl, wpc) : plan_items(g.ntiles, pl);
         tiles += g.ntiles;
     }
     if (items >= (1LL << 31)) return MQ_ERR_SHAPE;
@@ -385,6 +414,7 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
     a->pdl = g_pdl.load(std::memory_order_relaxed);
     a->nt = batch ? nt : 1;
     a->q8_stride = (unsigned)plane;
+    a->wpc = wpc;
     *need = batch ? 0 : ws_bytes_for(total_tiles, items, pl);  // small batch: splits meet in the CTA
     return MQ_OK;
 }
@@ -435,8 +465,9 @@ int batch_plan_of(int rows, int cols, int nt, Plan *p)
     DeviceLimits lim;
     if (!device_limits(&lim)) return MQ_ERR_CUDA;
     if ((size_t)nt * plane > lim.max_batch_planes) return MQ_ERR_SHAPE;
-    if (!batch_occupancy(&o, nt, 6, (size_t)nt * plane)) return MQ_ERR_CUDA;
-    *p = batch_plan_for(g.ntiles, g.nchunks, device_sms(), o, batch_warp_budget(nt, 6));
+    int wpc = 0;
+    if (!batch_occupancy(&o, nt, 6, (size_t)nt * plane, &wpc)) return MQ_ERR_CUDA;
+    *p = batch_plan_for(g.ntiles, g.nchunks, device_sms(), o, wpc);
     return MQ_OK;
 }
 
@@ -900,8 +931,10 @@ int mq_gemv_batch_plan_for(int rows, int cols, int nt, int sms, int regs_per_thr
     const int by_smem = (int)(233472 / ((long long)planes + kBatchStaticSmem + 1024));
     for (int w = 1; w <= kBatchMaxCtaWarps; ++w)
         if (o.ctas[w] > by_smem) o.ctas[w] = by_smem;
-    // the kernel's budget follows its register cap: 16 warps at 128, else 12
-    const int budget = regs_per_thread <= 128 ? kBatchMaxCtaWarps : 12;
+    // the kernel's budget follows its register cap: the warps the register
+    // file holds at that count, at most 16
+    const int fit = 65536 / (32 * regs_per_thread);
+    const int budget = fit < kBatchMaxCtaWarps ? (fit > 0 ? fit : 1) : kBatchMaxCtaWarps;
     const Plan p = batch_plan_for(g.ntiles, g.nchunks, sms, o, budget);
     *splits = p.splits;
     *chunks_per_split = p.cps;

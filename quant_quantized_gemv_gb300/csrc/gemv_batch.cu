@@ -21,9 +21,10 @@
 //   * A weight row's codes are decoded once per token group and used for
 //     every token of the group: the decode, not the dp4a, dominates the ALU
 //     work of a chunk.
-//   * One CTA per SM stages the planes once for all its warps: 16 warps at
-//     128 registers where the token count allows it without spilling (2
-//     tokens; 3 of q4_K / q5_K), else 12 warps at 168 registers.
+//   * One CTA per SM stages the planes once for all its warps: as many as
+//     the register file holds at the instance's register cap (16 warps at
+//     128 registers for 2 tokens, 14-15 for 3-4 tokens of most formats, 12
+//     at 168 otherwise).
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -191,7 +192,7 @@ template <int NT, int FMT>
 __device__ __forceinline__ void flush_tile(const GemvLaunch &a, const GemvPart &P, int t, bool valid,
                                            int iter, Acc<NT> &acc, int lane)
 {
-    constexpr int kWarps = batch_warp_budget(NT, FMT);
+    constexpr int kWarps = batch_warp_budget_max(NT, FMT);
     __shared__ float xchg[2][kWarps][NT][8];
     float v[NT];
 #pragma unroll
@@ -251,7 +252,7 @@ __device__ __forceinline__ void stage_planes(const GemvLaunch &a, uint8_t *xs)
     asm volatile("bar.sync 1, %0;" ::"r"(blockDim.x) : "memory");
 }
 
-// Work decomposition.  A CTA has S * G warps (S = a.splits, G = budget / S tiles
+// Work decomposition.  A CTA has S * G warps (S = a.splits, G = a.wpc / S tiles
 // per group): warp w takes split w % S of tile w / S of each group.  The CTA
 // runs a.tpi consecutive groups, so the staged planes serve a.tpi * G tiles.
 // Split s covers chunks [s * cps, min((s + 1) * cps, nchunks)) of a row.  A
@@ -277,7 +278,7 @@ __device__ __forceinline__ void run_batch(const GemvLaunch &a, const GemvPart &P
 {
     using W = typename Fmt<FMT>::W;
     constexpr int kChunkBytes = Fmt<FMT>::kChunkBytes;
-    const int S = a.splits, G = batch_warp_budget(NT, FMT) / S;
+    const int S = a.splits, G = a.wpc / S;
     const int w = threadIdx.x >> 5, sp = w % S, o = w / S;
     const int c_lo = sp * a.cps, c_hi = min(c_lo + a.cps, a.nchunks);
     const int group0 = blockIdx.x * a.tpi;
@@ -356,7 +357,7 @@ __device__ __forceinline__ void run_batch(const GemvLaunch &a, const GemvPart &P
 
 // One kernel per (tokens, format): each gets its own register allocation.
 template <int NT, int FMT>
-__global__ void __maxnreg__(batch_small_regs(NT, FMT) ? 128 : 168)
+__global__ void __maxnreg__(batch_reg_cap(NT, FMT))
     gemv_batch_kernel(const __grid_constant__ GemvLaunch a)
 {
     extern __shared__ __align__(16) uint8_t xs[];  // the nt q8 planes
@@ -395,7 +396,7 @@ cudaError_t launch_gemv_batch(const GemvLaunch &a, cudaStream_t st)
 {
     const KernelFn k = kernel_for(a.nt, a.part[0].fmt);
     if (!k) return cudaErrorInvalidValue;
-    const int warps = gemv_batch_cta_warps(a.splits, batch_warp_budget(a.nt, a.part[0].fmt));
+    const int warps = gemv_batch_cta_warps(a.splits, a.wpc);
     return launch_maybe_pdl(k, dim3((unsigned)a.n_items), dim3(32 * warps),
                             (size_t)a.nt * a.q8_bytes, a.pdl, st, a);
 }
@@ -408,7 +409,7 @@ int gemv_batch_ctas_per_sm(int nt, int fmt, int warps_per_cta, size_t smem)
     const cudaError_t e =
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k, 32 * warps_per_cta, smem);
     if (e != cudaSuccess) cuda_fail("small-batch GEMV occupancy", e);
-    return e == cudaSuccess ? blocks : 0;
+    return e == cudaSuccess ? blocks : -1;
 }
 
 size_t gemv_batch_max_smem()

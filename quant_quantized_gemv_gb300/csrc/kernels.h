@@ -47,6 +47,7 @@ struct GemvLaunch {
     int nt;                 // activation rows (tokens) of the small-batch kernel
     unsigned q8_stride;     // bytes from one token's plane to the next (small batch)
     unsigned *cover;        // coverage mode: a count per (global tile, chunk), else null
+    int wpc;                // small batch: warps a CTA may hold (its plan's G = wpc / splits)
 };
 
 cudaError_t launch_gemv(const GemvLaunch &a, cudaStream_t st);
@@ -72,7 +73,7 @@ bool gateup_opt_in(size_t max_plane);  // accept a staged plane of max_plane byt
 
 // Small-batch GEMV (gemv_batch.cu), 1 <= a.nt <= kMaxTokens, one part whose
 // y holds nt x rows outputs, token-major.  Its plan reads differently: each
-// CTA holds `splits` warps for each of batch_warp_budget / splits tiles (a
+// CTA holds `splits` warps for each of wpc / splits tiles (a
 // group) and runs tpi consecutive groups; n_items is the number of CTAs.
 cudaError_t launch_gemv_batch(const GemvLaunch &a, cudaStream_t st);
 
@@ -92,17 +93,25 @@ constexpr int kBatchMaxCtaSplits = 12;  // most splits of a tile (warps of one t
 constexpr int kBatchMaxCtaWarps = 16;   // most warps of a CTA (a whole SM at 128 registers)
 constexpr int kBatchStaticSmem = 2 * kBatchMaxCtaSplits * kMaxTokens * 8 * 4;  // split exchange (max)
 
-// Register cap and warps per CTA of the small-batch kernel for nt tokens of
-// format fmt.  Where the kernel fits 128 registers without spilling (2
-// tokens; 3 tokens of q4_K / q5_K) a CTA holds 16 warps, the whole SM;
-// otherwise 168 registers and 12 warps.
-__host__ __device__ constexpr bool batch_small_regs(int nt, int fmt)
+// Register cap of the small-batch kernel for nt tokens of format fmt: the
+// smallest that compiles without spilling (at most a few bytes), so that
+// as many warps as possible fit an SM; one token keeps two weight buffers
+// and 5..8 tokens need the full 168.
+__host__ __device__ constexpr int batch_reg_cap(int nt, int fmt)
 {
-    return nt == 2 || (nt == 3 && fmt != 6);
+    return nt == 2 ? 128
+         : nt == 3 ? (fmt == 6 ? 136 : 128)
+         : nt == 4 ? (fmt == 6 ? 168 : 144)
+         : 168;
 }
-__host__ __device__ constexpr int batch_warp_budget(int nt, int fmt)
+// Most warps a CTA can hold at that cap (at most 16): sizes the kernel's
+// split-exchange buffer.  The warps a CTA actually holds (GemvLaunch::wpc)
+// come from the device's occupancy query and never exceed this.
+__host__ __device__ constexpr int batch_warp_budget_max(int nt, int fmt)
 {
-    return batch_small_regs(nt, fmt) ? kBatchMaxCtaWarps : 12;
+    return 65536 / (32 * batch_reg_cap(nt, fmt)) < kBatchMaxCtaWarps
+               ? 65536 / (32 * batch_reg_cap(nt, fmt))
+               : kBatchMaxCtaWarps;
 }
 
 // Warps per CTA for a plan with `splits` splits.
@@ -119,8 +128,8 @@ inline int gemv_batch_cta_warps(int splits, int budget)
 }
 
 // Resident CTAs per SM of the small-batch kernel for nt tokens of format
-// fmt (0 on error), and the largest dynamic shared memory (all nt planes)
-// the small-batch kernels accept.
+// fmt (0 if such a CTA does not fit, -1 on error), and the largest dynamic
+// shared memory (all nt planes) the small-batch kernels accept.
 int gemv_batch_ctas_per_sm(int nt, int fmt, int warps_per_cta, size_t smem);
 size_t gemv_batch_max_smem();
 
