@@ -93,13 +93,16 @@ constexpr int kBatchMaxCtaSplits = 12;  // most splits of a tile (warps of one t
 constexpr int kBatchMaxCtaWarps = 16;   // most warps of a CTA (a whole SM at 128 registers)
 constexpr int kBatchStaticSmem = 2 * kBatchMaxCtaSplits * kMaxTokens * 8 * 4;  // split exchange (max)
 
-// Register cap of the small-batch kernel for nt tokens of format fmt: the
-// smallest that compiles without spilling (at most a few bytes), so that
-// as many warps as possible fit an SM; one token keeps two weight buffers
-// and 5..8 tokens need the full 168.
+// Register cap of the small-batch kernel for nt tokens of format fmt: for
+// q6_K and q5_K the smallest that compiles without spilling (at most a few
+// bytes), so that as many warps as possible fit an SM; one token keeps two
+// weight buffers and 5..8 tokens need the full 168.  q4_K keeps 168 (12
+// warps): more warps measured slower there (14B gate at 2 tokens 13.2
+// against 12.6 us).
 __host__ __device__ constexpr int batch_reg_cap(int nt, int fmt)
 {
-    return nt == 2 ? 128
+    return fmt == 4 ? 168
+         : nt == 2 ? 128
          : nt == 3 ? (fmt == 6 ? 136 : 128)
          : nt == 4 ? (fmt == 6 ? 168 : 144)
          : 168;
