@@ -267,9 +267,9 @@ struct Cursor {
 
 // Two register buffers of weights for one token (chunk u + 1 in flight while
 // chunk u is computed); with more tokens one buffer, issued as soon as the
-// previous chunk's compute is done: 12 warps per SM at 168 registers hide
-// each other's load latency better than 8 warps with two buffers (which
-// would need more registers than 168 and spill).
+// previous chunk's compute is done: the SM's other warps (12 to 16,
+// batch_reg_cap) hide each other's load latency better than 8 warps with
+// two buffers (which would need more than 168 registers and spill).
 template <int NT>
 constexpr bool kTwoBuffers = NT == 1;
 
