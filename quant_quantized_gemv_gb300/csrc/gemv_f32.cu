@@ -12,7 +12,9 @@
 // How (GB300 design).  The weights are the q8 path's repacked layout
 // (layout.h), streamed the same way: tiles of 8 rows, chunks of 4
 // super-blocks, lane i owns unit i (32 columns) of a chunk for all 8 rows,
-// two register buffers so one chunk is in flight while the other computes.
+// one register buffer at 128 registers so that 16 warps share an SM (two
+// buffers at 168 registers and 12 warps measured slower: 149 against 125 us
+// on the 152064 x 5120 head, 21.4 against 19.9 us on 3584 x 18944).
 // What differs is the activation: 4 bytes per value instead of ~1.06, so
 // every CTA stages the whole row in shared memory (up to 57856 values) and
 // each activation value is read from there once per tile row.  The staged
@@ -25,9 +27,9 @@
 // permute) and 2^23 + 32 is subtracted, exactly.  The subtraction and the
 // FMA run on pairs of values (Blackwell's f32x2 add and fma), each pair
 // accumulating its own partial sum of the sub-block; the two are added
-// before the scale is applied.  Measured against one value per instruction:
-// 149 against 167 us on the 152064 x 5120 head, 21.2 against 23.6 us on
-// 3584 x 18944.
+// before the scale is applied.  Measured against one value per instruction
+// (two-buffer form): 149 against 167 us on the 152064 x 5120 head, 21.2
+// against 23.6 us on 3584 x 18944.
 //
 // Plans are the single-token GEMV's (whole tiles per warp, or 2..12 splits
 // of a tile as the warps of one CTA meeting in shared memory); there is no
@@ -179,37 +181,29 @@ __device__ __forceinline__ void run_f32(const GemvLaunch &a, const GemvPart &P, 
 {
     constexpr int kChunkBytes = kQ6kChunkPerBlock * kChunkBlocks;
     const int nch = a.nchunks;
-    Q6kW A, B;
+    Q6kW A;
     int t = u0 / nch, c = u0 - t * nch;  // position of the next chunk to load
-    Unit xa = locate(a, P, t, c, lane, kChunkBytes), xb;
+    Unit xa = locate(a, P, t, c, lane, kChunkBytes);
     load_w(xa, lane, A);  // weights do not depend on the preceding kernel
     stage_x(a, xs);       // the activation does
     if (++c == nch) { c = 0; ++t; }
     float acc[8];
 #pragma unroll
     for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
-    for (int u = u0; u < u1; u += 2) {
-        const bool has_b = u + 1 < u1;
-        if (has_b) {
-            xb = locate(a, P, t, c, lane, kChunkBytes);
-            load_w(xb, lane, B);
-            if (++c == nch) { c = 0; ++t; }
-        }
+    for (int u = u0; u < u1; ++u) {
+        const int tcur = xa.t;
         compute_f32(A, xs, xa, lane, acc);
-        if (!has_b || xb.t != xa.t) flush_f32(a, P, xa.t, acc, lane);
-        if (!has_b) break;
-        const bool has_a = u + 2 < u1;
-        if (has_a) {
+        const bool more = u + 1 < u1;
+        if (more) {  // the next chunk into the same registers
             xa = locate(a, P, t, c, lane, kChunkBytes);
             load_w(xa, lane, A);
             if (++c == nch) { c = 0; ++t; }
         }
-        compute_f32(B, xs, xb, lane, acc);
-        if (!has_a || xa.t != xb.t) flush_f32(a, P, xb.t, acc, lane);
+        if (!more || xa.t != tcur) flush_f32(a, P, tcur, acc, lane);
     }
 }
 
-__global__ void __launch_bounds__(32 * kMaxCtaSplits, 1)
+__global__ void __maxnreg__(kGemvMaxRegs)
     gemv_q6k_f32_kernel(const __grid_constant__ GemvLaunch a)
 {
     extern __shared__ __align__(16) uint4 xs[];  // the activation row, swizzled
