@@ -348,12 +348,15 @@ class DeviceWorkload:
             elif o[0] == "gateup":
                 self._launch_gateup(o, c)
 
-    def run(self, k: int):
-        """Enqueue step k (weights copy k % n_copies) on the current stream."""
+    def run(self, k: int, producers_only: bool = False):
+        """Enqueue step k (weights copy k % n_copies) on the current stream;
+        with producers_only, just its producer launches (for their timing)."""
         mq = self.mq
         c = k % self.n_copies
         for o in self.ops:
             kind = o[0]
+            if producers_only and kind in ("gemv", "gemv32", "gateup"):
+                continue
             b = self.nt > 1
             if kind == "rms":
                 (mq.mq_rmsnorm_quant_q8_batch if b else mq.mq_rmsnorm_quant_q8)(o[1], o[2], 1e-6, y=o[3],
@@ -418,6 +421,9 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     mq.mq_set_pdl(False)
     n_kt = max(wl.n_copies, 16) if wl.n_gemv < 8 else 2
     kt_graph = capture(lambda: [wl.run_gemvs(i) for i in range(n_kt)], stream)
+    n_prod = sum(1 for o in wl.ops if o[0] in ("rms", "swiglu", "quant"))
+    pt_graph = (capture(lambda: [wl.run(i, producers_only=True) for i in range(n_kt)], stream)
+                if n_prod else None)
     # ---- the single-launch read floor of the same weight bytes (one-GEMV
     # workloads): a plain read of each step's weight copy, back to back
     floor_graph = None
@@ -486,6 +492,22 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
         e1.synchronize()
         kt.append(e0.elapsed_time(e1) / n_kt)
     gemv_step_ms = float(np.median(kt))
+    # ---- the producers alone, timed the same way (PDL off)
+    prod_step_ms = 0.0
+    if pt_graph is not None:
+        with torch.cuda.stream(stream):
+            pt_graph.replay()
+        torch.cuda.synchronize()
+        pt = []
+        for rep in range(5):
+            e0, e1 = make_event(), make_event()
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                pt_graph.replay()
+                e1.record(stream)
+            e1.synchronize()
+            pt.append(e0.elapsed_time(e1) / n_kt)
+        prod_step_ms = float(np.median(pt))
     floor_ms = None
     if floor_graph is not None:
         with torch.cuda.stream(stream):
@@ -593,7 +615,11 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
         line["roofline"]["read_floor_gbs"] = round(wl.weight_bytes / (floor_ms * 1e-3) / 1e9, 1)
         line["roofline"]["frac_of_read_floor"] = round(floor_ms / gemv_step_ms, 4)
     line["kernel_us"] = {"gemv_per_step_isolated": round(gemv_step_ms * 1e3, 3),
-                         "step": round(ms_per_step * 1e3, 3)}
+                         "producers_per_step_isolated": round(prod_step_ms * 1e3, 3),
+                         "producer_launches_per_step": n_prod,
+                         "step": round(ms_per_step * 1e3, 3),
+                         "how": "GEMV launches alone and producer launches alone, each as a graph of "
+                                f"{n_kt} steps back to back with PDL off; step: the PDL chain of both"}
     line["e2e"] = {"value": round(wl.weight_bytes / (e2e_ms * 1e-3) / 1e9 * ws_, 2), "unit": "GB/s",
                    "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
                    "d2h_bytes_per_step": int(d2h),
