@@ -121,7 +121,11 @@ __global__ void __launch_bounds__(256) swiglu_quant_q8_kernel(const float *g, co
 // per-warp partials added in warp order by every thread -- so all CTAs get
 // the same bits.  scale = 1/sqrt(ss/n + eps) (IEEE sqrt and division), then
 // each CTA writes y = (x * scale) * gain and its q8 blocks for its own slice.
-constexpr int kRmsThreads = 256;
+// 512 threads: the sum pass of a 13824-value row is one round of loads per
+// thread (14B decode sweep 2.234 ms per step, against 2.298 ms with 256
+// threads and 2.227 ms with 1024, which is slower on the single-layer
+// chains: rms -> gate||up -> down 28.85 against 28.58 us).
+constexpr int kRmsThreads = 512;
 constexpr int kRmsMaxCtas = 64;
 
 __global__ void __launch_bounds__(kRmsThreads) rmsnorm_quant_q8_kernel(
