@@ -393,12 +393,14 @@ int mq_check_coverage(int nchunks, int splits, int chunks_per_split);
  * the previous setting).  When on, every kernel is launched with CUDA's
  * programmatic stream serialization, so it may start while the previous
  * kernel in the stream drains: producers then wait (griddepcontrol.wait)
- * before reading anything, and a GEMV issues its first weight loads BEFORE
+ * before reading their activations (the rms producer reads its first slice
+ * of gain before waiting), and a GEMV issues its first weight loads BEFORE
  * waiting and touches the q8 plane, y and ws only after.  This hides launch
  * and ramp latency in a producer -> GEMV -> producer chain (the retry
  * condition of [D4-4] §5 for PDL: a purely bandwidth-bound chain).  Turn it
  * on only when the kernel that directly precedes a GEMV in the stream does
- * not write that GEMV's weight matrix.
+ * not write that GEMV's weight matrix, nor the kernel before an rms
+ * producer its gain (both are weights in a decode step).
  * ------------------------------------------------------------------------ */
 int mq_set_pdl(int enable);
 

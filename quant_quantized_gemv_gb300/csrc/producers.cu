@@ -134,13 +134,17 @@ __global__ void __launch_bounds__(kRmsThreads) rmsnorm_quant_q8_kernel(
 {
     __shared__ float warp_ss[kRmsThreads / 32];
     griddep_launch_dependents();
-    griddep_wait();  // x may come from the preceding kernel
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int n4 = n >> 2;
     const int first = blockIdx.x * kRmsThreads;  // this CTA's first float4
     const size_t row = blockIdx.y;
     const float4 *x4 = reinterpret_cast<const float4 *>(x + row * n);
     const float4 *g4 = reinterpret_cast<const float4 *>(gain);
+    // the gain is a weight (never written by the preceding kernel): its first
+    // slice is loaded before the wait, off the chain's critical path (14B
+    // decode sweep 2.234 -> 2.214 ms per step)
+    const float4 g_own = first + tid < n4 ? __ldg(g4 + first + tid) : make_float4(0.f, 0.f, 0.f, 0.f);
+    griddep_wait();  // x may come from the preceding kernel
     y += row * n;
     q8 += row * stride;
 
@@ -172,7 +176,7 @@ __global__ void __launch_bounds__(kRmsThreads) rmsnorm_quant_q8_kernel(
         float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
         if (valid) {
             const float4 v = base == first ? own : __ldcg(x4 + i);
-            const float4 gv = __ldcg(g4 + i);
+            const float4 gv = base == first ? g_own : __ldg(g4 + i);
             out.x = (v.x * scale) * gv.x;
             out.y = (v.y * scale) * gv.y;
             out.z = (v.z * scale) * gv.z;
