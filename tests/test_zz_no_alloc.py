@@ -30,7 +30,7 @@ def mq():
     return m
 
 
-@pytest.mark.parametrize("rows,cols", [(512, 18944), (1024, 5120)])
+@pytest.mark.parametrize("rows,cols", [(512, 18944), (1024, 5120), (968, 18944)])
 def test_noalloc_matches_regular_entry_point(mq, orc, rows, cols):
     import torch
     g = synth.rng("noalloc", rows, cols)
@@ -42,6 +42,9 @@ def test_noalloc_matches_regular_entry_point(mq, orc, rows, cols):
     assert splits > 1
     if rows == 512:                                      # few tiles, long rows: the scratch path
         assert mq.mq_gemv_workspace_bytes(rows, cols) > 0
+    if rows == 968:                                      # 121 tiles x 19 splits: more than 64 KiB
+        need = mq.mq_gemv_workspace_bytes(rows, cols)
+        assert need == 0 or need > 64 * 1024, need      # (device-dependent plan)
     ws = mq.mq_gemv_workspace(rows, cols)
     y_ref = mq.mq_gemv_q6k_q8(Wp, plane, rows, cols, ws=ws)
     d0, q0, _ = orc.quantize_q8(x)
