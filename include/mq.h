@@ -304,17 +304,20 @@ int mq_gemv_group_q8_plan(const mq_gemv_part *parts, int nparts, const void *q8,
  *   GB300, i.e. cols <= 26368 at nt = 8), else MQ_ERR_SHAPE.
  * Plans read differently from the single-token ones: splits S
  * (1..12) cuts every row into S ranges of chunks_per_split chunks (coverage
- * checked as above, no empty range); a CTA holds S warps for each of 12 / S
+ * checked as above, no empty range); a CTA holds S warps for each of B / S
  * tiles (a "group") and runs tiles_per_item consecutive groups, so the
- * staged planes serve tiles_per_item * (12 / S) tiles.  A tile's S splits
+ * staged planes serve tiles_per_item * (B / S) tiles.  B, the warps one CTA
+ * holds, is 12 to 16: the most that fit an SM at the register count of the
+ * kernel for nt tokens of that format (asked of the device once).  A tile's S splits
  * add their partial sums in shared memory in ascending split order; there
  * is no workspace.  The default plan picks S and tiles_per_item so that the
  * busiest warp streams the fewest chunks, scaled up when the grid leaves SMs
  * idle.
- * mq_gemv_batch_plan: the default plan for nt tokens on the current device
- *   (both formats plan alike).
+ * mq_gemv_batch_plan: the default plan for nt tokens of q6_K on the current
+ *   device (other formats may hold a different B).
  * mq_gemv_batch_plan_for: the same for a device with `sms` SMs and a kernel
- *   of regs_per_thread registers.  Host only.
+ *   of regs_per_thread registers (B = the warps that fit, at most 16).
+ *   Host only.
  * mq_gemv_*_q8_batch_plan: the GEMV with an explicit plan.
  * Errors: as mq_gemv_q6k_q8; MQ_ERR_SHAPE also for nt outside
  *         1..MQ_MAX_TOKENS; MQ_ERR_COVERAGE for a bad plan.
