@@ -44,3 +44,17 @@ def test_two_gloo_ranks():
     assert mx0 == mx1 == 15.0                                 # max over ranks
     assert v0 == pytest.approx(2 * 1e9 * 100 / 15e-3 / 1e9)   # both ranks' bytes / slowest time
     assert ref1 is None                                       # non-zero ranks report nothing
+
+
+@pytest.mark.parametrize("act,dtype", [("q8", "i8"), ("f32", "f32")])
+def test_reference_arm_line(act, dtype):
+    """The reference arm (the oracle on the host, one rank): its JSON line
+    carries the contract's keys, a zero-copy e2e and the oracle baseline."""
+    import bench
+    args = type("A", (), dict(steps=1, warmup=3, workload="q6k_512x2048", tokens=1, act=act))()
+    line = bench.bench_reference(args, 1, 0)
+    assert line["impl"] == "reference" and line["dtype"] == dtype
+    assert line["value"] > 0 and line["unit"] == "GB/s" and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert act in line["config"]["sample"]
