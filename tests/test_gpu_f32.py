@@ -159,11 +159,13 @@ def test_bad_calls_are_refused_and_nothing_runs(mq):
     assert torch.all(y == 7.0)
 
 
-def test_pdl_chain_with_the_rms_producer(mq):
+@pytest.mark.parametrize("h,rows", [(5120, 1024), (1024, 20000)])   # split CTAs; whole tiles
+def test_pdl_chain_with_the_rms_producer(mq, h, rows):
     """rms_norm (its f32 output) -> f32 GEMV, 6 steps, with and without PDL
     and under graph capture: identical outputs."""
     import torch
-    h, rows = 5120, 1024
+    s, _, _ = mq.mq_gemv_q6k_f32_plan_of(rows, h)
+    assert (s == 1) == (rows == 20000)
     g = synth.rng("f32-chain")
     Wp = dev(mq.mq_repack_q6k(synth.q6k_blocks(g, rows, h), rows, h))
     gain = dev(synth.normal(g, h, 1.0, 0.1))
