@@ -51,6 +51,7 @@ DESCR = {
     "lm_head_14b": "Qwen2.5-14B output head q6_K 152064x5120, rms_norm->q8, batch 1",
     "attn_v_14b": "Qwen2.5-14B attn_v q6_K 1024x5120, rms_norm->q8, batch 1",
     "q6k_2048x4864": "q6_K 2048x4864 GEMV, x -> standalone q8 quantize, batch 1",
+    "ffn_down_14b_q5k": "q5_K 5120x13824 (the 14B ffn_down shape), rms_norm->q8, batch 1",
     "ffn_14b": "Qwen2.5-14B FFN: rms_norm->q8 -> gate, up q4_K 13824x5120 -> SwiGLU->q8 -> "
                "down q6_K 5120x13824, batch 1",
     "sweep_14b": "Qwen2.5-14B decode weight sweep: 48 layers x {q,k,o,gate,up q4_K; v,down q6_K} "
@@ -199,8 +200,7 @@ class DeviceWorkload:
         for _, fmt, rows, cols, _ in self.wl.gemvs:
             if (fmt, rows, cols) not in base:
                 W = synth.blocks(fmt, g, rows, cols)
-                rep = mq.mq_repack_q6k if fmt == "q6k" else mq.mq_repack_q4k
-                base[(fmt, rows, cols)] = (W, torch.from_numpy(rep(W, rows, cols)).to(device))
+                base[(fmt, rows, cols)] = (W, torch.from_numpy(mq.mq_repack(fmt, W, rows, cols)).to(device))
         self.host_w = {k: v[0] for k, v in base.items()}
         self.ops = []
         self.inputs = []          # (device tensor, host pinned) pairs copied in by e2e
@@ -303,7 +303,7 @@ class DeviceWorkload:
 
     @staticmethod
     def _part_alg_bytes(fmt, rows, cols, nt=1, f32=False) -> int:
-        wb = rows * (cols // 256) * (210 if fmt == "q6k" else 144)
+        wb = rows * (cols // 256) * {"q6k": 210, "q4k": 144, "q5k": 176}[fmt]
         act = (cols // 32) * (34 if fmt == "q6k" else 38)      # codes + fp16 d (+ int32 sum)
         if f32:
             act = 4 * cols                                      # the f32 row
@@ -318,11 +318,11 @@ class DeviceWorkload:
         mq = self.mq
         if self.nt > 1:
             fmt, copies, rows, y, _ = parts[0]
-            fn = mq.mq_gemv_q6k_q8_batch if fmt == "q6k" else mq.mq_gemv_q4k_q8_batch
+            fn = getattr(mq, f"mq_gemv_{fmt}_q8_batch")
             fn(copies[c], plane, self.nt, rows, cols, y=y)
         elif len(parts) == 1:
             fmt, copies, rows, y, _ = parts[0]
-            fn = mq.mq_gemv_q6k_q8 if fmt == "q6k" else mq.mq_gemv_q4k_q8
+            fn = getattr(mq, f"mq_gemv_{fmt}_q8")
             fn(copies[c], plane, rows, cols, y=y, ws=ws)
         else:
             mq.mq_gemv_group_q8(self._spec(o, c), plane, cols, ys=[p[3] for p in parts], ws=ws)
@@ -603,8 +603,8 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
                         "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
                         "algorithmic_bytes_per_step": int(alg),
                         "kernel": ("gemv_q6k_f32_kernel (q6_K x f32 row)" if wl.f32 else
-                                   "gemv_kernel (q6_K/q4_K x q8)" if args.tokens == 1 else
-                                   f"gemv_batch_kernel<{args.tokens}> (q6_K/q4_K x {args.tokens} q8 rows)"),
+                                   "gemv_kernel (q6_K/q4_K/q5_K x q8)" if args.tokens == 1 else
+                                   f"gemv_batch_kernel<{args.tokens}> (q6_K/q4_K/q5_K x {args.tokens} q8 rows)"),
                         "gemv_us_per_step": round(gemv_step_ms * 1e3, 3),
                         "how": f"GEMV launches of {n_kt} steps back to back in one CUDA graph "
                                f"(PDL off, rotated copies), CUDA events around 5 replays, median"}

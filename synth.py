@@ -99,7 +99,7 @@ class Workload:
     gemvs: list = field(default_factory=list)
 
     def weight_bytes(self) -> int:
-        return sum(rows * (cols // QK) * (Q6K_BYTES if fmt == "q6k" else Q4K_BYTES)
+        return sum(rows * (cols // QK) * {"q6k": Q6K_BYTES, "q4k": Q4K_BYTES, "q5k": Q5K_BYTES}[fmt]
                    for _, fmt, rows, cols, _ in self.gemvs)
 
 
@@ -132,6 +132,8 @@ WORKLOADS = {
     # 14B attn_v alone, and 2048 x 4864
     "attn_v_14b": Workload("attn_v_14b", [("attn_v", "q6k", KV_14B, HIDDEN_14B, "rms")]),
     "q6k_2048x4864": Workload("q6k_2048x4864", [("w", "q6k", 2048, 4864, "quantize")]),
+    # the q5_K sibling class on the 14B ffn_down shape
+    "ffn_down_14b_q5k": Workload("ffn_down_14b_q5k", [("ffn_down", "q5k", HIDDEN_14B, INTER_14B, "rms")]),
     # the 152064 x 5120 q6_K output head, fed by rms_norm -> q8
     "lm_head_14b": Workload("lm_head_14b", [("output", "q6k", VOCAB, HIDDEN_14B, "rms")]),
     # the FFN half of a Qwen2.5-14B layer: rms_norm -> q8 -> gate, up (q4_K)
