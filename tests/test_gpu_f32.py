@@ -69,7 +69,7 @@ def setup(mq, rows, cols, tag, xs=1.0):
 
 
 SHAPES = [(512, 2048), (1024, 5120), (2048, 4864), (37, 1280), (1, 256), (8, 2304), (3584, 18944),
-          (13, 56576)]
+          (13, 56576), (152064, 5120)]
 
 
 @pytest.mark.parametrize("rows,cols", SHAPES)
