@@ -165,28 +165,38 @@ __device__ __forceinline__ void compute(const GemvLaunch &a, const uint8_t *xs, 
         load_x_group<FMT, G>(a, xs, 0, NT, x, lane, X);
         compute_group<NT, G>(W, X, 0, reinterpret_cast<float(&)[G][8]>(acc.v));
     } else {
-        auto group = [&](int t0) {
-            XCodes<G> X;
-            load_x_group<FMT, G>(a, xs, t0, NT, x, lane, X);
-            float part[G][8];
+        // one group of GS tokens starting at t0 (GS is a compile-time size)
+        auto group = [&](auto gs, int t0) {
+            constexpr int GS = decltype(gs)::value;
+            XCodes<GS> X;
+            load_x_group<FMT, GS>(a, xs, t0, NT, x, lane, X);
+            float part[GS][8];
 #pragma unroll
-            for (int j = 0; j < G; ++j)
+            for (int j = 0; j < GS; ++j)
 #pragma unroll
                 for (int r = 0; r < 8; ++r) part[j][r] = 0.0f;
-            compute_group<NT, G>(W, X, t0, part);
+            compute_group<NT, GS>(W, X, t0, part);
 #pragma unroll
-            for (int j = 0; j < G; ++j)
+            for (int j = 0; j < GS; ++j)
                 if (t0 + j < NT) acc.s[t0 + j] += reduce8(part[j], lane);
         };
+        using GroupG = std::integral_constant<int, G>;
         if constexpr (NT == 6 || NT == 8) {
             // one token group at a time: unrolled, the groups' live ranges
             // overlap and spill 190-360 bytes; rolled, only the row sums go
             // to (L1-resident) local memory (7B at 8 tokens 40.4 -> 36.3 us)
 #pragma unroll 1
-            for (int t0 = 0; t0 < NT; t0 += G) group(t0);
+            for (int t0 = 0; t0 < NT; t0 += G) group(GroupG{}, t0);
+        } else if constexpr (NT == 7) {
+            // 3 + 2 + 2: a group of three, then the pairs rolled -- spill-free
+            // at 168 registers (7B at 7 tokens 34.7 -> 31.8 us); four pairs
+            // with a masked last token spilled 120-290 bytes
+            group(std::integral_constant<int, 3>{}, 0);
+#pragma unroll 1
+            for (int t0 = 3; t0 < NT; t0 += 2) group(std::integral_constant<int, 2>{}, t0);
         } else {
 #pragma unroll
-            for (int t0 = 0; t0 < NT; t0 += G) group(t0);
+            for (int t0 = 0; t0 < NT; t0 += G) group(GroupG{}, t0);
         }
     }
 }
