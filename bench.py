@@ -251,6 +251,8 @@ class DeviceWorkload:
         for o in self.ops:                       # workspace per GEMV launch (default plan)
             if o[0] == "gemv" and nt == 1:
                 o[4] = mq.mq_gemv_group_workspace(self._spec(o), o[2], device=device)
+        if self.ops[-1][0] not in ("gemv", "gemv32"):
+            raise SystemExit(f"{name}: a step must end with a GEMV (its output is the step's result)")
         self.output = self.ops[-1][3][-1][3]
         gemv_ops = [o for o in self.ops if o[0] in ("gemv", "gateup", "gemv32")]
         self.n_gemv = sum(len(o[3]) for o in gemv_ops)
@@ -300,6 +302,26 @@ class DeviceWorkload:
             t.set_(self.in_dev.untyped_storage(), off, t.shape)   # ops keep this tensor object
         self.in_dev.copy_(self.in_host)
         self.h2d_bytes = total * 4 if self.inputs else 0
+        self.in_off = {id(t): off for (t, _), off in zip(self.inputs, offs)}
+        # e2e: inputs read once per element (by quantize or SwiGLU) are read
+        # by those producers from pinned host memory in place; rms_norm reads
+        # its row once per CTA and the f32 GEMV once per CTA, so inputs that
+        # reach either are copied in first (mq_copy)
+        once = {id(t) for o in self.ops if o[0] == "quant" for t in (o[1],)} | \
+               {id(t) for o in self.ops if o[0] == "swiglu" for t in (o[1], o[2])}
+        self.inputs_in_place = bool(self.inputs) and all(id(t) in once for t, _ in self.inputs)
+
+    def host_inputs(self, n: int):
+        """n pinned copies of the step input buffer (same layout as in_dev),
+        so that consecutive e2e steps read different host lines."""
+        return [self.in_host.clone().pin_memory() for _ in range(n)]
+
+    def _in(self, t, host_in):
+        """t, or its view in the pinned host buffer host_in when t is a step input."""
+        if host_in is None or id(t) not in self.in_off:
+            return t
+        off = self.in_off[id(t)]
+        return host_in[off:off + t.numel()].view(t.shape)
 
     @staticmethod
     def _part_alg_bytes(fmt, rows, cols, nt=1, f32=False) -> int:
@@ -313,24 +335,28 @@ class DeviceWorkload:
     def _spec(o, c=0):
         return [(fmt, copies[c], rows) for fmt, copies, rows, _, _ in o[3]]
 
-    def _launch(self, o, c):
+    def _launch(self, o, c, y_last=None):
+        """y_last: write the launch's last output there instead (e2e: pinned host)."""
         _, plane, cols, parts, ws = o
         mq = self.mq
+        ys = [p[3] for p in parts]
+        if y_last is not None:
+            ys[-1] = y_last
         if self.nt > 1:
-            fmt, copies, rows, y, _ = parts[0]
+            fmt, copies, rows, _, _ = parts[0]
             fn = getattr(mq, f"mq_gemv_{fmt}_q8_batch")
-            fn(copies[c], plane, self.nt, rows, cols, y=y)
+            fn(copies[c], plane, self.nt, rows, cols, y=ys[0])
         elif len(parts) == 1:
-            fmt, copies, rows, y, _ = parts[0]
+            fmt, copies, rows, _, _ = parts[0]
             fn = getattr(mq, f"mq_gemv_{fmt}_q8")
-            fn(copies[c], plane, rows, cols, y=y, ws=ws)
+            fn(copies[c], plane, rows, cols, y=ys[0], ws=ws)
         else:
-            mq.mq_gemv_group_q8(self._spec(o, c), plane, cols, ys=[p[3] for p in parts], ws=ws)
+            mq.mq_gemv_group_q8(self._spec(o, c), plane, cols, ys=ys, ws=ws)
 
-    def _launch32(self, o, c):
+    def _launch32(self, o, c, y_last=None):
         _, xsrc, cols, parts, _ = o
         _, copies, rows, y, _ = parts[0]
-        self.mq.mq_gemv_q6k_f32(copies[c], xsrc, rows, cols, y=y)
+        self.mq.mq_gemv_q6k_f32(copies[c], xsrc, rows, cols, y=y if y_last is None else y_last)
 
     def _launch_gateup(self, o, c):
         _, plane, cols, parts, act, plane_out = o
@@ -348,29 +374,34 @@ class DeviceWorkload:
             elif o[0] == "gateup":
                 self._launch_gateup(o, c)
 
-    def run(self, k: int, producers_only: bool = False):
+    def run(self, k: int, producers_only: bool = False, host_in=None, out=None):
         """Enqueue step k (weights copy k % n_copies) on the current stream;
-        with producers_only, just its producer launches (for their timing)."""
+        with producers_only, just its producer launches (for their timing).
+        host_in: a pinned host input buffer whose views the producers read
+        in place of the device inputs; out: pinned host tensor the last GEMV
+        writes its output into."""
         mq = self.mq
         c = k % self.n_copies
+        last = self.ops[-1]
         for o in self.ops:
             kind = o[0]
             if producers_only and kind in ("gemv", "gemv32", "gateup"):
                 continue
             b = self.nt > 1
             if kind == "rms":
-                (mq.mq_rmsnorm_quant_q8_batch if b else mq.mq_rmsnorm_quant_q8)(o[1], o[2], 1e-6, y=o[3],
-                                                                                q8=o[4])
+                (mq.mq_rmsnorm_quant_q8_batch if b else mq.mq_rmsnorm_quant_q8)(
+                    self._in(o[1], host_in), o[2], 1e-6, y=o[3], q8=o[4])
             elif kind == "swiglu":
-                (mq.mq_swiglu_quant_q8_batch if b else mq.mq_swiglu_quant_q8)(o[1], o[2], y=o[3], q8=o[4])
+                (mq.mq_swiglu_quant_q8_batch if b else mq.mq_swiglu_quant_q8)(
+                    self._in(o[1], host_in), self._in(o[2], host_in), y=o[3], q8=o[4])
             elif kind == "quant":
-                (mq.mq_quantize_q8_batch if b else mq.mq_quantize_q8)(o[1], q8=o[2])
+                (mq.mq_quantize_q8_batch if b else mq.mq_quantize_q8)(self._in(o[1], host_in), q8=o[2])
             elif kind == "gateup":
                 self._launch_gateup(o, c)
             elif kind == "gemv32":
-                self._launch32(o, c)
+                self._launch32(o, c, out if o is last else None)
             else:
-                self._launch(o, c)
+                self._launch(o, c, out if o is last else None)
 
 
 def make_event(timing=True, external=False):
@@ -531,11 +562,17 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
     torch.cuda.synchronize()
 
+    # every step reads its own pinned input buffer (rotated like the weight
+    # copies, so no step finds the previous one's input lines in L2)
+    hosts = wl.host_inputs(wl.n_copies) if wl.inputs else []
+
     def e2e_step(i):
-        if wl.inputs:
-            mq.mq_copy(wl.in_dev, wl.in_host)            # pinned host -> device, a kernel
-        wl.run(i)
-        mq.mq_copy(out_host, wl.output)                  # device -> pinned host, a kernel
+        hin = hosts[i % len(hosts)] if hosts else None
+        if hin is not None and not wl.inputs_in_place:
+            mq.mq_copy(wl.in_dev, hin)                   # pinned host -> device, a kernel
+        # the producers read in-place inputs over the host link, and the
+        # last GEMV writes its rows straight into pinned host memory
+        wl.run(i, host_in=hin if wl.inputs_in_place else None, out=out_host)
 
     with torch.cuda.stream(stream):
         for i in range(3):
@@ -623,11 +660,13 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     line["e2e"] = {"value": round(wl.weight_bytes / (e2e_ms * 1e-3) / 1e9 * ws_, 2), "unit": "GB/s",
                    "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
                    "d2h_bytes_per_step": int(d2h),
-                   "how": f"public API calls captured in CUDA graphs of {m} steps, every step with "
-                          f"one H2D copy of all its inputs from pinned memory, producers + GEMVs and the "
-                          f"D2H copy of the last GEMV output into pinned memory (both copies by mq_copy, "
-                          f"a kernel in the PDL chain); {n_blocks * m} steps, wall clock, synchronize "
-                          f"at both ends",
+                   "how": f"public API calls captured in CUDA graphs of {m} steps; every step takes "
+                          f"its inputs from its own pinned host buffer ({len(hosts)} rotated) "
+                          + ("read in place by the quantize/SwiGLU producers over NVLink-C2C"
+                             if wl.inputs_in_place else "copied in by mq_copy (a kernel in the PDL chain)")
+                          + f", and the last GEMV writes its output rows into pinned host memory; "
+                          f"{n_blocks * m} steps, wall clock, synchronize at both ends",
+                   "inputs": "in place" if wl.inputs_in_place else "mq_copy",
                    "eager": {"value": round(wl.weight_bytes / (e2e_eager_ms * 1e-3) / 1e9 * ws_, 2),
                              "ms_per_step": round(e2e_eager_ms, 4),
                              "how": "the same steps as eager Python API calls"}}

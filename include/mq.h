@@ -25,6 +25,17 @@
  *     below 2^31 elements.
  *   - Alignment: every device pointer must be 16-byte aligned (the vector
  *     loads of [D4-4] §3.3 "the dpl row base is not naturally 16B aligned").
+ *   - Host-resident activations: the inputs x, g, u of the producers (single
+ *     and batched) and the output rows y of the GEMVs may instead be pinned
+ *     host memory, passed by the address mq_device_address gives for it (on
+ *     GB300, with unified addressing, the host pointer of cudaHostAlloc
+ *     memory itself).  The kernels then read or write it over NVLink-C2C,
+ *     so a decode step needs no separate copy in or out.  Quantize and
+ *     SwiGLU read each input element once; rms_norm reads its row once per
+ *     CTA (the sum of squares), so a wide row is better copied in first
+ *     (mq_copy).  The host must not touch such a buffer while a kernel that
+ *     uses it may run.  Weights, q8 planes and workspaces stay in device
+ *     memory.
  *   - Not thread-safe for the same workspace: calls that share a workspace
  *     must be ordered on one stream.
  */
@@ -464,6 +475,16 @@ int mq_repack_device(int fmt, const void *gguf, void *dst, int rows, int cols, v
  *   while a copy that uses it may run (synchronize first).
  * Errors: MQ_ERR_NULL, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_ACCESS, MQ_ERR_CUDA. */
 int mq_copy(void *dst, const void *src, size_t bytes, void *stream);
+
+/* The address a kernel on the current device uses for p: p itself for
+ * device or managed memory of the current device, the device-side address of
+ * pinned host memory (cudaHostAlloc / cudaMallocHost / cudaHostRegister).
+ * Look a buffer up once and pass the result to the entry points above that
+ * take host-resident activations.
+ *   p: any pointer; *out: written on MQ_OK only.
+ * Errors: MQ_ERR_NULL (p or out NULL), MQ_ERR_ACCESS (pageable host memory,
+ * another device's memory, or a pointer CUDA does not know). */
+int mq_device_address(const void *p, void **out);
 
 /* Measurement aid: read `bytes` (a multiple of 16) at src (device, 16-byte
  * aligned) once, in one launch, and do nothing with them.  Its time is the

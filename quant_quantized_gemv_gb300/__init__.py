@@ -44,6 +44,7 @@ EXPORTS = [
     "mq_gemv_q5k_q8", "mq_gemv_q5k_q8_plan", "mq_gemv_q5k_q8_subdots", "mq_gemv_q5k_q8_batch",
     "mq_gemv_q5k_q8_batch_plan", "mq_read_floor", "mq_gemv_q6k_f32", "mq_gemv_q6k_f32_plan",
     "mq_gemv_q6k_f32_plan_of", "mq_copy", "mq_repack_device", "mq_gemv_group_q8_coverage",
+    "mq_device_address",
 ]
 
 
@@ -137,6 +138,7 @@ def lib():
         "mq_gemv_q6k_f32_plan": ([P, P, P, I, I, I, I, I, P], I),
         "mq_gemv_q6k_f32_plan_of": ([I, I, P, P, P], I),
         "mq_copy": ([P, P, S, P], I),
+        "mq_device_address": ([P, ctypes.POINTER(ctypes.c_void_p)], I),
         "mq_repack_device": ([I, P, P, I, I, P], I),
         "mq_gemv_group_q8_coverage": ([P, I, P, I, I, I, I, P, S, P, P], I),
     }
@@ -168,6 +170,28 @@ def _dev(t, dtype=None):
     if not t.is_contiguous():
         raise ValueError("expected a contiguous tensor")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _act(t, dtype=None):
+    """An activation input or a GEMV output: a CUDA tensor, or a pinned CPU
+    tensor that the kernels reach over the host link (its device address)."""
+    import torch
+    if isinstance(t, torch.Tensor) and not t.is_cuda:
+        if not t.is_pinned():
+            raise TypeError("a CPU tensor must be pinned (the kernels address it directly)")
+        if dtype is not None and t.dtype != dtype:
+            raise TypeError(f"expected {dtype}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError("expected a contiguous tensor")
+        return ctypes.c_void_p(mq_device_address(t.data_ptr()))
+    return _dev(t, dtype)
+
+
+def mq_device_address(ptr: int) -> int:
+    """The device-side address of ptr (device or pinned host memory)."""
+    out = ctypes.c_void_p(0)
+    _check(lib().mq_device_address(ctypes.c_void_p(ptr), ctypes.byref(out)), "mq_device_address")
+    return out.value or 0
 
 
 def _stream(stream=None):
@@ -263,10 +287,19 @@ def mq_q8_unpack_host(plane: np.ndarray, n: int):
     return d, qs, s
 
 
+def _gpu_of(like):
+    """Where outputs go by default: like's device, or the current CUDA device
+    when like is a (pinned) host input."""
+    import torch
+    if not isinstance(like, torch.Tensor) or not (like.is_cuda or like.is_pinned()):
+        raise TypeError("expected a CUDA tensor or a pinned CPU tensor (the library has no CPU path)")
+    return like.device if like.is_cuda else torch.device("cuda", torch.cuda.current_device())
+
+
 def _q8_out(n: int, like, q8):
     import torch
     if q8 is None:
-        q8 = torch.empty(mq_q8_bytes(n), dtype=torch.uint8, device=like.device)
+        q8 = torch.empty(mq_q8_bytes(n), dtype=torch.uint8, device=_gpu_of(like))
     return q8
 
 
@@ -275,7 +308,7 @@ def mq_quantize_q8(x, q8=None, stream=None):
     import torch
     n = x.numel()
     q8 = _q8_out(n, x, q8)
-    _check(lib().mq_quantize_q8(_dev(x, torch.float32), _dev(q8), n, _stream(stream)),
+    _check(lib().mq_quantize_q8(_act(x, torch.float32), _dev(q8), n, _stream(stream)),
            "mq_quantize_q8")
     return q8
 
@@ -283,9 +316,9 @@ def mq_quantize_q8(x, q8=None, stream=None):
 def mq_rmsnorm_quant_q8(x, gain, eps: float, y=None, q8=None, stream=None):
     import torch
     n = x.numel()
-    y = torch.empty_like(x) if y is None else y
+    y = torch.empty(x.shape, dtype=x.dtype, device=_gpu_of(x)) if y is None else y
     q8 = _q8_out(n, x, q8)
-    _check(lib().mq_rmsnorm_quant_q8(_dev(x, torch.float32), _dev(gain, torch.float32), float(eps),
+    _check(lib().mq_rmsnorm_quant_q8(_act(x, torch.float32), _dev(gain, torch.float32), float(eps),
                                      _dev(y, torch.float32), _dev(q8), n, _stream(stream)),
            "mq_rmsnorm_quant_q8")
     return y, q8
@@ -294,9 +327,9 @@ def mq_rmsnorm_quant_q8(x, gain, eps: float, y=None, q8=None, stream=None):
 def mq_swiglu_quant_q8(g, u, y=None, q8=None, stream=None):
     import torch
     n = g.numel()
-    y = torch.empty_like(g) if y is None else y
+    y = torch.empty(g.shape, dtype=g.dtype, device=_gpu_of(g)) if y is None else y
     q8 = _q8_out(n, g, q8)
-    _check(lib().mq_swiglu_quant_q8(_dev(g, torch.float32), _dev(u, torch.float32),
+    _check(lib().mq_swiglu_quant_q8(_act(g, torch.float32), _act(u, torch.float32),
                                     _dev(y, torch.float32), _dev(q8), n, _stream(stream)),
            "mq_swiglu_quant_q8")
     return y, q8
@@ -306,7 +339,7 @@ def mq_swiglu_quant_q8(g, u, y=None, q8=None, stream=None):
 def _q8_out_rows(n: int, nt: int, like, q8):
     import torch
     if q8 is None:
-        q8 = torch.empty(nt * mq_q8_bytes(n), dtype=torch.uint8, device=like.device)
+        q8 = torch.empty(nt * mq_q8_bytes(n), dtype=torch.uint8, device=_gpu_of(like))
     return q8
 
 
@@ -315,7 +348,7 @@ def mq_quantize_q8_batch(x, q8=None, stream=None):
     import torch
     nt, n = x.shape[0], x.shape[1]
     q8 = _q8_out_rows(n, nt, x, q8)
-    _check(lib().mq_quantize_q8_batch(_dev(x, torch.float32), _dev(q8), n, nt, _stream(stream)),
+    _check(lib().mq_quantize_q8_batch(_act(x, torch.float32), _dev(q8), n, nt, _stream(stream)),
            "mq_quantize_q8_batch")
     return q8
 
@@ -324,9 +357,9 @@ def mq_rmsnorm_quant_q8_batch(x, gain, eps: float, y=None, q8=None, stream=None)
     """x: [nt, n] f32, gain: [n] -> y [nt, n] and nt q8 planes."""
     import torch
     nt, n = x.shape[0], x.shape[1]
-    y = torch.empty_like(x) if y is None else y
+    y = torch.empty(x.shape, dtype=x.dtype, device=_gpu_of(x)) if y is None else y
     q8 = _q8_out_rows(n, nt, x, q8)
-    _check(lib().mq_rmsnorm_quant_q8_batch(_dev(x, torch.float32), _dev(gain, torch.float32),
+    _check(lib().mq_rmsnorm_quant_q8_batch(_act(x, torch.float32), _dev(gain, torch.float32),
                                            float(eps), _dev(y, torch.float32), _dev(q8), n, nt,
                                            _stream(stream)),
            "mq_rmsnorm_quant_q8_batch")
@@ -337,9 +370,9 @@ def mq_swiglu_quant_q8_batch(g, u, y=None, q8=None, stream=None):
     """g, u: [nt, n] f32 -> y [nt, n] and nt q8 planes."""
     import torch
     nt, n = g.shape[0], g.shape[1]
-    y = torch.empty_like(g) if y is None else y
+    y = torch.empty(g.shape, dtype=g.dtype, device=_gpu_of(g)) if y is None else y
     q8 = _q8_out_rows(n, nt, g, q8)
-    _check(lib().mq_swiglu_quant_q8_batch(_dev(g, torch.float32), _dev(u, torch.float32),
+    _check(lib().mq_swiglu_quant_q8_batch(_act(g, torch.float32), _act(u, torch.float32),
                                           _dev(y, torch.float32), _dev(q8), n, nt, _stream(stream)),
            "mq_swiglu_quant_q8_batch")
     return y, q8
@@ -447,10 +480,10 @@ def _gemv(name: str, Wp, q8, rows: int, cols: int, y, ws, stream, plan=None):
     wsp, wsb = _ws_args(ws)
     L = lib()
     if plan is None:
-        st = getattr(L, name)(_dev(Wp), _dev(q8), _dev(y, torch.float32), rows, cols, wsp, wsb,
+        st = getattr(L, name)(_dev(Wp), _dev(q8), _act(y, torch.float32), rows, cols, wsp, wsb,
                               _stream(stream))
     else:
-        st = getattr(L, name + "_plan")(_dev(Wp), _dev(q8), _dev(y, torch.float32), rows, cols,
+        st = getattr(L, name + "_plan")(_dev(Wp), _dev(q8), _act(y, torch.float32), rows, cols,
                                         int(plan[0]), int(plan[1]), int(plan[2]), wsp, wsb,
                                         _stream(stream))
     _check(st, name)
@@ -490,10 +523,10 @@ def mq_gemv_q6k_f32(Wp, x, rows: int, cols: int, y=None, stream=None, plan=None)
     y = torch.empty(rows, dtype=torch.float32, device=Wp.device) if y is None else y
     L = lib()
     if plan is None:
-        st = L.mq_gemv_q6k_f32(_dev(Wp), _dev(x, torch.float32), _dev(y, torch.float32), rows, cols,
+        st = L.mq_gemv_q6k_f32(_dev(Wp), _dev(x, torch.float32), _act(y, torch.float32), rows, cols,
                                _stream(stream))
     else:
-        st = L.mq_gemv_q6k_f32_plan(_dev(Wp), _dev(x, torch.float32), _dev(y, torch.float32), rows,
+        st = L.mq_gemv_q6k_f32_plan(_dev(Wp), _dev(x, torch.float32), _act(y, torch.float32), rows,
                                     cols, int(plan[0]), int(plan[1]), int(plan[2]), _stream(stream))
     _check(st, "mq_gemv_q6k_f32")
     return y
@@ -515,10 +548,10 @@ def _gemv_batch(name: str, Wp, q8, nt: int, rows: int, cols: int, y, stream, pla
     y = torch.empty((nt, rows), dtype=torch.float32, device=Wp.device) if y is None else y
     L = lib()
     if plan is None:
-        st = getattr(L, name)(_dev(Wp), _dev(q8), nt, _dev(y, torch.float32), rows, cols,
+        st = getattr(L, name)(_dev(Wp), _dev(q8), nt, _act(y, torch.float32), rows, cols,
                               _stream(stream))
     else:
-        st = getattr(L, name + "_plan")(_dev(Wp), _dev(q8), nt, _dev(y, torch.float32), rows, cols,
+        st = getattr(L, name + "_plan")(_dev(Wp), _dev(q8), nt, _act(y, torch.float32), rows, cols,
                                         int(plan[0]), int(plan[1]), int(plan[2]), _stream(stream))
     _check(st, name)
     return y
@@ -575,7 +608,7 @@ def _parts_array(parts, ys=None):
         arr[i].fmt = fmt_code(fmt)
         arr[i].rows = int(rows)
         arr[i].Wp = None if Wp is None else Wp.data_ptr()
-        arr[i].y = None if ys is None else ys[i].data_ptr()
+        arr[i].y = None if ys is None else _act(ys[i]).value   # device address (pinned host too)
     return arr
 
 
@@ -603,7 +636,7 @@ def mq_gemv_group_q8(parts, q8, cols: int, ys=None, ws=None, stream=None, plan=N
     if ys is None:
         ys = [torch.empty(rows, dtype=torch.float32, device=q8.device) for _, _, rows in parts]
     for y in ys:
-        _dev(y, torch.float32)
+        _act(y, torch.float32)
     arr = _parts_array(parts, ys)
     wsp, wsb = _ws_args(ws)
     if plan is None:
@@ -626,7 +659,7 @@ def mq_gemv_group_q8_coverage(parts, q8, cols: int, ys=None, ws=None, stream=Non
     if ys is None:
         ys = [torch.empty(rows, dtype=torch.float32, device=q8.device) for _, _, rows in parts]
     for y in ys:
-        _dev(y, torch.float32)
+        _act(y, torch.float32)
     tiles = sum(-(-rows // 8) for _, _, rows in parts)
     nch = -(-(cols // 256) // 4)
     counts = torch.zeros((tiles, nch), dtype=torch.int32, device=q8.device)
@@ -646,7 +679,7 @@ def mq_gemv_q6k_q8_noalloc(Wp, q8, rows: int, cols: int, y=None, stream=None):
     import torch
     if y is None:
         y = torch.empty(rows, dtype=torch.float32, device=Wp.device)
-    _check(lib().mq_gemv_q6k_q8_noalloc(_dev(Wp), _dev(q8), _dev(y, torch.float32), rows, cols,
+    _check(lib().mq_gemv_q6k_q8_noalloc(_dev(Wp), _dev(q8), _act(y, torch.float32), rows, cols,
                                         _stream(stream)), "mq_gemv_q6k_q8_noalloc")
     return y
 

@@ -1037,6 +1037,12 @@ int mq_copy(void *dst, const void *src, size_t bytes, void *stream)
     return e == cudaSuccess ? MQ_OK : cuda_fail("copy launch", e);
 }
 
+int mq_device_address(const void *p, void **out)
+{
+    if (!p || !out) return MQ_ERR_NULL;
+    return device_address(p, out);
+}
+
 int mq_read_floor(const void *src, size_t bytes, void *stream)
 {
     if (!src) return MQ_ERR_NULL;
