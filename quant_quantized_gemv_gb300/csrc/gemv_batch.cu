@@ -41,10 +41,17 @@ namespace {
 using namespace gemv_detail;
 
 // Tokens whose activation codes are held in registers at once: all of them
-// up to kGroup; beyond that pairs (groups of 3 or 4 out of 5..8 tokens spill
-// more registers at the 168-register cap).
+// up to kGroup.  Beyond that the groups run one at a time in a rolled loop,
+// and every group decodes the 8 rows again: q6_K and q5_K take two groups of
+// 3 or 4 at 6 and 8 tokens (spill-free at 168 registers; 8 tokens: 7B
+// 36.3 -> 33.9 us, head 267 -> 243 us), q4_K, whose decode is cheap, pairs
+// (its 8-token gate 25.7 against 26.5 us with groups of 4).  5 and 7 tokens
+// are arranged in compute().
 constexpr int kGroup = 4;
-__host__ __device__ constexpr int group_size(int nt) { return nt <= kGroup ? nt : 2; }
+__host__ __device__ constexpr int group_size(int nt, int fmt)
+{
+    return nt <= kGroup ? nt : fmt != 4 && (nt == 6 || nt == 8) ? nt / 2 : 2;
+}
 
 // Running sums of a work item.  Up to kGroup tokens each lane keeps its own
 // partial sums of the 8 rows (reduced across lanes when a tile is flushed,
@@ -159,7 +166,7 @@ template <int FMT, int NT>
 __device__ __forceinline__ void compute(const GemvLaunch &a, const uint8_t *xs, const Unit &x,
                                         int lane, const typename Fmt<FMT>::W &W, Acc<NT> &acc)
 {
-    constexpr int G = group_size(NT);
+    constexpr int G = group_size(NT, FMT);
     if constexpr (!Acc<NT>::kEach) {  // one group: accumulate straight into the per-lane partials
         XCodes<G> X;
         load_x_group<FMT, G>(a, xs, 0, NT, x, lane, X);
@@ -184,13 +191,15 @@ __device__ __forceinline__ void compute(const GemvLaunch &a, const uint8_t *xs, 
         if constexpr (NT == 6 || NT == 8) {
             // one token group at a time: unrolled, the groups' live ranges
             // overlap and spill 190-360 bytes; rolled, only the row sums go
-            // to (L1-resident) local memory (7B at 8 tokens 40.4 -> 36.3 us)
+            // to (L1-resident) local memory (7B at 8 tokens in pairs 40.4 ->
+            // 36.3 us)
 #pragma unroll 1
             for (int t0 = 0; t0 < NT; t0 += G) group(GroupG{}, t0);
         } else if constexpr (NT == 7) {
             // 3 + 2 + 2: a group of three, then the pairs rolled -- spill-free
             // at 168 registers (7B at 7 tokens 34.7 -> 31.8 us); four pairs
-            // with a masked last token spilled 120-290 bytes
+            // with a masked last token spilled 120-290 bytes, and two rolled
+            // groups of four with a masked token were slower (34.0 us)
             group(std::integral_constant<int, 3>{}, 0);
 #pragma unroll 1
             for (int t0 = 3; t0 < NT; t0 += 2) group(std::integral_constant<int, 2>{}, t0);
