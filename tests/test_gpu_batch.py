@@ -142,7 +142,7 @@ SHAPES = [(37, 4608), (64, 18944), (9, 1280), (8, 256), (200, 5120)]
 
 
 @pytest.mark.parametrize("fmt", ["q6k", "q4k", "q5k"])
-@pytest.mark.parametrize("nt", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("nt", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("rows,cols", SHAPES)
 def test_batch_gemv_matches_oracle_per_token(mq, orc, fmt, nt, rows, cols):
     W, Wp, x = make(mq, fmt, rows, cols, nt, 0)
@@ -226,7 +226,9 @@ def test_planes_too_large_for_shared_memory(mq):
 
 
 FULL = [("ffn_down_7b", "q6k", 3584, 18944, "swiglu", 4),
+        ("ffn_down_7b", "q6k", 3584, 18944, "swiglu", 7),
         ("ffn_down_7b", "q6k", 3584, 18944, "swiglu", 8),
+        ("ffn_down_14b_q5k", "q5k", 5120, 13824, "swiglu", 6),
         ("attn_v_14b", "q6k", 1024, 5120, "rms", 8),
         ("ffn_gate_14b", "q4k", 13824, 5120, "rms", 8),
         ("lm_head_14b", "q6k", 152064, 5120, "rms", 2),
