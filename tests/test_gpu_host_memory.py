@@ -193,3 +193,48 @@ def test_decode_steps_in_a_graph_with_pdl(mq):
         mq.mq_set_pdl(bool(prev))
     for o, e in zip(outs, expect):
         assert torch.equal(o, e)
+
+
+def test_rewritten_host_buffers_in_a_replayed_graph(mq):
+    """One pinned input buffer and one pinned output buffer, captured once
+    (SwiGLU -> q8 -> q6_K GEMV, PDL), the host writing a new input between
+    replays: every replay sees the new input and returns its own result."""
+    import torch
+    inter, rows = 13824, 1024
+    g = synth.rng("host-rewrite")
+    Wp = torch.from_numpy(mq.mq_repack_q6k(synth.q6k_blocks(g, rows, inter), rows, inter)).cuda()
+    gh = torch.empty(inter).pin_memory()
+    uh = torch.empty(inter).pin_memory()
+    yo = torch.empty(rows).pin_memory()
+    act = torch.empty(inter, device="cuda")
+    q8 = torch.empty(mq.mq_q8_bytes(inter), dtype=torch.uint8, device="cuda")
+    ws = mq.mq_gemv_workspace(rows, inter)
+    stream = torch.cuda.Stream()
+    prev = mq.mq_set_pdl(True)
+    try:
+        def step():
+            mq.mq_swiglu_quant_q8(gh, uh, y=act, q8=q8)
+            mq.mq_gemv_q6k_q8(Wp, q8, rows, inter, y=yo, ws=ws)
+        gh.copy_(torch.from_numpy(synth.normal(g, inter)))
+        uh.copy_(torch.from_numpy(synth.normal(g, inter)))
+        with torch.cuda.stream(stream):
+            step()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        seen = []
+        for _ in range(4):
+            a, b = synth.normal(g, inter), synth.normal(g, inter)
+            gh.copy_(torch.from_numpy(a))
+            uh.copy_(torch.from_numpy(b))
+            graph.replay()
+            torch.cuda.synchronize()
+            got = yo.clone()
+            _, qd = mq.mq_swiglu_quant_q8(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda())
+            want = mq.mq_gemv_q6k_q8(Wp, qd, rows, inter, ws=mq.mq_gemv_workspace(rows, inter)).cpu()
+            assert torch.equal(got, want)
+            seen.append(got)
+    finally:
+        mq.mq_set_pdl(bool(prev))
+    assert not torch.equal(seen[0], seen[1])
