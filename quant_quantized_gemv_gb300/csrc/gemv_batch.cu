@@ -312,6 +312,20 @@ struct Cursor {
 template <int NT>
 constexpr bool kTwoBuffers = NT == 1;
 
+// With one buffer, lane 0 asks L2 for chunk u + 1 (one bulk prefetch of its
+// contiguous bytes) before chunk u computes, so that the register loads
+// issued after the compute find it there: 7B at 2 and 4 tokens 14.8 -> 13.9
+// and 19.5 -> 18.6 us, the q4_K gate 7-9% faster.  q5_K at 4 tokens was
+// slower with it (22.6 against 22.0 us) and goes without.
+template <int NT, int FMT>
+constexpr bool kPrefetchNext = !kTwoBuffers<NT> && !(FMT == 5 && NT == 4);
+
+// Hint: move [p, p + bytes) toward L2 (p and bytes multiples of 16).
+__device__ __forceinline__ void prefetch_l2(const void *p, unsigned bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 template <int FMT, int NT>
 __device__ __forceinline__ void run_batch(const GemvLaunch &a, const GemvPart &P, uint8_t *xs, int lane)
 {
@@ -352,6 +366,10 @@ __device__ __forceinline__ void run_batch(const GemvLaunch &a, const GemvPart &P
     int done = 0;  // tiles flushed so far
     if constexpr (!kTwoBuffers<NT>) {  // one buffer: the next chunk's loads follow its compute
         for (int u = 0; u < n_units; ++u) {
+            if (kPrefetchNext<NT, FMT> && lane == 0 && u + 1 < n_units) {
+                const Unit nx = unit_at(next);
+                if (nx.t < P.ntiles) prefetch_l2(nx.seg, (unsigned)(kChunkBytes / kChunkBlocks * nx.cb));
+            }
             compute<FMT, NT>(a, xs, xa, lane, A, acc);
             const int t = xa.t;
             const bool last = xa.c == c_hi - 1;
