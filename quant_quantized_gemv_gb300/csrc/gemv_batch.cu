@@ -34,6 +34,7 @@
 #include "gemv_common.cuh"
 #include "kernels.h"
 #include "layout.h"
+#include "prefetch.cuh"
 
 namespace mq {
 namespace {
@@ -319,12 +320,6 @@ constexpr bool kTwoBuffers = NT == 1;
 // slower with it (22.6 against 22.0 us) and goes without.
 template <int NT, int FMT>
 constexpr bool kPrefetchNext = !kTwoBuffers<NT> && !(FMT == 5 && NT == 4);
-
-// Hint: move [p, p + bytes) toward L2 (p and bytes multiples of 16).
-__device__ __forceinline__ void prefetch_l2(const void *p, unsigned bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 
 template <int FMT, int NT>
 __device__ __forceinline__ void run_batch(const GemvLaunch &a, const GemvPart &P, uint8_t *xs, int lane)
