@@ -41,6 +41,7 @@
 #include "gemv_common.cuh"
 #include "kernels.h"
 #include "layout.h"
+#include "prefetch.cuh"
 
 namespace mq {
 namespace {
@@ -192,6 +193,15 @@ __device__ __forceinline__ void run_f32(const GemvLaunch &a, const GemvPart &P, 
     for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
     for (int u = u0; u < u1; ++u) {
         const int tcur = xa.t;
+        // Lane 0 asks L2 for chunk u + 1 (one bulk prefetch of its contiguous
+        // bytes) before chunk u computes, so the register loads issued after
+        // the compute find it there: 7B ffn_down 20.0 -> 18.5 us, 14B
+        // ffn_down 32.4 -> 28.0 us, head 125.5 -> 122.5 us (shapes with one
+        // chunk per warp issue none).
+        if (lane == 0 && u + 1 < u1) {
+            const Unit nx = locate(a, P, t, c, 0, kChunkBytes);
+            prefetch_l2(nx.seg, (unsigned)(kChunkBytes / kChunkBlocks * nx.cb));
+        }
         compute_f32(A, xs, xa, lane, acc);
         const bool more = u + 1 < u1;
         if (more) {  // the next chunk into the same registers
