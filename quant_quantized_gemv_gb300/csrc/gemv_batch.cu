@@ -16,8 +16,8 @@
 // What changes with nt:
 //   * All nt q8 planes are staged in shared memory once per CTA (after the
 //     grid-dependency wait), whatever the plan; each chunk's codes for a
-//     group of tokens (all of them up to 4, else pairs) are then read from
-//     there into registers.
+//     group of tokens (all of them up to 4, else groups of 2-4, see
+//     group_size and compute) are then read from there into registers.
 //   * A weight row's codes are decoded once per token group and used for
 //     every token of the group: the decode, not the dp4a, dominates the ALU
 //     work of a chunk.
@@ -25,6 +25,8 @@
 //     the register file holds at the instance's register cap (16 warps at
 //     128 registers for 2 tokens, 14-15 for 3-4 tokens of most formats, 12
 //     at 168 otherwise).
+//   * With one register buffer per warp, lane 0 prefetches the warp's next
+//     chunk into L2 while the current one computes (kPrefetchNext).
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
