@@ -198,6 +198,18 @@ def test_binding_refuses_cpu_tensors(mq):
     import torch
     with pytest.raises(TypeError):
         mq.mq_quantize_q8(torch.zeros(64))
+    with pytest.raises(TypeError):                       # pageable: the kernels cannot reach it
+        mq.mq_swiglu_quant_q8(torch.zeros(64), torch.zeros(64))
+
+
+def test_device_address_argument_checks(mq):
+    """NULL arguments are refused before any CUDA call."""
+    import ctypes
+    out = ctypes.c_void_p(0)
+    L = mq.lib()
+    assert L.mq_device_address(None, ctypes.byref(out)) == mq.MQ_ERR_NULL
+    assert L.mq_device_address(ctypes.c_void_p(16), None) == mq.MQ_ERR_NULL
+    assert out.value is None
 
 
 def test_group_workspace_and_validation(mq):
