@@ -308,8 +308,10 @@ int mq_gemv_group_q8_plan(const mq_gemv_part *parts, int nparts, const void *q8,
  *   q8: nt planes of cols values, back to back: token t's plane starts at
  *       q8 + t * mq_q8_bytes(cols) (what the _batch producers write).
  *   y:  nt x rows f32, token-major: y[t * rows + r].
- *   nt == 1 runs the same kernel for one token (no workspace, unlike
- *   mq_gemv_q6k_q8, whose long-row plans may need one).
+ *   nt == 1 (default plan) runs the single-token GEMV of the format when
+ *   its default plan needs no workspace, else this kernel for one token;
+ *   either way no workspace is taken (mq_gemv_q6k_q8's long-row plans may
+ *   need one).  The _plan forms always run this kernel.
  *   Every CTA stages all nt planes in shared memory: nt * mq_q8_bytes(cols)
  *   must not exceed the device's per-CTA limit less 8 KiB (about 219 KiB on
  *   GB300, i.e. cols <= 26368 at nt = 8), else MQ_ERR_SHAPE.

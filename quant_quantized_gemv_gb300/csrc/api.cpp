@@ -456,6 +456,20 @@ int gemv_common(int fmt, const void *Wp, const void *q8, float *y, int rows, int
     return gemv_group(&part, 1, q8, cols, explicit_plan, ws, ws_bytes, stream, nt);
 }
 
+// The small-batch entry points (default plan).  One token goes to the
+// single-token GEMV when that kernel's default plan needs no workspace (the
+// batch entry points take none): it streams one token faster (7B ffn_down
+// 11.2 against 12.8 us).  Otherwise, and for 2..8 tokens, the batch kernel.
+int batch_entry(int fmt, const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
+                void *stream)
+{
+    if (nt < 1) return MQ_ERR_SHAPE;
+    int s = 0, c = 0, t = 0;  // splits beyond kMaxCtaSplits meet in a workspace
+    if (nt == 1 && mq_gemv_plan(rows, cols, fmt, &s, &c, &t) == MQ_OK && s <= kMaxCtaSplits)
+        return gemv_common(fmt, Wp, q8, y, rows, cols, nullptr, nullptr, 0, stream, 0);
+    return gemv_common(fmt, Wp, q8, y, rows, cols, nullptr, nullptr, 0, stream, nt);
+}
+
 int batch_plan_of(int rows, int cols, int nt, Plan *p)
 {
     if (!gemv_shape_ok(rows, cols) || nt < 1 || nt > kMaxTokens) return MQ_ERR_SHAPE;
@@ -945,22 +959,19 @@ int mq_gemv_batch_plan_for(int rows, int cols, int nt, int sms, int regs_per_thr
 int mq_gemv_q6k_q8_batch(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
                          void *stream)
 {
-    if (nt < 1) return MQ_ERR_SHAPE;
-    return gemv_common(6, Wp, q8, y, rows, cols, nullptr, nullptr, 0, stream, nt);
+    return batch_entry(6, Wp, q8, nt, y, rows, cols, stream);
 }
 
 int mq_gemv_q4k_q8_batch(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
                          void *stream)
 {
-    if (nt < 1) return MQ_ERR_SHAPE;
-    return gemv_common(4, Wp, q8, y, rows, cols, nullptr, nullptr, 0, stream, nt);
+    return batch_entry(4, Wp, q8, nt, y, rows, cols, stream);
 }
 
 int mq_gemv_q5k_q8_batch(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,
                          void *stream)
 {
-    if (nt < 1) return MQ_ERR_SHAPE;
-    return gemv_common(5, Wp, q8, y, rows, cols, nullptr, nullptr, 0, stream, nt);
+    return batch_entry(5, Wp, q8, nt, y, rows, cols, stream);
 }
 
 int mq_gemv_q5k_q8_batch_plan(const void *Wp, const void *q8, int nt, float *y, int rows, int cols,

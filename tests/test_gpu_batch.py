@@ -216,6 +216,22 @@ def test_batch_of_one_needs_no_workspace(mq, orc, fmt):
     assert_close(yb, yref, absum)
 
 
+@pytest.mark.parametrize("fmt", ["q6k", "q4k", "q5k"])
+@pytest.mark.parametrize("rows,cols", [(3584, 18944), (1000, 5120), (13824, 5120)])
+def test_batch_of_one_is_the_single_token_gemv(mq, orc, fmt, rows, cols):
+    """One token whose single-token default plan needs no workspace runs the
+    single-token GEMV through the batch entry point: the same bits as
+    mq_gemv_*_q8, and the oracle's values within tolerance."""
+    W, Wp, x = make(mq, fmt, rows, cols, 1, 4)
+    plane = mq.mq_quantize_q8(dev(x[0]))
+    assert mq.mq_gemv_workspace_bytes(rows, cols) == 0
+    yb = host(batch_fn(mq, fmt)(Wp, plane, 1, rows, cols))
+    ys = host(getattr(mq, f"mq_gemv_{fmt}_q8")(Wp, plane, rows, cols))
+    assert np.array_equal(yb.reshape(-1), ys)
+    yref, absum = oracle_rows(orc, fmt, W, rows, cols, planes_fields(mq, plane, cols, 1))
+    assert_close(yb, yref, absum)
+
+
 def test_planes_too_large_for_shared_memory(mq):
     rows, cols, nt = 8, 65536, 8                 # 8 planes of 69.6 KB
     W, Wp, x = make(mq, "q4k", rows, cols, nt, 4)
