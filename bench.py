@@ -3,10 +3,20 @@
 
 A step is one pass of the whole hot path over one synthetic decode token:
 the q8 producer(s) followed by the GEMV(s) of the workload, with the weights
-resident in HBM.  The default workload is the Qwen2.5-7B-shaped ffn_down:
-SwiGLU(g, u) -> q8 -> q6_K 3584 x 18944 GEMV (74 super-blocks per row, so
-split-K).  L2 is defeated by rotating through enough device copies of the
-weights that one rotation exceeds 4x the L2 size.
+resident in HBM.  The default workload is the full Qwen2.5-14B-shaped decode
+weight sweep: 48 layers x {q, k, v, o, gate, up, down} plus the 152064 x 5120
+output head, 9.011 GB of k-quant weights per step, fed by the fused
+rms_norm / SwiGLU / quantize -> q8 producers (every layer's matrices are
+distinct device buffers, so one step's inputs exceed L2 many times over).
+Workloads smaller than 4x L2 rotate through enough device copies of their
+weights.  The sweep's line also reports the four other benchmark
+configurations (the 512 x 2048 GEMV, the 7B ffn_down, the 14B attn_v +
+ffn_down layer and the head), measured in the same process.
+
+Timing: R >= 5 timed regions of exactly K steps each (CUDA graphs of at most
+64 consecutive steps; one graph when K <= 64), CUDA events on the launching
+stream with a barrier and synchronize on both sides; the median region is
+reported, with the spread.
 
     python bench.py [--gpus N --steps K --warmup W] [--impl mq|reference]
                     [--workload NAME] [--tokens NT]
@@ -148,24 +158,31 @@ def measured_peak_gbs():
         return 6800.0, "fallback"
 
 
-def gemv_source_hash(act: str = "q8") -> str:
+def gemv_source_hash(act: str = "q8", gateup: bool = False) -> str:
+    """First 16 hex digits of the SHA-256 of the GEMV kernel sources (with
+    the gate||up kernel when the workload launches it)."""
     h = hashlib.sha256()
-    for f in ("gemv_f32.cu" if act == "f32" else "gemv.cu", "gemv_common.cuh", "layout.h"):
+    files = ["gemv_f32.cu" if act == "f32" else "gemv.cu", "gemv_common.cuh", "layout.h"]
+    if gateup:
+        files.append("gemv_gateup.cu")
+    for f in files:
         with open(os.path.join(ROOT, "quant_quantized_gemv_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str, act: str = "q8"):
-    """DRAM bytes per GEMV launch from the committed ncu summary of this
-    workload, if it was taken on the current kernel source (else None)."""
+def profiled_traffic(workload: str, act: str = "q8", gateup: bool = False):
+    """DRAM bytes (read + write) of the GEMV launches of one step, from the
+    committed ncu summary of this workload, if it was taken on the current
+    kernel source (else None).  A one-GEMV workload's summary gives them per
+    launch (= per step)."""
     p = os.path.join(ROOT, "profiles", f"gemv_{'f32_' if act == 'f32' else ''}{workload}.md")
     if not os.path.exists(p):
         return None
     txt = open(p).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    m = re.search(r"traffic_bytes_per_(?:launch|step):\s*([0-9.eE+]+)", txt)
     h = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
-    if not m or not h or h.group(1) != gemv_source_hash(act):
+    if not m or not h or h.group(1) != gemv_source_hash(act, gateup):
         return None
     return float(m.group(1))
 
@@ -324,6 +341,10 @@ class DeviceWorkload:
         return host_in[off:off + t.numel()].view(t.shape)
 
     @staticmethod
+    def _part_weight_bytes(fmt, rows, cols) -> int:
+        return rows * (cols // 256) * {"q6k": 210, "q4k": 144, "q5k": 176}[fmt]
+
+    @staticmethod
     def _part_alg_bytes(fmt, rows, cols, nt=1, f32=False) -> int:
         wb = rows * (cols // 256) * {"q6k": 210, "q4k": 144, "q5k": 176}[fmt]
         act = (cols // 32) * (34 if fmt == "q6k" else 38)      # codes + fp16 d (+ int32 sum)
@@ -363,16 +384,22 @@ class DeviceWorkload:
         (fmt, cg, rows, _, _), (_, cu, _, _, _) = parts
         self.mq.mq_gemv_gateup_swiglu_q8(fmt, cg[c], cu[c], plane, rows, cols, act=act, q8_out=plane_out)
 
-    def run_gemvs(self, k: int):
-        """Enqueue only the GEMV launches of step k (for kernel timing)."""
+    def launch_op(self, o, k: int):
+        """Enqueue one GEMV-type op of step k (weights copy k % n_copies)."""
         c = k % self.n_copies
+        if o[0] == "gemv":
+            self._launch(o, c)
+        elif o[0] == "gemv32":
+            self._launch32(o, c)
+        elif o[0] == "gateup":
+            self._launch_gateup(o, c)
+
+    def run_gemvs(self, k: int, kinds=None):
+        """Enqueue only the GEMV launches of step k (for kernel timing), or
+        only those of the given op kinds."""
         for o in self.ops:
-            if o[0] == "gemv":
-                self._launch(o, c)
-            elif o[0] == "gemv32":
-                self._launch32(o, c)
-            elif o[0] == "gateup":
-                self._launch_gateup(o, c)
+            if o[0] in ("gemv", "gemv32", "gateup") and (kinds is None or o[0] in kinds):
+                self.launch_op(o, k)
 
     def run(self, k: int, producers_only: bool = False, host_in=None, out=None):
         """Enqueue step k (weights copy k % n_copies) on the current stream;
@@ -419,6 +446,143 @@ def capture(fn, stream):
     return g
 
 
+class StepGraphs:
+    """CUDA graphs of consecutive steps of one step function, at most m steps
+    each, cached by (first weight copy, length): steps i and i + n_copies use
+    the same buffers, so one graph serves every segment with that phase."""
+
+    def __init__(self, fn, n_copies: int, m: int, stream):
+        self.fn, self.n_copies, self.m, self.stream = fn, n_copies, max(1, m), stream
+        self.cache = {}
+
+    def _segments(self, start: int, k: int):
+        s = start
+        while s < start + k:
+            n = min(self.m, start + k - s)
+            yield s, n
+            s += n
+
+    def _graph(self, s: int, n: int):
+        key = (s % self.n_copies, n)
+        if key not in self.cache:
+            self.cache[key] = capture(lambda: [self.fn(s + j) for j in range(n)], self.stream)
+        return self.cache[key]
+
+    def prepare(self, start: int, k: int):
+        """Capture (outside any timed region) every graph enqueue() will use."""
+        for s, n in self._segments(start, k):
+            self._graph(s, n)
+
+    def enqueue(self, start: int, k: int):
+        """Enqueue exactly k steps, start .. start + k - 1."""
+        for s, n in self._segments(start, k):
+            self._graph(s, n).replay()
+
+
+def replay_ms(graph, stream, reps: int = 5) -> list:
+    """Device time of `reps` replays of a graph, CUDA events on the stream."""
+    import torch
+    with torch.cuda.stream(stream):
+        graph.replay()                                   # warm
+    torch.cuda.synchronize()
+    out = []
+    for _ in range(reps):
+        e0, e1 = make_event(), make_event()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        e1.synchronize()
+        out.append(e0.elapsed_time(e1))
+    return out
+
+
+def spread(vals, scale: float = 1.0, nd: int = 3) -> dict:
+    v = sorted(x * scale for x in vals)
+    return {"median": round(float(np.median(v)), nd), "min": round(v[0], nd), "max": round(v[-1], nd),
+            "n": len(v)}
+
+
+def kernel_graphs(wl, stream, n_kt: int, kinds=None):
+    """One graph of the GEMV launches (of the given op kinds) of n_kt
+    consecutive steps back to back, PDL off, rotating weight copies."""
+    return capture(lambda: [wl.run_gemvs(i, kinds) for i in range(n_kt)], stream)
+
+
+def config_report(name: str, dev, l2: int, stream, peak: float, pdl: bool) -> dict:
+    """GEMV-alone and chained-step timing of one more workload, measured in
+    this process: per GEMV op µs, content GB/s and fraction of the peak."""
+    import torch
+    import quant_quantized_gemv_gb300 as mq
+    wl = DeviceWorkload(name, dev, l2)
+    with torch.cuda.stream(stream):
+        wl.run(0)
+    torch.cuda.synchronize()
+    mq.mq_set_pdl(False)
+    n_kt = max(wl.n_copies, 16)
+    ops = [o for o in wl.ops if o[0] in ("gemv", "gateup")]
+    gemvs = []
+    for idx, o in enumerate(ops):
+        g = capture(lambda o=o: [wl.launch_op(o, i) for i in range(n_kt)], stream)
+        t = replay_ms(g, stream)
+        us = float(np.median(t)) / n_kt * 1e3
+        wbytes = sum(DeviceWorkload._part_weight_bytes(p[0], p[2], o[2]) for p in o[3])
+        alg = sum(DeviceWorkload._part_alg_bytes(p[0], p[2], o[2]) for p in o[3])
+        gemvs.append({"gemv": "+".join(f"{p[4]} {p[0]} {p[2]}x{o[2]}" for p in o[3]),
+                      "us": round(us, 3), "us_spread": spread(t, 1e3 / n_kt),
+                      "content_gbs": round(wbytes / (us * 1e-6) / 1e9, 1),
+                      "frac": round(alg / (us * 1e-6) / 1e9 / peak, 4)})
+        del g
+    floor_us = None
+    if wl.n_gemv == 1:
+        wcopies = ops[0][3][0][1]
+        fg = capture(lambda: [mq.mq_read_floor(wcopies[i % wl.n_copies]) for i in range(n_kt)], stream)
+        floor_us = round(float(np.median(replay_ms(fg, stream))) / n_kt * 1e3, 3)
+        del fg
+    mq.mq_set_pdl(pdl)
+    m = 16
+    sg = StepGraphs(wl.run, wl.n_copies, m, stream)
+    nsteps = max(m, wl.n_copies)
+    sg.prepare(0, nsteps)
+    with torch.cuda.stream(stream):
+        sg.enqueue(0, nsteps)
+    torch.cuda.synchronize()
+    st = []
+    for _ in range(5):
+        e0, e1 = make_event(), make_event()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            sg.enqueue(0, nsteps)
+            e1.record(stream)
+        e1.synchronize()
+        st.append(e0.elapsed_time(e1) / nsteps)
+    mq.mq_set_pdl(False)
+    step_us = float(np.median(st)) * 1e3
+    gemv_us = sum(x["us"] for x in gemvs)
+    alg = float(sum(wl.gemv_bytes))
+    rep = {"workload": f"{name}: {DESCR[name]}",
+           "weight_content_bytes": wl.weight_bytes,
+           "gemv_us": round(gemv_us, 3),
+           "content_gbs": round(wl.weight_bytes / (gemv_us * 1e-6) / 1e9, 1),
+           "frac": round(alg / (gemv_us * 1e-6) / 1e9 / peak, 4),
+           "gemvs": gemvs,
+           "step_us": round(step_us, 3), "step_spread_us": spread(st, 1e3),
+           "step_content_gbs": round(wl.weight_bytes / (step_us * 1e-6) / 1e9, 1),
+           "l2": f"{wl.n_copies} rotated weight copies"}
+    if floor_us is not None:
+        rep["read_floor_us"] = floor_us
+        rep["frac_of_read_floor"] = round(floor_us / gemv_us, 4)
+    del sg, wl
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rep
+
+
+# the benchmark configurations reported beside the headline one (the
+# smallest GEMV, the 7B ffn_down, the 14B attn_v + ffn_down layer, the head)
+CONFIG_WORKLOADS = ["q6k_512x2048", "ffn_down_7b", "layer_14b", "lm_head_14b"]
+
+
 def bench_mq(args, ws_, rank, local) -> dict | None:
     import torch
     torch.cuda.set_device(local)
@@ -439,19 +603,24 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     with torch.cuda.stream(stream):
         wl.run(0)                                   # first launches outside capture
     torch.cuda.synchronize()
+    K, W, R = args.steps, args.warmup, max(5, args.repeats)
 
-    # ---- step graphs: m consecutive steps per graph (PDL edges between all
-    # kernels when enabled), rotating through the weight copies
+    # ---- step graphs: segments of at most m consecutive steps (PDL edges
+    # between all kernels of a segment when enabled); a timed region of K
+    # <= m steps is one graph of exactly K steps
     mq.mq_set_pdl(args.pdl)
-    m = max(1, min(args.steps_per_graph, args.steps))
-    n_big = max(1, math.ceil(wl.n_copies / m))
-    big = [capture(lambda j=j: [wl.run(j * m + s) for s in range(m)], stream) for j in range(n_big)]
-    single = [capture(lambda i=i: wl.run(i), stream) for i in range(wl.n_copies)]
+    m = max(1, min(args.steps_per_graph, K))
+    steps = StepGraphs(wl.run, wl.n_copies, m, stream)
+    steps.prepare(0, W)
+    for r in range(R):                              # repeat r times steps [r*K, (r+1)*K)
+        steps.prepare(r * K, K)
     # ---- kernel-timing graphs: the GEMVs of n_kt consecutive steps back to
     # back (no producers, PDL off so no two GEMVs overlap), rotating copies
     mq.mq_set_pdl(False)
     n_kt = max(wl.n_copies, 16) if wl.n_gemv < 8 else 2
-    kt_graph = capture(lambda: [wl.run_gemvs(i) for i in range(n_kt)], stream)
+    kt_graph = kernel_graphs(wl, stream, n_kt)
+    kinds = sorted({o[0] for o in wl.ops if o[0] in ("gemv", "gateup", "gemv32")})
+    kind_graphs = {k: kernel_graphs(wl, stream, n_kt, [k]) for k in kinds} if len(kinds) > 1 else {}
     n_prod = sum(1 for o in wl.ops if o[0] in ("rms", "swiglu", "quant"))
     pt_graph = (capture(lambda: [wl.run(i, producers_only=True) for i in range(n_kt)], stream)
                 if n_prod else None)
@@ -465,17 +634,10 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     mq.mq_set_pdl(args.pdl)
     torch.cuda.synchronize()
 
-    def run_steps(k):
-        """Enqueue exactly k steps: whole multi-step graphs, then single steps."""
-        nb_, rest = divmod(k, m)
-        for j in range(nb_):
-            big[j % n_big].replay()
-        for i in range(rest):
-            single[i % wl.n_copies].replay()
-
-    # ---- warm-up, then a clock-sampled window: soak / timed K steps / soak
+    # ---- warm-up, then a clock-sampled window: soak / R timed regions of
+    # exactly K steps / soak
     with torch.cuda.stream(stream):
-        run_steps(args.warmup)
+        steps.enqueue(0, W)
     torch.cuda.synchronize()
     sampler = ClockSampler(local) if rank == 0 or ws_ == 1 else None
     t_win0 = time.perf_counter()
@@ -484,82 +646,45 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
         t_end = time.perf_counter() + seconds
         with torch.cuda.stream(stream):
             while time.perf_counter() < t_end:
-                run_steps(16 * m)
+                for r in range(R):
+                    steps.enqueue(r * K, K)
                 torch.cuda.synchronize()
 
     soak(args.soak)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    start, stop = make_event(), make_event()
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        run_steps(args.steps)
-        stop.record(stream)
-    stop.synchronize()
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    ms_total = start.elapsed_time(stop)
+    region_ms = []
+    for r in range(R):
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        start, stop = make_event(), make_event()
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            steps.enqueue(r * K, K)
+            stop.record(stream)
+        stop.synchronize()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        region_ms.append(reduce_max(start.elapsed_time(stop), dist))
     t_timed1 = time.perf_counter()
     soak(args.soak)
     t_win1 = time.perf_counter()
     if sampler is not None:
         sampler.stop()
-    max_ms = reduce_max(ms_total, dist)
-    ms_per_step = max_ms / args.steps
+    max_ms = float(np.median(region_ms))
+    ms_per_step = max_ms / K
 
     # ---- kernel timing: replay the GEMV-only graph, events around each replay
-    with torch.cuda.stream(stream):
-        kt_graph.replay()
-    torch.cuda.synchronize()
-    kt = []
-    for rep in range(5):
-        e0, e1 = make_event(), make_event()
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            kt_graph.replay()
-            e1.record(stream)
-        e1.synchronize()
-        kt.append(e0.elapsed_time(e1) / n_kt)
-    gemv_step_ms = float(np.median(kt))
-    # ---- the producers alone, timed the same way (PDL off)
-    prod_step_ms = 0.0
-    if pt_graph is not None:
-        with torch.cuda.stream(stream):
-            pt_graph.replay()
-        torch.cuda.synchronize()
-        pt = []
-        for rep in range(5):
-            e0, e1 = make_event(), make_event()
-            with torch.cuda.stream(stream):
-                e0.record(stream)
-                pt_graph.replay()
-                e1.record(stream)
-            e1.synchronize()
-            pt.append(e0.elapsed_time(e1) / n_kt)
-        prod_step_ms = float(np.median(pt))
-    floor_ms = None
-    if floor_graph is not None:
-        with torch.cuda.stream(stream):
-            floor_graph.replay()
-        torch.cuda.synchronize()
-        ft = []
-        for rep in range(5):
-            e0, e1 = make_event(), make_event()
-            with torch.cuda.stream(stream):
-                e0.record(stream)
-                floor_graph.replay()
-                e1.record(stream)
-            e1.synchronize()
-            ft.append(e0.elapsed_time(e1) / n_kt)
-        floor_ms = float(np.median(ft))
+    kt = replay_ms(kt_graph, stream)
+    gemv_step_ms = float(np.median(kt)) / n_kt
+    kind_ms = {k: float(np.median(replay_ms(g, stream))) / n_kt for k, g in kind_graphs.items()}
+    prod_step_ms = float(np.median(replay_ms(pt_graph, stream))) / n_kt if pt_graph is not None else 0.0
+    floor_ms = float(np.median(replay_ms(floor_graph, stream))) / n_kt if floor_graph is not None else None
 
     # ---- e2e: the public API, pinned host inputs in, result out, every step
     out_host = torch.empty(wl.output.shape, dtype=torch.float32).pin_memory()
     h2d = wl.h2d_bytes
     d2h = out_host.numel() * 4
-    e2e_steps = max(3, min(args.steps, args.e2e_steps))
     torch.cuda.synchronize()
 
     # every step reads its own pinned input buffer (rotated like the weight
@@ -574,6 +699,7 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
         # last GEMV writes its rows straight into pinned host memory
         wl.run(i, host_in=hin if wl.inputs_in_place else None, out=out_host)
 
+    n_eager = max(3, min(K, args.e2e_steps))
     with torch.cuda.stream(stream):
         for i in range(3):
             e2e_step(i)
@@ -582,36 +708,45 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
         dist.barrier()
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
-        for i in range(e2e_steps):
+        for i in range(n_eager):
             e2e_step(i)
     torch.cuda.synchronize()
-    e2e_eager_ms = reduce_max((time.perf_counter() - t0) * 1e3, dist) / e2e_steps
-    # the same steps captured the way a decode loop runs them: CUDA graphs of
-    # m steps, every step with its own H2D input copies and D2H result copy
-    e2e_graphs = [capture(lambda j=j: [e2e_step(j * m + s) for s in range(m)], stream)
-                  for j in range(n_big)]
-    n_blocks = max(1, e2e_steps // m)
+    e2e_eager_ms = reduce_max((time.perf_counter() - t0) * 1e3, dist) / n_eager
+    # the same steps captured the way a decode loop runs them: K steps per
+    # region (graphs of at most m steps), every step with its host input
+    # and host result; >= 5 regions, each timed by the wall clock
+    e2e = StepGraphs(e2e_step, wl.n_copies, m, stream)
+    for r in range(R):
+        e2e.prepare(r * K, K)
     with torch.cuda.stream(stream):
-        for j in range(n_big):
-            e2e_graphs[j].replay()
+        e2e.enqueue(0, K)
     torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for j in range(n_blocks):
-            e2e_graphs[j % n_big].replay()
-    torch.cuda.synchronize()
-    e2e_ms = reduce_max((time.perf_counter() - t0) * 1e3, dist) / (n_blocks * m)
+    e2e_region = []
+    for r in range(R):
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            e2e.enqueue(r * K, K)
+        torch.cuda.synchronize()
+        e2e_region.append(reduce_max((time.perf_counter() - t0) * 1e3, dist))
+    e2e_ms = float(np.median(e2e_region)) / K
     mq.mq_set_pdl(False)
+
+    peak, peak_kind = measured_peak_gbs()
+    configs = None
+    if args.configs and args.workload == "sweep_14b" and args.tokens == 1 and not wl.f32:
+        configs = {}
+        for i, name in enumerate(CONFIG_WORKLOADS):
+            configs[f"config{i}"] = config_report(name, dev, l2, stream, peak, args.pdl)
 
     if rank != 0:
         return None
-    peak, peak_kind = measured_peak_gbs()
-    value = weak_scaling_value(wl.weight_bytes, args.steps, max_ms, ws_)
+    value = weak_scaling_value(wl.weight_bytes, K, max_ms, ws_)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws_,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "steps": K, "warmup": W, "ms_per_step": round(ms_per_step, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if wl.f32 else "i8", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {DESCR[args.workload]}",
@@ -622,29 +757,52 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
                    "gemvs_per_step": wl.n_gemv, "gemv_launches_per_step": wl.n_gemv_launches,
                    "fused_gateup_launches_per_step": sum(1 for o in wl.ops if o[0] == "gateup"),
                    "kernels_per_step": wl.n_kernels,
-                   "l2": f"{wl.n_copies} rotated weight copies "
-                         f"({wl.n_copies * wl.weight_bytes / 1e6:.0f} MB >= 4 x L2 {l2 / 1e6:.0f} MB)",
-                   "timing": f"CUDA graphs of {m} steps (+ single-step graphs for a remainder), "
-                             f"CUDA events on the launching stream; PDL {'on' if args.pdl else 'off'}",
+                   "l2": (f"inputs larger than L2: {wl.weight_bytes / 1e6:.0f} MB of weights per step "
+                          f"(L2 {l2 / 1e6:.0f} MB)" if wl.n_copies == 1 else
+                          f"{wl.n_copies} rotated weight copies "
+                          f"({wl.n_copies * wl.weight_bytes / 1e6:.0f} MB >= 4 x L2 {l2 / 1e6:.0f} MB)"),
+                   "timing": f"{R} timed regions of exactly {K} steps, each CUDA graphs of at most {m} "
+                             f"consecutive steps ({'one graph of ' + str(K) + ' steps' if K <= m else 'segments'}"
+                             f"), CUDA events on the launching stream, barrier + synchronize on both "
+                             f"sides; value and ms_per_step from the median region; "
+                             f"PDL {'on' if args.pdl else 'off'}",
                    "parallelism": f"replicas{ws_}" if ws_ > 1 else "single GPU"},
         "compute": ("6-bit codes x f32 FMA chains per sub-block, f32 scale combine" if wl.f32 else
                     "int8 x (6-bit|4-bit) dp4a dots, int32 sub-block sums, f32 scale combine"),
         "pct_of_hbm_peak": round(100 * value / ws_ / peak, 2),
-        "tokens_per_s": round(ws_ * args.tokens * args.steps / (max_ms * 1e-3), 1),
+        "tokens_per_s": round(ws_ * args.tokens * K / (max_ms * 1e-3), 1),
+        "step_ms_spread": spread([x / K for x in region_ms], 1.0, 6),
     }
     alg = float(sum(wl.gemv_bytes))
     achieved = alg / (gemv_step_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(args.workload, args.act) if wl.n_gemv == 1 and args.tokens == 1 else None
+    traffic = profiled_traffic(args.workload, args.act, "gateup" in kinds) if args.tokens == 1 else None
     line["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                         "unit": "GB/s", "frac": round(achieved / peak, 4),
                         "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
                         "algorithmic_bytes_per_step": int(alg),
                         "kernel": ("gemv_q6k_f32_kernel (q6_K x f32 row)" if wl.f32 else
-                                   "gemv_kernel (q6_K/q4_K/q5_K x q8)" if args.tokens == 1 else
+                                   "gemv_kernel (q6_K/q4_K/q5_K x q8)" +
+                                   (" and gemv_gateup_kernel (gate||up + SwiGLU -> q8)" if "gateup" in kinds else "")
+                                   if args.tokens == 1 else
                                    f"gemv_batch_kernel<{args.tokens}> (q6_K/q4_K/q5_K x {args.tokens} q8 rows)"),
                         "gemv_us_per_step": round(gemv_step_ms * 1e3, 3),
-                        "how": f"GEMV launches of {n_kt} steps back to back in one CUDA graph "
-                               f"(PDL off, rotated copies), CUDA events around 5 replays, median"}
+                        "gemv_us_spread": spread(kt, 1e3 / n_kt),
+                        "how": f"every GEMV launch of {n_kt} steps back to back in one CUDA graph "
+                               f"(PDL off), CUDA events around 5 replays, median; achieved = "
+                               f"algorithmic bytes per step / GEMV time per step; traffic = ncu DRAM "
+                               f"bytes per step from the committed profile when its source hash matches"}
+    if kind_ms:
+        names = {"gemv": "gemv_kernel", "gateup": "gemv_gateup_kernel", "gemv32": "gemv_q6k_f32_kernel"}
+        per = {}
+        for k, ms in kind_ms.items():
+            ab = float(sum(wl._part_alg_bytes(p[0], p[2], o[2], args.tokens, wl.f32)
+                           for o in wl.ops if o[0] == k for p in o[3]))
+            nl = sum(1 for o in wl.ops if o[0] == k)
+            per[names[k]] = {"launches_per_step": nl, "us_per_step": round(ms * 1e3, 3),
+                             "algorithmic_bytes_per_step": int(ab),
+                             "achieved": round(ab / (ms * 1e-3) / 1e9, 1),
+                             "frac": round(ab / (ms * 1e-3) / 1e9 / peak, 4)}
+        line["roofline"]["per_kernel"] = per
     if floor_ms is not None:
         # a plain one-launch read of the same weight copies (mq_read_floor),
         # timed the same way: what any single launch of these bytes costs here
@@ -652,29 +810,35 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
         line["roofline"]["read_floor_gbs"] = round(wl.weight_bytes / (floor_ms * 1e-3) / 1e9, 1)
         line["roofline"]["frac_of_read_floor"] = round(floor_ms / gemv_step_ms, 4)
     line["kernel_us"] = {"gemv_per_step_isolated": round(gemv_step_ms * 1e3, 3),
+                         "gemv_spread": spread(kt, 1e3 / n_kt),
                          "producers_per_step_isolated": round(prod_step_ms * 1e3, 3),
                          "producer_launches_per_step": n_prod,
                          "step": round(ms_per_step * 1e3, 3),
+                         "step_spread": spread([x / K for x in region_ms], 1e3),
                          "how": "GEMV launches alone and producer launches alone, each as a graph of "
                                 f"{n_kt} steps back to back with PDL off; step: the PDL chain of both"}
     line["e2e"] = {"value": round(wl.weight_bytes / (e2e_ms * 1e-3) / 1e9 * ws_, 2), "unit": "GB/s",
                    "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
                    "d2h_bytes_per_step": int(d2h),
-                   "how": f"public API calls captured in CUDA graphs of {m} steps; every step takes "
-                          f"its inputs from its own pinned host buffer ({len(hosts)} rotated) "
+                   "ms_per_step_spread": spread([x / K for x in e2e_region], 1.0, 4),
+                   "how": f"public API calls captured as {R} regions of {K} steps (graphs of at most "
+                          f"{m} steps); every step takes its inputs from its own pinned host buffer "
+                          f"({len(hosts)} rotated) "
                           + ("read in place by the quantize/SwiGLU producers over NVLink-C2C"
                              if wl.inputs_in_place else "copied in by mq_copy (a kernel in the PDL chain)")
-                          + f", and the last GEMV writes its output rows into pinned host memory; "
-                          f"{n_blocks * m} steps, wall clock, synchronize at both ends",
+                          + "; the last GEMV writes its output rows into pinned host memory; each region "
+                            "timed by the wall clock with a synchronize at both ends, median region",
                    "inputs": "in place" if wl.inputs_in_place else "mq_copy",
                    "eager": {"value": round(wl.weight_bytes / (e2e_eager_ms * 1e-3) / 1e9 * ws_, 2),
                              "ms_per_step": round(e2e_eager_ms, 4),
-                             "how": "the same steps as eager Python API calls"}}
-    line["gpu_launches"] = wl.n_kernels * args.steps
+                             "how": f"the same steps as eager Python API calls ({n_eager} steps)"}}
+    line["gpu_launches"] = wl.n_kernels * K
     clocks = sampler.summary(t_win0, t_win1) if sampler else None
     line["clocks"] = clocks or {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-    line["clocks_window"] = (f"{args.soak:.1f}s soak + timed steps + {args.soak:.1f}s soak of the same "
-                             f"graphs ({(t_timed1 - t_win0):.2f}s to end of timed region)")
+    line["clocks_window"] = (f"{args.soak:.1f}s soak + timed regions + {args.soak:.1f}s soak of the same "
+                             f"graphs ({(t_timed1 - t_win0):.2f}s to end of timed regions)")
+    if configs is not None:
+        line["configs"] = configs
     if ws_ == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds, args.tokens, args.act)
     return line
@@ -692,7 +856,7 @@ def oracle_sample(workload: str, rows_cap: int, nt: int = 1):
         if key in seen:
             continue
         r = min(rows, rows_cap)
-        W = synth.blocks(fmt, g, rows, cols)[:r].copy()
+        W = synth.blocks(fmt, g, r, cols)         # the sample's rows only, same distribution
         inps = []
         for _ in range(nt):
             if producer == "rms":
@@ -777,13 +941,19 @@ def bench_reference(args, ws_, rank) -> dict | None:
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--repeats", type=int, default=5,
+                    help="timed regions of exactly --steps steps (at least 5); the median is reported")
     ap.add_argument("--impl", default="mq", choices=["mq", "reference"])
-    ap.add_argument("--workload", default="ffn_down_7b", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="sweep_14b", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--soak", type=float, default=0.6, help="seconds of identical load around the timed steps")
-    ap.add_argument("--e2e-steps", type=int, default=500)
-    ap.add_argument("--steps-per-graph", type=int, default=16)
+    ap.add_argument("--e2e-steps", type=int, default=20, help="steps of the eager e2e figure")
+    ap.add_argument("--steps-per-graph", type=int, default=64,
+                    help="most consecutive steps in one CUDA graph")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="with the 14B sweep, skip the per-configuration report of the other four "
+                         "benchmark configurations")
     ap.add_argument("--no-pdl", dest="pdl", action="store_false",
                     help="launch without programmatic dependent launch")
     ap.add_argument("--no-group", dest="group", action="store_false",

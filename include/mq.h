@@ -311,7 +311,10 @@ int mq_gemv_group_q8_plan(const mq_gemv_part *parts, int nparts, const void *q8,
  *   nt == 1 (default plan) runs the single-token GEMV of the format when
  *   its default plan needs no workspace, else this kernel for one token;
  *   either way no workspace is taken (mq_gemv_q6k_q8's long-row plans may
- *   need one).  The _plan forms always run this kernel.
+ *   need one).  The _plan forms always run this kernel.  So at nt == 1 the
+ *   default form's y equals mq_gemv_*_q8's bit for bit whenever that
+ *   kernel ran, and may differ in the last bits from the _plan form's y and
+ *   from token 0 of an nt >= 2 call (another f32 reduction order).
  *   Every CTA stages all nt planes in shared memory: nt * mq_q8_bytes(cols)
  *   must not exceed the device's per-CTA limit less 8 KiB (about 219 KiB on
  *   GB300, i.e. cols <= 26368 at nt = 8), else MQ_ERR_SHAPE.

@@ -464,9 +464,21 @@ int batch_entry(int fmt, const void *Wp, const void *q8, int nt, float *y, int r
                 void *stream)
 {
     if (nt < 1) return MQ_ERR_SHAPE;
-    int s = 0, c = 0, t = 0;  // splits beyond kMaxCtaSplits meet in a workspace
-    if (nt == 1 && mq_gemv_plan(rows, cols, fmt, &s, &c, &t) == MQ_OK && s <= kMaxCtaSplits)
-        return gemv_common(fmt, Wp, q8, y, rows, cols, nullptr, nullptr, 0, stream, 0);
+    if (nt == 1) {
+        // the single-token plan is worked out once and launched as checked
+        if (!Wp || !q8 || !y) return MQ_ERR_NULL;
+        const Part part{fmt, rows, Wp, y};
+        GemvLaunch a;
+        size_t need = 0;
+        const int st = prepare_group(&part, 1, q8, cols, nullptr, &a, &need, false, 0);
+        if (st == MQ_OK && need == 0) {
+            const cudaError_t e = launch_gemv(a, (cudaStream_t)stream);
+            return e == cudaSuccess ? MQ_OK : cuda_fail("GEMV launch", e);
+        }
+        // a shape the single-token kernel refuses is the batch kernel's to
+        // judge; any other failure is the caller's answer
+        if (st != MQ_OK && st != MQ_ERR_SHAPE) return st;
+    }
     return gemv_common(fmt, Wp, q8, y, rows, cols, nullptr, nullptr, 0, stream, nt);
 }
 

@@ -286,7 +286,7 @@ def test_full_size_every_row(mq, orc, name, fmt, rows, cols, producer):
     y1 = host(gemv(mq, fmt, Wp, plane, rows, cols, ws=ws))
     y2 = host(gemv(mq, fmt, Wp, plane, rows, cols, ws=ws))
     assert np.all(np.isfinite(y1)) and np.array_equal(y1, y2)
-    # the oracle on sampled rows, fed the oracle's own quantization of the
+    # every row against the oracle, fed the oracle's own quantization of the
     # producer output (checked bit-exact against the plane above)
     d, q, _ = orc.quantize_q8(host(yprod))
     dg, qg, _ = q8_fields(mq, plane, cols)

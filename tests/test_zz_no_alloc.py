@@ -5,8 +5,9 @@ not allocate device memory, so they cannot pass the split-K workspace the
 regular entry point needs.  This file runs last so that a failure here comes
 after every other test has run; it also passes on its own in a fresh
 process.  It calls the entry point through the C ABI twice in a row and
-checks each result against mq_gemv_q6k_q8 (same tolerance as the parity
-tests: |dy| <= 1e-4 * sum |terms| per row) and against the oracle."""
+checks each result against mq_gemv_q6k_q8 with a caller workspace (the
+same kernel and default plan, so the same bits) and against the oracle
+(the parity tests' bar: |dy| <= 1e-4 * sum |terms| per row)."""
 import ctypes
 
 import numpy as np
@@ -40,15 +41,21 @@ def test_noalloc_matches_regular_entry_point(mq, orc, rows, cols):
     plane = mq.mq_quantize_q8(torch.from_numpy(x).cuda())
     splits, _, _ = mq.mq_gemv_plan(rows, cols, "q6k")
     assert splits > 1
+    need = mq.mq_gemv_workspace_bytes(rows, cols)
     if rows == 512:                                      # few tiles, long rows: the scratch path
-        assert mq.mq_gemv_workspace_bytes(rows, cols) > 0
-    if rows == 968:                                      # 121 tiles x 19 splits: more than 64 KiB
-        need = mq.mq_gemv_workspace_bytes(rows, cols)
-        assert need == 0 or need > 64 * 1024, need      # (device-dependent plan)
+        assert need > 0
+    if rows == 968:
+        # 121 tiles x 19 splits on a 152-SM GB300: more than 64 KiB of scratch.
+        # The plan depends on the device; say so rather than pass vacuously.
+        if need == 0:
+            pytest.skip(f"default plan {mq.mq_gemv_plan(rows, cols, 'q6k')} needs no scratch on "
+                        f"this device ({mq.mq_device_sms()} SMs): the large-scratch case is not covered")
+        assert 64 * 1024 < need <= 128 * 1024, need
     ws = mq.mq_gemv_workspace(rows, cols)
-    y_ref = mq.mq_gemv_q6k_q8(Wp, plane, rows, cols, ws=ws)
+    y_ref = mq.mq_gemv_q6k_q8(Wp, plane, rows, cols, ws=ws).cpu().numpy()
     d0, q0, _ = orc.quantize_q8(x)
     y_or, absum = orc.gemv("q6k", W, d0, q0, rows, cols, threads=8)
+    assert np.all(np.abs(y_ref.astype(np.float64) - y_or) <= TOL * absum)
     L = mq.lib()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for _ in range(2):                                   # two calls in a row share the array
@@ -57,9 +64,10 @@ def test_noalloc_matches_regular_entry_point(mq, orc, rows, cols):
                                       ctypes.c_void_p(y.data_ptr()), rows, cols, stream)
         assert st == mq.MQ_OK, mq.lib().mq_strerror(st)
         torch.cuda.synchronize()
-        yn = y.cpu().numpy().astype(np.float64)
-        assert np.all(np.abs(yn - y_ref.cpu().numpy()) <= TOL * absum)
-        assert np.all(np.abs(yn - y_or) <= TOL * absum)
+        yn = y.cpu().numpy()
+        # the same kernel with the same default plan: the same bits
+        assert np.array_equal(yn, y_ref)
+        assert np.all(np.abs(yn.astype(np.float64) - y_or) <= TOL * absum)
 
 
 def test_noalloc_rejects_bad_arguments_before_launch(mq):
