@@ -64,6 +64,12 @@ DESCR = {
     "ffn_down_14b_q5k": "q5_K 5120x13824 (the 14B ffn_down shape), rms_norm->q8, batch 1",
     "ffn_14b": "Qwen2.5-14B FFN: rms_norm->q8 -> gate, up q4_K 13824x5120 -> SwiGLU->q8 -> "
                "down q6_K 5120x13824, batch 1",
+    "attn_q_14b": "Qwen2.5-14B attn_q q4_K 5120x5120 (the attn_output shape too), rms_norm->q8, "
+                  "batch 1",
+    "ffn_gate_14b": "Qwen2.5-14B ffn_gate q4_K 13824x5120 (the ffn_up shape too) as a plain GEMV, "
+                    "rms_norm->q8, batch 1",
+    "attn_qkv_14b": "Qwen2.5-14B attn q 5120x5120 q4_K, k 1024x5120 q4_K, v 1024x5120 q6_K in one "
+                    "grouped launch over one rms_norm->q8 plane, batch 1",
     "sweep_14b": "Qwen2.5-14B decode weight sweep: 48 layers x {q,k,o,gate,up q4_K; v,down q6_K} "
                  "+ q6_K head, fused rms/swiglu/quantize producers, batch 1",
 }
@@ -594,6 +600,9 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     if dist is not None:
         dist.barrier()
     import quant_quantized_gemv_gb300 as mq
+    if args.gemv_ring is not None:
+        sp = [int(v) for v in str(args.gemv_ring).split(",")]
+        mq.mq_set_gemv_ring(sp[0], sp[1] if len(sp) > 1 else -1)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
     wl = DeviceWorkload(args.workload, dev, l2, group=args.group, nt=args.tokens, fuse=args.fuse,
@@ -766,7 +775,8 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
                              f"), CUDA events on the launching stream, barrier + synchronize on both "
                              f"sides; value and ms_per_step from the median region; "
                              f"PDL {'on' if args.pdl else 'off'}",
-                   "parallelism": f"replicas{ws_}" if ws_ > 1 else "single GPU"},
+                   "parallelism": f"replicas{ws_}" if ws_ > 1 else "single GPU",
+                   "gemv_ring": args.gemv_ring or "library default"},
         "compute": ("6-bit codes x f32 FMA chains per sub-block, f32 scale combine" if wl.f32 else
                     "int8 x (6-bit|4-bit) dp4a dots, int32 sub-block sums, f32 scale combine"),
         "pct_of_hbm_peak": round(100 * value / ws_ / peak, 2),
@@ -954,6 +964,9 @@ def main(argv=None):
     ap.add_argument("--no-configs", dest="configs", action="store_false",
                     help="with the 14B sweep, skip the per-configuration report of the other four "
                          "benchmark configurations")
+    ap.add_argument("--gemv-ring", default=None, metavar="S[,P]",
+                    help="weight-ring depth S of the single-token GEMV (0 = none) and the stages P "
+                         "requested before the grid-dependency wait (default: the library's)")
     ap.add_argument("--no-pdl", dest="pdl", action="store_false",
                     help="launch without programmatic dependent launch")
     ap.add_argument("--no-group", dest="group", action="store_false",

@@ -178,15 +178,17 @@ int mq_swiglu_quant_q8(const float *g, const float *u, float *y, void *q8, int n
  * only when that still leaves the wave less than half full (very few tiles,
  * rows longer than 12 chunks).
  *
- * mq_gemv_workspace_bytes(rows, cols): workspace the default plans (q6_K and
- *   q4_K) need on the current device (0 unless splits > 12).  ws must be
+ * mq_gemv_workspace_bytes(rows, cols): workspace the default plans (q6_K,
+ *   q4_K and q5_K) need on the current device (0 unless splits > 12).  ws must be
  *   device memory, zero-filled before its first use; every completed call
  *   leaves it zero-filled again.  ws may be NULL when 0 bytes are needed.
  * mq_gemv_workspace_bytes_for: the same for an explicit plan (0 if invalid).
  * mq_gemv_plan: the default plan for format 6 (q6_K), 4 (q4_K) or 5 (q5_K)
  *   on the current device (from the kernel's measured occupancy).
  * mq_gemv_plan_for: the default plan for a device with `sms` SMs and a
- *   kernel using regs_per_thread registers (64K registers per SM).  Host only.
+ *   kernel using regs_per_thread registers (64K registers per SM), from the
+ *   register limit alone (the weight ring's shared memory is not modelled).
+ *   Host only.
  * mq_gemv_*_q8_plan: the GEMV with an explicit plan.
  * Errors: MQ_ERR_NULL, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_WORKSPACE,
  *         MQ_ERR_COVERAGE, MQ_ERR_CUDA.
@@ -422,6 +424,28 @@ int mq_check_coverage(int nchunks, int splits, int chunks_per_split);
  * producer its gain (both are weights in a decode step).
  * ------------------------------------------------------------------------ */
 int mq_set_pdl(int enable);
+
+/* ------------------------------------------------------------------------
+ * Weight ring of the single-token GEMV (process-wide tuning control; no
+ * counterpart on the pages, whose kernels read each unit straight into
+ * registers).  Each warp of mq_gemv_*_q8 / mq_gemv_group_q8 keeps `stages`
+ * chunks of its weight range in flight in its own shared-memory slots
+ * (16-byte asynchronous copies) while it computes the previous chunk from
+ * registers; `pre_wait` of them are requested before the kernel waits for
+ * its predecessor under programmatic dependent launch (mq_set_pdl).
+ *   stages: 0 = no ring (each chunk is loaded straight into registers, one
+ *           chunk per warp in flight), 1..3, or -1 = the default (0: on
+ *           GB300 the ring measured slower on every matrix of the 14B decode
+ *           step and faster only on whole-tile q4_K shapes with few warps,
+ *           e.g. a 13824 x 5120 q4_K GEMV at 2 stages).  Clamped so that the
+ *           largest CTA fits the device's shared memory.
+ *   pre_wait: 0..stages, or -1 = all of them.
+ * Plans chosen after a change account for the ring's shared memory (it can
+ * lower the resident CTAs per SM, and so change a default plan).  Results
+ * do not depend on the setting: the same sub-dots in the same order.
+ * Returns the previous stages value.
+ * ------------------------------------------------------------------------ */
+int mq_set_gemv_ring(int stages, int pre_wait);
 
 /* ------------------------------------------------------------------------
  * Integer sub-block dots (device), for bit-exact testing of the GEMV's

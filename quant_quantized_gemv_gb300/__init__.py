@@ -44,7 +44,7 @@ EXPORTS = [
     "mq_gemv_q5k_q8", "mq_gemv_q5k_q8_plan", "mq_gemv_q5k_q8_subdots", "mq_gemv_q5k_q8_batch",
     "mq_gemv_q5k_q8_batch_plan", "mq_read_floor", "mq_gemv_q6k_f32", "mq_gemv_q6k_f32_plan",
     "mq_gemv_q6k_f32_plan_of", "mq_copy", "mq_repack_device", "mq_gemv_group_q8_coverage",
-    "mq_device_address",
+    "mq_device_address", "mq_set_gemv_ring",
 ]
 
 
@@ -106,6 +106,7 @@ def lib():
         "mq_check_coverage": ([I, I, I], I),
         "mq_gemv_plan_for": ([I, I, I, I, P, P, P], I),
         "mq_set_pdl": ([I], I),
+        "mq_set_gemv_ring": ([I, I], I),
         "mq_gemv_q6k_q8_noalloc": ([P, P, P, I, I, P], I),
         "mq_gemv_group_workspace_bytes": ([P, I, I, I, I, I], S),
         "mq_gemv_group_q8": ([P, I, P, I, P, S, P], I),
@@ -411,6 +412,12 @@ def mq_gemv_plan_for(rows: int, cols: int, sms: int, regs_per_thread: int = 128)
 def mq_set_pdl(enable: bool) -> bool:
     """Programmatic dependent launch for every later launch (process-wide)."""
     return bool(lib().mq_set_pdl(1 if enable else 0))
+
+
+def mq_set_gemv_ring(stages: int = -1, pre_wait: int = -1) -> int:
+    """Weight-ring depth of the single-token GEMV (process-wide; -1 = default).
+    Returns the previous stages setting."""
+    return int(lib().mq_set_gemv_ring(int(stages), int(pre_wait)))
 
 
 def mq_read_floor(buf, nbytes: int = None, stream=None):

@@ -7,6 +7,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "kernels.h"
 #include "layout.h"
@@ -36,6 +37,10 @@ std::atomic<int> g_sms[kMaxDevices];
 // resident GEMV CTAs per SM: [device][warps per CTA]
 std::atomic<int> g_ctas[kMaxDevices][kMaxCtaSplits + 1];
 std::atomic<int> g_pdl{0};
+// single-token GEMV weight ring (mq_set_gemv_ring): stages per warp and how
+// many of them are requested before the grid-dependency wait; -1 = default
+std::atomic<int> g_ring_stages{-1};
+std::atomic<int> g_ring_pre{-1};
 // resident small-batch CTAs per SM (register limit): [device][nt][warps per CTA]
 std::atomic<int> g_batch_ctas[kMaxDevices][kMaxTokens + 1][7][kBatchMaxCtaWarps + 1];  // [..][fmt]
 // resident gate||up CTAs per SM (register limit): [device][warps per CTA]
@@ -123,28 +128,94 @@ bool device_limits(DeviceLimits *out)
     return true;
 }
 
-// CTAs per SM: the register limit (measured once per device and CTA shape)
-// and the shared-memory limit of a plane of `plane` bytes.
-bool device_occupancy(Occupancy *o, size_t plane)
+// The single-token GEMV's weight ring for a launch over parts of the given
+// formats (mq_set_gemv_ring; off unless set): one slot holds the largest
+// full chunk among them; the depth is clamped so that the largest CTA
+// (kMaxCtaSplits warps, or 4 warps beside the staged plane) fits the
+// device's shared memory.
+struct Ring {
+    int stages, pre;
+    size_t slot;
+};
+
+Ring ring_for(const int *fmts, int n, size_t plane, const DeviceLimits &lim)
 {
-    const int dev = current_device();
-    DeviceLimits lim;
-    if (dev < 0 || !device_limits(&lim)) return false;
-    const long long per_cta = (long long)plane + kGemvStaticSmem + lim.smem_reserved;
-    const int by_smem = (int)(lim.smem_per_sm / per_cta);
-    for (int w = 1; w <= kMaxCtaSplits; ++w) {
+    Ring r{0, 0, 0};
+    for (int i = 0; i < n; ++i) {
+        const size_t c = (size_t)kTileRows * kChunkBlocks * block_bytes(fmts[i]);
+        if (c > r.slot) r.slot = c;
+    }
+    int st = g_ring_stages.load(std::memory_order_relaxed);
+    if (st < 0) st = 0;  // default: no ring (measured slower on the decode shapes)
+    if (st > kGemvMaxStages) st = kGemvMaxStages;
+    while (st > 0 && r.slot > 0 &&
+           ((size_t)kMaxCtaSplits * st * r.slot > lim.max_plane ||
+            gemv_dyn_smem(kGemvWarpsPerBlock, true, plane, st, r.slot) > lim.max_plane))
+        --st;
+    r.stages = r.slot > 0 ? st : 0;
+    if (r.stages == 0) {
+        r.slot = 0;
+        return r;
+    }
+    const int pre = g_ring_pre.load(std::memory_order_relaxed);
+    r.pre = pre < 0 || pre > r.stages ? r.stages : pre;
+    return r;
+}
+
+// Resident GEMV CTAs per SM with w warps and dyn bytes of dynamic shared
+// memory, asked of the device once per (device, w, dyn).
+struct OccEntry {
+    int w;
+    size_t dyn;
+    int ctas;
+};
+std::vector<OccEntry> g_occ[kMaxDevices];
+std::mutex g_occ_mutex;
+
+int gemv_ctas(int dev, int w, size_t dyn)
+{
+    if (dyn == 0) {  // register limit only: lock-free cache
         std::atomic<int> &slot = g_ctas[dev][w];
         int v = slot.load(std::memory_order_relaxed);
         if (v <= 0) {
             v = gemv_ctas_per_sm(w, 0);
-            if (v <= 0) return false;
-            slot.store(v, std::memory_order_relaxed);
+            if (v > 0) slot.store(v, std::memory_order_relaxed);
         }
-        o->ctas[w] = v;  // split CTAs stage nothing
+        return v;
     }
-    // whole-tile CTAs stage the plane in shared memory
-    o->ctas_tiles = o->ctas[kGemvWarpsPerBlock] < by_smem ? o->ctas[kGemvWarpsPerBlock] : by_smem;
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
+    for (const OccEntry &e : g_occ[dev])
+        if (e.w == w && e.dyn == dyn) return e.ctas;
+    const int v = gemv_ctas_per_sm(w, dyn);
+    if (v > 0) g_occ[dev].push_back(OccEntry{w, dyn, v});
+    return v;
+}
+
+// CTAs per SM of the single-token GEMV: split CTAs of w warps hold their
+// warps' ring slots; whole-tile CTAs (kGemvWarpsPerBlock warps) also the
+// staged plane of `plane` bytes.
+bool device_occupancy(Occupancy *o, size_t plane, const Ring &ring)
+{
+    const int dev = current_device();
+    DeviceLimits lim;
+    if (dev < 0 || !device_limits(&lim)) return false;
+    for (int w = 1; w <= kMaxCtaSplits; ++w) {
+        const int v = gemv_ctas(dev, w, gemv_dyn_smem(w, false, plane, ring.stages, ring.slot));
+        if (v < 0) return false;
+        o->ctas[w] = v;
+    }
+    o->ctas_tiles = gemv_ctas(dev, kGemvWarpsPerBlock,
+                              gemv_dyn_smem(kGemvWarpsPerBlock, true, plane, ring.stages, ring.slot));
     return o->ctas_tiles > 0;
+}
+
+// The ring of a launch over the given formats on the current device.
+bool device_ring(const int *fmts, int n, size_t plane, Ring *r)
+{
+    DeviceLimits lim;
+    if (!device_limits(&lim)) return false;
+    *r = ring_for(fmts, n, plane, lim);
+    return true;
 }
 
 // Resident CTAs per SM of the small-batch kernel for nt tokens of format fmt
@@ -368,13 +439,19 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
             return MQ_ERR_SHAPE;
         if (batch && (wpc = batch_budget(nt, parts[0].fmt)) < 1) return MQ_ERR_CUDA;
     }
+    Ring ring{0, 0, 0};  // asked of the device only when a launch or a default plan needs it
+    if (!batch && (!sizes_only || !explicit_plan)) {
+        int fmts[kMaxParts];
+        for (int p = 0; p < nparts; ++p) fmts[p] = parts[p].fmt;
+        if (!device_ring(fmts, nparts, plane, &ring)) return MQ_ERR_CUDA;
+    }
     Plan pl;
     if (explicit_plan) {
         pl = *explicit_plan;
     } else {
         Occupancy o;
         if (!batch) {
-            if (!device_occupancy(&o, plane)) return MQ_ERR_CUDA;
+            if (!device_occupancy(&o, plane, ring)) return MQ_ERR_CUDA;
             pl = plan_for((int)total_tiles, nchunks, device_sms(), o);
         } else {
             if (!batch_occupancy(&o, nt, parts[0].fmt, (size_t)nt * plane, &wpc)) return MQ_ERR_CUDA;
@@ -415,6 +492,10 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
     a->nt = batch ? nt : 1;
     a->q8_stride = (unsigned)plane;
     a->wpc = wpc;
+    a->stages = ring.stages;
+    a->pre = ring.pre;
+    a->slot_bytes = (unsigned)ring.slot;
+    a->ring_off = (unsigned)gemv_ring_off(pl.splits == 1, plane);
     *need = batch ? 0 : ws_bytes_for(total_tiles, items, pl);  // small batch: splits meet in the CTA
     return MQ_OK;
 }
@@ -824,9 +905,12 @@ int mq_gemv_plan(int rows, int cols, int fmt, int *splits, int *chunks_per_split
     if (!splits || !chunks_per_split || !tiles_per_item) return MQ_ERR_NULL;
     if (block_bytes(fmt) == 0) return MQ_ERR_SHAPE;
     if (!gemv_shape_ok(rows, cols)) return MQ_ERR_SHAPE;
+    const size_t plane = q8_plane_bytes(cols);
+    Ring ring;
+    if (!device_ring(&fmt, 1, plane, &ring)) return MQ_ERR_CUDA;
     Occupancy o;
-    if (!device_occupancy(&o, q8_plane_bytes(cols))) return MQ_ERR_CUDA;
-    const Geom g = make_geom(rows, cols, kQ6kBytes);
+    if (!device_occupancy(&o, plane, ring)) return MQ_ERR_CUDA;
+    const Geom g = make_geom(rows, cols, block_bytes(fmt));
     const Plan p = plan_for(g.ntiles, g.nchunks, device_sms(), o);
     *splits = p.splits;
     *chunks_per_split = p.cps;
@@ -846,9 +930,16 @@ size_t mq_gemv_workspace_bytes_for(int rows, int cols, int splits, int chunks_pe
 
 size_t mq_gemv_workspace_bytes(int rows, int cols)
 {
-    int s = 0, c = 0, t = 0;
-    if (mq_gemv_plan(rows, cols, 6, &s, &c, &t) != MQ_OK) return 0;
-    return mq_gemv_workspace_bytes_for(rows, cols, s, c, t);
+    // the default plan can depend on the format (its ring slots change the
+    // occupancy): enough for the default plan of any format
+    size_t most = 0;
+    for (int fmt : {6, 4, 5}) {
+        int s = 0, c = 0, t = 0;
+        if (mq_gemv_plan(rows, cols, fmt, &s, &c, &t) != MQ_OK) return 0;
+        const size_t b = mq_gemv_workspace_bytes_for(rows, cols, s, c, t);
+        if (b > most) most = b;
+    }
+    return most;
 }
 
 size_t mq_gemv_group_workspace_bytes(const mq_gemv_part *parts, int nparts, int cols, int splits,
@@ -1080,6 +1171,14 @@ int mq_read_floor(const void *src, size_t bytes, void *stream)
 int mq_set_pdl(int enable)
 {
     return g_pdl.exchange(enable ? 1 : 0);
+}
+
+int mq_set_gemv_ring(int stages, int pre_wait)
+{
+    if (stages < -1) stages = -1;
+    if (stages > kGemvMaxStages) stages = kGemvMaxStages;
+    g_ring_pre.store(pre_wait < -1 ? -1 : pre_wait, std::memory_order_relaxed);
+    return g_ring_stages.exchange(stages);
 }
 
 int mq_gemv_q6k_q8(const void *Wp, const void *q8, float *y, int rows, int cols, void *ws,

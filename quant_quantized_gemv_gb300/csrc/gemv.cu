@@ -10,9 +10,10 @@
 // How (GB300 design; layout.h describes the byte order):
 //   * The work is a pure HBM stream (page "67 · D3", §2.1: 93.4% of decode
 //     kernel time is weight streaming), so there are no tensor cores and the
-//     weights go straight to registers: each lane issues 14 (q6_K) or 13 (q4_K)
-//     independent 16-byte loads per chunk, every warp-wide load instruction
-//     covers 512 contiguous bytes, and the weight loads bypass L1
+//     weights go straight to registers: each lane issues 14 (q6_K), 9 (q4_K)
+//     or 11 (q5_K) independent 16-byte loads per chunk, every warp-wide load
+//     of a plane covers 512 contiguous bytes (q4_K's scales and block scales
+//     included: one META entry per lane), and the weight loads bypass L1
 //     (ld.global.nc.L1::no_allocate) because each byte is used once.
 //   * One register buffer per lane and a 128-register cap, so 16 warps fit
 //     an SM: a warp issues chunk u+1's loads (~7 KB per warp) as soon as
@@ -43,6 +44,12 @@
 //     from there: each plane byte leaves L2 once per CTA instead of once per
 //     warp and tile.  Split plans read each activation chunk from L2 with
 //     its weights, one chunk ahead (a CTA there reads each byte once).
+//   * Opt-in (mq_set_gemv_ring): a ring of 1..3 shared-memory slots per warp
+//     filled with 16-byte cp.async copies, so that the next chunks stream
+//     while one is computed from registers.  Bitwise the same results; off
+//     by default because it measured slower on every matrix of the 14B
+//     decode step on GB300 (faster only for whole-tile q4_K shapes with few
+//     warps per SM).
 //   * With programmatic dependent launch the first chunk's weight loads are
 //     issued before griddepcontrol.wait, so the weight stream starts while
 //     the preceding kernel (the q8 producer) drains; the q8 plane, the
@@ -196,6 +203,106 @@ __device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P
     }
 }
 
+// The same through the warp's ring of S shared-memory slots.  Every lane
+// copies 16-byte words lane, lane + 32, ... of each upcoming chunk (the chunk
+// verbatim, so the layout's offsets hold in the slot) with asynchronous
+// copies, one copy group per chunk.  Chunk u's group is complete when at most
+// S - 1 newer groups are pending; a __syncwarp then makes every lane's words
+// visible to the warp.  The warp moves the chunk into its registers, meets
+// again (every lane has read the slot), refills the slot with the chunk S
+// ahead -- before computing, so the next chunks stream while this one is
+// computed -- and computes.  Cursors advance incrementally (no division).
+template <int FMT, int MODE, int S>
+__device__ __forceinline__ void run_range_ring(const GemvLaunch &a, const GemvPart &P,
+                                               uint8_t *smem, int item, int u0, int u1, int lane)
+{
+    using Regs = typename Fmt<FMT>::Regs;
+    using X = typename Fmt<FMT>::X;
+    constexpr int kChunkBytes = Fmt<FMT>::kChunkBytes;
+    constexpr int kWords = kChunkBytes / 16;           // 16-byte words of a full chunk
+    constexpr int kPerLane = (kWords + 31) / 32;       // copies per lane of a full chunk
+    constexpr bool SUBDOTS = MODE == kModeSubdots;
+    const int nch = a.nchunks;
+    const int last_words = (a.nb - kChunkBlocks * (nch - 1)) * (kWords / kChunkBlocks);
+    const size_t tile_bytes = (size_t)P.tile_bytes_div16 * 16;
+    const uint32_t ring =
+        smem_addr(smem) + a.ring_off + (uint32_t)(threadIdx.x >> 5) * (uint32_t)(S * a.slot_bytes);
+    // issue cursor: the next chunk to copy, its slot, how many remain
+    int it = u0 / nch, ic = u0 - it * nch, is = 0, left = u1 - u0;
+    const uint8_t *isrc = P.W + (size_t)it * tile_bytes + (size_t)ic * kChunkBytes;
+    auto issue = [&]() {
+        if (left > 0) {
+            const int words = ic == nch - 1 ? last_words : kWords;
+            const uint32_t dst = ring + (uint32_t)is * a.slot_bytes + 16u * (uint32_t)lane;
+            const uint8_t *src = isrc + 16 * lane;
+#pragma unroll
+            for (int k = 0; k < kPerLane; ++k)
+                if (lane + 32 * k < words) cp_async16(dst + 512u * k, src + 512 * k);
+            --left;
+            is = is + 1 == S ? 0 : is + 1;
+            if (++ic == nch) {
+                ic = 0;
+                ++it;
+                isrc = P.W + (size_t)it * tile_bytes;
+            } else {
+                isrc += kChunkBytes;
+            }
+        }
+        cp_async_commit();
+    };
+    const int npre = min(a.pre, S);
+    for (int j = 0; j < npre; ++j) issue();     // weights do not depend on the preceding kernel
+    const uint8_t *xs = stage_plane(a, smem);  // the q8 plane, y and the workspace do
+    for (int j = npre; j < S; ++j) issue();
+    int t = u0 / nch, c = u0 - t * nch, rs = 0;  // compute cursor and its slot
+    Unit x = locate(a, P, t, c, lane, kChunkBytes);
+    X xn;  // the activation of chunk x, loaded a chunk ahead
+    load_x(a, xs, x, lane, xn);
+
+    float acc[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
+    Regs A;
+    for (int u = u0; u < u1; ++u) {
+        if (S == 1)
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        else if (S == 2)
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        else
+            asm volatile("cp.async.wait_group 2;" ::: "memory");
+        __syncwarp();  // every lane's words of chunk u are visible
+        load_w_from(SharedChunk{ring + (uint32_t)rs * a.slot_bytes}, x, lane, A);
+        static_cast<X &>(A) = xn;
+        rs = rs + 1 == S ? 0 : rs + 1;
+        __syncwarp();  // every lane has read the slot: refill it
+        issue();
+        const Unit xc = x;
+        if (u + 1 < u1) {
+            if (++c == nch) { c = 0; ++t; }
+            x = locate(a, P, t, c, lane, kChunkBytes);
+            load_x(a, xs, x, lane, xn);
+        }
+        if constexpr (MODE == kModeCover) {
+            if (lane == 0) atomicAdd(a.cover + ((size_t)(P.tile0 + xc.t) * nch + xc.c), 1u);
+        }
+        compute<SUBDOTS>(a, P, A, xc, lane, acc);
+        if (!SUBDOTS && (u + 1 == u1 || x.t != xc.t)) flush_tile(a, P, xc.t, acc, item, u0, u1, lane);
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");  // only empty groups remain
+}
+
+template <int FMT, int MODE>
+__device__ __forceinline__ void run_ring(const GemvLaunch &a, const GemvPart &P, uint8_t *smem,
+                                         int item, int u0, int u1, int lane)
+{
+    if (a.stages == 1)
+        run_range_ring<FMT, MODE, 1>(a, P, smem, item, u0, u1, lane);
+    else if (a.stages == 2)
+        run_range_ring<FMT, MODE, 2>(a, P, smem, item, u0, u1, lane);
+    else
+        run_range_ring<FMT, MODE, 3>(a, P, smem, item, u0, u1, lane);
+}
+
 // CTA shapes: splits == 1 (whole tiles) and splits > kMaxCtaSplits use CTAs
 // of kGemvWarpsPerBlock independent warps; 2..kMaxCtaSplits splits use one
 // CTA per tile whose warps are its splits.  The part of a work item is found
@@ -236,12 +343,21 @@ __global__ void __maxnreg__(MODE == kModeSubdots ? 168 : kGemvMaxRegs)
         u0 = li * a.tpi * nch;
         u1 = min(u0 + a.tpi * nch, P.ntiles * nch);
     }
-    if (P.fmt == 6)
-        run_range<6, MODE>(a, P, xs, item, u0, u1, lane);
-    else if (P.fmt == 5)
-        run_range<5, MODE>(a, P, xs, item, u0, u1, lane);
-    else
-        run_range<4, MODE>(a, P, xs, item, u0, u1, lane);
+    if (a.stages > 0) {
+        if (P.fmt == 6)
+            run_ring<6, MODE>(a, P, xs, item, u0, u1, lane);
+        else if (P.fmt == 5)
+            run_ring<5, MODE>(a, P, xs, item, u0, u1, lane);
+        else
+            run_ring<4, MODE>(a, P, xs, item, u0, u1, lane);
+    } else {
+        if (P.fmt == 6)
+            run_range<6, MODE>(a, P, xs, item, u0, u1, lane);
+        else if (P.fmt == 5)
+            run_range<5, MODE>(a, P, xs, item, u0, u1, lane);
+        else
+            run_range<4, MODE>(a, P, xs, item, u0, u1, lane);
+    }
 }
 
 template <int MODE>
@@ -249,8 +365,9 @@ cudaError_t launch(const GemvLaunch &a, cudaStream_t st)
 {
     const int warps = gemv_cta_warps(a.splits, MODE == kModeSubdots);
     const long long blocks = (a.n_items + warps - 1) / warps;
-    return launch_maybe_pdl(gemv_kernel<MODE>, dim3((unsigned)blocks), dim3(32 * warps),
-                            a.splits == 1 ? (size_t)a.q8_bytes : 0, a.pdl, st, a);
+    const size_t smem = gemv_dyn_smem(warps, a.splits == 1, a.q8_bytes, a.stages, a.slot_bytes);
+    return launch_maybe_pdl(gemv_kernel<MODE>, dim3((unsigned)blocks), dim3(32 * warps), smem,
+                            a.pdl, st, a);
 }
 
 using KernelFn = void (*)(GemvLaunch);

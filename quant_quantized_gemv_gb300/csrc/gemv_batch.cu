@@ -71,6 +71,7 @@ struct Acc {
 // Activation codes of one unit for the tokens [t0, t0 + G) of a group.
 template <int G>
 struct XCodes {
+    static constexpr int kG = G;
     uint4 xa[G], xb[G];  // codes 0..15 and 16..31 of the unit's q8 block
     float d8[G];         // fp16 activation scale
     int k0[G], k1[G];    // q6_K: -32 * sum(xa), -32 * sum(xb); q4_K: k0 = the block's sum
@@ -144,8 +145,8 @@ __device__ __forceinline__ void compute_group(const Q6kW &W, const XCodes<G> &X,
 // q4_K gate at 5 tokens 19.9 -> 18.1 us); q5_K up to 4 tokens keeps the
 // per-token form, which spills less there (at 4 tokens 22.2 against 21.9 us).
 template <int NT, int G, bool LEAN, class Q4like>
-__device__ __forceinline__ void compute_group(const Q4like &W, const XCodes<G> &X, int t0,
-                                              float (&out)[G][8])
+__device__ __forceinline__ void compute_group(const Q4like &W, const Q4kDec &D, const XCodes<G> &X,
+                                              int t0, float (&out)[G][8])
 {
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
@@ -154,7 +155,7 @@ __device__ __forceinline__ void compute_group(const Q4like &W, const XCodes<G> &
         for (int m = 0; m < 4; ++m) codes(W, r, m, lo[m], hi[m]);
         int sc, mn;
         float d, dmin;
-        q4k_scales(W, r, sc, mn, d, dmin);
+        q4k_scales(D, r, sc, mn, d, dmin);
         const float dsc = d * (float)sc, dmm = dmin * (float)mn;  // LEAN: shared by the tokens
 #pragma unroll
         for (int j = 0; j < G; ++j) {
@@ -181,10 +182,20 @@ __device__ __forceinline__ void compute(const GemvLaunch &a, const uint8_t *xs, 
 {
     constexpr int G = group_size(NT, FMT);
     constexpr bool kLean = !(FMT == 5 && NT <= kGroup);
+    // q4_K / q5_K: the unit's scales for its 8 rows, decoded once per chunk
+    // (every lane takes part: the block scales move by shuffles)
+    Q4kDec D;
+    if constexpr (FMT != 6) decode_q4k(W, lane, D);
+    auto run_group = [&](const auto &X, int t0, auto &out) {
+        if constexpr (FMT == 6)
+            compute_group<NT, std::remove_reference_t<decltype(X)>::kG, kLean>(W, X, t0, out);
+        else
+            compute_group<NT, std::remove_reference_t<decltype(X)>::kG, kLean>(W, D, X, t0, out);
+    };
     if constexpr (!Acc<NT>::kEach) {  // one group: accumulate straight into the per-lane partials
         XCodes<G> X;
         load_x_group<FMT, G>(a, xs, 0, NT, x, lane, X);
-        compute_group<NT, G, kLean>(W, X, 0, reinterpret_cast<float(&)[G][8]>(acc.v));
+        run_group(X, 0, reinterpret_cast<float(&)[G][8]>(acc.v));
     } else {
         // one group of GS tokens starting at t0 (GS is a compile-time size)
         auto group = [&](auto gs, int t0) {
@@ -196,7 +207,7 @@ __device__ __forceinline__ void compute(const GemvLaunch &a, const uint8_t *xs, 
             for (int j = 0; j < GS; ++j)
 #pragma unroll
                 for (int r = 0; r < 8; ++r) part[j][r] = 0.0f;
-            compute_group<NT, GS, kLean>(W, X, t0, part);
+            run_group(X, t0, part);
 #pragma unroll
             for (int j = 0; j < GS; ++j)
                 if (t0 + j < NT) acc.s[t0 + j] += reduce8(part[j], lane);

@@ -10,6 +10,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "kernels.h"
 #include "layout.h"
 
@@ -36,6 +38,48 @@ __device__ __forceinline__ uint32_t ld_stream4(const uint8_t *p)
     asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
     return v;
 }
+
+// Shared-memory loads by 32-bit shared address.
+__device__ __forceinline__ uint4 ld_smem16(uint32_t a)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_smem4(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Asynchronous 16-byte global -> shared copies (L1 bypassed), grouped per
+// thread: a thread's copies become visible to it after cp.async.wait_group,
+// to the other lanes of its warp after that and a __syncwarp.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const uint8_t *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Where a chunk's bytes are read from: global memory (streaming loads) or a
+// verbatim copy of the chunk in shared memory (same offsets).
+struct GlobalChunk {
+    const uint8_t *base;
+    __device__ __forceinline__ uint4 v16(size_t off) const { return ld_stream16(base + off); }
+    __device__ __forceinline__ uint32_t v4(size_t off) const { return ld_stream4(base + off); }
+};
+struct SharedChunk {
+    uint32_t base;
+    __device__ __forceinline__ uint4 v16(size_t off) const { return ld_smem16(base + (uint32_t)off); }
+    __device__ __forceinline__ uint32_t v4(size_t off) const { return ld_smem4(base + (uint32_t)off); }
+};
 
 __device__ __forceinline__ uint32_t word(const uint4 &v, int k)
 {
@@ -87,17 +131,17 @@ struct Q6kW {
     uint4 ql[8], qh[4], sc, dd;  // weights of one chunk (8 rows)
 };
 
-__device__ __forceinline__ void load_w(const Unit &x, int lane, Q6kW &R)
+template <class Src>
+__device__ __forceinline__ void load_w_from(const Src &src, const Unit &x, int lane, Q6kW &R)
 {
     const int nu = 8 * x.cb, cb = x.cb;
     if (x.active) {
 #pragma unroll
-        for (int r = 0; r < 8; ++r) R.ql[r] = ld_stream16(x.seg + ((size_t)r * nu + lane) * 16);
+        for (int r = 0; r < 8; ++r) R.ql[r] = src.v16(((size_t)r * nu + lane) * 16);
 #pragma unroll
-        for (int p = 0; p < 4; ++p)
-            R.qh[p] = ld_stream16(x.seg + (size_t)kQ6kQH * cb + ((size_t)p * nu + lane) * 16);
-        R.sc = ld_stream16(x.seg + (size_t)kQ6kSC * cb + (size_t)lane * 16);
-        R.dd = ld_stream16(x.seg + (size_t)kQ6kD * cb + (size_t)(lane >> 3) * 16);
+        for (int p = 0; p < 4; ++p) R.qh[p] = src.v16((size_t)kQ6kQH * cb + ((size_t)p * nu + lane) * 16);
+        R.sc = src.v16((size_t)kQ6kSC * cb + (size_t)lane * 16);
+        R.dd = src.v16((size_t)kQ6kD * cb + (size_t)(lane >> 3) * 16);
     } else {
 #pragma unroll
         for (int r = 0; r < 8; ++r) R.ql[r] = make_uint4(0, 0, 0, 0);
@@ -105,6 +149,11 @@ __device__ __forceinline__ void load_w(const Unit &x, int lane, Q6kW &R)
         for (int p = 0; p < 4; ++p) R.qh[p] = make_uint4(0, 0, 0, 0);
         R.sc = R.dd = make_uint4(0, 0, 0, 0);
     }
+}
+
+__device__ __forceinline__ void load_w(const Unit &x, int lane, Q6kW &R)
+{
+    load_w_from(GlobalChunk{x.seg}, x, lane, R);
 }
 
 // The unsigned 6-bit codes of row r, weights 4m..4m+3 (q0, sub-block 0 of
@@ -129,36 +178,34 @@ __device__ __forceinline__ void q6k_scales(const Q6kW &R, int r, int &sc0, int &
 
 // ---- q4_K ------------------------------------------------------------------
 struct Q4kW {
-    uint4 qs[8], dm0, dm1;       // nibbles of 8 rows; (d, dmin) of 8 rows
-    uint32_t s0, s1, s2;         // 6-bit scales and mins of 8 rows, packed
+    uint4 qs[8];  // nibbles of 8 rows
+    uint4 meta;   // the unit's META entry (layout.h)
 };
 
-// The QS, SM and DM planes (q4_K, and q5_K at other SM / DM offsets).
-template <int SM, int DM>
-__device__ __forceinline__ void load_w_q4like(const Unit &x, int lane, Q4kW &R)
+// The QS and META planes (q4_K, and q5_K at another META offset).
+template <int META, class Src>
+__device__ __forceinline__ void load_w_q4like(const Src &src, const Unit &x, int lane, Q4kW &R)
 {
     const int nu = 8 * x.cb, cb = x.cb;
     if (x.active) {
 #pragma unroll
-        for (int r = 0; r < 8; ++r) R.qs[r] = ld_stream16(x.seg + ((size_t)r * nu + lane) * 16);
-        const uint8_t *smp = x.seg + (size_t)SM * cb + (size_t)lane * 4;
-        R.s0 = ld_stream4(smp);
-        R.s1 = ld_stream4(smp + (size_t)nu * 4);
-        R.s2 = ld_stream4(smp + (size_t)nu * 8);
-        const uint8_t *dmp = x.seg + (size_t)DM * cb + (size_t)(lane >> 3) * 32;
-        R.dm0 = ld_stream16(dmp);
-        R.dm1 = ld_stream16(dmp + 16);
+        for (int r = 0; r < 8; ++r) R.qs[r] = src.v16(((size_t)r * nu + lane) * 16);
+        R.meta = src.v16((size_t)META * cb + (size_t)lane * 16);
     } else {
 #pragma unroll
         for (int r = 0; r < 8; ++r) R.qs[r] = make_uint4(0, 0, 0, 0);
-        R.s0 = R.s1 = R.s2 = 0;
-        R.dm0 = R.dm1 = make_uint4(0, 0, 0, 0);
+        R.meta = make_uint4(0, 0, 0, 0);
     }
 }
 
+template <class Src>
+__device__ __forceinline__ void load_w_from(const Src &src, const Unit &x, int lane, Q4kW &R)
+{
+    load_w_q4like<kQ4kMeta>(src, x, lane, R);
+}
 __device__ __forceinline__ void load_w(const Unit &x, int lane, Q4kW &R)
 {
-    load_w_q4like<kQ4kSM, kQ4kDM>(x, lane, R);
+    load_w_from(GlobalChunk{x.seg}, x, lane, R);
 }
 
 // Row r's codes for words m of the unit: weights 4m..4m+3 (lo, against the
@@ -170,16 +217,44 @@ __device__ __forceinline__ void codes(const Q4kW &R, int r, int m, uint32_t &lo,
     hi = (w >> 4) & kLo4;
 }
 
+// The scales of a unit for its 8 rows, decoded once per chunk: the 6-bit
+// scales and mins one per byte (rows 0, 2, 4, 6 and rows 1, 3, 5, 7), and
+// each row's (d, dmin) taken from the META entry of the block's unit with
+// that row's index.  Every lane of the warp must call this (shuffles).
+struct Q4kDec {
+    uint32_t sce, sco, me, mo;
+    uint32_t dm[8];
+};
+
+__device__ __forceinline__ void decode_q4k(const Q4kW &R, int lane, Q4kDec &D)
+{
+    const uint32_t s0 = R.meta.x, s1 = R.meta.y, s2 = R.meta.z;
+    D.sce = (s0 & kLo4) | ((s2 << 4) & 0x30303030u);
+    D.sco = ((s0 >> 4) & kLo4) | (s2 & 0x30303030u);
+    D.me = (s1 & kLo4) | ((s2 << 2) & 0x30303030u);
+    D.mo = ((s1 >> 4) & kLo4) | ((s2 >> 2) & 0x30303030u);
+    const int base = lane & ~7;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) D.dm[r] = __shfl_sync(kFull, R.meta.w, base + r);
+}
+
 // Row r's 6-bit scale and min and fp16 d, dmin.
-__device__ __forceinline__ void q4k_scales(const Q4kW &R, int r, int &sc, int &mn, float &d,
+__device__ __forceinline__ void q4k_scales(const Q4kDec &D, int r, int &sc, int &mn, float &d,
                                            float &dmin)
 {
-    const int hi = (int)((R.s2 >> (4 * r)) & 15u);
-    sc = (int)((R.s0 >> (4 * r)) & 15u) | ((hi & 3) << 4);
-    mn = (int)((R.s1 >> (4 * r)) & 15u) | ((hi >> 2) << 4);
-    const uint32_t dmw = word(r < 4 ? R.dm0 : R.dm1, r & 3);
-    d = half_lo(dmw);
-    dmin = half_hi(dmw);
+    const int sh = 8 * (r >> 1);
+    sc = (int)((((r & 1) ? D.sco : D.sce) >> sh) & 0xffu);
+    mn = (int)((((r & 1) ? D.mo : D.me) >> sh) & 0xffu);
+    d = half_lo(D.dm[r]);
+    dmin = half_hi(D.dm[r]);
+}
+
+// dp4a with unsigned bytes in a and signed bytes in b.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
 }
 
 // ---- q5_K: q4_K's fields plus each code's fifth bit -------------------------
@@ -187,16 +262,21 @@ struct Q5kW : Q4kW {
     uint4 qh[2];  // fifth-bit words H of rows 0..3 and 4..7
 };
 
-__device__ __forceinline__ void load_w(const Unit &x, int lane, Q5kW &R)
+template <class Src>
+__device__ __forceinline__ void load_w_from(const Src &src, const Unit &x, int lane, Q5kW &R)
 {
-    load_w_q4like<kQ5kSM, kQ5kDM>(x, lane, R);
+    load_w_q4like<kQ5kMeta>(src, x, lane, R);
     if (x.active) {
-        const uint8_t *hp = x.seg + (size_t)kQ5kQH * x.cb + (size_t)lane * 32;
-        R.qh[0] = ld_stream16(hp);
-        R.qh[1] = ld_stream16(hp + 16);
+        const size_t hp = (size_t)kQ5kQH * x.cb + (size_t)lane * 32;
+        R.qh[0] = src.v16(hp);
+        R.qh[1] = src.v16(hp + 16);
     } else {
         R.qh[0] = R.qh[1] = make_uint4(0, 0, 0, 0);
     }
+}
+__device__ __forceinline__ void load_w(const Unit &x, int lane, Q5kW &R)
+{
+    load_w_from(GlobalChunk{x.seg}, x, lane, R);
 }
 
 // As for q4_K, with bit 4 of every byte taken from the fifth-bit word.
@@ -215,13 +295,14 @@ __device__ __forceinline__ void codes(const Q5kW &R, int r, int m, uint32_t &lo,
 // path may be hoisted above the grid-dependency wait).  With SUBDOTS the
 // integer sub-block dots are written to a.isums instead of being combined.
 // ---- q6_K ------------------------------------------------------------------
-struct Q6kRegs : Q6kW {
+struct X6 {               // the unit's activation codes and scale
     uint4 xa, xb;        // activation codes 0..15, 16..31 of the unit
     unsigned short dh;   // activation fp16 scale
 };
+struct Q6kRegs : Q6kW, X6 {};
 
 __device__ __forceinline__ void load_x(const GemvLaunch &a, const uint8_t *xs, const Unit &x,
-                                       int lane, Q6kRegs &R)
+                                       int lane, X6 &R)
 {
     if (x.active) {
         const int U = 32 * x.c + lane;
@@ -312,22 +393,38 @@ __device__ __forceinline__ void load_x(const GemvLaunch &a, const uint8_t *xs, c
 }
 
 // q4_K / q5_K: the unit is one 32-weight sub-block; term = d*sc*isum -
-// dmin*m*qsum (qsum = the q8 block's code sum).
+// dmin*m*qsum (qsum = the q8 block's code sum).  q4_K's high nibbles go to
+// dp4a in place (16 x the code, bytes read unsigned), the sum shifted back
+// once per row: the same integer isum as nibble by nibble.
 template <bool SUBDOTS, class Regs>
 __device__ __forceinline__ void compute_q4like(const GemvLaunch &a, const GemvPart &P,
                                                const Regs &R, const Unit &x, int lane,
                                                float (&acc)[8])
 {
+    constexpr bool kQ5 = std::is_base_of<Q5kW, Regs>::value;
     const float d8 = __half2float(__ushort_as_half(R.dh));
+    Q4kDec D;
+    if (!SUBDOTS) decode_q4k(R, lane, D);
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
         int dot = 0;
+        if constexpr (kQ5) {
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            uint32_t lo, hi;
-            codes(R, r, m, lo, hi);
-            dot = __dp4a((int)lo, (int)word(R.xa, m), dot);
-            dot = __dp4a((int)hi, (int)word(R.xb, m), dot);
+            for (int m = 0; m < 4; ++m) {
+                uint32_t lo, hi;
+                codes(R, r, m, lo, hi);
+                dot = __dp4a((int)lo, (int)word(R.xa, m), dot);
+                dot = __dp4a((int)hi, (int)word(R.xb, m), dot);
+            }
+        } else {
+            int hi16 = 0;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t w = word(R.qs[r], m);
+                dot = __dp4a((int)(w & kLo4), (int)word(R.xa, m), dot);
+                hi16 = dp4a_us(w & ~kLo4, word(R.xb, m), hi16);
+            }
+            dot += hi16 >> 4;  // exact: hi16 is a multiple of 16
         }
         if (SUBDOTS) {
             const int row = x.t * kTileRows + r;
@@ -338,7 +435,7 @@ __device__ __forceinline__ void compute_q4like(const GemvLaunch &a, const GemvPa
         } else {
             int sc, mn;
             float d, dmin;
-            q4k_scales(R, r, sc, mn, d, dmin);
+            q4k_scales(D, r, sc, mn, d, dmin);
             const float term = fmaf(d, (float)(sc * dot), -dmin * (float)(mn * R.qsum));
             acc[r] = fmaf(d8, term, acc[r]);
         }
@@ -367,18 +464,21 @@ template <>
 struct Fmt<6> {
     using Regs = Q6kRegs;
     using W = Q6kW;
+    using X = X6;
     static constexpr int kChunkBytes = kQ6kChunkPerBlock * kChunkBlocks;
 };
 template <>
 struct Fmt<4> {
     using Regs = Q4kRegs;
     using W = Q4kW;
+    using X = XSum;
     static constexpr int kChunkBytes = kQ4kChunkPerBlock * kChunkBlocks;
 };
 template <>
 struct Fmt<5> {
     using Regs = Q5kRegs;
     using W = Q5kW;
+    using X = XSum;
     static constexpr int kChunkBytes = kQ5kChunkPerBlock * kChunkBlocks;
 };
 

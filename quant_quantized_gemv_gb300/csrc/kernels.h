@@ -48,6 +48,13 @@ struct GemvLaunch {
     unsigned q8_stride;     // bytes from one token's plane to the next (small batch)
     unsigned *cover;        // coverage mode: a count per (global tile, chunk), else null
     int wpc;                // small batch: warps a CTA may hold (its plan's G = wpc / splits)
+    // single-token GEMV weight ring: each warp keeps `stages` chunks in
+    // flight in its own shared-memory slots of slot_bytes (the largest chunk
+    // of the launch's formats), after the staged plane (ring_off bytes, 0 on
+    // split plans); `pre` of them are requested before the grid-dependency
+    // wait.  stages == 0: chunks go straight to registers.
+    int stages, pre;
+    unsigned slot_bytes, ring_off;
 };
 
 cudaError_t launch_gemv(const GemvLaunch &a, cudaStream_t st);
@@ -103,8 +110,8 @@ __host__ __device__ constexpr int batch_reg_cap(int nt, int fmt)
 {
     return fmt == 4 ? 168
          : nt == 2 ? 128
-         : nt == 3 ? (fmt == 6 ? 136 : 128)
-         : nt == 4 ? (fmt == 6 ? 168 : 144)
+         : nt == 3 ? 136
+         : nt == 4 ? (fmt == 6 ? 168 : 152)
          : 168;
 }
 // Most warps a CTA can hold at that cap (at most 16): sizes the kernel's
@@ -115,6 +122,18 @@ __host__ __device__ constexpr int batch_warp_budget_max(int nt, int fmt)
     return 65536 / (32 * batch_reg_cap(nt, fmt)) < kBatchMaxCtaWarps
                ? 65536 / (32 * batch_reg_cap(nt, fmt))
                : kBatchMaxCtaWarps;
+}
+
+// Single-token GEMV weight ring (GemvLaunch::stages): most stages a warp
+// may keep, and the dynamic shared memory of a CTA of `warps` warps.
+constexpr int kGemvMaxStages = 3;
+inline size_t gemv_ring_off(bool whole_tiles, size_t plane)
+{
+    return whole_tiles ? (plane + 127) & ~(size_t)127 : 0;
+}
+inline size_t gemv_dyn_smem(int warps, bool whole_tiles, size_t plane, int stages, size_t slot)
+{
+    return gemv_ring_off(whole_tiles, plane) + (size_t)warps * stages * slot;
 }
 
 // Warps per CTA for a plan with `splits` splits.

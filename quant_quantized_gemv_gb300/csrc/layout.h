@@ -30,23 +30,27 @@
 //   SC  @1536*cb  [unit nu][row 8][2 B]  the unit's two int8 sub-block scales
 //   D   @1664*cb  [block cb][row 8][2 B] the block's fp16 d
 // q4_K chunk (1152*cb bytes):
-//   QS  @0        [row 8][unit nu][16 B]  unit = one 32-weight sub-block;
-//                 byte k: low nibble = weight k, high nibble = weight 16+k
-//   SM  @1024*cb  [word 3][unit nu][4 B]  word0 bits 4r..4r+3 = sc_r & 15,
-//                 word1 bits 4r.. = m_r & 15, word2 bits 4r,4r+1 = sc_r >> 4
-//                 and bits 4r+2,4r+3 = m_r >> 4   (r = row within the tile)
-//   DM  @1120*cb  [block cb][row 8][d fp16, dmin fp16]
+//   QS   @0        [row 8][unit nu][16 B]  unit = one 32-weight sub-block;
+//                  byte k: low nibble = weight k, high nibble = weight 16+k
+//   META @1024*cb  [unit nu][16 B]  the unit's scales and one row's block
+//                  scales, so that a lane gets all it reads besides its
+//                  codes with one 16-byte load:
+//                  word0 bits 4r..4r+3 = sc_r & 15, word1 bits 4r.. = m_r & 15,
+//                  word2 bits 4r,4r+1 = sc_r >> 4 and bits 4r+2,4r+3 = m_r >> 4
+//                  (r = row within the tile); word3 = (d, dmin) fp16 of row
+//                  (unit & 7) of the unit's block (unit >> 3): the 8 units of
+//                  a block hold its 8 rows' (d, dmin), which the kernels pass
+//                  between the block's 8 lanes with shuffles
 // q5_K chunk (1408*cb bytes): q4_K's planes plus the fifth bits
-//   QS  @0        as q4_K (low 4 bits of each code)
-//   QH  @1024*cb  [unit nu][row 8][4 B]  word H of (unit, row): bit
-//                 8b + 4h + m = fifth bit of weight 16h + 4m + b, so that
-//                 ((H >> m) & 0x01010101) << 4 lines up with the low-nibble
-//                 word m and ((H >> (m+4)) & 0x01010101) << 4 with the high
-//   SM  @1280*cb  as q4_K
-//   DM  @1376*cb  as q4_K
-// Every plane offset and every per-lane load address is 16-byte aligned for
-// QL/QH/QS/D/DM and 4-byte aligned for SM, because 8 rows x 210 B,
-// 8 rows x 144 B and 8 rows x 176 B are all multiples of 16.
+//   QS   @0        as q4_K (low 4 bits of each code)
+//   QH   @1024*cb  [unit nu][row 8][4 B]  word H of (unit, row): bit
+//                  8b + 4h + m = fifth bit of weight 16h + 4m + b, so that
+//                  ((H >> m) & 0x01010101) << 4 lines up with the low-nibble
+//                  word m and ((H >> (m+4)) & 0x01010101) << 4 with the high
+//   META @1280*cb  as q4_K
+// Every plane offset and every per-lane load address is 16-byte aligned,
+// because 8 rows x 210 B, 8 rows x 144 B and 8 rows x 176 B are all
+// multiples of 16.
 #pragma once
 #include <stddef.h>
 #include <stdint.h>
@@ -63,9 +67,9 @@ constexpr int kQ5kBytes = 176;
 // q6_K chunk plane offsets, per block of the chunk (multiply by cb)
 constexpr int kQ6kQH = 1024, kQ6kSC = 1536, kQ6kD = 1664, kQ6kChunkPerBlock = 1680;
 // q4_K chunk plane offsets, per block of the chunk (multiply by cb)
-constexpr int kQ4kSM = 1024, kQ4kDM = 1120, kQ4kChunkPerBlock = 1152;
+constexpr int kQ4kMeta = 1024, kQ4kChunkPerBlock = 1152;
 // q5_K chunk plane offsets, per block of the chunk (multiply by cb)
-constexpr int kQ5kQH = 1024, kQ5kSM = 1280, kQ5kDM = 1376, kQ5kChunkPerBlock = 1408;
+constexpr int kQ5kQH = 1024, kQ5kMeta = 1280, kQ5kChunkPerBlock = 1408;
 
 // Bytes of one super-block (= per block of a chunk / 8 rows) by format code
 // (6 = q6_K, 4 = q4_K, 5 = q5_K); 0 for an unknown code.

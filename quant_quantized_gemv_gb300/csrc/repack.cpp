@@ -68,9 +68,10 @@ inline int q5k_bit(const uint8_t *blk, int k, int l) { return (blk[16 + l] >> k)
 // (= 16h + 4m + b) of the unit: 8b + 4h + m (layout.h).
 inline int q5k_hpos(int l) { return 8 * (l & 3) + 4 * (l >> 4) + ((l >> 2) & 3); }
 
-// The QS / SM / DM planes of a q4_K or q5_K unit (SM, DM: plane offsets).
-void put_q4like(uint8_t *out, size_t seg, int cb, int r, int i, const uint8_t *blk, int sm_off,
-                int dm_off, int nib_off)
+// The QS and META planes of a q4_K or q5_K unit i for tile row r (meta_off:
+// the META plane's offset per block of the chunk; layout.h).
+void put_q4like(uint8_t *out, size_t seg, int cb, int r, int i, const uint8_t *blk, int meta_off,
+                int nib_off)
 {
     const int nu = 8 * cb, k = i & 7;
     uint8_t *qs = out + seg + ((size_t)r * nu + i) * 16;
@@ -80,21 +81,18 @@ void put_q4like(uint8_t *out, size_t seg, int cb, int r, int i, const uint8_t *b
     }
     int sc, m;
     q4k_get_sm(blk + 4, k, &sc, &m);
+    uint8_t *meta = out + seg + (size_t)meta_off * cb + (size_t)i * 16;
     uint32_t w[3];
-    uint8_t *smp = out + seg + (size_t)sm_off * cb;
-    for (int j = 0; j < 3; ++j) memcpy(&w[j], smp + ((size_t)j * nu + i) * 4, 4);
+    memcpy(w, meta, 12);
     w[0] |= (uint32_t)(sc & 15) << (4 * r);
     w[1] |= (uint32_t)(m & 15) << (4 * r);
     w[2] |= (uint32_t)((sc >> 4) | ((m >> 4) << 2)) << (4 * r);
-    for (int j = 0; j < 3; ++j) memcpy(smp + ((size_t)j * nu + i) * 4, &w[j], 4);
-    if (k == 0) {
-        uint8_t *dm = out + seg + (size_t)dm_off * cb + (size_t)(i >> 3) * 32 + r * 4;
-        memcpy(dm, blk, 4);
-    }
+    memcpy(meta, w, 12);
+    if (r == k) memcpy(meta + 12, blk, 4);  // (d, dmin) of row k of the block
 }
 
-void get_q4like(const uint8_t *in, size_t seg, int cb, int r, int i, uint8_t *blk, int sm_off,
-                int dm_off, int nib_off)
+void get_q4like(const uint8_t *in, size_t seg, int cb, int r, int i, uint8_t *blk, int meta_off,
+                int nib_off)
 {
     const int nu = 8 * cb, k = i & 7;
     const uint8_t *qs = in + seg + ((size_t)r * nu + i) * 16;
@@ -102,17 +100,14 @@ void get_q4like(const uint8_t *in, size_t seg, int cb, int r, int i, uint8_t *bl
         const int v = l < 16 ? (qs[l] & 15) : (qs[l - 16] >> 4);
         blk[nib_off + 32 * (k >> 1) + l] |= (uint8_t)((k & 1) ? v << 4 : v);
     }
+    const uint8_t *meta = in + seg + (size_t)meta_off * cb + (size_t)i * 16;
     uint32_t w[3];
-    const uint8_t *smp = in + seg + (size_t)sm_off * cb;
-    for (int j = 0; j < 3; ++j) memcpy(&w[j], smp + ((size_t)j * nu + i) * 4, 4);
+    memcpy(w, meta, 12);
     const int hi = (w[2] >> (4 * r)) & 15;
     const int sc = (int)((w[0] >> (4 * r)) & 15) | ((hi & 3) << 4);
     const int m = (int)((w[1] >> (4 * r)) & 15) | ((hi >> 2) << 4);
     q4k_put_sm(blk + 4, k, sc, m);
-    if (k == 0) {
-        const uint8_t *dm = in + seg + (size_t)dm_off * cb + (size_t)(i >> 3) * 32 + r * 4;
-        memcpy(blk, dm, 4);
-    }
+    if (r == k) memcpy(blk, meta + 12, 4);
 }
 
 bool shape_ok(int rows, int cols)
@@ -232,7 +227,7 @@ int mq_repack_q4k(const void *gguf, void *dst, int rows, int cols)
     memset(out, 0, (size_t)g.ntiles * g.tile_bytes);
     for_each_unit(g, kQ4kBytes, [&](size_t seg, int cb, int r, int row, int b, int i) {
         const uint8_t *blk = src + ((size_t)row * g.nb + b) * kQ4kBytes;
-        put_q4like(out, seg, cb, r, i, blk, kQ4kSM, kQ4kDM, 16);
+        put_q4like(out, seg, cb, r, i, blk, kQ4kMeta, 16);
     });
     return MQ_OK;
 }
@@ -247,7 +242,7 @@ int mq_unrepack_q4k(const void *packed, void *gguf, int rows, int cols)
     memset(dst, 0, (size_t)rows * g.nb * kQ4kBytes);
     for_each_unit(g, kQ4kBytes, [&](size_t seg, int cb, int r, int row, int b, int i) {
         uint8_t *blk = dst + ((size_t)row * g.nb + b) * kQ4kBytes;
-        get_q4like(in, seg, cb, r, i, blk, kQ4kSM, kQ4kDM, 16);
+        get_q4like(in, seg, cb, r, i, blk, kQ4kMeta, 16);
     });
     return MQ_OK;
 }
@@ -269,7 +264,7 @@ int mq_repack_q5k(const void *gguf, void *dst, int rows, int cols)
     memset(out, 0, (size_t)g.ntiles * g.tile_bytes);
     for_each_unit(g, kQ5kBytes, [&](size_t seg, int cb, int r, int row, int b, int i) {
         const uint8_t *blk = src + ((size_t)row * g.nb + b) * kQ5kBytes;
-        put_q4like(out, seg, cb, r, i, blk, kQ5kSM, kQ5kDM, 48);
+        put_q4like(out, seg, cb, r, i, blk, kQ5kMeta, 48);
         const int k = i & 7;
         uint32_t H = 0;
         for (int l = 0; l < 32; ++l) H |= (uint32_t)q5k_bit(blk, k, l) << q5k_hpos(l);
@@ -288,7 +283,7 @@ int mq_unrepack_q5k(const void *packed, void *gguf, int rows, int cols)
     memset(dst, 0, (size_t)rows * g.nb * kQ5kBytes);
     for_each_unit(g, kQ5kBytes, [&](size_t seg, int cb, int r, int row, int b, int i) {
         uint8_t *blk = dst + ((size_t)row * g.nb + b) * kQ5kBytes;
-        get_q4like(in, seg, cb, r, i, blk, kQ5kSM, kQ5kDM, 48);
+        get_q4like(in, seg, cb, r, i, blk, kQ5kMeta, 48);
         const int k = i & 7;
         uint32_t H;
         memcpy(&H, in + seg + (size_t)kQ5kQH * cb + ((size_t)i * 8 + r) * 4, 4);

@@ -93,14 +93,14 @@ __device__ void repack_unit_q6k(const RepackArgs &A, int t, int c, int i)
 // [qh 32 |] qs 128.  Unit i is sub-block k = i & 7 of block b: weight l is
 // the low (k even) or high (k odd) nibble of qs[32 (k/2) + l]; q5_K adds the
 // fifth bit, bit k of qh[l].
-template <int SM, int DM, int QH, int NIB, int BLOCK, int CHUNK>
+template <int META, int QH, int NIB, int BLOCK, int CHUNK>
 __device__ void repack_unit_q4like(const RepackArgs &A, int t, int c, int i)
 {
     const int cb = min(kChunkBlocks, A.nb - kChunkBlocks * c);
     if (i >= 8 * cb) return;
     const int nu = 8 * cb, k = i & 7, b = kChunkBlocks * c + (i >> 3);
     uint8_t *seg = A.dst + (size_t)t * A.tile_bytes + (size_t)c * CHUNK;
-    uint32_t w0 = 0, w1 = 0, w2 = 0;
+    uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
     for (int r = 0; r < kTileRows; ++r) {
         const int row = t * kTileRows + r;
         if (row >= A.rows) break;  // padded rows stay zero
@@ -127,13 +127,8 @@ __device__ void repack_unit_q4like(const RepackArgs &A, int t, int c, int i)
         w0 |= (uint32_t)(sc & 15) << (4 * r);
         w1 |= (uint32_t)(m & 15) << (4 * r);
         w2 |= (uint32_t)((sc >> 4) | ((m >> 4) << 2)) << (4 * r);
-        if (k == 0) {
-            uint8_t *dm = seg + (size_t)DM * cb + (size_t)(i >> 3) * 32 + r * 4;
-            dm[0] = blk[0];
-            dm[1] = blk[1];
-            dm[2] = blk[2];
-            dm[3] = blk[3];
-        }
+        if (r == k)  // (d, dmin) of row k of the block
+            w3 = pack4(blk[0], blk[1], blk[2], blk[3]);
         if (QH > 0) {  // fifth bits: bit 8b + 4h + m of H = weight 16h + 4m + b
             uint32_t H = 0;
 #pragma unroll
@@ -142,10 +137,7 @@ __device__ void repack_unit_q4like(const RepackArgs &A, int t, int c, int i)
             *reinterpret_cast<uint32_t *>(seg + (size_t)QH * cb + ((size_t)i * 8 + r) * 4) = H;
         }
     }
-    uint32_t *smp = reinterpret_cast<uint32_t *>(seg + (size_t)SM * cb);
-    smp[i] = w0;
-    smp[nu + i] = w1;
-    smp[2 * nu + i] = w2;
+    *reinterpret_cast<uint4 *>(seg + (size_t)META * cb + (size_t)i * 16) = make_uint4(w0, w1, w2, w3);
 }
 
 template <int FMT>
@@ -159,10 +151,9 @@ __global__ void __launch_bounds__(256) repack_kernel(const RepackArgs A)
     if (FMT == 6)
         repack_unit_q6k(A, t, c, i);
     else if (FMT == 4)
-        repack_unit_q4like<kQ4kSM, kQ4kDM, 0, 16, kQ4kBytes, kQ4kChunkPerBlock * kChunkBlocks>(A, t, c, i);
+        repack_unit_q4like<kQ4kMeta, 0, 16, kQ4kBytes, kQ4kChunkPerBlock * kChunkBlocks>(A, t, c, i);
     else
-        repack_unit_q4like<kQ5kSM, kQ5kDM, kQ5kQH, 48, kQ5kBytes, kQ5kChunkPerBlock * kChunkBlocks>(A, t, c,
-                                                                                                   i);
+        repack_unit_q4like<kQ5kMeta, kQ5kQH, 48, kQ5kBytes, kQ5kChunkPerBlock * kChunkBlocks>(A, t, c, i);
 }
 
 }  // namespace

@@ -141,6 +141,14 @@ WORKLOADS = {
     "ffn_14b": Workload("ffn_14b", [("ffn_gate", "q4k", INTER_14B, HIDDEN_14B, "rms"),
                                     ("ffn_up", "q4k", INTER_14B, HIDDEN_14B, "rms"),
                                     ("ffn_down", "q6k", HIDDEN_14B, INTER_14B, "swiglu")]),
+    # single launches of the sweep's q4_K shapes: attn_q (and attn_output)
+    # 5120 x 5120, ffn_gate (and ffn_up) 13824 x 5120, and the q, k, v
+    # matrices of a layer grouped in one launch over one rms_norm -> q8 plane
+    "attn_q_14b": Workload("attn_q_14b", [("attn_q", "q4k", HIDDEN_14B, HIDDEN_14B, "rms")]),
+    "ffn_gate_14b": Workload("ffn_gate_14b", [("ffn_gate", "q4k", INTER_14B, HIDDEN_14B, "rms")]),
+    "attn_qkv_14b": Workload("attn_qkv_14b", [("attn_q", "q4k", HIDDEN_14B, HIDDEN_14B, "rms"),
+                                              ("attn_k", "q4k", KV_14B, HIDDEN_14B, "rms"),
+                                              ("attn_v", "q6k", KV_14B, HIDDEN_14B, "rms")]),
     # full 48-layer 14B decode weight sweep plus the head
     "sweep_14b": Workload("sweep_14b", _sweep_14b()),
 }
