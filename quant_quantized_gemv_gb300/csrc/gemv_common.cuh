@@ -22,20 +22,34 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr uint32_t kLo4 = 0x0f0f0f0fu;
 constexpr uint32_t kOnes = 0x01010101u;
 
+// L2 policy of the weight stream: evict first.  Every weight byte is read
+// once per decode step and a step streams far more than L2 holds, so the
+// weights are the lines to drop first; the kernels' code, the q8 planes, the
+// outputs and the producers' data then stay in L2 across the launches of a
+// step.
+__device__ __forceinline__ uint64_t stream_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // 16-byte streaming load: read-only path, no L1 allocation (each weight
-// byte is used once).
-__device__ __forceinline__ uint4 ld_stream16(const uint8_t *p)
+// byte is used once), evict-first in L2.
+__device__ __forceinline__ uint4 ld_stream16(const uint8_t *p, uint64_t pol)
 {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
+                 : "l"(p), "l"(pol));
     return v;
 }
-__device__ __forceinline__ uint32_t ld_stream4(const uint8_t *p)
+__device__ __forceinline__ uint32_t ld_stream4(const uint8_t *p, uint64_t pol)
 {
     uint32_t v;
-    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;"
+                 : "=r"(v)
+                 : "l"(p), "l"(pol));
     return v;
 }
 
@@ -72,8 +86,9 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 // verbatim copy of the chunk in shared memory (same offsets).
 struct GlobalChunk {
     const uint8_t *base;
-    __device__ __forceinline__ uint4 v16(size_t off) const { return ld_stream16(base + off); }
-    __device__ __forceinline__ uint32_t v4(size_t off) const { return ld_stream4(base + off); }
+    uint64_t pol = stream_policy();
+    __device__ __forceinline__ uint4 v16(size_t off) const { return ld_stream16(base + off, pol); }
+    __device__ __forceinline__ uint32_t v4(size_t off) const { return ld_stream4(base + off, pol); }
 };
 struct SharedChunk {
     uint32_t base;
