@@ -809,6 +809,10 @@ int device_address(const void *p, void **out)
 
 }  // namespace
 
+namespace mq {
+int pdl_setting() { return g_pdl.load(std::memory_order_relaxed); }
+}  // namespace mq
+
 extern "C" {
 
 const char *mq_strerror(int status)

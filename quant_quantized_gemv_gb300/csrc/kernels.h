@@ -187,6 +187,9 @@ cudaError_t launch_repack(int fmt, const void *src, void *dst, int rows, int col
 // (copy.cu), as a kernel that takes part in the launch chain.
 cudaError_t launch_copy(void *dst, const void *src, size_t bytes, int pdl, cudaStream_t st);
 
+// The process-wide programmatic-dependent-launch setting (mq_set_pdl).
+int pdl_setting();
+
 // Record the library's last CUDA failure on this thread (`where` and the CUDA
 // error, readable with mq_last_error); returns MQ_ERR_CUDA.
 int cuda_fail(const char *where, cudaError_t e);

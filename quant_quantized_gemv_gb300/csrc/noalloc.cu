@@ -59,6 +59,18 @@ int scratch_address(void **out)
     return MQ_OK;
 }
 
+// Zero the arrival counters at the head of the scratch.  A kernel rather
+// than a memset so that a decode chain with programmatic dependent launch
+// stays a chain: it waits for its predecessor (which may be the previous
+// call still using the array) before it writes, and lets the GEMV behind it
+// start streaming weights meanwhile.
+__global__ void clear_counters_kernel(unsigned *cnt, int n)
+{
+    griddep_launch_dependents();
+    griddep_wait();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) cnt[i] = 0u;
+}
+
 }  // namespace
 
 extern "C" int mq_gemv_q6k_q8_noalloc(const void *Wp, const void *q8, float *y, int rows, int cols,
@@ -80,8 +92,9 @@ extern "C" int mq_gemv_q6k_q8_noalloc(const void *Wp, const void *q8, float *y, 
     if (st != MQ_OK) return st;
     // The counters must start at zero; a finished call leaves them at zero,
     // but clear them anyway so that an interrupted earlier call cannot leak.
-    const size_t counter_bytes = round16((size_t)ceil_div(rows, kTileRows) * 4);
-    const cudaError_t e = cudaMemsetAsync(ws, 0, counter_bytes, (cudaStream_t)stream);
+    const int ncnt = ceil_div(rows, kTileRows);
+    const cudaError_t e = launch_maybe_pdl(clear_counters_kernel, dim3(1), dim3(256), 0, pdl_setting(),
+                                           (cudaStream_t)stream, (unsigned *)ws, ncnt);
     if (e != cudaSuccess) return cuda_fail("clearing the scratch counters", e);
     return mq_gemv_q6k_q8_plan(Wp, q8, y, rows, cols, splits, cps, tpi, ws, kNoAllocScratchBytes,
                                stream);

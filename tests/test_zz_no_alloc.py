@@ -74,3 +74,52 @@ def test_noalloc_rejects_bad_arguments_before_launch(mq):
     L = mq.lib()
     null = ctypes.c_void_p(0)
     assert L.mq_gemv_q6k_q8_noalloc(null, null, null, 8, 1024, null) == mq.MQ_ERR_NULL
+
+
+def test_noalloc_in_a_pdl_graph_chain(mq, orc):
+    """quantize -> no-alloc GEMV steps with programmatic dependent launch,
+    captured in one CUDA graph and replayed: every step's output equals the
+    regular entry point's (same plan, caller workspace) bit for bit.  The
+    first call on the device comes before the capture (it looks up the
+    array's device address)."""
+    import torch
+    rows, cols = 512, 18944                              # a plan with scratch
+    g = synth.rng("noalloc-pdl")
+    W = synth.q6k_blocks(g, rows, cols)
+    Wp = torch.from_numpy(mq.mq_repack_q6k(W, rows, cols)).cuda()
+    xs = [torch.from_numpy(synth.normal(g, cols)).cuda() for _ in range(4)]
+    x = torch.empty(cols, device="cuda")
+    plane = torch.empty(mq.mq_q8_bytes(cols), dtype=torch.uint8, device="cuda")
+    y = torch.empty(rows, device="cuda")
+    L = mq.lib()
+
+    def noalloc_step(stream):
+        mq.mq_quantize_q8(x, q8=plane)
+        st = L.mq_gemv_q6k_q8_noalloc(ctypes.c_void_p(Wp.data_ptr()), ctypes.c_void_p(plane.data_ptr()),
+                                      ctypes.c_void_p(y.data_ptr()), rows, cols, ctypes.c_void_p(stream))
+        assert st == mq.MQ_OK, mq.lib().mq_strerror(st)
+
+    ws = mq.mq_gemv_workspace(rows, cols)
+    refs = []
+    for xi in xs:                                        # regular entry point, no PDL
+        refs.append(mq.mq_gemv_q6k_q8(Wp, mq.mq_quantize_q8(xi), rows, cols, ws=ws).cpu().numpy())
+    prev = mq.mq_set_pdl(True)
+    try:
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            x.copy_(xs[0])
+            noalloc_step(s.cuda_stream)                  # first call outside capture
+            torch.cuda.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=s):
+                noalloc_step(s.cuda_stream)
+            outs = []
+            for xi in xs:
+                x.copy_(xi)
+                gr.replay()
+                outs.append(y.clone())
+        torch.cuda.synchronize()
+    finally:
+        mq.mq_set_pdl(prev)
+    for a, b in zip(outs, refs):
+        assert np.array_equal(a.cpu().numpy(), b)
