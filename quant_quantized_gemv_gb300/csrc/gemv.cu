@@ -312,7 +312,16 @@ __device__ __forceinline__ void run_ring(const GemvLaunch &a, const GemvPart &P,
 // kernel functions from one GEMV to the next costs more than the branch.
 // Measured on the 14B sweep: 2.39 ms with one kernel for all formats
 // against 2.49 ms with a kernel per format set (qkv, o, down alternating).
-template <int MODE>
+// Code a launch never runs still costs it on GB300, so the kernel comes in
+// three instances (KIND): q6_K and q4_K parts only, every format, and the
+// weight ring (every format; launched only when a.stages > 0).  With the
+// ring's code compiled into the default kernel the 14B sweep's GEMVs took
+// 2174 against 2114 us per step and its PDL step 2219 against 2178 us
+// (single shapes 1-2%); without the q5_K path as well the step took 2161
+// against 2171 us.  Every launch of the sweep uses the first instance, so
+// its chain never switches kernel functions.
+constexpr int kKindQ46 = 0, kKindAll = 1, kKindRing = 2;
+template <int MODE, int KIND>
 __global__ void __maxnreg__(MODE == kModeSubdots ? 168 : kGemvMaxRegs)
     gemv_kernel(const __grid_constant__ GemvLaunch a)
 {
@@ -343,13 +352,18 @@ __global__ void __maxnreg__(MODE == kModeSubdots ? 168 : kGemvMaxRegs)
         u0 = li * a.tpi * nch;
         u1 = min(u0 + a.tpi * nch, P.ntiles * nch);
     }
-    if (a.stages > 0) {
+    if constexpr (KIND == kKindRing) {
         if (P.fmt == 6)
             run_ring<6, MODE>(a, P, xs, item, u0, u1, lane);
         else if (P.fmt == 5)
             run_ring<5, MODE>(a, P, xs, item, u0, u1, lane);
         else
             run_ring<4, MODE>(a, P, xs, item, u0, u1, lane);
+    } else if constexpr (KIND == kKindQ46) {
+        if (P.fmt == 6)
+            run_range<6, MODE>(a, P, xs, item, u0, u1, lane);
+        else
+            run_range<4, MODE>(a, P, xs, item, u0, u1, lane);
     } else {
         if (P.fmt == 6)
             run_range<6, MODE>(a, P, xs, item, u0, u1, lane);
@@ -366,12 +380,21 @@ cudaError_t launch(const GemvLaunch &a, cudaStream_t st)
     const int warps = gemv_cta_warps(a.splits, MODE == kModeSubdots);
     const long long blocks = (a.n_items + warps - 1) / warps;
     const size_t smem = gemv_dyn_smem(warps, a.splits == 1, a.q8_bytes, a.stages, a.slot_bytes);
-    return launch_maybe_pdl(gemv_kernel<MODE>, dim3((unsigned)blocks), dim3(32 * warps), smem,
-                            a.pdl, st, a);
+    const dim3 grid((unsigned)blocks), block(32 * warps);
+    if (a.stages > 0) return launch_maybe_pdl(gemv_kernel<MODE, kKindRing>, grid, block, smem, a.pdl, st, a);
+    bool q5 = false;
+    for (int p = 0; p < a.nparts; ++p) q5 = q5 || a.part[p].fmt == 5;
+    if (MODE == kModeGemv && !q5)
+        return launch_maybe_pdl(gemv_kernel<MODE, kKindQ46>, grid, block, smem, a.pdl, st, a);
+    return launch_maybe_pdl(gemv_kernel<MODE, kKindAll>, grid, block, smem, a.pdl, st, a);
 }
 
 using KernelFn = void (*)(GemvLaunch);
-const KernelFn kAllKernels[] = {gemv_kernel<kModeGemv>, gemv_kernel<kModeSubdots>, gemv_kernel<kModeCover>};
+const KernelFn kAllKernels[] = {
+    gemv_kernel<kModeGemv, kKindQ46>,    gemv_kernel<kModeGemv, kKindAll>,
+    gemv_kernel<kModeGemv, kKindRing>,   gemv_kernel<kModeSubdots, kKindAll>,
+    gemv_kernel<kModeSubdots, kKindRing>, gemv_kernel<kModeCover, kKindAll>,
+    gemv_kernel<kModeCover, kKindRing>};
 
 }  // namespace
 
@@ -383,7 +406,7 @@ int gemv_ctas_per_sm(int warps_per_cta, size_t smem)
 {
     int blocks = 0;
     const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &blocks, gemv_kernel<kModeGemv>, 32 * warps_per_cta, smem);
+        &blocks, gemv_kernel<kModeGemv, kKindAll>, 32 * warps_per_cta, smem);  // the others: the same
     if (e != cudaSuccess) cuda_fail("GEMV occupancy", e);
     return e == cudaSuccess ? blocks : 0;
 }
