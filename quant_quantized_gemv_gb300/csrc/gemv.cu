@@ -74,6 +74,8 @@ using namespace gemv_detail;
 
 // Tile t of part P is finished for this warp (work item `item`, covering the
 // part's units [u0, u1)): write it, or combine it with the tile's other splits.
+// WS: the workspace combine (splits > kMaxCtaSplits) is compiled in.
+template <bool WS>
 __device__ __forceinline__ void flush_tile(const GemvLaunch &a, const GemvPart &P, int t,
                                            float (&acc)[8], int item, int u0, int u1, int lane)
 {
@@ -104,6 +106,7 @@ __device__ __forceinline__ void flush_tile(const GemvLaunch &a, const GemvPart &
         }
         return;
     }
+    if constexpr (!WS) return;  // the launch never gives this instance such a plan
     // more splits than a CTA holds: lane 0 publishes the 8 partials to the
     // workspace, fences them and takes a ticket (writer and ticket holder are
     // one thread); the last of the tile's splits adds them all
@@ -167,7 +170,7 @@ constexpr int kModeGemv = 0, kModeSubdots = 1, kModeCover = 2;
 // Stream the part's units [u0, u1) through one register buffer: compute a
 // chunk, issue the next chunk's loads into the same registers, then finish
 // the tile if the chunk was its last.
-template <int FMT, int MODE>
+template <int FMT, int MODE, bool WS = true>
 __device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P, uint8_t *smem,
                                           int item, int u0, int u1, int lane)
 {
@@ -199,7 +202,7 @@ __device__ __forceinline__ void run_range(const GemvLaunch &a, const GemvPart &P
             load_x(a, xs, xa, lane, A);
             if (++c == nch) { c = 0; ++t; }
         }
-        if (!SUBDOTS && (!more || xa.t != tcur)) flush_tile(a, P, tcur, acc, item, u0, u1, lane);
+        if (!SUBDOTS && (!more || xa.t != tcur)) flush_tile<WS>(a, P, tcur, acc, item, u0, u1, lane);
     }
 }
 
@@ -286,7 +289,7 @@ __device__ __forceinline__ void run_range_ring(const GemvLaunch &a, const GemvPa
             if (lane == 0) atomicAdd(a.cover + ((size_t)(P.tile0 + xc.t) * nch + xc.c), 1u);
         }
         compute<SUBDOTS>(a, P, A, xc, lane, acc);
-        if (!SUBDOTS && (u + 1 == u1 || x.t != xc.t)) flush_tile(a, P, xc.t, acc, item, u0, u1, lane);
+        if (!SUBDOTS && (u + 1 == u1 || x.t != xc.t)) flush_tile<true>(a, P, xc.t, acc, item, u0, u1, lane);
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");  // only empty groups remain
 }
@@ -313,13 +316,15 @@ __device__ __forceinline__ void run_ring(const GemvLaunch &a, const GemvPart &P,
 // Measured on the 14B sweep: 2.39 ms with one kernel for all formats
 // against 2.49 ms with a kernel per format set (qkv, o, down alternating).
 // Code a launch never runs still costs it on GB300, so the kernel comes in
-// three instances (KIND): q6_K and q4_K parts only, every format, and the
-// weight ring (every format; launched only when a.stages > 0).  With the
-// ring's code compiled into the default kernel the 14B sweep's GEMVs took
-// 2174 against 2114 us per step and its PDL step 2219 against 2178 us
-// (single shapes 1-2%); without the q5_K path as well the step took 2161
-// against 2171 us.  Every launch of the sweep uses the first instance, so
-// its chain never switches kernel functions.
+// three instances (KIND): q6_K and q4_K parts with at most kMaxCtaSplits
+// splits (no workspace combine), every format and plan, and the weight ring
+// (every format; launched only when a.stages > 0).  With the ring's code
+// compiled into the default kernel the 14B sweep's GEMVs took 2174 against
+// 2114 us per step and its PDL step 2219 against 2178 us (single shapes
+// 1-2%); without the q5_K path as well the step took 2161 against 2171 us;
+// without the workspace combine as well the GEMVs took 2105 against 2114 us
+// (5120 x 5120 q4_K 5.48 against 5.59 us).  Every launch of the sweep uses
+// the first instance, so its chain never switches kernel functions.
 constexpr int kKindQ46 = 0, kKindAll = 1, kKindRing = 2;
 template <int MODE, int KIND>
 __global__ void __maxnreg__(MODE == kModeSubdots ? 168 : kGemvMaxRegs)
@@ -361,9 +366,9 @@ __global__ void __maxnreg__(MODE == kModeSubdots ? 168 : kGemvMaxRegs)
             run_ring<4, MODE>(a, P, xs, item, u0, u1, lane);
     } else if constexpr (KIND == kKindQ46) {
         if (P.fmt == 6)
-            run_range<6, MODE>(a, P, xs, item, u0, u1, lane);
+            run_range<6, MODE, false>(a, P, xs, item, u0, u1, lane);
         else
-            run_range<4, MODE>(a, P, xs, item, u0, u1, lane);
+            run_range<4, MODE, false>(a, P, xs, item, u0, u1, lane);
     } else {
         if (P.fmt == 6)
             run_range<6, MODE>(a, P, xs, item, u0, u1, lane);
@@ -384,7 +389,7 @@ cudaError_t launch(const GemvLaunch &a, cudaStream_t st)
     if (a.stages > 0) return launch_maybe_pdl(gemv_kernel<MODE, kKindRing>, grid, block, smem, a.pdl, st, a);
     bool q5 = false;
     for (int p = 0; p < a.nparts; ++p) q5 = q5 || a.part[p].fmt == 5;
-    if (MODE == kModeGemv && !q5)
+    if (MODE == kModeGemv && !q5 && a.splits <= kMaxCtaSplits)
         return launch_maybe_pdl(gemv_kernel<MODE, kKindQ46>, grid, block, smem, a.pdl, st, a);
     return launch_maybe_pdl(gemv_kernel<MODE, kKindAll>, grid, block, smem, a.pdl, st, a);
 }
