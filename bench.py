@@ -633,6 +633,11 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     n_prod = sum(1 for o in wl.ops if o[0] in ("rms", "swiglu", "quant"))
     pt_graph = (capture(lambda: [wl.run(i, producers_only=True) for i in range(n_kt)], stream)
                 if n_prod else None)
+    # the same GEMV launches chained with PDL, as a decode step runs them (each
+    # still waits for its predecessor before it reads its plane or writes)
+    mq.mq_set_pdl(True)
+    kc_graph = kernel_graphs(wl, stream, n_kt) if args.pdl else None
+    mq.mq_set_pdl(False)
     # ---- the single-launch read floor of the same weight bytes (one-GEMV
     # workloads): a plain read of each step's weight copy, back to back
     floor_graph = None
@@ -688,6 +693,7 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     gemv_step_ms = float(np.median(kt)) / n_kt
     kind_ms = {k: float(np.median(replay_ms(g, stream))) / n_kt for k, g in kind_graphs.items()}
     prod_step_ms = float(np.median(replay_ms(pt_graph, stream))) / n_kt if pt_graph is not None else 0.0
+    kc = replay_ms(kc_graph, stream) if kc_graph is not None else None
     floor_ms = float(np.median(replay_ms(floor_graph, stream))) / n_kt if floor_graph is not None else None
 
     # ---- e2e: the public API, pinned host inputs in, result out, every step
@@ -822,11 +828,21 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     line["kernel_us"] = {"gemv_per_step_isolated": round(gemv_step_ms * 1e3, 3),
                          "gemv_spread": spread(kt, 1e3 / n_kt),
                          "producers_per_step_isolated": round(prod_step_ms * 1e3, 3),
+                         **({"gemv_per_step_pdl_chain": round(float(np.median(kc)) / n_kt * 1e3, 3),
+                             "gemv_pdl_chain_achieved_gbs": round(
+                                 alg / (float(np.median(kc)) / n_kt * 1e-3) / 1e9, 1),
+                             "gemv_pdl_chain_frac": round(
+                                 alg / (float(np.median(kc)) / n_kt * 1e-3) / 1e9 / peak, 4)}
+                            if kc is not None else {}),
                          "producer_launches_per_step": n_prod,
                          "step": round(ms_per_step * 1e3, 3),
                          "step_spread": spread([x / K for x in region_ms], 1e3),
                          "how": "GEMV launches alone and producer launches alone, each as a graph of "
-                                f"{n_kt} steps back to back with PDL off; step: the PDL chain of both"}
+                                f"{n_kt} steps back to back with PDL off; gemv_per_step_pdl_chain: the "
+                                "same GEMV launches with PDL on (each overlaps its ramp with the "
+                                "previous launch's tail and still waits for it before touching its "
+                                "plane or outputs), context beside roofline.frac, which uses the "
+                                "PDL-off time; step: the PDL chain of GEMVs and producers"}
     line["e2e"] = {"value": round(wl.weight_bytes / (e2e_ms * 1e-3) / 1e9 * ws_, 2), "unit": "GB/s",
                    "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
                    "d2h_bytes_per_step": int(d2h),
