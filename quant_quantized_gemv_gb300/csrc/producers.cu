@@ -150,7 +150,11 @@ __global__ void __launch_bounds__(kRmsThreads) rmsnorm_quant_q8_kernel(
 
     float ss = 0.0f;
     float4 own = make_float4(0.f, 0.f, 0.f, 0.f);  // x[first + tid], kept from the sum pass
-#pragma unroll 8
+    // unrolled by 2: each thread's 2-3 loads of a 5120-value row are in
+    // flight together, in less code than 8-fold unrolling (14B decode sweep
+    // 2153 -> 2126 us per step, layer_14b 18.97 -> 18.40 us; not unrolled:
+    // 2153 us).  The per-lane order of the sum is the same either way.
+#pragma unroll 2
     for (int i = tid; i < n4; i += kRmsThreads) {
         const float4 v = __ldcg(x4 + i);
         if (i == first + tid) own = v;
