@@ -389,8 +389,10 @@ cudaError_t launch(const GemvLaunch &a, cudaStream_t st)
     if (a.stages > 0) return launch_maybe_pdl(gemv_kernel<MODE, kKindRing>, grid, block, smem, a.pdl, st, a);
     bool q5 = false;
     for (int p = 0; p < a.nparts; ++p) q5 = q5 || a.part[p].fmt == 5;
-    if (MODE == kModeGemv && !q5 && a.splits <= kMaxCtaSplits)
-        return launch_maybe_pdl(gemv_kernel<MODE, kKindQ46>, grid, block, smem, a.pdl, st, a);
+    if constexpr (MODE == kModeGemv) {  // (no q6_K/q4_K instance of the other modes is built)
+        if (!q5 && a.splits <= kMaxCtaSplits)
+            return launch_maybe_pdl(gemv_kernel<MODE, kKindQ46>, grid, block, smem, a.pdl, st, a);
+    }
     return launch_maybe_pdl(gemv_kernel<MODE, kKindAll>, grid, block, smem, a.pdl, st, a);
 }
 

@@ -174,6 +174,8 @@ __global__ void __launch_bounds__(kRmsThreads) rmsnorm_quant_q8_kernel(
 
     // The slice loop's trip count is uniform across the CTA, so the
     // quantizer's shuffles always see full warps.
+    // one slice per CTA up to 64 CTAs (256 K values): not unrolled
+#pragma unroll 1
     for (int base = first; base < n4; base += gridDim.x * kRmsThreads) {
         const int i = base + tid;
         const bool valid = i < n4;
