@@ -169,43 +169,46 @@ struct OccEntry {
     size_t dyn;
     int ctas;
 };
-std::vector<OccEntry> g_occ[kMaxDevices];
+std::vector<OccEntry> g_occ[kMaxDevices][2];  // [device][lo]
+std::atomic<int> g_ctas_lo[kMaxDevices][kMaxCtaSplits + 1];
 std::mutex g_occ_mutex;
 
-int gemv_ctas(int dev, int w, size_t dyn)
+// lo: the grouped launches' instance (kGemvGroupRegs registers).
+int gemv_ctas(int dev, int w, size_t dyn, bool lo = false)
 {
+    auto query = [&](size_t d) { return lo ? gemv_ctas_per_sm_lo(w, d) : gemv_ctas_per_sm(w, d); };
     if (dyn == 0) {  // register limit only: lock-free cache
-        std::atomic<int> &slot = g_ctas[dev][w];
+        std::atomic<int> &slot = lo ? g_ctas_lo[dev][w] : g_ctas[dev][w];
         int v = slot.load(std::memory_order_relaxed);
         if (v <= 0) {
-            v = gemv_ctas_per_sm(w, 0);
+            v = query(0);
             if (v > 0) slot.store(v, std::memory_order_relaxed);
         }
         return v;
     }
     std::lock_guard<std::mutex> lock(g_occ_mutex);
-    for (const OccEntry &e : g_occ[dev])
+    for (const OccEntry &e : g_occ[dev][lo])
         if (e.w == w && e.dyn == dyn) return e.ctas;
-    const int v = gemv_ctas_per_sm(w, dyn);
-    if (v > 0) g_occ[dev].push_back(OccEntry{w, dyn, v});
+    const int v = query(dyn);
+    if (v > 0) g_occ[dev][lo].push_back(OccEntry{w, dyn, v});
     return v;
 }
 
 // CTAs per SM of the single-token GEMV: split CTAs of w warps hold their
 // warps' ring slots; whole-tile CTAs (kGemvWarpsPerBlock warps) also the
 // staged plane of `plane` bytes.
-bool device_occupancy(Occupancy *o, size_t plane, const Ring &ring)
+bool device_occupancy(Occupancy *o, size_t plane, const Ring &ring, bool lo = false)
 {
     const int dev = current_device();
     DeviceLimits lim;
     if (dev < 0 || !device_limits(&lim)) return false;
     for (int w = 1; w <= kMaxCtaSplits; ++w) {
-        const int v = gemv_ctas(dev, w, gemv_dyn_smem(w, false, plane, ring.stages, ring.slot));
+        const int v = gemv_ctas(dev, w, gemv_dyn_smem(w, false, plane, ring.stages, ring.slot), lo);
         if (v < 0) return false;
         o->ctas[w] = v;
     }
     o->ctas_tiles = gemv_ctas(dev, kGemvWarpsPerBlock,
-                              gemv_dyn_smem(kGemvWarpsPerBlock, true, plane, ring.stages, ring.slot));
+                              gemv_dyn_smem(kGemvWarpsPerBlock, true, plane, ring.stages, ring.slot), lo);
     return o->ctas_tiles > 0;
 }
 
@@ -446,12 +449,18 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
         if (!device_ring(fmts, nparts, plane, &ring)) return MQ_ERR_CUDA;
     }
     Plan pl;
+    bool lo = false;
     if (explicit_plan) {
         pl = *explicit_plan;
     } else {
         Occupancy o;
         if (!batch) {
-            if (!device_occupancy(&o, plane, ring)) return MQ_ERR_CUDA;
+            // a group of q6_K/q4_K parts without a ring runs the kernel's
+            // kGemvGroupRegs instance (gemv.cu), planned with its occupancy
+            bool q5 = false;
+            for (int p = 0; p < nparts; ++p) q5 = q5 || parts[p].fmt == 5;
+            lo = nparts >= 2 && !q5 && ring.stages == 0;
+            if (!device_occupancy(&o, plane, ring, lo)) return MQ_ERR_CUDA;
             pl = plan_for((int)total_tiles, nchunks, device_sms(), o);
         } else {
             if (!batch_occupancy(&o, nt, parts[0].fmt, (size_t)nt * plane, &wpc)) return MQ_ERR_CUDA;
@@ -496,6 +505,7 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
     a->pre = ring.pre;
     a->slot_bytes = (unsigned)ring.slot;
     a->ring_off = (unsigned)gemv_ring_off(pl.splits == 1, plane);
+    a->lo = lo ? 1 : 0;
     *need = batch ? 0 : ws_bytes_for(total_tiles, items, pl);  // small batch: splits meet in the CTA
     return MQ_OK;
 }

@@ -325,9 +325,21 @@ __device__ __forceinline__ void run_ring(const GemvLaunch &a, const GemvPart &P,
 // without the workspace combine as well the GEMVs took 2105 against 2114 us
 // (5120 x 5120 q4_K 5.48 against 5.59 us).  Every launch of the sweep uses
 // the first instance, so its chain never switches kernel functions.
-constexpr int kKindQ46 = 0, kKindAll = 1, kKindRing = 2;
+// A fourth instance (kKindQ46Lo), the first one compiled at kGemvGroupRegs
+// registers, serves grouped launches: 21 warps per SM let the 14B q/k/v group (896 tiles
+// of 5 chunks) run 3 splits per tile (at most 2 chunks per warp) in one
+// wave, and its CTAs become resident sooner behind the previous kernel of a
+// PDL chain.  The 14B sweep's PDL step took 2091.6 against 2115.9 us with
+// it (q/k/v 7.33 against 8.38 us); its GEMVs back to back 2099.7 against
+// 2093.6 us, the cost of switching kernel functions between q/k/v and the
+// other launches.  At 96 registers for every launch the single shapes were
+// slower (5120 x 5120 q4_K 5.90 against 5.60 us, the head 98.7 against
+// 95.8 us).
+constexpr int kKindQ46 = 0, kKindAll = 1, kKindRing = 2, kKindQ46Lo = 3;
 template <int MODE, int KIND>
-__global__ void __maxnreg__(MODE == kModeSubdots ? 168 : kGemvMaxRegs)
+__global__ void __maxnreg__(MODE == kModeSubdots ? 168
+                            : KIND == kKindQ46Lo ? kGemvGroupRegs
+                                                 : kGemvMaxRegs)
     gemv_kernel(const __grid_constant__ GemvLaunch a)
 {
     extern __shared__ __align__(16) uint8_t xs[];  // the q8 plane, staged per CTA
@@ -364,7 +376,7 @@ __global__ void __maxnreg__(MODE == kModeSubdots ? 168 : kGemvMaxRegs)
             run_ring<5, MODE>(a, P, xs, item, u0, u1, lane);
         else
             run_ring<4, MODE>(a, P, xs, item, u0, u1, lane);
-    } else if constexpr (KIND == kKindQ46) {
+    } else if constexpr (KIND == kKindQ46 || KIND == kKindQ46Lo) {
         if (P.fmt == 6)
             run_range<6, MODE, false>(a, P, xs, item, u0, u1, lane);
         else
@@ -390,6 +402,8 @@ cudaError_t launch(const GemvLaunch &a, cudaStream_t st)
     bool q5 = false;
     for (int p = 0; p < a.nparts; ++p) q5 = q5 || a.part[p].fmt == 5;
     if constexpr (MODE == kModeGemv) {  // (no q6_K/q4_K instance of the other modes is built)
+        if (!q5 && a.splits <= kMaxCtaSplits && a.lo)
+            return launch_maybe_pdl(gemv_kernel<MODE, kKindQ46Lo>, grid, block, smem, a.pdl, st, a);
         if (!q5 && a.splits <= kMaxCtaSplits)
             return launch_maybe_pdl(gemv_kernel<MODE, kKindQ46>, grid, block, smem, a.pdl, st, a);
     }
@@ -401,7 +415,7 @@ const KernelFn kAllKernels[] = {
     gemv_kernel<kModeGemv, kKindQ46>,    gemv_kernel<kModeGemv, kKindAll>,
     gemv_kernel<kModeGemv, kKindRing>,   gemv_kernel<kModeSubdots, kKindAll>,
     gemv_kernel<kModeSubdots, kKindRing>, gemv_kernel<kModeCover, kKindAll>,
-    gemv_kernel<kModeCover, kKindRing>};
+    gemv_kernel<kModeCover, kKindRing>,   gemv_kernel<kModeGemv, kKindQ46Lo>};
 
 }  // namespace
 
@@ -414,6 +428,15 @@ int gemv_ctas_per_sm(int warps_per_cta, size_t smem)
     int blocks = 0;
     const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         &blocks, gemv_kernel<kModeGemv, kKindAll>, 32 * warps_per_cta, smem);  // the others: the same
+    if (e != cudaSuccess) cuda_fail("GEMV occupancy", e);
+    return e == cudaSuccess ? blocks : 0;
+}
+
+int gemv_ctas_per_sm_lo(int warps_per_cta, size_t smem)
+{
+    int blocks = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &blocks, gemv_kernel<kModeGemv, kKindQ46Lo>, 32 * warps_per_cta, smem);
     if (e != cudaSuccess) cuda_fail("GEMV occupancy", e);
     return e == cudaSuccess ? blocks : 0;
 }

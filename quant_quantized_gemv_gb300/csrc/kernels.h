@@ -55,6 +55,9 @@ struct GemvLaunch {
     // wait.  stages == 0: chunks go straight to registers.
     int stages, pre;
     unsigned slot_bytes, ring_off;
+    // grouped launches (q6_K/q4_K parts, default plan, no ring): the
+    // kGemvGroupRegs instance, planned with its own occupancy
+    int lo;
 };
 
 cudaError_t launch_gemv(const GemvLaunch &a, cudaStream_t st);
@@ -93,6 +96,9 @@ size_t gemv_f32_max_x_bytes();  // largest row it stages; opts the kernel in
 
 constexpr int kGemvWarpsPerBlock = 4;   // CTA of independent warps
 constexpr int kGemvMaxRegs = 128;       // single-token GEMV registers per thread: 16 warps per SM
+constexpr int kGemvGroupRegs = 96;      // its grouped launches' instance: 21 warps per SM
+// Resident CTAs per SM of that instance (0 on error).
+int gemv_ctas_per_sm_lo(int warps_per_cta, size_t smem);
 constexpr int kMaxCtaSplits = 12;       // largest CTA whose warps are one tile's splits
 constexpr int kGemvStaticSmem = kMaxCtaSplits * 8 * 4;  // the split-combine buffer
 constexpr int kMaxTokens = 8;           // activation rows of the small-batch GEMV
