@@ -352,3 +352,36 @@ def test_read_floor_runs(mq):
     torch.cuda.synchronize()
     with pytest.raises(mq.MQError):
         mq.mq_read_floor(buf, 4095)
+
+
+def test_group_instance_matches_the_standard_instance(mq, orc):
+    """A default-plan grouped launch of q6_K/q4_K parts runs the kernel's
+    grouped-launch instance (fewer registers, its own occupancy); explicit
+    plans run the standard instance.  Both compute the same sub-dots in the
+    same order, so the default launch must equal, bit for bit, the explicit
+    launch of whichever plan it chose -- here on the 14B q, k, v shapes."""
+    import torch
+    g = synth.rng("group-instance")
+    cols = 5120
+    spec = [("q4k", 5120), ("q4k", 1024), ("q6k", 1024)]
+    Ws = [synth.blocks(f, g, r, cols) for f, r in spec]
+    parts = [(f, repack_dev(mq, f, W, r, cols), r) for (f, r), W in zip(spec, Ws)]
+    x = synth.normal(g, cols)
+    plane = mq.mq_quantize_q8(dev(x))
+    ys = mq.mq_gemv_group_q8(parts, plane, cols, ws=mq.mq_gemv_group_workspace(parts, cols))
+    got = [host(y) for y in ys]
+    nch = cols // 256 // 4
+    plans = [(s, -(-nch // s), 1) for s in range(2, nch + 1)
+             if (s - 1) * -(-nch // s) < nch]  # no empty split
+    plans += [(1, nch, t) for t in (1, 2, 3, 4)]
+    matches = []
+    for plan in plans:
+        ws = mq.mq_gemv_group_workspace(parts, cols, plan=plan)
+        ref = [host(y) for y in mq.mq_gemv_group_q8(parts, plane, cols, ws=ws, plan=plan)]
+        if all(np.array_equal(a, b) for a, b in zip(got, ref)):
+            matches.append(plan)
+    assert matches, "the default grouped launch matches no explicit plan bit for bit"
+    d, q, _ = orc.quantize_q8(x)
+    for (f, r), W, y in zip(spec, Ws, got):
+        yref, absum = orc.gemv(f, W, d, q, r, cols, threads=len(os.sched_getaffinity(0)))
+        assert_gemv_close(y, yref, absum)
