@@ -164,11 +164,13 @@ def measured_peak_gbs():
         return 6800.0, "fallback"
 
 
-def gemv_source_hash(act: str = "q8", gateup: bool = False) -> str:
+def gemv_source_hash(act: str = "q8", gateup: bool = False, batch: bool = False) -> str:
     """First 16 hex digits of the SHA-256 of the GEMV kernel sources (with
-    the gate||up kernel when the workload launches it)."""
+    the gate||up kernel when the workload launches it; the small-batch
+    kernel's for nt > 1 tokens)."""
     h = hashlib.sha256()
-    files = ["gemv_f32.cu" if act == "f32" else "gemv.cu", "gemv_common.cuh", "layout.h"]
+    main = "gemv_f32.cu" if act == "f32" else "gemv_batch.cu" if batch else "gemv.cu"
+    files = [main, "gemv_common.cuh", "layout.h"]
     if gateup:
         files.append("gemv_gateup.cu")
     for f in files:
@@ -177,18 +179,21 @@ def gemv_source_hash(act: str = "q8", gateup: bool = False) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str, act: str = "q8", gateup: bool = False):
+def profiled_traffic(workload: str, act: str = "q8", gateup: bool = False, tokens: int = 1):
     """DRAM bytes (read + write) of the GEMV launches of one step, from the
     committed ncu summary of this workload, if it was taken on the current
     kernel source (else None).  A one-GEMV workload's summary gives them per
-    launch (= per step)."""
-    p = os.path.join(ROOT, "profiles", f"gemv_{'f32_' if act == 'f32' else ''}{workload}.md")
+    launch (= per step); the small-batch summary per launch and token count
+    (traffic_bytes_per_launch_nt<N>)."""
+    prefix = "f32_" if act == "f32" else "batch_" if tokens > 1 else ""
+    p = os.path.join(ROOT, "profiles", f"gemv_{prefix}{workload}.md")
     if not os.path.exists(p):
         return None
     txt = open(p).read()
-    m = re.search(r"traffic_bytes_per_(?:launch|step):\s*([0-9.eE+]+)", txt)
+    key = f"traffic_bytes_per_launch_nt{tokens}" if tokens > 1 else r"traffic_bytes_per_(?:launch|step)"
+    m = re.search(key + r":\s*([0-9.eE+]+)", txt)
     h = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
-    if not m or not h or h.group(1) != gemv_source_hash(act, gateup):
+    if not m or not h or h.group(1) != gemv_source_hash(act, gateup, tokens > 1):
         return None
     return float(m.group(1))
 
@@ -791,7 +796,7 @@ def bench_mq(args, ws_, rank, local) -> dict | None:
     }
     alg = float(sum(wl.gemv_bytes))
     achieved = alg / (gemv_step_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(args.workload, args.act, "gateup" in kinds) if args.tokens == 1 else None
+    traffic = profiled_traffic(args.workload, args.act, "gateup" in kinds, args.tokens)
     line["roofline"] = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                         "unit": "GB/s", "frac": round(achieved / peak, 4),
                         "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",

@@ -62,3 +62,32 @@ def test_spread_reports_median_and_range():
     import bench
     s = bench.spread([3.0, 1.0, 2.0, 5.0, 4.0], 10.0, 1)
     assert s == {"median": 30.0, "min": 10.0, "max": 50.0, "n": 5}
+
+
+def test_profiled_traffic_matches_kernel_source_and_token_count(tmp_path, monkeypatch):
+    """roofline.traffic comes from a committed summary only when its source
+    hash is the current one of the kernel the line times: gemv.cu for one
+    token, gemv_batch.cu for nt > 1 (per token count), gemv_f32.cu for f32."""
+    import os
+    import shutil
+    import bench
+    csrc = tmp_path / "quant_quantized_gemv_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in ("gemv.cu", "gemv_batch.cu", "gemv_f32.cu", "gemv_common.cuh", "layout.h", "gemv_gateup.cu"):
+        shutil.copy(os.path.join(bench.ROOT, "quant_quantized_gemv_gb300", "csrc", f), csrc / f)
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    one, batch, f32 = bench.gemv_source_hash(), bench.gemv_source_hash(batch=True), bench.gemv_source_hash("f32")
+    assert len({one, batch, f32}) == 3
+    (tmp_path / "profiles" / "gemv_w.md").write_text(f"source_sha256_16: {one}\ntraffic_bytes_per_launch: 100\n")
+    (tmp_path / "profiles" / "gemv_batch_w.md").write_text(
+        f"source_sha256_16: {batch}\ntraffic_bytes_per_launch_nt2: 200\ntraffic_bytes_per_launch_nt4: 400\n")
+    (tmp_path / "profiles" / "gemv_f32_w.md").write_text(f"source_sha256_16: {one}\ntraffic_bytes_per_launch: 300\n")
+    assert bench.profiled_traffic("w") == 100
+    assert bench.profiled_traffic("w", tokens=2) == 200 and bench.profiled_traffic("w", tokens=4) == 400
+    assert bench.profiled_traffic("w", tokens=8) is None                 # no capture at that count
+    assert bench.profiled_traffic("w", "f32") is None                    # taken on another kernel's source
+    assert bench.profiled_traffic("w", gateup=True) is None              # the source set differs
+    (csrc / "gemv_batch.cu").write_text("// changed\n")
+    assert bench.profiled_traffic("w", tokens=2) is None                 # kernel changed since the capture
+    assert bench.profiled_traffic("w") == 100
