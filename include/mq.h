@@ -178,6 +178,10 @@ int mq_swiglu_quant_q8(const float *g, const float *u, float *y, void *q8, int n
  * only when that still leaves the wave less than half full (very few tiles,
  * rows longer than 12 chunks).
  *
+ * Whole-tile CTAs stage the q8 plane in shared memory, so for every plan
+ * mq_q8_bytes(cols) rounded up to 128 bytes must fit one CTA's opt-in shared
+ * memory less 1 KiB (cols <= 194816 on GB300), else MQ_ERR_SHAPE.
+ *
  * mq_gemv_workspace_bytes(rows, cols): workspace the default plans (q6_K,
  *   q4_K and q5_K) need on the current device (0 unless splits > 12).  ws must be
  *   device memory, zero-filled before its first use; every completed call
@@ -319,7 +323,8 @@ int mq_gemv_group_q8_plan(const mq_gemv_part *parts, int nparts, const void *q8,
  *   from token 0 of an nt >= 2 call (another f32 reduction order).
  *   Every CTA stages all nt planes in shared memory: nt * mq_q8_bytes(cols)
  *   must not exceed the device's per-CTA limit less 8 KiB (about 219 KiB on
- *   GB300, i.e. cols <= 26368 at nt = 8), else MQ_ERR_SHAPE.
+ *   GB300, i.e. cols <= 23552 at nt = 8 and 188672 at nt = 1), else
+ *   MQ_ERR_SHAPE.
  * Plans read differently from the single-token ones: splits S
  * (1..12) cuts every row into S ranges of chunks_per_split chunks (coverage
  * checked as above, no empty range); a CTA holds S warps for each of B / S

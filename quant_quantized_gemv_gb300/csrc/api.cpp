@@ -437,8 +437,10 @@ int prepare_group(const Part *parts, int nparts, const void *q8, int cols, const
     if (!sizes_only) {
         DeviceLimits lim;
         if (!device_limits(&lim)) return MQ_ERR_CUDA;
-        // the plane(s) must fit in shared memory
-        if (!batch ? plane > lim.max_plane : (size_t)nt * plane > lim.max_batch_planes)
+        // the plane(s) must fit in shared memory (a whole-tile CTA stages its
+        // plane rounded up to 128 bytes)
+        if (!batch ? gemv_dyn_smem(kGemvWarpsPerBlock, true, plane, 0, 0) > lim.max_plane
+                   : (size_t)nt * plane > lim.max_batch_planes)
             return MQ_ERR_SHAPE;
         if (batch && (wpc = batch_budget(nt, parts[0].fmt)) < 1) return MQ_ERR_CUDA;
     }

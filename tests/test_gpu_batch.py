@@ -241,6 +241,34 @@ def test_planes_too_large_for_shared_memory(mq):
     assert e.value.status == mq.MQ_ERR_SHAPE
 
 
+@pytest.mark.parametrize("fmt,nt", [("q6k", 8), ("q4k", 2), ("q5k", 5)])
+def test_widest_row_the_staged_planes_allow(mq, orc, fmt, nt):
+    """Maximum size: the widest row whose nt q8 planes every CTA still stages,
+    in the opt-in shared memory less 8 KiB (23552 values at 8 tokens on
+    GB300).  Every row of every token against the oracle; one super-block
+    wider is refused before anything runs (y untouched)."""
+    import torch
+    optin = getattr(torch.cuda.get_device_properties(0), "shared_memory_per_block_optin", 0)
+    if not optin:
+        pytest.skip("the device's opt-in shared memory per block is not reported")
+    limit = (optin - 8192) & ~15
+    cols = 256
+    while nt * mq.mq_q8_bytes(cols + 256) <= limit:
+        cols += 256
+    rows = 19                                            # 3 tiles, the last ragged
+    W, Wp, x = make(mq, fmt, rows, cols, nt, 6)
+    planes = mq.mq_quantize_q8_batch(dev(x))
+    fn = batch_fn(mq, fmt)
+    y = host(fn(Wp, planes, nt, rows, cols))
+    yref, absum = oracle_rows(orc, fmt, W, rows, cols, planes_fields(mq, planes, cols, nt))
+    assert_close(y, yref, absum)
+    yw = torch.full((nt, rows), 7.0, device="cuda")
+    with pytest.raises(mq.MQError) as e:
+        fn(Wp, planes, nt, rows, cols + 256, y=yw)
+    assert e.value.status == mq.MQ_ERR_SHAPE
+    assert bool((yw == 7.0).all())
+
+
 FULL = [("ffn_down_7b", "q6k", 3584, 18944, "swiglu", 4),
         ("ffn_down_7b", "q6k", 3584, 18944, "swiglu", 7),
         ("ffn_down_7b", "q6k", 3584, 18944, "swiglu", 8),

@@ -174,6 +174,49 @@ def test_gemv_matches_oracle(mq, orc, fmt, rows, cols):
     assert_gemv_close(y, yref, absum)
 
 
+def widest_cols(reserve, staged_bytes):
+    """The widest row (a multiple of 256 values) whose staged shared memory,
+    staged_bytes(cols), fits one CTA's opt-in shared memory less `reserve`
+    bytes (rounded down to 16, as the library rounds it)."""
+    import torch
+    optin = getattr(torch.cuda.get_device_properties(0), "shared_memory_per_block_optin", 0)
+    if not optin:
+        pytest.skip("the device's opt-in shared memory per block is not reported")
+    limit = (optin - reserve) & ~15
+    cols = 256
+    while staged_bytes(cols + 256) <= limit:
+        cols += 256
+    return cols
+
+
+@pytest.mark.parametrize("fmt", ["q6k", "q4k"])
+def test_widest_row_the_staged_plane_allows(mq, orc, fmt):
+    """Maximum size: the widest row whose q8 plane (rounded up to 128 bytes)
+    a whole-tile CTA still stages, in the opt-in shared memory less 1 KiB
+    (194816 values on GB300).  The default plan (workspace splits for 2
+    tiles) and an explicit whole-tile plan, every row against the oracle;
+    one super-block wider is refused before anything runs (y untouched)."""
+    import torch
+    cols = widest_cols(1024, lambda c: (mq.mq_q8_bytes(c) + 127) & ~127)
+    rows = 11                                            # 2 tiles, the second ragged
+    g = synth.rng("widest", fmt, cols)
+    W = synth.blocks(fmt, g, rows, cols)
+    x = special_activation(cols, "widest")
+    Wp = repack_dev(mq, fmt, W, rows, cols)
+    plane = mq.mq_quantize_q8(dev(x))
+    d0, q0, _ = orc.quantize_q8(x)
+    yref, absum = orc.gemv(fmt, W, d0, q0, rows, cols, threads=8)
+    nch = -(-(cols // 256) // 4)
+    for plan in (None, (1, nch, 1)):
+        assert_gemv_close(host(gemv(mq, fmt, Wp, plane, rows, cols, plan=plan)), yref, absum)
+    y = torch.full((rows,), 7.0, device="cuda")
+    for plan in (None, (1, -(-((cols + 256) // 256) // 4), 1)):
+        with pytest.raises(mq.MQError) as e:
+            mq.mq_gemv(fmt, Wp, plane, rows, cols + 256, y=y, plan=plan)
+        assert e.value.status == mq.MQ_ERR_SHAPE
+    assert bool((y == 7.0).all())
+
+
 def all_plans(ntiles, nch):
     plans = []
     for s in range(2, nch + 1):
