@@ -194,6 +194,33 @@ def test_validation_rejects_before_launch(mq):
     assert mq.mq_repacked_bytes_q6k(8, 1000) == 0
 
 
+def test_empty_and_negative_sizes_are_shape_errors(mq):
+    """Empty inputs (no rows, no columns, no values, no tokens) and negative
+    sizes are refused with MQ_ERR_SHAPE before anything runs; sizes of
+    empty buffers are 0."""
+    L = mq.lib()
+    A, B, Y = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30000)
+    N = S = ctypes.c_void_p(0)
+    E = mq.MQ_ERR_SHAPE
+    for rows, cols in ((8, 0), (0, 256), (8, -256), (-8, 256)):
+        assert L.mq_gemv_q6k_q8(A, B, Y, rows, cols, N, 0, S) == E
+        assert L.mq_gemv_q4k_q8(A, B, Y, rows, cols, N, 0, S) == E
+        assert L.mq_gemv_q5k_q8(A, B, Y, rows, cols, N, 0, S) == E
+        assert L.mq_gemv_q6k_f32(A, A, Y, rows, cols, S) == E
+        assert L.mq_gemv_q6k_q8_batch(A, B, 2, Y, rows, cols, S) == E
+        assert L.mq_gemv_gateup_swiglu_q8(4, A, A, B, rows, cols, Y, B, S) == E
+    for n in (0, -32):
+        assert L.mq_quantize_q8(A, B, n, S) == E
+        assert L.mq_rmsnorm_quant_q8(A, A, ctypes.c_float(1e-6), Y, B, n, S) == E
+        assert L.mq_swiglu_quant_q8(A, A, Y, B, n, S) == E
+        assert L.mq_quantize_q8_batch(A, B, n, 2, S) == E
+    for nt in (0, -1, mq.MQ_MAX_TOKENS + 1):
+        assert L.mq_gemv_q6k_q8_batch(A, B, nt, Y, 8, 256, S) == E
+        assert L.mq_quantize_q8_batch(A, B, 256, nt, S) == E
+    assert mq.mq_q8_bytes(0) == 0
+    assert mq.mq_repacked_bytes_q6k(0, 256) == 0 and mq.mq_repacked_bytes_q4k(8, 0) == 0
+
+
 def test_binding_refuses_cpu_tensors(mq):
     import torch
     with pytest.raises(TypeError):
