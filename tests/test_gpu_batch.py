@@ -186,6 +186,24 @@ def test_batch_every_plan_agrees_and_is_deterministic(mq, orc, fmt, nt):
         assert_close(y1, yref, absum)
 
 
+@pytest.mark.parametrize("fmt", ["q6k", "q4k", "q5k"])
+@pytest.mark.parametrize("nt", [3, 8])
+def test_batch_zero_token_gives_exact_zeros(mq, orc, fmt, nt):
+    """A degenerate token (an all-zero activation row: every q8 block d = 0,
+    q = 0, sum = 0) among ordinary ones: its outputs are 0.0 exactly, the
+    other tokens' are within the bar of the oracle."""
+    rows, cols = 37, 4608
+    W, Wp, x = make(mq, fmt, rows, cols, nt, 7)
+    z = nt // 2
+    x[z] = 0.0
+    planes = mq.mq_quantize_q8_batch(dev(x))
+    y = host(batch_fn(mq, fmt)(Wp, planes, nt, rows, cols))
+    assert np.array_equal(y[z], np.zeros(rows, np.float32))
+    yref, absum = oracle_rows(orc, fmt, W, rows, cols, planes_fields(mq, planes, cols, nt))
+    keep = [t for t in range(nt) if t != z]
+    assert_close(y[keep], yref[keep], absum[keep])
+
+
 def test_batch_bad_plans_refused(mq):
     import torch
     rows, cols, nt = 16, 4096, 2                  # 4 chunks

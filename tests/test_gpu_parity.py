@@ -217,6 +217,31 @@ def test_widest_row_the_staged_plane_allows(mq, orc, fmt):
     assert bool((y == 7.0).all())
 
 
+@pytest.mark.parametrize("fmt", ["q6k", "q4k", "q5k"])
+def test_zero_activation_or_zero_scales_give_exact_zeros(mq, fmt):
+    """Degenerate cases with an exact answer: an all-zero activation row
+    (every q8 block d = 0, q = 0, sum = 0) and weights whose fp16 scales d
+    (and dmin) are all zero give y == 0.0 exactly, under the default plan, a
+    CTA-split plan and a workspace-split plan."""
+    import torch
+    rows, cols = 37, 18944                                   # 5 tiles (ragged) x 19 chunks
+    g = synth.rng("zeros", fmt)
+    W = synth.blocks(fmt, g, rows, cols)
+    x = synth.normal(g, cols)
+    bb = {"q6k": 210, "q4k": 144, "q5k": 176}[fmt]
+    Wz = W.copy().reshape(rows, cols // 256, bb)
+    if fmt == "q6k":
+        Wz[:, :, 208:210] = 0                                # d (fp16) is the last field
+    else:
+        Wz[:, :, 0:4] = 0                                    # d and dmin lead the block
+    cases = [(repack_dev(mq, fmt, W, rows, cols), mq.mq_quantize_q8(dev(np.zeros(cols, np.float32)))),
+             (repack_dev(mq, fmt, Wz.reshape(W.shape), rows, cols), mq.mq_quantize_q8(dev(x)))]
+    for Wp, plane in cases:
+        for plan in (None, (4, 5, 1), (19, 1, 1)):
+            y = host(gemv(mq, fmt, Wp, plane, rows, cols, plan=plan))
+            assert np.array_equal(y, np.zeros(rows, np.float32)), plan
+
+
 def all_plans(ntiles, nch):
     plans = []
     for s in range(2, nch + 1):
