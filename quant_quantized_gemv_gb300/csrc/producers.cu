@@ -121,13 +121,16 @@ __global__ void __launch_bounds__(256) swiglu_quant_q8_kernel(const float *g, co
 // per-warp partials added in warp order by every thread -- so all CTAs get
 // the same bits.  scale = 1/sqrt(ss/n + eps) (IEEE sqrt and division), then
 // each CTA writes y = (x * scale) * gain and its q8 blocks for its own slice.
-// 512 threads: the sum pass of a 13824-value row is one round of loads per
-// thread (14B decode sweep 2.234 ms per step, against 2.298 ms with 256
-// threads and 2.227 ms with 1024, which is slower on the single-layer
-// chains: rms -> gate||up -> down 28.85 against 28.58 us).
+// 512 threads (14B decode sweep 2.234 ms per step, against 2.298 ms with
+// 256 threads and 2.227 ms with 1024, which is slower on the single-layer
+// chains: rms -> gate||up -> down 28.85 against 28.58 us).  K: the float4
+// groups per thread loaded before the sum chain starts (4 for rows up to
+// 8192 values, else 8), so that a thread's loads are one round trip, not
+// one per pair of groups.
 constexpr int kRmsThreads = 512;
 constexpr int kRmsMaxCtas = 64;
 
+template <int K>
 __global__ void __launch_bounds__(kRmsThreads) rmsnorm_quant_q8_kernel(
     const float *__restrict__ x, const float *__restrict__ gain, float eps, float *__restrict__ y,
     uint8_t *__restrict__ q8, int n, unsigned stride, unsigned d_off, unsigned sum_off)
@@ -150,12 +153,30 @@ __global__ void __launch_bounds__(kRmsThreads) rmsnorm_quant_q8_kernel(
 
     float ss = 0.0f;
     float4 own = make_float4(0.f, 0.f, 0.f, 0.f);  // x[first + tid], kept from the sum pass
-    // unrolled by 2: each thread's 2-3 loads of a 5120-value row are in
-    // flight together, in less code than 8-fold unrolling (14B decode sweep
-    // 2153 -> 2126 us per step, layer_14b 18.97 -> 18.40 us; not unrolled:
-    // 2153 us).  The per-lane order of the sum is the same either way.
+    // The thread's first K groups are all requested before the first fmaf:
+    // with the loop below alone (2-fold unrolled), the third group of a
+    // 5120-value row waited for the first two's arithmetic, a second round
+    // trip (14B decode sweep 2092.8 -> 2061.4 us per step, same bits).  A
+    // group past the row adds fmaf(0, 0, ss) = ss, which leaves the bits
+    // unchanged, so the per-lane order and result are the loop's.
+    {
+        float4 v[K];
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int i = tid + k * kRmsThreads;
+            v[k] = i < n4 ? __ldcg(x4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            if (k * kRmsThreads == first) own = v[k];
+            ss = fmaf(v[k].x, v[k].x, ss);
+            ss = fmaf(v[k].y, v[k].y, ss);
+            ss = fmaf(v[k].z, v[k].z, ss);
+            ss = fmaf(v[k].w, v[k].w, ss);
+        }
+    }
 #pragma unroll 2
-    for (int i = tid; i < n4; i += kRmsThreads) {
+    for (int i = tid + K * kRmsThreads; i < n4; i += kRmsThreads) {
         const float4 v = __ldcg(x4 + i);
         if (i == first + tid) own = v;
         ss = fmaf(v.x, v.x, ss);
@@ -222,8 +243,9 @@ cudaError_t launch_rmsnorm_quant_q8(const float *x, const float *gain, float eps
                                     unsigned sum_off, int pdl, cudaStream_t st)
 {
     const unsigned ctas = std::min(blocks_for(n / 4, kRmsThreads), (unsigned)kRmsMaxCtas);
-    return launch_maybe_pdl(rmsnorm_quant_q8_kernel, dim3(ctas, (unsigned)rows), dim3(kRmsThreads),
-                            0, pdl, st, x, gain, eps, y, q8, n, stride, d_off, sum_off);
+    const auto kernel = n / 4 <= 4 * kRmsThreads ? rmsnorm_quant_q8_kernel<4> : rmsnorm_quant_q8_kernel<8>;
+    return launch_maybe_pdl(kernel, dim3(ctas, (unsigned)rows), dim3(kRmsThreads), 0, pdl, st, x, gain,
+                            eps, y, q8, n, stride, d_off, sum_off);
 }
 
 }  // namespace mq
