@@ -156,8 +156,8 @@ __device__ __forceinline__ const uint8_t *stage_plane(const GemvLaunch &a, uint8
     const uint4 *src = reinterpret_cast<const uint4 *>(a.q8);
     uint4 *dst = reinterpret_cast<uint4 *>(xs);
     const int n16 = (int)(a.q8_bytes >> 4);
-#pragma unroll 4
-    for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = __ldcg(src + i);
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) copy16_async(dst + i, src + i);
+    copy_async_wait_all();
     asm volatile("bar.sync 1, %0;" ::"r"(blockDim.x) : "memory");
     return xs;
 }

@@ -306,11 +306,10 @@ __device__ __forceinline__ void stage_planes(const GemvLaunch &a, uint8_t *xs)
     const uint4 *src = reinterpret_cast<const uint4 *>(a.q8);
     uint4 *dst = reinterpret_cast<uint4 *>(xs);
     const int per = (int)(a.q8_bytes >> 4), stride = (int)(a.q8_stride >> 4);
-    for (int t = 0; t < a.nt; ++t) {
-#pragma unroll 4
+    for (int t = 0; t < a.nt; ++t)
         for (int i = threadIdx.x; i < per; i += blockDim.x)
-            dst[(size_t)t * per + i] = __ldcg(src + (size_t)t * stride + i);
-    }
+            copy16_async(dst + (size_t)t * per + i, src + (size_t)t * stride + i);
+    copy_async_wait_all();
     asm volatile("bar.sync 1, %0;" ::"r"(blockDim.x) : "memory");
 }
 

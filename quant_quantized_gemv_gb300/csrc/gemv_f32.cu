@@ -55,11 +55,11 @@ __device__ __forceinline__ void stage_x(const GemvLaunch &a, uint4 *xs)
     griddep_wait();
     const uint4 *src = reinterpret_cast<const uint4 *>(a.q8);
     const int n16 = (int)(a.q8_bytes >> 4);
-#pragma unroll 4
     for (int i = threadIdx.x; i < n16; i += blockDim.x) {
         const int U = i >> 3;
-        xs[(i & ~7) | ((i ^ U) & 7)] = __ldcg(src + i);
+        copy16_async(xs + ((i & ~7) | ((i ^ U) & 7)), src + i);
     }
+    copy_async_wait_all();
     asm volatile("bar.sync 1, %0;" ::"r"(blockDim.x) : "memory");
 }
 

@@ -46,8 +46,8 @@ __device__ __forceinline__ void stage(const GemvLaunch &a, uint8_t *xs)
     // 2-fold: a 5120-value plane is ~3 copies per thread (unrolled 4-fold the
     // 14B decode sweep took 2120 against 2109 us per step, with the rms write
     // loop below not unrolled)
-#pragma unroll 2
-    for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = __ldcg(src + i);
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) copy16_async(dst + i, src + i);
+    copy_async_wait_all();
     asm volatile("bar.sync 1, %0;" ::"r"(blockDim.x) : "memory");
 }
 
