@@ -107,17 +107,21 @@ constexpr int kBatchMaxCtaWarps = 16;   // most warps of a CTA (a whole SM at 12
 constexpr int kBatchStaticSmem = 2 * kBatchMaxCtaSplits * kMaxTokens * 8 * 4;  // split exchange (max)
 
 // Register cap of the small-batch kernel for nt tokens of format fmt: for
-// q6_K and q5_K the smallest that compiles without spilling (at most a few
-// bytes), so that as many warps as possible fit an SM; one token keeps two
-// weight buffers and 5..8 tokens need the full 168.  q4_K keeps 168 (12
+// q6_K and q5_K the smallest that compiles without spilling, so that as
+// many warps as possible fit an SM; one token keeps two weight buffers and
+// 5..8 tokens take 168.  At 5 tokens 168 still spills (q6_K 164 bytes,
+// q5_K 16), but 176 or 184 registers (11 warps) measured far slower (7B
+// 22.4 -> 28.8 us).  3 tokens of q6_K spilled 24 bytes at 136 and are
+// faster spill-free at 144 with a warp less (head 108.9 -> 103.0 us), 4 of
+// q5_K spilled 8 at 152 (22.59 -> 22.44 us at 160).  q4_K keeps 168 (12
 // warps): more warps measured slower there (14B gate at 2 tokens 13.2
 // against 12.6 us).
 __host__ __device__ constexpr int batch_reg_cap(int nt, int fmt)
 {
     return fmt == 4 ? 168
          : nt == 2 ? 128
-         : nt == 3 ? 136
-         : nt == 4 ? (fmt == 6 ? 168 : 152)
+         : nt == 3 ? (fmt == 6 ? 144 : 136)
+         : nt == 4 ? (fmt == 6 ? 168 : 160)
          : 168;
 }
 // Most warps a CTA can hold at that cap (at most 16): sizes the kernel's
