@@ -54,9 +54,10 @@
 //     issued before griddepcontrol.wait, so the weight stream starts while
 //     the preceding kernel (the q8 producer) drains; the q8 plane, the
 //     output and the workspace are touched only after the wait.  The plane
-//     is read with ld.global.cg, never the non-coherent path: the compiler
-//     treats non-coherent loads as invariant and may hoist them above the
-//     wait, and under PDL the plane is still being written then.
+//     is read through L2 (ld.global.cg, or cp.async.cg copies into shared
+//     memory), never the non-coherent path: the compiler treats
+//     non-coherent loads as invariant and may hoist them above the wait,
+//     and under PDL the plane is still being written then.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -143,8 +144,8 @@ __device__ __forceinline__ void flush_tile(const GemvLaunch &a, const GemvPart &
 }
 
 // Wait for the producer.  Whole-tile plans (splits == 1) then copy the whole
-// q8 plane into shared memory once per CTA (coalesced 16-byte coherent
-// loads) and meet at named barrier 1: every warp of such a CTA calls this
+// q8 plane into shared memory once per CTA (16-byte cp.async copies through
+// L2, all in flight at once) and meet at named barrier 1: every warp of such a CTA calls this
 // exactly once, from whichever code path it is on (a named barrier counts
 // arrivals, not call sites).  Returns where the activation is read from:
 // the shared copy, or null for the global plane (split plans, whose CTAs

@@ -298,8 +298,10 @@ __device__ __forceinline__ void flush_tile(const GemvLaunch &a, const GemvPart &
 }
 
 // Wait for the producer, then stage the nt q8 planes in shared memory
-// (coalesced coherent 16-byte loads) and meet at named barrier 1.  Every
-// warp of the CTA calls this exactly once.
+// (16-byte cp.async copies through L2, every copy of a thread in flight at
+// once: one round trip, where a token at a time took nt; 7B at 4 tokens
+// 18.47 -> 16.17 us) and meet at named barrier 1.  Every warp of the CTA
+// calls this exactly once.
 __device__ __forceinline__ void stage_planes(const GemvLaunch &a, uint8_t *xs)
 {
     griddep_wait();

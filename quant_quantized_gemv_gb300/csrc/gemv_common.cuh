@@ -110,22 +110,22 @@ __device__ __forceinline__ float half_hi(uint32_t w)
     return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
 }
 
-// Sum of the 16 int8 codes in v.
-// Staging of q8 planes into shared memory: 16-byte asynchronous copies
-// through L2 (cp.async.cg, coherent with what the preceding kernel wrote
-// before its completion released the grid-dependency wait), all of a
-// thread's copies in flight at once with no registers held; then the thread
-// waits for its own copies, and a CTA barrier publishes them to the others.
+// Staging of q8 planes (and the f32 row) into shared memory: 16-byte
+// asynchronous copies through L2 (cp.async.cg: coherent with what the
+// preceding kernel wrote before its completion released the grid-dependency
+// wait), all of a thread's copies in flight at once with no registers held;
+// then the thread waits for its own copies, and a CTA barrier publishes them
+// to the others.
 __device__ __forceinline__ void copy16_async(void *smem_dst, const void *gmem_src)
 {
-    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+    cp_async16(smem_addr(smem_dst), static_cast<const uint8_t *>(gmem_src));
 }
 __device__ __forceinline__ void copy_async_wait_all()
 {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// Sum of the 16 int8 codes in v.
 __device__ __forceinline__ int sum16(const uint4 &v)
 {
     int s = __dp4a((int)v.x, (int)kOnes, 0);
